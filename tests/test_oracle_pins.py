@@ -1,0 +1,384 @@
+"""Pins for the CPU oracle: each checks it against something other than itself.
+
+Codecs against the OCP tables and torch's independent fp8 / bf16 conversions;
+sizes against the pages' printed numbers; the router against the pages' printed
+rank weights, closed forms and a library softmax; the NVFP4 matvec and the
+expert FFN against hand-built matrices with closed-form results; the LRU trace
+against a hand-computed trace and an exhaustive history-scan brute force.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workload
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ codecs
+
+# OCP MX v1.0, FP4 E2M1 value table (codes 0..7; codes 8..15 are their negatives)
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_exhaustive(orc):
+    for code in range(16):
+        v = orc.e2m1(code)
+        want = E2M1_TABLE[code & 7] * (-1.0 if code & 8 else 1.0)
+        assert v == want and math.copysign(1.0, v) == (-1.0 if code & 8 else 1.0), code
+
+
+def test_e4m3_exhaustive_vs_torch(orc):
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    for code in range(256):
+        v, r = orc.e4m3(code), ref[code].item()
+        if math.isnan(r):
+            assert math.isnan(v), code
+        else:
+            assert v == r and math.copysign(1, v) == math.copysign(1, r), code
+    # spot values from the OCP table
+    assert orc.e4m3(0x30) == 0.5 and orc.e4m3(0x3F) == 1.875 and orc.e4m3(0x38) == 1.0
+    assert orc.e4m3(0x7E) == 448.0 and orc.e4m3(0x01) == 2.0 ** -9 and math.isnan(orc.e4m3(0xFF))
+
+
+def test_bf16_vs_torch(orc):
+    rng = np.random.default_rng(0)
+    bits = np.concatenate([rng.integers(0, 1 << 16, 4000), [0, 0x8000, 0x3F80, 0x7F7F, 0x0001]])
+    ref = torch.from_numpy(bits.astype(np.int32).astype(np.int16)).view(torch.bfloat16).double()
+    for b, r in zip(bits, ref.tolist()):
+        v = orc.bf16(int(b))
+        assert (math.isnan(v) and math.isnan(r)) or v == r
+
+
+# ------------------------------------------------------------------- sizes
+
+def test_expert_sizes_match_pages(orc):
+    g = _golden("sizes.json")
+    glm, fl = g["glm"], g["flash"]
+    bw, bs = orc.expert_bytes(glm["hidden"], glm["inter"])
+    assert round(bw / 1e6, 3) == glm["weights_MB"]
+    assert round(bs / 1e6, 3) == glm["scales_MB"]
+    assert round((bw + bs) / 1e6, 3) == glm["expert_MB"]
+    assert (bw + bs) / 2 ** 20 == glm["expert_MiB"]
+    assert bs / bw == glm["scale_fraction"]
+    per_layer = (bw + bs) * glm["experts"]
+    assert round(per_layer / 2 ** 30, 2) == glm["layer_GiB"]
+    assert round(per_layer * glm["layers"] / 2 ** 30) == glm["all_layers_GiB"]
+    assert bw * glm["experts"] * glm["layers"] / 2 ** 30 == glm["all_layers_weights_GiB"]
+    assert round(bs * glm["experts"] / 1e9, 1) == glm["layer_scales_GB"]
+    assert round(bs * glm["experts"] * glm["layers"] / 1e9, 1) == glm["all_layers_scales_GB"]
+    assert round(bw * 2 / 3 * glm["experts"] / 1e9, 2) == glm["w13_slab_GB"]
+    assert round(bw / 3 * glm["experts"] / 1e9, 2) == glm["w2_slab_GB"]
+    bw, bs = orc.expert_bytes(fl["hidden"], fl["inter"])
+    assert (bw + bs) / 2 ** 20 == fl["expert_MiB"]
+    assert round(fl["layers"] * fl["top_k"] * (bw + bs) / 2 ** 30, 2) == fl["per_token_GiB"]
+    # the input generator lays banks out with the same sizes
+    assert workload.storage_bytes(fl["hidden"], fl["inter"]) == (bw, bs)
+
+
+# ------------------------------------------------------------------ router
+
+def test_router_reproduces_printed_rank_weights(orc):
+    g = _golden("router_rank_weights.json")
+    w = np.array(g["weights"])
+    assert abs(w.sum() - 1.0) <= g["print_precision"] * len(w)
+    rng = np.random.default_rng(1)
+    E = 288
+    logits = np.log(w.min()) - 5.0 - rng.random(E)      # the other experts rank below
+    chosen = rng.choice(E, size=8, replace=False)
+    logits[chosen] = np.log(w) + 3.0                     # any common offset
+    ids, wts, flags = orc.route(logits.astype(np.float32), 8)
+    assert flags == 0
+    assert list(ids) == list(chosen)                     # rank order = weight order
+    assert np.allclose(wts, w / w.sum(), atol=1e-6)      # renormalised over the k
+    assert np.max(np.abs(wts - w)) <= g["print_precision"] + 1e-6
+
+
+def test_router_closed_forms(orc):
+    # two experts a log-ratio ln 3 apart: weights 3/4 and 1/4
+    lg = np.full(16, -10.0, np.float32)
+    lg[5], lg[9] = math.log(3.0), 0.0
+    ids, w, _ = orc.route(lg, 2)
+    assert list(ids) == [5, 9] and abs(w[0] - 0.75) < 1e-7 and abs(w[1] - 0.25) < 1e-7
+    # top-1 always has weight 1
+    ids, w, _ = orc.route(np.random.default_rng(2).standard_normal(40).astype(np.float32), 1)
+    assert w[0] == 1.0
+    # k = E is a full softmax (library routine)
+    from scipy.special import softmax
+    lg = np.random.default_rng(3).standard_normal(12).astype(np.float32)
+    ids, w, _ = orc.route(lg, 12)
+    assert np.allclose(w, softmax(lg.astype(np.float64))[ids], rtol=1e-12, atol=0)
+    assert list(ids) == list(np.argsort(-lg, kind="stable"))
+
+
+def test_router_ties_nan_and_signed_zero(orc):
+    # all equal: ids 0..k-1 (stable expert order), uniform weights
+    ids, w, f = orc.route(np.zeros(10, np.float32), 4)
+    assert list(ids) == [0, 1, 2, 3] and np.allclose(w, 0.25) and f == 0
+    # -0 and +0 tie: the lower id wins
+    lg = np.array([-1.0, -0.0, 0.0, -2.0], np.float32)
+    ids, w, _ = orc.route(lg, 2)
+    assert list(ids) == [1, 2] and np.allclose(w, 0.5)
+    # NaN ranks below -inf and raises the flag; +inf takes all the weight
+    lg = np.array([np.nan, 1.0, -np.inf, np.inf, 0.5], np.float32)
+    ids, w, f = orc.route(lg, 5)
+    assert list(ids) == [3, 1, 4, 2, 0] and f == 1
+    assert list(w) == [1.0, 0.0, 0.0, 0.0, 0.0]
+    # every selected logit -inf / NaN: uniform weights, still defined
+    ids, w, f = orc.route(np.array([np.nan, -np.inf, -np.inf], np.float32), 2)
+    assert list(ids) == [1, 2] and list(w) == [0.5, 0.5] and f == 1
+
+
+def test_router_invariants_random(orc):
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        E = int(rng.integers(2, 40))
+        k = int(rng.integers(1, E + 1))
+        lg = rng.integers(-3, 4, E).astype(np.float32)   # many ties
+        ids, w, _ = orc.route(lg, k)
+        assert len(set(ids)) == k
+        sel = set(ids.tolist())
+        others = [e for e in range(E) if e not in sel]
+        if others:   # every selected logit >= every unselected one; on equality the selected id is lower
+            for e in others:
+                assert all(lg[i] > lg[e] or (lg[i] == lg[e] and i < e) for i in ids)
+        assert abs(w.sum() - 1.0) < 1e-12 and np.all(np.diff(w) <= 1e-15)
+
+
+# ------------------------------------------------------------ NVFP4 matvec
+
+def test_matvec_nibble_order_and_scale_blocks(orc):
+    K = 64
+    codes = np.zeros((2, K // 2), np.uint8)
+    scales = np.full((2, K // 16), 0x38, np.uint8)       # 1.0
+    codes[0, 0] = 0x21                                   # element 0 = code 1 (0.5), element 1 = code 2 (1.0)
+    codes[0, 9] = 0x07                                   # element 18 = code 7 (6.0), element 19 = 0
+    scales[0, 1] = 0x40                                  # block 1 (elements 16..31) scale 2.0
+    codes[1, 31] = 0xF0                                  # element 63 = code 15 (-6.0)
+    scales[1, 3] = 0x30                                  # block 3 scale 0.5
+    for p, want0, want1 in [(0, 0.5, 0.0), (1, 1.0, 0.0), (18, 12.0, 0.0), (19, 0.0, 0.0),
+                            (63, 0.0, -3.0)]:
+        v = np.zeros(K)
+        v[p] = 1.0
+        out = orc.nvfp4_matvec(codes, scales, 0.25, 2, K, v)
+        assert list(out) == [want0 * 0.25, want1 * 0.25], p
+
+
+def test_matvec_constant_matrix_closed_form(orc):
+    rng = np.random.default_rng(5)
+    rows, K = 5, 128
+    for code, scode, sval in [(3, 0x38, 1.0), (0xB, 0x48, 4.0), (7, 0x30, 0.5)]:
+        codes = np.full((rows, K // 2), code | (code << 4), np.uint8)
+        scales = np.full((rows, K // 16), scode, np.uint8)
+        v = rng.standard_normal(K)
+        out = orc.nvfp4_matvec(codes, scales, 1 / 64, rows, K, v)
+        want = E2M1_TABLE[code & 7] * (-1 if code & 8 else 1) * sval / 64 * np.sum(v)
+        assert np.allclose(out, want, rtol=1e-13, atol=1e-13)
+
+
+def test_matvec_equals_dense_library_product(orc):
+    """Random NVFP4 matrix: the oracle equals a dense float64 matrix built from the
+    OCP E2M1 table and torch's fp8 decode, multiplied by numpy."""
+    rng = np.random.default_rng(6)
+    rows, K = 24, 96
+    codes = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+    scales = (0x30 | (rng.integers(0, 256, (rows, K // 16)) & 0xF)).astype(np.uint8)
+    tab = np.array(E2M1_TABLE + [-x for x in E2M1_TABLE])
+    lo, hi = tab[codes & 0xF], tab[codes >> 4]
+    elem = np.stack([lo, hi], axis=-1).reshape(rows, K)
+    sc = torch.from_numpy(scales).view(torch.float8_e4m3fn).double().numpy()
+    W = elem * np.repeat(sc, 16, axis=1) * 0.75
+    v = rng.standard_normal(K)
+    assert np.allclose(orc.nvfp4_matvec(codes, scales, 0.75, rows, K, v), W @ v, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------- expert FFN
+
+def _const_expert(H, I, a, b, c):
+    bw, bs = workload.storage_bytes(H, I)
+    w = np.empty(bw, np.uint8)
+    w[: I * H // 2] = a | (a << 4)
+    w[I * H // 2: I * H] = b | (b << 4)
+    w[I * H:] = c | (c << 4)
+    s = np.full(bs, 0x38, np.uint8)
+    return w, s
+
+
+def test_ffn_closed_form(orc):
+    H, I = 64, 32
+    w, s = _const_expert(H, I, 2, 3, 0xA)   # gate 1.0, up 1.5, down -1.0
+    gs = np.array([0.5, 0.25, 2.0], np.float32)
+    x = np.random.default_rng(7).standard_normal(H)
+    y, h = orc.expert_ffn(w, s, gs, H, I, x)
+    S = np.sum(x)
+    g, u = 1.0 * 0.5 * S, 1.5 * 0.25 * S
+    hh = g / (1 + math.exp(-g)) * u
+    assert np.allclose(h, hh, rtol=1e-12)
+    assert np.allclose(y, -1.0 * 2.0 * I * hh, rtol=1e-12)
+    # gate rows are the first I rows: zero gate codes => h = silu(0) * u = 0
+    w0, s0 = _const_expert(H, I, 0, 3, 0xA)
+    y0, h0 = orc.expert_ffn(w0, s0, gs, H, I, x)
+    assert not h0.any() and not y0.any()
+
+
+def test_ffn_one_hot_input_reads_one_column(orc):
+    """x = e_p makes g and u the p-th dequantised columns of the gate and up blocks."""
+    H, I = 64, 16
+    rng = np.random.default_rng(8)
+    bw, bs = workload.storage_bytes(H, I)
+    w = rng.integers(0, 256, bw, dtype=np.uint8)
+    s = (0x30 | (rng.integers(0, 256, bs) & 0xF)).astype(np.uint8)
+    gs = np.array([1.0, 1.0, 1.0], np.float32)
+    tab = np.array(E2M1_TABLE + [-x for x in E2M1_TABLE])
+    sc = torch.from_numpy(s).view(torch.float8_e4m3fn).double().numpy()
+    for p in (0, 1, 17, 63):
+        x = np.zeros(H)
+        x[p] = 1.0
+        _, h = orc.expert_ffn(w, s, gs, H, I, x)
+        for r in range(I):
+            byte_g = w[r * H // 2 + p // 2]
+            byte_u = w[(I + r) * H // 2 + p // 2]
+            cg = tab[(byte_g >> (4 * (p & 1))) & 0xF] * sc[r * H // 16 + p // 16]
+            cu = tab[(byte_u >> (4 * (p & 1))) & 0xF] * sc[(I + r) * H // 16 + p // 16]
+            assert abs(h[r] - cg / (1 + math.exp(-cg)) * cu) < 1e-12
+
+
+def test_moe_rows_special_cases(orc):
+    H, I, E = 64, 32, 4
+    rng = np.random.default_rng(9)
+    bw, bs = workload.storage_bytes(H, I)
+    w = rng.integers(0, 256, E * bw, dtype=np.uint8)
+    s = (0x30 | (rng.integers(0, 256, E * bs) & 0xF)).astype(np.uint8)
+    gs = workload.global_scales(E)
+    x = workload.to_bf16_bits(rng.standard_normal((1, H)).astype(np.float32))
+    xd = np.array([orc.bf16(int(b)) for b in x[0]])
+    # top-1 reduces to the single chosen expert
+    lg = np.array([[0.0, 3.0, 1.0, 2.0]], np.float32)
+    out, ids, wts, _ = orc.moe_rows(w, s, gs, E, H, I, 1, lg, x)
+    y1, _ = orc.expert_ffn(w[bw:2 * bw], s[bs:2 * bs], gs[1], H, I, xd)
+    assert ids[0, 0] == 1 and wts[0, 0] == 1.0 and np.array_equal(out[0], y1)
+    # two equal logits: the average of the two experts
+    lg = np.array([[5.0, -1.0, 5.0, 0.0]], np.float32)
+    out, ids, wts, _ = orc.moe_rows(w, s, gs, E, H, I, 2, lg, x)
+    y0, _ = orc.expert_ffn(w[:bw], s[:bs], gs[0], H, I, xd)
+    y2, _ = orc.expert_ffn(w[2 * bw:3 * bw], s[2 * bs:3 * bs], gs[2], H, I, xd)
+    assert list(ids[0]) == [0, 2] and np.allclose(out[0], 0.5 * y0 + 0.5 * y2, rtol=1e-13, atol=1e-13)
+    # identical experts: the output does not depend on the routing
+    wi = np.tile(w[:bw], E)
+    si = np.tile(s[:bs], E)
+    o1, *_ = orc.moe_rows(wi, si, gs, E, H, I, 3, np.array([[1, 2, 3, 4]], np.float32), x)
+    o2, *_ = orc.moe_rows(wi, si, gs, E, H, I, 3, np.array([[4, -3, 2, 0.5]], np.float32), x)
+    assert np.allclose(o1, o2, rtol=1e-12, atol=1e-12) and np.allclose(o1[0], y0, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- LRU trace
+
+def test_lru_hand_computed_trace(orc):
+    g = _golden("lru_tie_trace.json")
+    sim = orc.LRUSim(g["experts"], g["slots"])
+    for st in g["steps"]:
+        rec = sim.step(np.array(st["ids"]))
+        assert list(rec["hit"]) == st["hit"]
+        assert list(rec["slot"]) == st["slot"]
+        got = [[int(a), int(b), int(c)] for a, b, c in zip(rec["miss_e"], rec["miss_v"], rec["miss_evicted"])]
+        assert got == st["misses"]
+    assert list(sim.owner) == g["final_owner"]
+
+
+def _lru_by_history(E, S, trace):
+    """Brute-force LRU from the full history: the victim is the slot not used this
+    step whose most recent use (scanned back through the history) is oldest,
+    lowest slot id on ties; empty slots count as never used."""
+    owner = [-1] * S
+    history = []          # per cached step: set of slots used
+    out = []
+    for ids in trace:
+        U = sorted(set(ids))
+        resident = {owner[v]: v for v in range(S) if owner[v] >= 0}
+        hit = [int(e in resident) for e in ids]
+        if len(U) > S:
+            out.append(("bypass", hit))
+            continue
+        used = {resident[e] for e in U if e in resident}
+        misses = []
+        for e in U:
+            if e in resident:
+                continue
+
+            def last_use(v):
+                for t in range(len(history) - 1, -1, -1):
+                    if v in history[t]:
+                        return t + 1
+                return 0
+            v = min((v for v in range(S) if v not in used), key=lambda v: (last_use(v), v))
+            misses.append((e, v, owner[v]))
+            owner[v] = e
+            used.add(v)
+        history.append(used)
+        where = {owner[v]: v for v in range(S) if owner[v] >= 0}
+        out.append((hit, [where[e] for e in ids], misses))
+    return out
+
+
+def _check_trace(orc, E, S, trace):
+    sim = orc.LRUSim(E, S)
+    want = _lru_by_history(E, S, trace)
+    for ids, w in zip(trace, want):
+        rec = sim.step(np.array(ids))
+        if w[0] == "bypass":
+            assert rec["bypass"] and list(rec["hit"]) == w[1]
+            continue
+        assert not rec["bypass"]
+        assert list(rec["hit"]) == w[0] and list(rec["slot"]) == w[1]
+        assert list(zip(rec["miss_e"].tolist(), rec["miss_v"].tolist(),
+                        rec["miss_evicted"].tolist())) == w[2]
+
+
+def test_lru_exhaustive_small_traces(orc):
+    E, steps = 5, 4
+    for k in (1, 2):
+        rows = list(itertools.combinations(range(E), k))
+        for S in (2, 3):
+            for tr in itertools.product(rows, repeat=steps):
+                _check_trace(orc, E, S, [list(r) for r in tr])
+
+
+def test_lru_multirow_with_bypass_random(orc):
+    rng = np.random.default_rng(10)
+    for _ in range(300):
+        E, S, k, M = 7, int(rng.integers(2, 5)), 2, int(rng.integers(1, 4))
+        trace = []
+        for _ in range(6):
+            trace.append([int(e) for m in range(M) for e in rng.choice(E, k, replace=False)])
+        _check_trace(orc, E, S, trace)
+
+
+def test_lru_counters_and_generator_statistics(orc):
+    """Counters balance, and the routing generator has the pages' statistics:
+    step-to-step overlap near 0.27 and an LRU hit rate near 0.8 at ~98 slots
+    ("GB300 GLM 5.3 Testing": exact-replay LRU 0.802 at 7,360 slots over 75 layers)."""
+    cfg = workload.CONFIGS["glm"]
+    rt = workload.Routing(cfg)
+    sim = orc.LRUSim(cfg.experts, 98, check_list=False)
+    prev, overlaps = None, []
+    for t in range(600):
+        ids, _, _ = orc.route(rt.step()[0], cfg.top_k)
+        rec = sim.step(ids)
+        if prev is not None:
+            overlaps.append(len(set(ids) & set(prev)) / cfg.top_k)
+        prev = ids
+    st = sim.stats
+    assert st["picks"] == 600 * cfg.top_k and st["hits"] + st["misses"] == st["picks"]
+    assert st["evictions"] == st["misses"] - 98
+    assert 0.22 < np.mean(overlaps) < 0.32
+    assert 0.70 < 1 - (st["misses"] - 98) / (st["picks"] - 98) < 0.9
