@@ -1,0 +1,434 @@
+"""Benchmark: GLM-shape slot-cache MoE decode layer-steps/s (M=1, S=128).
+
+One step = one layer-step of the whole hot path (route + remap/LRU, miss copy
+over the host link, NVFP4 gate/up + SwiGLU, down + combine) on one row, GLM
+shape (hidden 6144, inter 2048, 256 experts, top-8, 128 slots), seeded
+synthetic routing (Zipf(1.1) popularity, ~0.27 step-to-step overlap) and
+weights.  The cache is warmed to steady state first; each timed step routes a
+fresh row, so misses are real and counted.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Our arm: inputs resident in HBM, the K steps captured as CUDA graphs and
+replayed; per-kernel times come from event-record nodes in the last graph of
+the timed region.  N > 1 (torchrun): independent replicas, one per GPU
+("replicas only": the layer has no exchange step), value = all ranks' steps /
+max time.  The reference arm (--impl reference) times the CPU oracle as it
+stands on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+METRIC = "GLM-shape MoE decode layer-steps/s (M=1, S=128); % of HBM+host-link roofline"
+UNIT = "layer-steps/s"
+GLM_MOE_LAYERS = 75  # tok/s-equivalent = layer-steps/s / 75 MoE layers
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return 6800.0, "fallback (6.8 TB/s)"
+
+
+def _src_sha() -> str:
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "hbm_slot_cache_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        h.update(open(os.path.join(cs, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("src_sha") != _src_sha():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.path = None
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "50"]
+            if uuid:
+                cmd += ["-i", uuid]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_layer_steps(cfg, banks, seconds: float, max_steps: int) -> dict:
+    """Full oracle layer-steps (route, LRU, 8-expert FFN, combine), one thread."""
+    import oracle
+    import workload
+    rt = workload.Routing(cfg)
+    xs = workload.activations(cfg.seed, 0, max_steps, 1, cfg.hidden)
+    sim = oracle.LRUSim(cfg.experts, cfg.slots, check_list=False)
+    w, s, g = banks.layer_arrays(0)
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps and (n == 0 or time.perf_counter() - t0 < seconds):
+        lg = rt.step()
+        _, ids, _, _ = oracle.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
+                                       lg, xs[n])
+        sim.step(ids)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} full GLM layer-steps (route, LRU, 8 experts x 3 NVFP4 matvecs in "
+                      f"double, combine) in {dt:.1f} s, single-threaded C"}
+
+
+def oracle_sampled_step(cfg, banks, sim, rt, x, frac: float) -> float:
+    """One reference-arm step: route + LRU in full, then for each of the k picked
+    experts the NVFP4 matvecs on a fraction `frac` of the gate/up rows (K = hidden)
+    and of the down rows (K = inter); returns the time scaled to a full layer-step."""
+    import oracle
+    t0 = time.perf_counter()
+    lg = rt.step()
+    ids, _, _ = oracle.route(lg[0], cfg.top_k)
+    sim.step(ids)
+    t1 = time.perf_counter()
+    H, I = cfg.hidden, cfg.inter
+    w, s, _ = banks.layer_arrays(0)
+    bw, bs = banks.Bw, banks.Bs
+    xd = (x[0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    hv = np.tanh(xd[:I])
+    n_gu = max(1, int(round(2 * I * frac)))
+    n_dn = max(1, int(round(H * frac)))
+    for e in ids.tolist():
+        we, se = w[e * bw:(e + 1) * bw], s[e * bs:(e + 1) * bs]
+        oracle.nvfp4_matvec(we, se, 1 / 64, n_gu, H, xd)
+        oracle.nvfp4_matvec(we[I * H:], se[I * H // 8:], 1 / 64, n_dn, I, hv)
+    t2 = time.perf_counter()
+    return (t1 - t0) + (t2 - t1) / frac
+
+
+def run_reference(args) -> None:
+    import workload
+    from harness import Banks
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cfg = workload.CONFIGS["glm"]
+    banks = Banks(cfg)
+    rt = workload.Routing(cfg)
+    sim = oracle.LRUSim(cfg.experts, cfg.slots, check_list=False)
+    # size the per-step sample so warmup + steps take about a minute
+    budget_s = 60.0
+    full_step_s = 7.0
+    frac = min(1.0, max(1.0 / 2048, budget_s / (full_step_s * (args.steps + args.warmup))))
+    xs = workload.activations(cfg.seed, 0, 1, 1, cfg.hidden)
+    for _ in range(args.warmup):
+        oracle_sampled_step(cfg, banks, sim, rt, xs[0], frac)
+    t = [oracle_sampled_step(cfg, banks, sim, rt, xs[0], frac) for _ in range(args.steps)]
+    sec = float(np.sum(t))
+    value = args.steps / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "glm-layer M=1 S=128 (hidden 6144, inter 2048, 256 experts, top-8)",
+                       "global_batch": 1, "parallelism": "cpu oracle, 1 thread"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"per step: route + LRU in full, expert FFN on {frac:.5f} "
+                                       "of each matrix's rows, time scaled to a full layer-step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    banks.close()
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import workload
+    from harness import Banks, make_cache
+    import hbm_slot_cache_gb300 as hsc
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hsc.build()
+
+    cfg = workload.CONFIGS["glm"]
+    E, H, k = cfg.experts, cfg.hidden, cfg.top_k
+    banks = Banks(cfg)
+    cache = make_cache(cfg, banks, layers=1)
+    prewarm = 64
+    W, K = args.warmup, args.steps
+    G = min(K, 200)  # steps in the final (event-instrumented) graph
+    total = prewarm + W + K
+    rt = workload.Routing(cfg)
+    lgs = np.stack([rt.step() for _ in range(total)])                 # [T, 1, E]
+    xs = workload.activations(cfg.seed, 0, total, 1, H)               # [T, 1, H] bf16 bits
+    lg_d = torch.from_numpy(lgs).cuda()
+    x_d = torch.from_numpy(xs.view(np.int16)).cuda().view(torch.bfloat16)
+    out_d = torch.empty((1, H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def steps_on(t0, t1):
+        for t in range(t0, t1):
+            cache.step(0, lg_d[t], x_d[t], out_d)
+
+    with torch.cuda.stream(stream):
+        steps_on(0, prewarm)                      # fill the ring to steady state (eager)
+    stream.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(G)]
+    for row in evs:
+        for e in row:
+            e.record(stream)                      # materialise the event handles
+    stream.synchronize()
+
+    def capture(t0, t1, with_events=False):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(t0, t1):
+                if with_events:
+                    hsc.moe_cache_set_timing_events(cache.h, [e.cuda_event for e in evs[t - t0]])
+                cache.step(0, lg_d[t], x_d[t], out_d)
+            hsc.moe_cache_set_timing_events(cache.h, None)
+        return g
+
+    t_w = prewarm + W
+    g_warm = capture(prewarm, t_w)
+    g_main = capture(t_w, t_w + K - G) if K > G else None
+    g_ev = capture(t_w + K - G, t_w + K, with_events=True)
+
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    stream.synchronize()
+    s0 = cache.stats(0)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(uuid)
+    time.sleep(0.15)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        if g_main is not None:
+            g_main.replay()
+        g_ev.replay()
+        end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = start.elapsed_time(end)
+    t_max = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms_total_max = float(t_max.item())
+    s1 = cache.stats(0)
+    misses = s1["misses"] - s0["misses"]
+    hits = s1["hits"] - s0["hits"]
+    picks = s1["picks"] - s0["picks"]
+    assert s1["error_flags"] == 0, s1
+
+    # per-kernel times over the instrumented graph (last G steps of the timed region)
+    names = ["route_remap", "miss_copy", "gemv_gateup", "gemv_down"]
+    per = {n: 0.0 for n in names}
+    for row in evs:
+        for i, n in enumerate(names):
+            per[n] += row[i].elapsed_time(row[i + 1])
+    per_launch_ms = {n: per[n] / G for n in names}
+
+    # host-link bandwidth probed in the same session
+    from hbm_slot_cache_gb300 import HostBank, moe_probe_host_link
+    nb = 1 << 30
+    hb = HostBank(nb)
+    hb.array[::4096] = 1
+    dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    link_sm = moe_probe_host_link(hb.ptr, dst.data_ptr(), nb, 0, 5)
+    link_ce = moe_probe_host_link(hb.ptr, dst.data_ptr(), nb, 1, 5)
+    del dst
+    hb.close()
+    link_peak = max(link_sm, link_ce)
+    hbm_peak, hbm_src = _peaks()
+
+    Bexp = banks.Bw + banks.Bs
+    ms_step = ms_total_max / K
+    value = world * K / (ms_total_max * 1e-3)
+    miss_per_step = misses / K
+    hbm_bytes = k * Bexp                       # expert bytes the kernels read per step
+    link_bytes = miss_per_step * Bexp           # miss bytes over the host link per step
+    t_roof_s = hbm_bytes / (hbm_peak * 1e9) + link_bytes / (link_peak * 1e9)
+    path_frac = t_roof_s / (ms_step * 1e-3)
+
+    # kernel rooflines (per launch, averaged over the instrumented steps)
+    gemv_bytes_gu = k * (2 * cfg.inter * (H // 2 + H // 16))
+    gemv_bytes_dn = k * (H * (cfg.inter // 2 + cfg.inter // 16))
+    ev_misses = None
+    kern = {}
+    for n, nbytes, peak, unit, bound in (
+            ("gemv_gateup", gemv_bytes_gu, hbm_peak, "GB/s", "hbm"),
+            ("gemv_down", gemv_bytes_dn, hbm_peak, "GB/s", "hbm")):
+        t = per_launch_ms[n] * 1e-3
+        kern[n] = {"bound": bound, "achieved": nbytes / t / 1e9, "peak": peak, "unit": unit,
+                   "frac": nbytes / t / 1e9 / peak, "traffic": _traffic(n),
+                   "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": per_launch_ms[n]}
+    # the miss copy: bytes moved per launch over the link, against the link probe
+    copy_bytes = miss_per_step * Bexp
+    t = per_launch_ms["miss_copy"] * 1e-3
+    kern["miss_copy"] = {"bound": "host-link", "achieved": copy_bytes / t / 1e9 if t else None,
+                         "peak": link_peak, "unit": "GB/s",
+                         "frac": copy_bytes / t / 1e9 / link_peak if t else None,
+                         "traffic": _traffic("miss_copy"),
+                         "algorithmic_bytes_per_launch": copy_bytes,
+                         "ms_per_launch": per_launch_ms["miss_copy"],
+                         "note": "bytes = the timed region's mean miss bytes per step"}
+    kern["route_remap"] = {"ms_per_launch": per_launch_ms["route_remap"]}
+    dom = max(("gemv_gateup", "gemv_down", "miss_copy"), key=lambda n: per_launch_ms[n])
+    roofline = dict(kern[dom])
+    roofline["kernel"] = dom
+    roofline["peak_source"] = (hbm_src if roofline["bound"] == "hbm"
+                               else "moe_probe_host_link, same session (best of SM copy / cudaMemcpyAsync)")
+    del ev_misses
+
+    # end to end through the public API: pinned host inputs -> step -> host output
+    Ke = min(K, 1000)
+    lg_h = torch.from_numpy(lgs[prewarm:prewarm + Ke].copy()).pin_memory()
+    x_h = torch.from_numpy(xs[prewarm:prewarm + Ke].view(np.int16).copy()).pin_memory().view(torch.bfloat16)
+    out_h = torch.empty((Ke, 1, H), dtype=torch.float32).pin_memory()
+    lg_in = torch.empty((1, E), dtype=torch.float32, device="cuda")
+    x_in = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for t in range(Ke):
+            lg_in.copy_(lg_h[t], non_blocking=True)
+            x_in.copy_(x_h[t], non_blocking=True)
+            cache.step(0, lg_in, x_in, out_d)
+            out_h[t].copy_(out_d, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = world * Ke / (float(e2e_ms.item()) * 1e-3)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_layer_steps(cfg, banks, seconds=12.0, max_steps=8)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4 weights, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": "glm-layer M=1 S=128: hidden 6144, inter 2048, 256 experts, "
+                                   "top-8, 128 HBM slots, Zipf(1.1) routing, steady state",
+                       "global_batch": world, "seq_len": 1,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2: 170 MB of expert bytes per step > 126 MB L2; "
+                             "2.7 GB slot ring", "graph": "CUDA graphs, eager prewarm of 64 steps"},
+            "tok_s_equivalent": value / GLM_MOE_LAYERS,
+            "path_roofline": {"frac": path_frac, "t_roofline_us": t_roof_s * 1e6,
+                              "t_measured_us": ms_step * 1e3, "hbm_bytes_per_step": hbm_bytes,
+                              "link_bytes_per_step": link_bytes, "hbm_peak_gbs": hbm_peak,
+                              "hbm_peak_source": hbm_src, "link_peak_gbs": link_peak,
+                              "link_probe_sm_gbs": link_sm, "link_probe_memcpy_gbs": link_ce,
+                              "misses_per_step": miss_per_step,
+                              "hit_rate": hits / picks if picks else None},
+            "roofline": roofline, "kernels": kern,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": E * 4 + H * 2,
+                    "d2h_bytes_per_step": H * 4, "steps": Ke},
+            "gpu_launches": K * 4, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    cache.close()
+    banks.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

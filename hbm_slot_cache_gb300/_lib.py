@@ -1,0 +1,207 @@
+"""ctypes binding of libmoe_slot_cache.so: the C ABI of include/moe_slot_cache.h.
+
+Argument marshalling only.  Every step of the layer runs in the library's CUDA
+kernels; there is no Python or CPU path.  Loading fails loudly when the shared
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_SO = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_slot_cache.so")
+
+MOE_OK = 0
+MOE_ERR_ARG = -1
+MOE_ERR_NOT_PINNED = -2
+MOE_ERR_OOM = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_UNSUPPORTED = -5
+MOE_FLAG_NONFINITE_LOGIT = 0x1
+MOE_FLAG_WAIT_TIMEOUT = 0x2
+MOE_MAX_EXPERTS = 1024
+MOE_MAX_TOPK = 16
+MOE_MAX_CACHED_ROWS = 16
+MOE_MAX_PICKS = MOE_MAX_CACHED_ROWS * MOE_MAX_TOPK
+MOE_MAX_DIM = 8192
+MOE_COPY_SM = 0
+
+EXPORTS = ("moe_cache_create", "moe_cache_step", "moe_cache_stats", "moe_cache_slot_map",
+           "moe_cache_slot_bytes", "moe_cache_trace", "moe_cache_reset", "moe_cache_destroy",
+           "moe_cache_strerror", "moe_expert_bytes", "moe_host_alloc", "moe_host_free",
+           "moe_probe_host_link", "moe_cache_set_timing_events")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+class HostLayer(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("s", ctypes.c_void_p), ("gscale", ctypes.c_void_p)]
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("copy_backend", ctypes.c_int), ("bypass_rows", ctypes.c_int),
+                ("all_resident", ctypes.c_int), ("trace_capacity", ctypes.c_int),
+                ("max_rows", ctypes.c_int)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_uint64), ("picks", ctypes.c_uint64), ("hits", ctypes.c_uint64),
+                ("misses", ctypes.c_uint64), ("evictions", ctypes.c_uint64),
+                ("bytes_copied", ctypes.c_uint64), ("bypass_calls", ctypes.c_uint64),
+                ("error_flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+_P = MOE_MAX_PICKS
+
+
+class StepRecord(ctypes.Structure):
+    _fields_ = [("clock", ctypes.c_uint32), ("rows", ctypes.c_int32), ("n_union", ctypes.c_int32),
+                ("n_miss", ctypes.c_int32), ("bypass", ctypes.c_int32),
+                ("ids", ctypes.c_int32 * _P), ("weights", ctypes.c_float * _P),
+                ("slot", ctypes.c_int32 * _P), ("hit", ctypes.c_int32 * _P),
+                ("miss_expert", ctypes.c_int32 * _P), ("miss_slot", ctypes.c_int32 * _P),
+                ("miss_evicted", ctypes.c_int32 * _P)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_SO):
+            raise RuntimeError(f"{_SO} is missing: build it with hbm_slot_cache_gb300.build.build() "
+                               "(needs nvcc); there is no fallback implementation")
+        L = ctypes.CDLL(_SO)
+        P, I, U64P = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)
+        L.moe_cache_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, I, P, P]
+        L.moe_cache_step.argtypes = [P, I, I, P, P, P, P]
+        L.moe_cache_stats.argtypes = [P, I, ctypes.POINTER(Stats)]
+        L.moe_cache_slot_map.argtypes = [P, I, P]
+        L.moe_cache_slot_bytes.argtypes = [P, I, I, P, P]
+        L.moe_cache_trace.argtypes = [P, I, P, I, ctypes.POINTER(ctypes.c_int)]
+        L.moe_cache_reset.argtypes = [P]
+        L.moe_cache_destroy.argtypes = [P]
+        L.moe_cache_strerror.argtypes = [I]
+        L.moe_cache_strerror.restype = ctypes.c_char_p
+        L.moe_expert_bytes.argtypes = [I, I, U64P, U64P]
+        L.moe_host_alloc.argtypes = [ctypes.POINTER(P), ctypes.c_size_t]
+        L.moe_host_free.argtypes = [P]
+        L.moe_probe_host_link.argtypes = [P, P, ctypes.c_size_t, I, I,
+                                          ctypes.POINTER(ctypes.c_double)]
+        L.moe_cache_set_timing_events.argtypes = [P, P]
+        for name in EXPORTS:
+            if name != "moe_cache_strerror":
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().moe_cache_strerror(code).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+# ------------------------------------------------------------------- C ABI
+
+def moe_expert_bytes(hidden: int, inter: int) -> tuple[int, int]:
+    bw, bs = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(lib().moe_expert_bytes(hidden, inter, ctypes.byref(bw), ctypes.byref(bs)),
+           "moe_expert_bytes")
+    return bw.value, bs.value
+
+
+def moe_cache_create(layers: int, experts: int, slots: int, hidden: int, inter: int, top_k: int,
+                     host_layers, copy_backend: int = MOE_COPY_SM, bypass_rows: int = 0,
+                     all_resident: bool = False, trace_capacity: int = 0,
+                     max_rows: int = 0) -> int:
+    """host_layers: sequence of (w_ptr, s_ptr, gscale_ptr) per layer. Returns the handle."""
+    arr = (HostLayer * layers)(*[HostLayer(int(w), int(s), int(g)) for (w, s, g) in host_layers])
+    o = Opts(copy_backend, bypass_rows, int(all_resident), trace_capacity, max_rows)
+    h = ctypes.c_void_p()
+    _check(lib().moe_cache_create(ctypes.byref(h), layers, experts, slots, hidden, inter, top_k,
+                                  ctypes.cast(arr, ctypes.c_void_p), ctypes.byref(o)),
+           "moe_cache_create")
+    return h.value
+
+
+def moe_cache_step(h: int, layer: int, rows: int, router_logits: int, x: int, out: int,
+                   stream: int = 0) -> None:
+    _check(lib().moe_cache_step(h, layer, rows, router_logits, x, out, stream), "moe_cache_step")
+
+
+def moe_cache_stats(h: int, layer: int = -1) -> dict:
+    st = Stats()
+    _check(lib().moe_cache_stats(h, layer, ctypes.byref(st)), "moe_cache_stats")
+    return st.as_dict()
+
+
+def moe_cache_slot_map(h: int, layer: int, slots: int) -> np.ndarray:
+    out = np.empty(slots, np.int32)
+    _check(lib().moe_cache_slot_map(h, layer, out.ctypes.data), "moe_cache_slot_map")
+    return out
+
+
+def moe_cache_slot_bytes(h: int, layer: int, slot: int, bw: int, bs: int):
+    w = np.empty(bw, np.uint8)
+    s = np.empty(bs, np.uint8)
+    _check(lib().moe_cache_slot_bytes(h, layer, slot, w.ctypes.data, s.ctypes.data),
+           "moe_cache_slot_bytes")
+    return w, s
+
+
+def moe_cache_trace(h: int, layer: int, max_recs: int) -> list[StepRecord]:
+    recs = (StepRecord * max_recs)()
+    n = ctypes.c_int()
+    _check(lib().moe_cache_trace(h, layer, ctypes.cast(recs, ctypes.c_void_p), max_recs,
+                                 ctypes.byref(n)), "moe_cache_trace")
+    return list(recs[:n.value])
+
+
+def moe_cache_reset(h: int) -> None:
+    _check(lib().moe_cache_reset(h), "moe_cache_reset")
+
+
+def moe_cache_destroy(h: int) -> None:
+    _check(lib().moe_cache_destroy(h), "moe_cache_destroy")
+
+
+def moe_cache_set_timing_events(h: int, events) -> None:
+    """events: 5 cudaEvent_t handles (ints), or None to stop recording."""
+    if events is None:
+        _check(lib().moe_cache_set_timing_events(h, None), "moe_cache_set_timing_events")
+        return
+    arr = (ctypes.c_void_p * 5)(*[int(e) for e in events])
+    _check(lib().moe_cache_set_timing_events(h, ctypes.cast(arr, ctypes.c_void_p)),
+           "moe_cache_set_timing_events")
+
+
+def moe_host_alloc(nbytes: int) -> int:
+    p = ctypes.c_void_p()
+    _check(lib().moe_host_alloc(ctypes.byref(p), nbytes), "moe_host_alloc")
+    return p.value
+
+
+def moe_host_free(p: int) -> None:
+    _check(lib().moe_host_free(p), "moe_host_free")
+
+
+def moe_probe_host_link(host_src: int, dev_dst: int, nbytes: int, method: int = 0,
+                        iters: int = 5) -> float:
+    g = ctypes.c_double()
+    _check(lib().moe_probe_host_link(host_src, dev_dst, nbytes, method, iters, ctypes.byref(g)),
+           "moe_probe_host_link")
+    return g.value

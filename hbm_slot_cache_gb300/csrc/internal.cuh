@@ -1,0 +1,181 @@
+// Internal definitions shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/moe_slot_cache.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ state
+
+// Per-layer device counters; summed/OR-ed by moe_cache_stats.
+struct DevStats {
+  unsigned long long steps, picks, hits, misses, evictions, bytes_copied, bypass_calls;
+  unsigned int flags;
+  unsigned int pad;
+};
+
+// Everything the remap kernel needs about one layer (passed by value).
+struct LayerDev {
+  int32_t* map;           // [E]  expert -> slot or -1
+  int32_t* owner;         // [S]  slot -> expert or -1
+  uint32_t* stamp;        // [S]  last-use step, 0 = never
+  uint32_t* clock;        // [1]  cached steps so far
+  uint8_t* slot_w;        // [S][Bw]
+  uint8_t* slot_s;        // [S][Bs]
+  const uint8_t* host_w;  // [E][Bw] pinned host (device-visible address)
+  const uint8_t* host_s;  // [E][Bs]
+  const float* gscale;    // [E][3] device copy
+  DevStats* stats;
+  moe_step_record_t* trace;  // [trace_cap] or null
+  uint32_t* trace_head;      // records written so far
+  uint32_t trace_cap;
+};
+
+// The per-step plan written by the remap kernel and read by the copy and
+// expert kernels.  One per handle: steps run in order on one stream.
+struct Plan {
+  int32_t rows, npicks, n_union, n_miss, bypass, pad[3];
+  int32_t ids[MOE_MAX_PICKS];
+  float wts[MOE_MAX_PICKS];
+  int32_t miss_e[MOE_MAX_PICKS];
+  int32_t miss_v[MOE_MAX_PICKS];
+  const uint8_t* wptr[MOE_MAX_PICKS];  // expert codes this pick reads (slot or host)
+  const uint8_t* sptr[MOE_MAX_PICKS];  // expert scales
+  float gs[MOE_MAX_PICKS][4];          // (gate, up, down, unused) global scales
+};
+
+// ------------------------------------------------------------ launchers
+
+// route + remap/LRU for rows <= MOE_MAX_CACHED_ROWS (one CTA).
+cudaError_t launch_route_remap(cudaStream_t st, const float* logits, int rows, int E, int k,
+                               int S, long long Bw, long long Bs, const LayerDev& L, Plan* plan,
+                               int all_resident);
+
+// miss copy host -> slot, SM kernel; reads the miss list from the plan.
+cudaError_t launch_miss_copy(cudaStream_t st, const Plan* plan, const uint8_t* host_w,
+                             const uint8_t* host_s, uint8_t* slot_w, uint8_t* slot_s,
+                             long long Bw, long long Bs, int grid);
+cudaError_t launch_link_probe(cudaStream_t st, const void* src, void* dst, size_t bytes,
+                              int grid);
+
+// M = 1 expert path: gate/up + SwiGLU -> hbuf [k][I]; down + combine -> out [H].
+struct GemvWorkspace {
+  float* hbuf;        // [MOE_MAX_PICKS][I]
+  float* ypart;       // [MOE_MAX_TOPK][H]
+  uint32_t* tile_cnt; // [H / down rows per tile]
+  uint32_t* flags;    // error flags word for waits (per layer stats flags)
+};
+cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
+                               int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms);
+cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
+                             const GemvWorkspace& ws, float* out, uint32_t* flags, int num_sms);
+int gemv_down_tile_rows(int H, int I);
+
+// ------------------------------------------------------- device helpers
+
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits on an mbarrier phase for at most ~2 s; on timeout sets
+// MOE_FLAG_WAIT_TIMEOUT in *flags and returns false (never traps).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t* flags) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(flags, MOE_FLAG_WAIT_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completion counted on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 16-byte streaming load that does not allocate in L1 (host or device memory).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Two E2M1 codes (element 2i in the low nibble) -> two floats, exact.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+  __half2_raw r = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte), __NV_E2M1);
+  __half2 h = *reinterpret_cast<__half2*>(&r);
+  return __half22float2(h);
+}
+
+// Two E4M3 bytes (first in the low byte) -> two floats, exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  __half2_raw r =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+  __half2 h = *reinterpret_cast<__half2*>(&r);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits) {
+  return __uint_as_float(bits << 16);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace moe

@@ -1,0 +1,436 @@
+// Host side of the C ABI: handle lifetime, validation, per-step kernel
+// sequence, counters and traces.  All device memory is allocated at create
+// (fixed addresses; "GLM 5.3 Testing: HBM Expert Allocation", "What the slot
+// cache is": fixed addresses and shapes keep the step CUDA-graph safe), and a
+// step only enqueues kernels.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "internal.cuh"
+
+using namespace moe;
+
+struct moe_cache {
+  int L, E, S, H, I, k;
+  long long Bw, Bs;
+  moe_cache_opts_t opts;
+  int device, num_sms;
+  // device state, per layer blocks
+  uint8_t* slot_w = nullptr;   // [L][S][Bw]
+  uint8_t* slot_s = nullptr;   // [L][S][Bs]
+  float* gscale = nullptr;     // [L][E][3]
+  int32_t* map = nullptr;      // [L][E]
+  int32_t* owner = nullptr;    // [L][S]
+  uint32_t* stamp = nullptr;   // [L][S]
+  uint32_t* clock = nullptr;   // [L]
+  DevStats* stats = nullptr;   // [L]
+  moe_step_record_t* trace = nullptr;  // [L][cap]
+  uint32_t* trace_head = nullptr;      // [L]
+  // per-step workspace
+  Plan* plan = nullptr;
+  GemvWorkspace gemv{};
+  // host backing (device-visible addresses)
+  std::vector<const uint8_t*> host_w, host_s;
+  // optional per-kernel timing events (caller-owned)
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool timing = false;
+};
+
+namespace {
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <class T>
+cudaError_t dalloc(T** p, size_t count) {
+  return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T) + (count == 0 ? 16 : 0));
+}
+
+void free_all(moe_cache* h) {
+  cudaFree(h->slot_w);
+  cudaFree(h->slot_s);
+  cudaFree(h->gscale);
+  cudaFree(h->map);
+  cudaFree(h->owner);
+  cudaFree(h->stamp);
+  cudaFree(h->clock);
+  cudaFree(h->stats);
+  cudaFree(h->trace);
+  cudaFree(h->trace_head);
+  cudaFree(h->plan);
+  cudaFree(h->gemv.hbuf);
+  cudaFree(h->gemv.ypart);
+  cudaFree(h->gemv.tile_cnt);
+}
+
+// Resolve a pinned host pointer to the address kernels use; -1 if not pinned.
+int device_view(const void* p, const uint8_t** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NOT_PINNED;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return MOE_ERR_NOT_PINNED;
+  *out = static_cast<const uint8_t*>(a.devicePointer);
+  return MOE_OK;
+}
+
+int init_state(moe_cache* h) {
+  const size_t LE = (size_t)h->L * h->E, LS = (size_t)h->L * h->S;
+  std::vector<int32_t> map(LE, -1), owner(LS, -1);
+  if (h->opts.all_resident) {
+    for (int l = 0; l < h->L; ++l)
+      for (int e = 0; e < h->E; ++e) {
+        map[(size_t)l * h->E + e] = e;
+        owner[(size_t)l * h->S + e] = e;
+      }
+  }
+  cudaError_t e = cudaMemcpy(h->map, map.data(), LE * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->owner, owner.data(), LS * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(h->stamp, 0, LS * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->clock, 0, (size_t)h->L * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->stats, 0, (size_t)h->L * sizeof(DevStats));
+  if (e == cudaSuccess) e = cudaMemset(h->trace_head, 0, (size_t)h->L * 4);
+  if (e == cudaSuccess)
+    e = cudaMemset(h->gemv.tile_cnt, 0, sizeof(uint32_t) * (size_t)(h->H / gemv_down_tile_rows(h->H, h->I) + 1));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return cuda_err(e);
+}
+
+LayerDev layer_dev(moe_cache* h, int l) {
+  LayerDev d;
+  d.map = h->map + (size_t)l * h->E;
+  d.owner = h->owner + (size_t)l * h->S;
+  d.stamp = h->stamp + (size_t)l * h->S;
+  d.clock = h->clock + l;
+  d.slot_w = h->slot_w + (size_t)l * h->S * h->Bw;
+  d.slot_s = h->slot_s + (size_t)l * h->S * h->Bs;
+  d.host_w = h->host_w[l];
+  d.host_s = h->host_s[l];
+  d.gscale = h->gscale + (size_t)l * h->E * 3;
+  d.stats = h->stats + l;
+  d.trace_cap = (uint32_t)h->opts.trace_capacity;
+  d.trace = h->opts.trace_capacity ? h->trace + (size_t)l * h->opts.trace_capacity : nullptr;
+  d.trace_head = h->trace_head + l;
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_expert_bytes(int hidden, int inter, uint64_t* Bw, uint64_t* Bs) {
+  if (hidden <= 0 || inter <= 0 || !Bw || !Bs) return MOE_ERR_ARG;
+  const uint64_t n = 3ull * (uint64_t)hidden * (uint64_t)inter;
+  *Bw = n / 2;
+  *Bs = n / 16;
+  return MOE_OK;
+}
+
+int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int hidden, int inter,
+                     int top_k, const moe_host_layer_t* host_backing,
+                     const moe_cache_opts_t* opts) {
+  if (!out) return MOE_ERR_ARG;
+  *out = nullptr;
+  moe_cache_opts_t o{};
+  o.copy_backend = MOE_COPY_SM;
+  o.bypass_rows = MOE_MAX_CACHED_ROWS;
+  o.max_rows = MOE_MAX_CACHED_ROWS;
+  if (opts) {
+    o = *opts;
+    if (o.bypass_rows <= 0) o.bypass_rows = MOE_MAX_CACHED_ROWS;
+    if (o.max_rows <= 0) o.max_rows = MOE_MAX_CACHED_ROWS;
+  }
+  if (layers < 1 || experts < 1 || top_k < 1 || hidden < 1 || inter < 1 || !host_backing)
+    return MOE_ERR_ARG;
+  if (o.trace_capacity < 0 || o.copy_backend != MOE_COPY_SM) return MOE_ERR_ARG;
+  if (experts > MOE_MAX_EXPERTS || top_k > MOE_MAX_TOPK || top_k > experts ||
+      hidden % 128 || inter % 128 || hidden > MOE_MAX_DIM || inter > MOE_MAX_DIM ||
+      o.bypass_rows > MOE_MAX_CACHED_ROWS)
+    return MOE_ERR_UNSUPPORTED;
+  if (o.all_resident) slots = experts;
+  if (slots < top_k || slots > experts) return MOE_ERR_ARG;
+
+  moe_cache* h = new (std::nothrow) moe_cache();
+  if (!h) return MOE_ERR_OOM;
+  h->L = layers;
+  h->E = experts;
+  h->S = slots;
+  h->H = hidden;
+  h->I = inter;
+  h->k = top_k;
+  h->opts = o;
+  uint64_t bw, bs;
+  moe_expert_bytes(hidden, inter, &bw, &bs);
+  h->Bw = (long long)bw;
+  h->Bs = (long long)bs;
+  int rc = MOE_OK;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  h->host_w.resize(layers);
+  h->host_s.resize(layers);
+  std::vector<float> gs((size_t)layers * experts * 3);
+  for (int l = 0; l < layers; ++l) {
+    const moe_host_layer_t& hl = host_backing[l];
+    if (!hl.w || !hl.s || !hl.gscale || ((uintptr_t)hl.w & 15) || ((uintptr_t)hl.s & 15)) {
+      delete h;
+      return MOE_ERR_ARG;
+    }
+    if ((rc = device_view(hl.w, &h->host_w[l])) != MOE_OK ||
+        (rc = device_view(hl.s, &h->host_s[l])) != MOE_OK) {
+      delete h;
+      return rc;
+    }
+    std::memcpy(gs.data() + (size_t)l * experts * 3, hl.gscale, sizeof(float) * experts * 3);
+  }
+  const size_t LS = (size_t)layers * slots, LE = (size_t)layers * experts;
+  const int cap = o.trace_capacity;
+  bool ok = dalloc(&h->slot_w, LS * (size_t)h->Bw) == cudaSuccess &&
+            dalloc(&h->slot_s, LS * (size_t)h->Bs) == cudaSuccess &&
+            dalloc(&h->gscale, LE * 3) == cudaSuccess && dalloc(&h->map, LE) == cudaSuccess &&
+            dalloc(&h->owner, LS) == cudaSuccess && dalloc(&h->stamp, LS) == cudaSuccess &&
+            dalloc(&h->clock, (size_t)layers) == cudaSuccess &&
+            dalloc(&h->stats, (size_t)layers) == cudaSuccess &&
+            dalloc(&h->trace, (size_t)layers * (cap ? cap : 1)) == cudaSuccess &&
+            dalloc(&h->trace_head, (size_t)layers) == cudaSuccess &&
+            dalloc(&h->plan, 1) == cudaSuccess &&
+            dalloc(&h->gemv.hbuf, (size_t)MOE_MAX_PICKS * inter) == cudaSuccess &&
+            dalloc(&h->gemv.ypart, (size_t)MOE_MAX_TOPK * hidden) == cudaSuccess &&
+            dalloc(&h->gemv.tile_cnt, (size_t)(hidden / gemv_down_tile_rows(hidden, inter) + 1)) ==
+                cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_all(h);
+    delete h;
+    return MOE_ERR_OOM;
+  }
+  e = cudaMemcpy(h->gscale, gs.data(), gs.size() * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && o.all_resident) {
+    for (int l = 0; l < layers && e == cudaSuccess; ++l) {
+      e = cudaMemcpy(h->slot_w + (size_t)l * slots * h->Bw, host_backing[l].w,
+                     (size_t)experts * h->Bw, cudaMemcpyHostToDevice);
+      if (e == cudaSuccess)
+        e = cudaMemcpy(h->slot_s + (size_t)l * slots * h->Bs, host_backing[l].s,
+                       (size_t)experts * h->Bs, cudaMemcpyHostToDevice);
+    }
+  }
+  if (e != cudaSuccess || (rc = init_state(h)) != MOE_OK) {
+    free_all(h);
+    delete h;
+    return rc != MOE_OK ? rc : MOE_ERR_CUDA;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logits,
+                   const uint16_t* x, float* out, void* stream) {
+  if (!h || layer < 0 || layer >= h->L || rows < 1 || !router_logits || !x || !out)
+    return MOE_ERR_ARG;
+  if ((uintptr_t)x & 15) return MOE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows > h->opts.bypass_rows || rows > 1) return MOE_ERR_UNSUPPORTED;
+  const LayerDev L = layer_dev(h, layer);
+  // inside a capture an event record must be an external node to be replayed
+  auto mark = [&](int i) -> cudaError_t {
+    if (!h->timing) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecordWithFlags(
+        h->ev[i], st, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u);
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess)
+    e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
+                           h->opts.all_resident);
+  if (e == cudaSuccess) e = mark(1);
+  if (e == cudaSuccess && !h->opts.all_resident)
+    e = launch_miss_copy(st, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
+                         2 * h->num_sms);
+  if (e == cudaSuccess) e = mark(2);
+  uint32_t* flags = &(h->stats + layer)->flags;
+  if (e == cudaSuccess)
+    e = launch_gemv_gateup(st, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms);
+  if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess)
+    e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, out, flags, h->num_sms);
+  if (e == cudaSuccess) e = mark(4);
+  return cuda_err(e);
+}
+
+int moe_cache_stats(const moe_cache_t* h, int layer, moe_cache_stats_t* out) {
+  if (!h || !out || layer < -1 || layer >= h->L) return MOE_ERR_ARG;
+  std::vector<DevStats> ds(h->L);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(ds.data(), h->stats, sizeof(DevStats) * h->L, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  std::memset(out, 0, sizeof *out);
+  for (int l = 0; l < h->L; ++l) {
+    if (layer >= 0 && l != layer) continue;
+    out->steps += ds[l].steps;
+    out->picks += ds[l].picks;
+    out->hits += ds[l].hits;
+    out->misses += ds[l].misses;
+    out->evictions += ds[l].evictions;
+    out->bytes_copied += ds[l].bytes_copied;
+    out->bypass_calls += ds[l].bypass_calls;
+    out->error_flags |= ds[l].flags;
+  }
+  return MOE_OK;
+}
+
+int moe_cache_slot_map(const moe_cache_t* h, int layer, int32_t* expert_of_slot) {
+  if (!h || !expert_of_slot || layer < 0 || layer >= h->L) return MOE_ERR_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(expert_of_slot, h->owner + (size_t)layer * h->S, sizeof(int32_t) * h->S,
+                   cudaMemcpyDeviceToHost);
+  return cuda_err(e);
+}
+
+int moe_cache_slot_bytes(const moe_cache_t* h, int layer, int slot, void* w_dst, void* s_dst) {
+  if (!h || layer < 0 || layer >= h->L || slot < 0 || slot >= h->S) return MOE_ERR_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  const size_t ls = (size_t)layer * h->S + slot;
+  if (e == cudaSuccess && w_dst)
+    e = cudaMemcpy(w_dst, h->slot_w + ls * h->Bw, h->Bw, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && s_dst)
+    e = cudaMemcpy(s_dst, h->slot_s + ls * h->Bs, h->Bs, cudaMemcpyDeviceToHost);
+  return cuda_err(e);
+}
+
+int moe_cache_trace(const moe_cache_t* h, int layer, moe_step_record_t* recs, int max_recs,
+                    int* n_recs) {
+  if (!h || !recs || !n_recs || max_recs < 0 || layer < 0 || layer >= h->L) return MOE_ERR_ARG;
+  const int cap = h->opts.trace_capacity;
+  if (cap <= 0) return MOE_ERR_ARG;
+  uint32_t head = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(&head, h->trace_head + layer, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t n = head < (uint32_t)cap ? head : (uint32_t)cap;
+  if (n > (uint32_t)max_recs) n = (uint32_t)max_recs;
+  const moe_step_record_t* base = h->trace + (size_t)layer * cap;
+  for (uint32_t i = 0; i < n && e == cudaSuccess; ++i) {
+    const uint32_t idx = (head - n + i) % (uint32_t)cap;
+    e = cudaMemcpy(recs + i, base + idx, sizeof(moe_step_record_t), cudaMemcpyDeviceToHost);
+  }
+  *n_recs = (int)n;
+  return cuda_err(e);
+}
+
+int moe_cache_reset(moe_cache_t* h) {
+  if (!h) return MOE_ERR_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return init_state(h);
+}
+
+int moe_cache_destroy(moe_cache_t* h) {
+  if (!h) return MOE_OK;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return MOE_OK;
+}
+
+int moe_cache_set_timing_events(moe_cache_t* h, void* const* events) {
+  if (!h) return MOE_ERR_ARG;
+  if (!events) {
+    h->timing = false;
+    return MOE_OK;
+  }
+  for (int i = 0; i < 5; ++i) {
+    if (!events[i]) return MOE_ERR_ARG;
+    h->ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  h->timing = true;
+  return MOE_OK;
+}
+
+const char* moe_cache_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_NOT_PINNED: return "host backing is not pinned, device-mapped memory";
+    case MOE_ERR_OOM: return "out of memory";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_UNSUPPORTED: return "shape or row count outside the supported limits";
+    default: return "unknown error";
+  }
+}
+
+int moe_host_alloc(void** out, size_t bytes) {
+  if (!out || bytes == 0) return MOE_ERR_ARG;
+  *out = nullptr;
+  void* p = nullptr;
+  if (cudaHostAlloc(&p, bytes, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_OOM;
+  }
+  void* dp = nullptr;
+  if (cudaHostGetDevicePointer(&dp, p, 0) != cudaSuccess || dp != p) {
+    cudaGetLastError();
+    cudaFreeHost(p);
+    return MOE_ERR_NOT_PINNED;
+  }
+  *out = p;
+  return MOE_OK;
+}
+
+int moe_host_free(void* p) {
+  if (!p) return MOE_OK;
+  return cuda_err(cudaFreeHost(p));
+}
+
+int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int method, int iters,
+                        double* best_gbps) {
+  if (!host_src || !dev_dst || !best_gbps || bytes == 0 || (bytes & 15) || iters < 1 ||
+      ((uintptr_t)host_src & 15) || ((uintptr_t)dev_dst & 15) || (method != 0 && method != 1))
+    return MOE_ERR_ARG;
+  const uint8_t* src = nullptr;
+  int rc = device_view(host_src, &src);
+  if (rc != MOE_OK) return rc;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaStream_t st;
+  cudaEvent_t a, b;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  double best = 0.0;
+  cudaError_t e = cudaSuccess;
+  for (int it = 0; it < iters + 1 && e == cudaSuccess; ++it) {
+    cudaEventRecord(a, st);
+    if (method == 0)
+      e = launch_link_probe(st, src, dev_dst, bytes, 2 * sms);
+    else
+      e = cudaMemcpyAsync(dev_dst, host_src, bytes, cudaMemcpyHostToDevice, st);
+    cudaEventRecord(b, st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(b);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
+    if (e == cudaSuccess && it > 0 && ms > 0.f) {
+      const double g = (double)bytes / (ms * 1e-3) / 1e9;
+      if (g > best) best = g;
+    }
+  }
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  cudaStreamDestroy(st);
+  *best_gbps = best;
+  return cuda_err(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,211 @@
+/*
+ * moe_slot_cache — decode-time routed-MoE layer with an HBM expert slot cache
+ * (GB300 / sm_103a).  C ABI.
+ *
+ * The method (web page "GLM 5.3 Testing: HBM Expert Allocation", section
+ * "What the slot cache is"): every routed expert of every MoE layer lives in
+ * pinned host memory; each layer owns a fixed ring of S HBM slots.  Before the
+ * expert computation the router's top-k expert ids are mapped to slot ids on
+ * the device; a missing expert's weight row and scale row are copied into the
+ * least-recently-used slot, then the map is updated; the expert kernel reads
+ * the same bytes it would read if every expert were in HBM, only the index
+ * changes.  Fixed addresses and fixed shapes make a decode round replayable as
+ * a CUDA graph.  Steps with more than 16 rows (prefill) bypass the cache and
+ * read experts zero-copy from host memory, so no expert is ever unreachable.
+ *
+ * Conventions
+ *  - Every function returns MOE_OK (0) or a negative MOE_ERR_* code; nothing
+ *    throws across the ABI.  moe_cache_strerror() names a code.
+ *  - "host" pointers are CPU addresses, "device" pointers are CUDA device
+ *    addresses on the device that was current at moe_cache_create.
+ *  - A handle is used from one host thread at a time; calls are not
+ *    thread-safe.  All device work of a handle goes to the stream passed to
+ *    moe_cache_step, which must be the same stream (or a stream ordered after
+ *    it) for every step of the handle.
+ *  - Device-side anomalies (non-finite router logits, a device wait that gave
+ *    up) never trap: they set sticky bits in moe_cache_stats_t.error_flags and
+ *    the step still completes with defined (possibly meaningless) output.
+ */
+#ifndef MOE_SLOT_CACHE_H
+#define MOE_SLOT_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ----------------------------------------------------------------- codes */
+#define MOE_OK 0
+#define MOE_ERR_ARG (-1)         /* bad argument, shape or pointer */
+#define MOE_ERR_NOT_PINNED (-2)  /* host backing is not device-accessible pinned memory */
+#define MOE_ERR_OOM (-3)         /* device or pinned host allocation failed */
+#define MOE_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
+#define MOE_ERR_UNSUPPORTED (-5) /* shape outside the compiled limits below */
+
+/* sticky device flags (moe_cache_stats_t.error_flags) */
+#define MOE_FLAG_NONFINITE_LOGIT 0x1u /* a router logit was NaN or +-inf */
+#define MOE_FLAG_WAIT_TIMEOUT 0x2u    /* a kernel's bounded wait on its own copies gave up */
+
+/* limits */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 16
+#define MOE_MAX_CACHED_ROWS 16                       /* rows of one cached step */
+#define MOE_MAX_PICKS (MOE_MAX_CACHED_ROWS * MOE_MAX_TOPK)
+#define MOE_MAX_DIM 8192                             /* hidden and inter */
+
+/* copy backends (moe_cache_opts_t.copy_backend) */
+#define MOE_COPY_SM 0 /* SM kernel, 16-byte loads from pinned host memory; graph-capturable */
+
+/* --------------------------------------------------------------- types */
+
+typedef struct moe_cache moe_cache_t; /* opaque, library-owned */
+
+/* One layer's backing store, caller-owned (the library never frees it; it must
+ * outlive the handle).  Expert e's bytes:
+ *   w + e*Bw, Bw = 3*hidden*inter/2 bytes of E2M1 codes, two per byte, element
+ *     2i in the low nibble of byte i.  Rows in order: gate [inter][hidden/2],
+ *     up [inter][hidden/2], down [hidden][inter/2].
+ *   s + e*Bs, Bs = 3*hidden*inter/16 bytes of E4M3 block scales, one per 16
+ *     consecutive elements of a row, same row order: [rows][K/16].
+ *   gscale[3*e .. 3*e+2]: fp32 global scales (gate, up, down).
+ * The weight of row r, element i is e2m1(code) * e4m3(scale) * gscale.
+ * w and s must be pinned, mapped host memory (e.g. from moe_host_alloc or
+ * cudaHostAlloc with cudaHostAllocMapped), 16-byte aligned, of at least
+ * experts*Bw and experts*Bs bytes.  gscale is ordinary host memory, read once
+ * at create. */
+typedef struct {
+  const void* w;
+  const void* s;
+  const float* gscale;
+} moe_host_layer_t;
+
+typedef struct {
+  int copy_backend;   /* MOE_COPY_SM (default) */
+  int bypass_rows;    /* steps with more rows bypass the cache; default and max 16 */
+  int all_resident;   /* 1: every expert lives in HBM (S = experts, loaded at create);
+                         same kernels, used to check that caching changes no output bit */
+  int trace_capacity; /* per-layer ring of moe_step_record_t for cached steps (0 = off) */
+  int max_rows;       /* largest rows of any step (sizes the bypass workspace); default 16 */
+} moe_cache_opts_t;
+
+typedef struct {
+  uint64_t steps;        /* moe_cache_step calls on the layer(s) */
+  uint64_t picks;        /* routed picks of cached steps (rows * top_k) */
+  uint64_t hits;         /* picks whose expert was resident at step start */
+  uint64_t misses;       /* unique missing experts (one copy each) */
+  uint64_t evictions;    /* misses that replaced a resident expert */
+  uint64_t bytes_copied; /* host->HBM bytes moved by miss copies */
+  uint64_t bypass_calls; /* steps that bypassed the cache */
+  uint32_t error_flags;  /* MOE_FLAG_* (sticky) */
+  uint32_t reserved;
+} moe_cache_stats_t;
+
+/* One cached layer-step, for checking the cache trace against a reference. */
+typedef struct {
+  uint32_t clock;  /* layer's LRU clock after the step (advances on cached steps only) */
+  int32_t rows;
+  int32_t n_union; /* distinct experts over all rows */
+  int32_t n_miss;
+  int32_t bypass;  /* 1: union larger than S, step read host memory, cache untouched */
+  int32_t ids[MOE_MAX_PICKS];       /* rank order per row, row-major [rows][top_k] */
+  float weights[MOE_MAX_PICKS];
+  int32_t slot[MOE_MAX_PICKS];      /* slot read by each pick (-1 on bypass) */
+  int32_t hit[MOE_MAX_PICKS];       /* resident at step start */
+  int32_t miss_expert[MOE_MAX_PICKS]; /* ascending expert id */
+  int32_t miss_slot[MOE_MAX_PICKS];
+  int32_t miss_evicted[MOE_MAX_PICKS]; /* previous owner, -1 if the slot was empty */
+} moe_step_record_t;
+
+/* --------------------------------------------------------------- cache */
+
+/* Build a slot cache of `layers` MoE layers, each with `experts` routed experts
+ * of shape (hidden, inter), top_k routing and `slots` HBM slots.  Allocates all
+ * device state (slots, maps, stamps, counters, workspaces) once; addresses never
+ * change afterwards.  Caches start empty.  host_backing has `layers` entries.
+ * opts may be NULL (defaults).  Limits: experts <= MOE_MAX_EXPERTS,
+ * top_k <= min(experts, MOE_MAX_TOPK), top_k <= slots <= experts,
+ * hidden and inter multiples of 128 and <= MOE_MAX_DIM.
+ * Errors: MOE_ERR_ARG, MOE_ERR_NOT_PINNED, MOE_ERR_OOM, MOE_ERR_CUDA,
+ * MOE_ERR_UNSUPPORTED.  On error *out is NULL and nothing leaks. */
+int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int hidden,
+                     int inter, int top_k, const moe_host_layer_t* host_backing,
+                     const moe_cache_opts_t* opts);
+
+/* One layer-step for `rows` tokens:
+ *   router_logits: device fp32 [rows][experts]
+ *   x:             device bf16 bits [rows][hidden]
+ *   out:           device fp32 [rows][hidden] (written, not accumulated)
+ *   stream:        cudaStream_t (NULL = legacy default stream)
+ * rows <= bypass_rows: route (top-k by logit, ties to the lower id; weights =
+ * softmax of the k selected logits), map ids to slots, copy misses host->slot,
+ * run gate/up -> SwiGLU -> down on slot-resident bytes and combine with the
+ * router weights.  rows > bypass_rows: same result, experts read from host
+ * memory, cache untouched.  Enqueues kernels only (no host sync, no
+ * allocation); capturable into a CUDA graph.  Buffers must keep their
+ * addresses across graph replays.  Errors: MOE_ERR_ARG, MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_CUDA (launch failure). */
+int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logits,
+                   const uint16_t* x, float* out, void* stream);
+
+/* Counters of one layer (layer >= 0) or summed over all layers (layer == -1;
+ * error_flags OR-ed).  Waits for all device work (device synchronize). */
+int moe_cache_stats(const moe_cache_t* h, int layer, moe_cache_stats_t* out);
+
+/* expert_of_slot: host int32 [slots]; -1 = empty.  Device synchronize. */
+int moe_cache_slot_map(const moe_cache_t* h, int layer, int32_t* expert_of_slot);
+
+/* Copy one slot's resident bytes to host memory (w_dst: Bw bytes, s_dst: Bs
+ * bytes; either may be NULL).  Device synchronize. */
+int moe_cache_slot_bytes(const moe_cache_t* h, int layer, int slot, void* w_dst, void* s_dst);
+
+/* Copy up to max_recs of the layer's most recent step records, oldest first,
+ * into recs (host); *n_recs receives the count.  Requires trace_capacity > 0.
+ * Device synchronize. */
+int moe_cache_trace(const moe_cache_t* h, int layer, moe_step_record_t* recs, int max_recs,
+                    int* n_recs);
+
+/* Empty every ring, zero counters, flags and traces (all_resident: reload
+ * identity map).  Device synchronize. */
+int moe_cache_reset(moe_cache_t* h);
+
+/* Free everything the handle owns (not the host backing).  NULL is a no-op. */
+int moe_cache_destroy(moe_cache_t* h);
+
+const char* moe_cache_strerror(int code);
+
+/* Byte sizes of one expert's codes (Bw) and scales (Bs) for (hidden, inter). */
+int moe_expert_bytes(int hidden, int inter, uint64_t* Bw, uint64_t* Bs);
+
+/* ---------------------------------------------------------- host memory */
+
+/* Exact-size pinned host allocation, portable and mapped, with its device view
+ * checked to be the same address (UVA).  ("GLM 5.3 Testing: HBM Expert
+ * Allocation", "Five launches, four failures": allocators that round pinned
+ * blocks up to powers of two wasted a third of host memory; allocate exactly.)
+ * Errors: MOE_ERR_ARG, MOE_ERR_OOM, MOE_ERR_NOT_PINNED (no UVA view). */
+int moe_host_alloc(void** out, size_t bytes);
+int moe_host_free(void* p);
+
+/* --------------------------------------------------------- measurement */
+
+/* Host->HBM read bandwidth over the host link, measured with the same SM copy
+ * the miss path uses (method 0) or cudaMemcpyAsync (method 1): copies `bytes`
+ * from pinned host_src to device dev_dst `iters` times and returns the best
+ * GB/s (1e9 bytes/s).  Synchronous.  Both pointers 16-byte aligned. */
+int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int method,
+                        int iters, double* best_gbps);
+
+/* Per-kernel timing hook: events points at 5 cudaEvent_t (created by the
+ * caller).  While set, every moe_cache_step records events[0] before its first
+ * kernel and events[1..4] after route/remap, miss copy, gate/up and
+ * down/combine, on the step's stream (also inside a CUDA-graph capture, where
+ * they become event-record nodes).  NULL stops recording.  The library does
+ * not own the events. */
+int moe_cache_set_timing_events(moe_cache_t* h, void* const* events);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_SLOT_CACHE_H */
