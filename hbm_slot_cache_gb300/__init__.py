@@ -19,7 +19,7 @@ __all__ = ["HostBank", "MoeCache", "MoeError", "build"]
 
 
 def build(**kw) -> str:
-    from .build import build as _b
+    from .builder import build as _b
     return _b(**kw)
 
 

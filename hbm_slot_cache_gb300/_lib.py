@@ -31,7 +31,7 @@ MOE_COPY_SM = 0
 EXPORTS = ("moe_cache_create", "moe_cache_step", "moe_cache_stats", "moe_cache_slot_map",
            "moe_cache_slot_bytes", "moe_cache_trace", "moe_cache_reset", "moe_cache_destroy",
            "moe_cache_strerror", "moe_expert_bytes", "moe_host_alloc", "moe_host_free",
-           "moe_probe_host_link", "moe_cache_set_timing_events")
+           "moe_probe_host_link", "moe_cache_set_timing_events", "moe_expert_pass_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -79,7 +79,7 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(_SO):
-            raise RuntimeError(f"{_SO} is missing: build it with hbm_slot_cache_gb300.build.build() "
+            raise RuntimeError(f"{_SO} is missing: build it with hbm_slot_cache_gb300.build() "
                                "(needs nvcc); there is no fallback implementation")
         L = ctypes.CDLL(_SO)
         P, I, U64P = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)
@@ -99,6 +99,7 @@ def lib() -> ctypes.CDLL:
         L.moe_probe_host_link.argtypes = [P, P, ctypes.c_size_t, I, I,
                                           ctypes.POINTER(ctypes.c_double)]
         L.moe_cache_set_timing_events.argtypes = [P, P]
+        L.moe_expert_pass_noalloc.argtypes = [I, I, I, P, P, P, P, P, P, P]
         for name in EXPORTS:
             if name != "moe_cache_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -187,6 +188,21 @@ def moe_cache_set_timing_events(h: int, events) -> None:
     arr = (ctypes.c_void_p * 5)(*[int(e) for e in events])
     _check(lib().moe_cache_set_timing_events(h, ctypes.cast(arr, ctypes.c_void_p)),
            "moe_cache_set_timing_events")
+
+
+def moe_expert_pass_noalloc(k: int, hidden: int, inter: int, expert_w, expert_s, gscale,
+                            weights, x: int, out: int, stream: int = 0) -> None:
+    """One-row expert pass without any device allocation (see the header).
+
+    expert_w / expert_s: k device addresses; gscale float32 [k, 3]; weights float32 [k]."""
+    wa = (ctypes.c_void_p * k)(*[int(p) for p in expert_w])
+    sa = (ctypes.c_void_p * k)(*[int(p) for p in expert_s])
+    g = np.ascontiguousarray(gscale, np.float32).reshape(k, 3)
+    w = np.ascontiguousarray(weights, np.float32).reshape(k)
+    _check(lib().moe_expert_pass_noalloc(k, hidden, inter, ctypes.cast(wa, ctypes.c_void_p),
+                                         ctypes.cast(sa, ctypes.c_void_p), g.ctypes.data,
+                                         w.ctypes.data, x, out, stream),
+           "moe_expert_pass_noalloc")
 
 
 def moe_host_alloc(nbytes: int) -> int:

@@ -205,6 +205,31 @@ int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int m
  * not own the events. */
 int moe_cache_set_timing_events(moe_cache_t* h, void* const* events);
 
+/* ------------------------------------------------------ no-allocation pass */
+
+/* The one-row expert pass (gate/up -> SwiGLU -> down -> combine with the
+ * router weights) over k experts already resident in device memory, for
+ * callers that cannot allocate device memory: e.g. a serving engine that has
+ * reserved all free HBM for its own pools and owns every further byte, or a
+ * decode loop that cannot afford an allocation's implicit synchronisation.
+ * The pages have no counterpart: it is the library's own addition.
+ *   expert_w[j], expert_s[j]: host arrays of k device addresses of expert j's
+ *     codes (Bw bytes) and scales (Bs bytes), storage layout as in
+ *     moe_host_layer_t, 16-byte aligned;
+ *   gscale: host [k][3]; weights: host [k] (router weights, rank order);
+ *   x: device bf16 [hidden]; out: device fp32 [hidden] (written).
+ * Allocates nothing: its scratch (about 1.1 MB: plan, h, per-expert partial
+ * outputs, tile tickets) is one file-scope device array, fixed in size for
+ * k <= MOE_MAX_TOPK and hidden, inter <= MOE_MAX_DIM, held by every GPU that
+ * loads the library until the process exits; larger sizes return
+ * MOE_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
+ * address (make it before any stream capture).  All calls share the array:
+ * calls whose work overlaps on the GPU race and must be ordered by the caller.
+ * Errors: MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+int moe_expert_pass_noalloc(int k, int hidden, int inter, const void* const* expert_w,
+                            const void* const* expert_s, const float* gscale,
+                            const float* weights, const uint16_t* x, float* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
