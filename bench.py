@@ -271,10 +271,12 @@ def run_ours(args) -> None:
     sampler = ClockSampler(uuid)
     time.sleep(0.15)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mid = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
         if g_main is not None:
             g_main.replay()
+        mid.record(stream)
         g_ev.replay()
         end.record(stream)
     stream.synchronize()
@@ -300,6 +302,10 @@ def run_ours(args) -> None:
         for i, n in enumerate(names):
             per[n] += row[i].elapsed_time(row[i + 1])
     per_launch_ms = {n: per[n] / G for n in names}
+    gap_ms = sum(evs[t][4].elapsed_time(evs[t + 1][0]) for t in range(G - 1)) / max(G - 1, 1)
+    timing_split = {"ms_per_step_plain_graph": start.elapsed_time(mid) / (K - G) if K > G else None,
+                    "ms_per_step_event_graph": mid.elapsed_time(end) / G,
+                    "ms_between_steps": gap_ms}
 
     # host-link bandwidth probed in the same session
     from hbm_slot_cache_gb300 import HostBank, moe_probe_host_link
@@ -401,7 +407,7 @@ def run_ours(args) -> None:
                               "link_probe_sm_gbs": link_sm, "link_probe_memcpy_gbs": link_ce,
                               "misses_per_step": miss_per_step,
                               "hit_rate": hits / picks if picks else None},
-            "roofline": roofline, "kernels": kern,
+            "roofline": roofline, "kernels": kern, "timing_split": timing_split,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": E * 4 + H * 2,
                     "d2h_bytes_per_step": H * 4, "steps": Ke},

@@ -5,47 +5,86 @@
 // expert kernel reads the same bytes as in the all-HBM case, only the index
 // changes; "A correction first": 0.041 ms for the all-HBM layer under graphs.)
 //
-// Design (HBM-bound GEMV, ~3.6 flop/byte):
-//  - persistent grid, one CTA per SM; work is cut into units of whole weight
-//    rows and handed out round-robin;
-//  - each unit's code rows and scale rows are contiguous in the slot and are
-//    staged into shared memory by 1-D TMA bulk copies (cp.async.bulk) on an
-//    mbarrier, NS stages deep (~220 KB in flight per SM);
-//  - a thread owns one 16-element block (8 code bytes + 1 scale byte) of every
-//    row it touches and keeps the matching 16 activations in registers, so
-//    shared memory carries each code byte once; E2M1 and E4M3 decode with the
-//    hardware conversions (exact), products accumulate in fp32;
-//  - row sums reduce across the row's threads with a reduce-scatter butterfly
-//    of warp shuffles, then across warps in shared memory, in a fixed order.
-// Gate/up unit: R row pairs of one pick (gate rows r.., up rows I+r..), whose
-// epilogue writes h = silu(gate) * up.  Down unit: R2 output rows of one pick,
-// writing y_j = W2_j h_j; the last of a row tile's k units (atomic ticket)
-// combines out = sum_j w_j y_j in rank order.  Every order is fixed, so a
-// cached step and an all-resident step give the same bits.
+// Both kernels are HBM-bound GEMVs (~3.6 flop per weight byte) whose limit on
+// CUDA cores is the instruction issue rate of FP4 decode, so the inner loops
+// are built around the cheapest exact decode: the hardware E2M1x2 -> f16x2
+// conversion, then products into fp32 accumulators.
+//
+// gate/up + SwiGLU: persistent grid, 2 CTAs per SM.  A unit is R row pairs of
+// one pick (gate rows r.., up rows I+r..), contiguous in the slot; its code
+// and scale rows are staged into shared memory by 1-D TMA bulk copies
+// (cp.async.bulk on an mbarrier), NS units in flight per CTA.  A thread owns a
+// 16-element block of every row it touches and keeps the matching 16
+// activations in registers as f16 (the row is prescaled by a power of two so
+// no activation overflows f16; bf16 -> f16 is then exact apart from f16
+// subnormals), so each product is one mixed-precision fma.rn.f32.f16.  Row
+// sums: reduce-scatter butterfly of shuffles, then a fixed-order sum across
+// warps.  The epilogue writes h = silu(gate) * up in fp32.
+//
+// down + combine: persistent grid, 1 CTA per SM.  A thread owns one
+// (pick j, 32-element block of I) pair and keeps gscale_j * w_j * h_j for it in
+// registers for the whole kernel; a unit is R2 output rows of all k picks, so
+// out[row] = sum over all threads of their partial dot products -- the router
+// weights are applied before the down matvec, the combine is the fixed-order
+// reduction, and nothing else is written.  Every order is fixed, so a cached
+// step and an all-resident step give the same bits.
 #include "internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kMaxThreads = 512;
-constexpr int kGateUpRows = 8;   // row pairs per gate/up unit
-constexpr int kDownRows = 32;    // output rows per down unit
-constexpr int kSmemBudget = 227 * 1024;
+constexpr int kGateUpRows = 4;     // row pairs per gate/up unit
+constexpr int kGateUpThreads = 512;
+constexpr int kDownRows = 4;       // output rows per down unit
+constexpr int kDownThreads = 512;
+constexpr int kSmemPerSm = 227 * 1024;
 
-// 16 E2M1 codes (8 bytes, element 2i in the low nibble) times 16 fp32 values.
-__device__ __forceinline__ float dot16(uint2 codes, const float* __restrict__ v) {
+// Four E2M1 pairs of one 32-bit word -> four f16x2 (element 2i in the low half).
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t& h0, uint32_t& h1,
+                                                uint32_t& h2, uint32_t& h3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+}
+
+// s0 += lo(c) * lo(x), s1 += hi(c) * hi(x): f16 operands, fp32 fma.
+__device__ __forceinline__ void fma_f16x2_f32(uint32_t c, uint32_t x, float& s0, float& s1) {
+  asm("{\n\t.reg .b16 cl, ch, xl, xh;\n\t"
+      "mov.b32 {cl, ch}, %2;\n\t"
+      "mov.b32 {xl, xh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, cl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %1, ch, xh, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(c), "r"(x));
+}
+
+// 16 codes (8 bytes) times 16 f16 activations (8 f16x2 words).
+__device__ __forceinline__ float dot16_f16(uint2 codes, const uint32_t* __restrict__ xh) {
+  uint32_t h[8];
+  e2m1x8_to_f16x8(codes.x, h[0], h[1], h[2], h[3]);
+  e2m1x8_to_f16x8(codes.y, h[4], h[5], h[6], h[7]);
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const float2 f = e2m1x2_to_float2((codes.x >> (8 * b)) & 0xFFu);
+  for (int b = 0; b < 8; ++b) fma_f16x2_f32(h[b], xh[b], s0, s1);
+  return s0 + s1;
+}
+
+// 16 codes (8 bytes) times 16 fp32 values.
+__device__ __forceinline__ float dot16_f32(uint32_t lo, uint32_t hi, const float* __restrict__ v) {
+  uint32_t h[8];
+  e2m1x8_to_f16x8(lo, h[0], h[1], h[2], h[3]);
+  e2m1x8_to_f16x8(hi, h[4], h[5], h[6], h[7]);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
     s0 = fmaf(f.x, v[2 * b], s0);
     s1 = fmaf(f.y, v[2 * b + 1], s1);
-  }
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const float2 f = e2m1x2_to_float2((codes.y >> (8 * b)) & 0xFFu);
-    s0 = fmaf(f.x, v[8 + 2 * b], s0);
-    s1 = fmaf(f.y, v[8 + 2 * b + 1], s1);
   }
   return s0 + s1;
 }
@@ -54,8 +93,8 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
   return e4m3x2_to_float2(byte & 0xFFu).x;
 }
 
-// Reduce-scatter V values across the 32 lanes: afterwards lane l holds in a[0]
-// the warp sum of value (l >> (5 - log2 V)) & (V - 1).
+// Reduce-scatter V values across the 32 lanes: afterwards lane l holds the
+// warp sum of value (l >> (5 - log2 V)) & (V - 1).
 template <int V>
 __device__ __forceinline__ float warp_reduce_scatter(float (&a)[V], int lane) {
 #pragma unroll
@@ -78,10 +117,10 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&a)[V], int lane) {
   return a[0];
 }
 
-constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 
-// Writes the per-thread partials `a` of row group g to `red` so that
-// sum_partial(g, i) can add them in a fixed order.
+// Partials of row group g (C threads) to shared memory; sum_partial adds them
+// in a fixed order.
 template <int V, bool WARP_RED>
 __device__ __forceinline__ void stash_partials(float (&a)[V], float* red, int g, int c, int C,
                                                int lane) {
@@ -128,15 +167,20 @@ __device__ void drain_fills(const Stages& S, int i, int NS, int my_units, uint32
     if (!mbar_wait_bounded(&S.full[ii % NS], (uint32_t)((ii / NS) & 1), flags)) return;
 }
 
+__device__ __forceinline__ int units_of_block(int nunits) {
+  return nunits > (int)blockIdx.x ? (nunits - 1 - (int)blockIdx.x) / gridDim.x + 1 : 0;
+}
+
 // ----------------------------------------------------------- gate / up
 
 template <int RPT, bool WARP_RED>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+__global__ void __launch_bounds__(kGateUpThreads, 2)
 gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
                    float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags) {
   constexpr int V = 2 * RPT;
   constexpr int R = kGateUpRows;
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_xmax[kGateUpThreads / 32];
   const int C = H / 16;
   const int tid = threadIdx.x, lane = tid & 31;
   const int g = tid / C, c = tid - g * C;
@@ -146,7 +190,7 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
 
   const int upp = I / R;  // units per pick
   const int nunits = plan->npicks * upp;
-  const int my_units = nunits > (int)blockIdx.x ? (nunits - 1 - (int)blockIdx.x) / gridDim.x + 1 : 0;
+  const int my_units = units_of_block(nunits);
 
   auto issue = [&](int unit, int stage) {
     const int j = unit / upp, rb = unit - j * upp;
@@ -169,17 +213,35 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   if (tid == 0)
     for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
 
-  // this thread's 16 activations
-  float xv[16];
+  // this thread's 16 activations, as f16 after a power-of-two prescale of the
+  // whole row that keeps max |x| below 2^15
+  float xf[16];
+  float amax = 0.f;
   {
     const uint4* xp = reinterpret_cast<const uint4*>(x + c * 16);
     const uint4 a = __ldg(xp), b = __ldg(xp + 1);
     const uint32_t wds[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      xv[2 * i] = bf16_bits_to_float(wds[i] & 0xFFFFu);
-      xv[2 * i + 1] = bf16_bits_to_float(wds[i] >> 16);
+      xf[2 * i] = bf16_bits_to_float(wds[i] & 0xFFFFu);
+      xf[2 * i + 1] = bf16_bits_to_float(wds[i] >> 16);
+      amax = fmaxf(amax, fmaxf(fabsf(xf[2 * i]), fabsf(xf[2 * i + 1])));
     }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if (lane == 0) s_xmax[tid >> 5] = amax;
+  __syncthreads();
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, s_xmax[w]);
+  int e2 = 0;
+  frexpf(amax, &e2);                    // amax < 2^e2
+  const int xshift = e2 > 15 ? e2 - 15 : 0;
+  const float xdown = ldexpf(1.0f, -xshift), xup = ldexpf(1.0f, xshift);
+  uint32_t xh[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __half2 p = __floats2half2_rn(xf[2 * i] * xdown, xf[2 * i + 1] * xdown);
+    xh[i] = *reinterpret_cast<const uint32_t*>(&p);
   }
 
   for (int i = 0; i < my_units; ++i) {
@@ -200,8 +262,8 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
       const uint2 cu = *reinterpret_cast<const uint2*>(st + cb + r * (H / 2) + c * 8);
       const uint32_t sg = st[2 * cb + r * (H / 16) + c];
       const uint32_t su = st[2 * cb + sb + r * (H / 16) + c];
-      a[q] = dot16(cg, xv) * e4m3_to_float(sg);
-      a[RPT + q] = dot16(cu, xv) * e4m3_to_float(su);
+      a[q] = dot16_f16(cg, xh) * e4m3_to_float(sg);
+      a[RPT + q] = dot16_f16(cu, xh) * e4m3_to_float(su);
     }
     stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
     __syncthreads();
@@ -209,8 +271,8 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     if (tid < RL * RPT) {
       const int gg = tid / RPT, q = tid - gg * RPT;
       const int j = unit / upp, rb = unit - j * upp;
-      const float gate = plan->gs[j][0] * sum_partial<V, WARP_RED>(S.red, gg, q, C);
-      const float up = plan->gs[j][1] * sum_partial<V, WARP_RED>(S.red, gg, RPT + q, C);
+      const float gate = plan->gs[j][0] * xup * sum_partial<V, WARP_RED>(S.red, gg, q, C);
+      const float up = plan->gs[j][1] * xup * sum_partial<V, WARP_RED>(S.red, gg, RPT + q, C);
       const float h = gate / (1.0f + expf(-gate)) * up;
       hbuf[(size_t)j * I + rb * R + gg + q * RL] = h;
     }
@@ -219,35 +281,33 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
 
 // ---------------------------------------------------------- down + combine
 
-template <int RPT, bool WARP_RED>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+template <int R2>
+__global__ void __launch_bounds__(kDownThreads, 1)
 gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
-                 float* __restrict__ ypart, uint32_t* __restrict__ tile_cnt,
-                 float* __restrict__ out, int H, int I, int RL, int NS, uint32_t* flags) {
-  constexpr int V = RPT;
-  constexpr int R = kDownRows;
+                 float* __restrict__ out, int H, int I, int NS, uint32_t* flags) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_last;
-  const int C = I / 16;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int g = tid / C, c = tid - g * C;
-  const int cb = R * I / 2, sb = R * I / 16;
-  const int stage_bytes = cb + sb;
+  const int C = I / 32;
+  const int k = plan->npicks;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool active = tid < k * C;
+  const int j = active ? tid / C : 0, c = active ? tid - j * C : 0;
+  const int cb = R2 * I / 2, sb = R2 * I / 16;  // per pick
+  const int stage_bytes = k * (cb + sb);
   Stages S = carve(smem, NS, stage_bytes);
 
-  const int k = plan->npicks;
-  const int nunits = (H / R) * k;
-  const int my_units = nunits > (int)blockIdx.x ? (nunits - 1 - (int)blockIdx.x) / gridDim.x + 1 : 0;
+  const int nunits = H / R2;
+  const int my_units = units_of_block(nunits);
   const size_t w2_codes = (size_t)I * H;        // 2I rows of H/2 bytes precede W2
   const size_t w2_scales = (size_t)I * H / 8;   // 2I rows of H/16 bytes
 
   auto issue = [&](int unit, int stage) {
-    const int tile = unit / k, j = unit - tile * k;
     uint8_t* dst = S.base + (size_t)stage * stage_bytes;
     mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
-    bulk_g2s(dst, plan->wptr[j] + w2_codes + (size_t)tile * R * (I / 2), cb, &S.full[stage]);
-    bulk_g2s(dst + cb, plan->sptr[j] + w2_scales + (size_t)tile * R * (I / 16), sb,
-             &S.full[stage]);
+    for (int jj = 0; jj < k; ++jj) {
+      bulk_g2s(dst + jj * cb, plan->wptr[jj] + w2_codes + (size_t)unit * cb, cb, &S.full[stage]);
+      bulk_g2s(dst + k * cb + jj * sb, plan->sptr[jj] + w2_scales + (size_t)unit * sb, sb,
+               &S.full[stage]);
+    }
   };
 
   if (tid == 0) {
@@ -259,23 +319,24 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
   if (tid == 0)
     for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
 
+  // gscale_j * w_j * h_j for this thread's 32 inputs, for the whole kernel
+  float hv[32];
+  {
+    const float f = active ? plan->gs[j][2] * plan->wts[j] : 0.f;
+    const float4* hp = reinterpret_cast<const float4*>(hbuf + (size_t)j * I + c * 32);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = active ? __ldg(hp + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      hv[4 * q] = f * v.x;
+      hv[4 * q + 1] = f * v.y;
+      hv[4 * q + 2] = f * v.z;
+      hv[4 * q + 3] = f * v.w;
+    }
+  }
+
   for (int i = 0; i < my_units; ++i) {
     const int unit = blockIdx.x + i * gridDim.x;
-    const int tile = unit / k, j = unit - tile * k;
     const int stage = i % NS;
-    // h_j for this thread's 16 inputs (written by the gate/up kernel)
-    float hv[16];
-    {
-      const float4* hp = reinterpret_cast<const float4*>(hbuf + (size_t)j * I + c * 16);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = __ldg(hp + q);
-        hv[4 * q] = v.x;
-        hv[4 * q + 1] = v.y;
-        hv[4 * q + 2] = v.z;
-        hv[4 * q + 3] = v.w;
-      }
-    }
     if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
     __syncthreads();
     if (*S.abort_flag) {
@@ -283,45 +344,32 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
       return;
     }
     const uint8_t* st = S.base + (size_t)stage * stage_bytes;
-    float a[V];
+    float a[R2];
 #pragma unroll
-    for (int q = 0; q < RPT; ++q) {
-      const int r = g + q * RL;
-      const uint2 cw = *reinterpret_cast<const uint2*>(st + r * (I / 2) + c * 8);
-      const uint32_t sw = st[cb + r * (I / 16) + c];
-      a[q] = dot16(cw, hv) * e4m3_to_float(sw);
+    for (int r = 0; r < R2; ++r) {
+      a[r] = 0.f;
+      if (active) {
+        const uint4 cw = *reinterpret_cast<const uint4*>(st + j * cb + r * (I / 2) + c * 16);
+        const uint32_t s2 = *reinterpret_cast<const uint16_t*>(st + k * cb + j * sb +
+                                                               r * (I / 16) + c * 2);
+        const float2 sc = e4m3x2_to_float2(s2);
+        a[r] = dot16_f32(cw.x, cw.y, hv) * sc.x + dot16_f32(cw.z, cw.w, hv + 16) * sc.y;
+      }
     }
-    stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
+    const float s = warp_reduce_scatter<R2>(a, lane);
+    constexpr int sh = 5 - ilog2(R2);
+    if ((lane & ((1 << sh) - 1)) == 0) S.red[warp * R2 + (lane >> sh)] = s;
     __syncthreads();
     if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
-    if (tid < RL * RPT) {
-      const int gg = tid / RPT, q = tid - gg * RPT;
-      const int row = tile * R + gg + q * RL;
-      ypart[(size_t)j * H + row] = plan->gs[j][2] * sum_partial<V, WARP_RED>(S.red, gg, q, C);
-      __threadfence();
-    }
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&tile_cnt[tile], 1u) == (uint32_t)(k - 1);
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      for (int t = tid; t < R; t += blockDim.x) {
-        const int row = tile * R + t;
-        float acc = 0.f;
-        for (int jj = 0; jj < k; ++jj) acc = fmaf(plan->wts[jj], __ldcg(ypart + (size_t)jj * H + row), acc);
-        out[row] = acc;
-      }
-      if (tid == 0) tile_cnt[tile] = 0;
+    if (tid < R2) {
+      float acc = 0.f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) acc += S.red[w * R2 + tid];
+      out[unit * R2 + tid] = acc;
     }
   }
 }
 
 // ------------------------------------------------------------- dispatch
-
-struct Shape {
-  int C, RL, RPT, NT, NS, smem;
-  bool warp_red;
-};
 
 int pow2_floor(int v) {
   int p = 1;
@@ -329,29 +377,35 @@ int pow2_floor(int v) {
   return p;
 }
 
-// K = inner dimension, R = rows (or row pairs) per unit, vals = partials per row
-Shape plan_shape(int K, int R, int rows_per_unit_factor, int stage_bytes) {
-  Shape s;
-  s.C = K / 16;
-  int lim = 256 / s.C;
+struct GateUpShape {
+  int C, RL, RPT, NT, NS, smem;
+  bool warp_red;
+};
+
+GateUpShape gateup_shape(int H) {
+  GateUpShape s;
+  const int R = kGateUpRows;
+  s.C = H / 16;
+  int lim = kGateUpThreads / s.C;
   if (lim < 1) lim = 1;
   if (lim > R) lim = R;
   s.RL = pow2_floor(lim);
   s.RPT = R / s.RL;
   s.NT = s.C * s.RL;
   s.warp_red = (s.C % 32) == 0;
-  const int V = rows_per_unit_factor * s.RPT;
+  const int V = 2 * s.RPT;
   const int red_floats = s.warp_red ? s.RL * (s.C / 32) * V : s.NT * V;
-  const int fixed = 16 + 8 + red_floats * 4 + 128;
-  int ns = (kSmemBudget - fixed) / stage_bytes;
-  if (ns > 4) ns = 4;
+  const int stage = 2 * R * H / 2 + 2 * R * H / 16;
+  const int per_cta = kSmemPerSm / 2 - 1024;  // two CTAs per SM
+  int ns = (per_cta - 16 - red_floats * 4) / stage;
+  if (ns > 6) ns = 6;
   s.NS = ns;
-  s.smem = ns * stage_bytes + 8 * ns + 8 + red_floats * 4;
+  s.smem = ns * stage + 8 * ns + 8 + red_floats * 4;
   return s;
 }
 
 template <int RPT, bool WR>
-cudaError_t run_gateup(cudaStream_t st, int grid, const Shape& s, const Plan* plan,
+cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
                        const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags) {
   auto kern = gemv_gateup_kernel<RPT, WR>;
   static int smem_set = 0;  // raise the opt-in limit once per size (not a stream operation)
@@ -364,22 +418,12 @@ cudaError_t run_gateup(cudaStream_t st, int grid, const Shape& s, const Plan* pl
   return cudaGetLastError();
 }
 
-template <int RPT, bool WR>
-cudaError_t run_down(cudaStream_t st, int grid, const Shape& s, const Plan* plan,
-                     const float* hbuf, float* ypart, uint32_t* cnt, float* out, int H, int I,
-                     uint32_t* flags) {
-  auto kern = gemv_down_kernel<RPT, WR>;
-  static int smem_set = 0;
-  if (s.smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
-    if (e != cudaSuccess) return e;
-    smem_set = s.smem;
-  }
-  kern<<<grid, s.NT, s.smem, st>>>(plan, hbuf, ypart, cnt, out, H, I, s.RL, s.NS, flags);
-  return cudaGetLastError();
-}
-
 }  // namespace
+
+bool gemv_supported(int H, int I, int k) {
+  return H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM &&
+         k * (I / 32) <= kDownThreads && H / 16 <= kGateUpThreads * kGateUpRows;
+}
 
 int gemv_down_tile_rows(int H, int I) {
   (void)H;
@@ -389,37 +433,41 @@ int gemv_down_tile_rows(int H, int I) {
 
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
                                int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms) {
-  const int R = kGateUpRows;
-  const Shape s = plan_shape(H, R, 2, R * H + R * H / 8);
-  if (s.NS < 2 || s.NT > kMaxThreads) return cudaErrorInvalidConfiguration;
-  const int nunits = k * (I / R);
-  const int grid = nunits < num_sms ? nunits : num_sms;
+  const GateUpShape s = gateup_shape(H);
+  if (s.NS < 2 || s.NT > kGateUpThreads) return cudaErrorInvalidConfiguration;
+  const int nunits = k * (I / kGateUpRows);
+  const int grid = nunits < 2 * num_sms ? nunits : 2 * num_sms;
 #define GU(N)                                                                            \
   if (s.RPT == N)                                                                        \
     return s.warp_red ? run_gateup<N, true>(st, grid, s, plan, x, ws.hbuf, H, I, flags) \
                       : run_gateup<N, false>(st, grid, s, plan, x, ws.hbuf, H, I, flags);
-  GU(1) GU(2) GU(4) GU(8)
+  GU(1) GU(2) GU(4)
 #undef GU
   return cudaErrorInvalidConfiguration;
 }
 
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
                              const GemvWorkspace& ws, float* out, uint32_t* flags, int num_sms) {
-  const int R = kDownRows;
-  const Shape s = plan_shape(I, R, 1, R * I / 2 + R * I / 16);
-  if (s.NS < 2 || s.NT > kMaxThreads) return cudaErrorInvalidConfiguration;
-  const int nunits = (H / R) * k;
+  constexpr int R2 = kDownRows;
+  if (k * (I / 32) > kDownThreads) return cudaErrorInvalidConfiguration;
+  const int stage = k * (R2 * I / 2 + R2 * I / 16);
+  const int red_floats = (kDownThreads / 32) * R2;
+  int ns = (kSmemPerSm - 1024 - 16 - red_floats * 4) / stage;
+  if (ns > 8) ns = 8;
+  if (ns < 2) return cudaErrorInvalidConfiguration;
+  const int smem = ns * stage + 8 * ns + 8 + red_floats * 4;
+  const int nunits = H / R2;
   const int grid = nunits < num_sms ? nunits : num_sms;
-#define DN(N)                                                                              \
-  if (s.RPT == N)                                                                          \
-    return s.warp_red                                                                      \
-               ? run_down<N, true>(st, grid, s, plan, ws.hbuf, ws.ypart, ws.tile_cnt, out, \
-                                   H, I, flags)                                            \
-               : run_down<N, false>(st, grid, s, plan, ws.hbuf, ws.ypart, ws.tile_cnt, out, \
-                                    H, I, flags);
-  DN(1) DN(2) DN(4) DN(8) DN(16) DN(32)
-#undef DN
-  return cudaErrorInvalidConfiguration;
+  int nt = ((k * (I / 32) + 31) / 32) * 32;
+  auto kern = gemv_down_kernel<R2>;
+  static int smem_set = 0;
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  kern<<<grid, nt, smem, st>>>(plan, ws.hbuf, out, H, I, ns, flags);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

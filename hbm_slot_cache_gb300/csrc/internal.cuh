@@ -77,6 +77,8 @@ cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
                              const GemvWorkspace& ws, float* out, uint32_t* flags, int num_sms);
 int gemv_down_tile_rows(int H, int I);
+// Shapes the M = 1 expert kernels handle (top_k * inter <= 16384, dims % 128 == 0).
+bool gemv_supported(int H, int I, int k);
 
 // ------------------------------------------------------- device helpers
 

@@ -148,7 +148,7 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
   if (o.trace_capacity < 0 || o.copy_backend != MOE_COPY_SM) return MOE_ERR_ARG;
   if (experts > MOE_MAX_EXPERTS || top_k > MOE_MAX_TOPK || top_k > experts ||
       hidden % 128 || inter % 128 || hidden > MOE_MAX_DIM || inter > MOE_MAX_DIM ||
-      o.bypass_rows > MOE_MAX_CACHED_ROWS)
+      o.bypass_rows > MOE_MAX_CACHED_ROWS || !gemv_supported(hidden, inter, top_k))
     return MOE_ERR_UNSUPPORTED;
   if (o.all_resident) slots = experts;
   if (slots < top_k || slots > experts) return MOE_ERR_ARG;

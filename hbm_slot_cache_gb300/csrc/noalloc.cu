@@ -110,7 +110,8 @@ extern "C" int moe_expert_pass_noalloc(int k, int hidden, int inter, const void*
   if (k < 1 || hidden < 1 || inter < 1 || !expert_w || !expert_s || !gscale || !weights || !x ||
       !out || ((uintptr_t)x & 15) || ((uintptr_t)out & 3))
     return MOE_ERR_ARG;
-  if (k > kMaxK || hidden > kMaxDim || inter > kMaxDim || hidden % 128 || inter % 128)
+  if (k > kMaxK || hidden > kMaxDim || inter > kMaxDim || hidden % 128 || inter % 128 ||
+      !gemv_supported(hidden, inter, k))
     return MOE_ERR_UNSUPPORTED;
   for (int j = 0; j < k; ++j)
     if (!expert_w[j] || !expert_s[j] || ((uintptr_t)expert_w[j] & 15) ||

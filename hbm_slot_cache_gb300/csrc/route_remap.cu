@@ -3,6 +3,9 @@
 // One CTA does the whole step (the pages fuse all bookkeeping into a single
 // kernel: "GLM 5.3 Testing: HBM Expert Allocation", "The build, measured ...":
 // remap, miss detection and LRU in one launch instead of a dozen tiny ops).
+// The layer's map, owners and last-use stamps are read into shared memory in
+// one coalesced pass, all decisions are taken there, and only what changed is
+// written back, so the kernel costs about one global round trip.
 //
 // Router ("What the slot cache is": the router chooses top-8 expert ids before
 // the expert kernel; "TensorFold GLM-5.3 explained": ties break by a stable
@@ -24,13 +27,20 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kWords = MOE_MAX_EXPERTS / 32;
 
 __device__ __forceinline__ uint32_t rank_key(float f) {
-  if (isnan(f)) return 0u;                       // below -inf
+  if (isnan(f)) return 0u;                              // below -inf
   uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);  // -0 ranks as +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+// KPL = keys per lane = ceil(E / 32) rounded up to a power of two.
+template <int KPL>
 __global__ void __launch_bounds__(kThreads, 1)
 route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int S, long long Bw,
                    long long Bs, LayerDev L, Plan* __restrict__ plan, int all_resident) {
@@ -40,34 +50,41 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   __shared__ int32_t s_miss_e[MOE_MAX_PICKS];
   __shared__ int32_t s_victim[MOE_MAX_PICKS];
   __shared__ int32_t s_evicted[MOE_MAX_PICKS];
-  __shared__ uint32_t s_union[MOE_MAX_EXPERTS / 32];
-  __shared__ uint32_t s_missmask[MOE_MAX_EXPERTS / 32];
-  __shared__ int32_t s_misspre[MOE_MAX_EXPERTS / 32];
-  __shared__ unsigned long long s_key[MOE_MAX_EXPERTS];
+  __shared__ int32_t s_map[MOE_MAX_EXPERTS];               // expert -> slot
+  __shared__ int32_t s_owner[MOE_MAX_EXPERTS];             // slot -> expert
+  __shared__ unsigned long long s_key[MOE_MAX_EXPERTS];    // (stamp, slot); ~0 = used now
+  __shared__ uint32_t s_union[kWords];
+  __shared__ uint32_t s_missmask[kWords];
   __shared__ int32_t s_n_union, s_n_miss, s_n_hits, s_n_evict;
-  __shared__ uint32_t s_flags;
+  __shared__ uint32_t s_flags, s_clock;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int npicks = rows * k;
 
+  // ---- state into shared memory (overlaps the router's logit loads)
+  if (tid < kWords) {
+    s_union[tid] = 0;
+    s_missmask[tid] = 0;
+  }
   if (tid == 0) {
     s_flags = 0;
     s_n_hits = 0;
     s_n_evict = 0;
+    s_clock = *L.clock;
   }
-  if (tid < MOE_MAX_EXPERTS / 32) {
-    s_union[tid] = 0;
-    s_missmask[tid] = 0;
+  for (int e = tid; e < E; e += kThreads) s_map[e] = L.map[e];
+  for (int v = tid; v < S; v += kThreads) {
+    s_owner[v] = L.owner[v];
+    s_key[v] = ((unsigned long long)L.stamp[v] << 32) | (unsigned)v;
   }
-  __syncthreads();
 
   // ---- router: warp per row
   for (int m = warp; m < rows; m += kThreads / 32) {
     const float* lr = logits + (size_t)m * E;
-    unsigned long long key[MOE_MAX_EXPERTS / 32];
+    unsigned long long key[KPL];
     bool bad = false;
 #pragma unroll
-    for (int i = 0; i < MOE_MAX_EXPERTS / 32; ++i) {
+    for (int i = 0; i < KPL; ++i) {
       const int e = lane + 32 * i;
       key[i] = 0ull;
       if (e < E) {
@@ -77,66 +94,85 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       }
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(&s_flags, MOE_FLAG_NONFINITE_LOGIT);
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) best = umax64(best, key[i]);
+    float lsel = 0.f;  // lane j < k keeps the j-th selected logit
     for (int j = 0; j < k; ++j) {
-      unsigned long long best = 0ull;
+      unsigned long long w = best;
 #pragma unroll
-      for (int i = 0; i < MOE_MAX_EXPERTS / 32; ++i) best = key[i] > best ? key[i] : best;
+      for (int o = 16; o > 0; o >>= 1) w = umax64(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+      const int e = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
+      if ((e & 31) == lane) {  // the owning lane drops the winner and rescans
+        best = 0ull;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = other > best ? other : best;
+        for (int i = 0; i < KPL; ++i) {
+          if (lane + 32 * i == e) key[i] = 0ull;
+          best = umax64(best, key[i]);
+        }
       }
-      const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-#pragma unroll
-      for (int i = 0; i < MOE_MAX_EXPERTS / 32; ++i)
-        if (lane + 32 * i == e) key[i] = 0ull;
       if (lane == 0) s_ids[m * k + j] = e;
+      if (lane == j) lsel = lr[e];
     }
-    __syncwarp();
-    if (lane == 0) {
-      // softmax over the k selected logits; NaN counts as -inf; a logit equal
-      // to the maximum contributes exactly 1
-      float lmax = -INFINITY;
-      for (int j = 0; j < k; ++j) {
-        float l = lr[s_ids[m * k + j]];
-        if (isnan(l)) l = -INFINITY;
-        lmax = fmaxf(lmax, l);
-      }
-      float sum = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        float l = lr[s_ids[m * k + j]];
-        if (isnan(l)) l = -INFINITY;
-        const float ej = (l == lmax) ? 1.0f : expf(l - lmax);
-        s_wts[m * k + j] = ej;
-        sum += ej;
-      }
-      for (int j = 0; j < k; ++j) s_wts[m * k + j] = s_wts[m * k + j] / sum;
-    }
+    // softmax over the k selected logits; NaN counts as -inf; a logit equal to
+    // the maximum contributes exactly 1
+    float l = (lane < k) ? (isnan(lsel) ? -INFINITY : lsel) : -INFINITY;
+    float lmax = l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    const float ej = (lane < k) ? ((l == lmax) ? 1.0f : expf(l - lmax)) : 0.0f;
+    // sum in rank order (lane 0 first) for a fixed rounding
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ej, j);
+    if (lane < k) s_wts[m * k + lane] = ej / sum;
   }
   __syncthreads();
 
-  // ---- union of the picks
+  // ---- union, hits (slot marked used), missing ids
   for (int p = tid; p < npicks; p += kThreads) {
     const int e = s_ids[p];
     atomicOr(&s_union[e >> 5], 1u << (e & 31));
+    const int v = s_map[e];
+    s_hit[p] = v >= 0;
+    if (v >= 0) {
+      s_key[v] = ~0ull;
+      atomicAdd(&s_n_hits, 1);
+    } else {
+      atomicOr(&s_missmask[e >> 5], 1u << (e & 31));
+    }
   }
   __syncthreads();
   if (warp == 0) {
-    int c = 0;
-    for (int w = lane; w < MOE_MAX_EXPERTS / 32; w += 32) c += __popc(s_union[w]);
+    const int nu = __popc(s_union[lane]);
+    const uint32_t mm = s_missmask[lane];
+    const int nm = __popc(mm);
+    int incl = nm, tot_u = nu;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-    if (lane == 0) s_n_union = c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += a;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot_u += __shfl_xor_sync(0xFFFFFFFFu, tot_u, o);
+    int i = incl - nm;
+    uint32_t bits = mm;
+    while (bits) {  // misses in ascending expert id
+      const int b = __ffs(bits) - 1;
+      s_miss_e[i++] = 32 * lane + b;
+      bits &= bits - 1;
+    }
+    if (lane == 31) s_n_miss = incl;
+    if (lane == 0) s_n_union = tot_u;
   }
   __syncthreads();
   const int n_union = s_n_union;
-  const bool bypass = (!all_resident) && (n_union > S);
+  const int n_miss = s_n_miss;
+  DevStats* st = L.stats;
 
-  if (bypass) {
+  if (!all_resident && n_union > S) {
     // read every expert from host memory; cache state untouched
     for (int p = tid; p < npicks; p += kThreads) {
       const int e = s_ids[p];
-      s_hit[p] = L.map[e] >= 0;
       plan->ids[p] = e;
       plan->wts[p] = s_wts[p];
       plan->wptr[p] = L.host_w + (long long)e * Bw;
@@ -144,77 +180,40 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       plan->gs[p][0] = L.gscale[3 * e + 0];
       plan->gs[p][1] = L.gscale[3 * e + 1];
       plan->gs[p][2] = L.gscale[3 * e + 2];
+      if (L.trace_cap) {
+        moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
+        r->ids[p] = e;
+        r->weights[p] = s_wts[p];
+        r->slot[p] = -1;
+        r->hit[p] = s_hit[p];
+      }
     }
+    __syncthreads();
     if (tid == 0) {
       plan->rows = rows;
       plan->npicks = npicks;
       plan->n_union = n_union;
       plan->n_miss = 0;
       plan->bypass = 1;
-      DevStats* st = L.stats;
       st->steps += 1;
       st->bypass_calls += 1;
       if (s_flags) atomicOr(&st->flags, s_flags);
-    }
-    __syncthreads();
-    if (L.trace_cap && tid == 0) {
-      moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
-      r->clock = *L.clock;
-      r->rows = rows;
-      r->n_union = n_union;
-      r->n_miss = 0;
-      r->bypass = 1;
-      for (int p = 0; p < npicks; ++p) {
-        r->ids[p] = s_ids[p];
-        r->weights[p] = s_wts[p];
-        r->slot[p] = -1;
-        r->hit[p] = s_hit[p];
+      if (L.trace_cap) {
+        moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
+        r->clock = s_clock;
+        r->rows = rows;
+        r->n_union = n_union;
+        r->n_miss = 0;
+        r->bypass = 1;
+        *L.trace_head += 1;
       }
-      *L.trace_head += 1;
     }
     return;
   }
 
-  const uint32_t t = *L.clock + 1u;
+  const uint32_t t = s_clock + 1u;
 
-  // ---- hits: mark their slots used this step; collect missing ids
-  for (int v = tid; v < S; v += kThreads)
-    s_key[v] = ((unsigned long long)L.stamp[v] << 32) | (unsigned)v;
-  __syncthreads();
-  for (int p = tid; p < npicks; p += kThreads) {
-    const int e = s_ids[p];
-    const int v = L.map[e];
-    s_hit[p] = v >= 0;
-    if (v >= 0) {
-      s_key[v] = ~0ull;  // used this step: never a victim
-      atomicAdd(&s_n_hits, 1);
-    } else {
-      atomicOr(&s_missmask[e >> 5], 1u << (e & 31));
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int c = 0;
-    for (int w = 0; w < MOE_MAX_EXPERTS / 32; ++w) {
-      s_misspre[w] = c;
-      c += __popc(s_missmask[w]);
-    }
-    s_n_miss = c;
-  }
-  __syncthreads();
-  const int n_miss = s_n_miss;
-
-  // ---- misses in ascending expert id
-  for (int w = tid; w < MOE_MAX_EXPERTS / 32; w += kThreads) {
-    uint32_t bits = s_missmask[w];
-    int i = s_misspre[w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      s_miss_e[i++] = 32 * w + b;
-      bits &= bits - 1;
-    }
-  }
-  // ---- victims: the n_miss smallest (stamp, slot) among unused slots
+  // ---- victims: the n_miss smallest (stamp, slot) among slots unused this step
   if (n_miss > 0) {
     for (int v = tid; v < S; v += kThreads) {
       const unsigned long long kv = s_key[v];
@@ -229,7 +228,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   // ---- fill: evict the previous owner, then map the missing expert
   for (int i = tid; i < n_miss; i += kThreads) {
     const int e = s_miss_e[i], v = s_victim[i];
-    const int ev = L.owner[v];
+    const int ev = s_owner[v];
     if (ev >= 0) {
       L.map[ev] = -1;
       atomicAdd(&s_n_evict, 1);
@@ -237,6 +236,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     L.map[e] = v;
     L.owner[v] = e;
     L.stamp[v] = t;
+    s_map[e] = v;
     s_evicted[i] = ev;
     plan->miss_e[i] = e;
     plan->miss_v[i] = v;
@@ -246,9 +246,10 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   __syncthreads();
 
   // ---- per pick: the slot it reads
+  moe_step_record_t* r = L.trace_cap ? L.trace + (*L.trace_head % L.trace_cap) : nullptr;
   for (int p = tid; p < npicks; p += kThreads) {
     const int e = s_ids[p];
-    const int v = L.map[e];
+    const int v = s_map[e];
     plan->ids[p] = e;
     plan->wts[p] = s_wts[p];
     plan->wptr[p] = L.slot_w + (long long)v * Bw;
@@ -256,16 +257,14 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     plan->gs[p][0] = L.gscale[3 * e + 0];
     plan->gs[p][1] = L.gscale[3 * e + 1];
     plan->gs[p][2] = L.gscale[3 * e + 2];
-    if (L.trace_cap) {
-      moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
+    if (r) {
       r->ids[p] = e;
       r->weights[p] = s_wts[p];
       r->slot[p] = v;
       r->hit[p] = s_hit[p];
     }
   }
-  if (L.trace_cap) {
-    moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
+  if (r) {
     for (int i = tid; i < n_miss; i += kThreads) {
       r->miss_expert[i] = s_miss_e[i];
       r->miss_slot[i] = s_victim[i];
@@ -280,7 +279,6 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     plan->n_miss = n_miss;
     plan->bypass = 0;
     *L.clock = t;
-    DevStats* st = L.stats;
     st->steps += 1;
     st->picks += (unsigned long long)npicks;
     st->hits += (unsigned long long)s_n_hits;
@@ -288,8 +286,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     st->evictions += (unsigned long long)s_n_evict;
     st->bytes_copied += (unsigned long long)n_miss * (unsigned long long)(Bw + Bs);
     if (s_flags) atomicOr(&st->flags, s_flags);
-    if (L.trace_cap) {
-      moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
+    if (r) {
       r->clock = t;
       r->rows = rows;
       r->n_union = n_union;
@@ -305,9 +302,16 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
 cudaError_t launch_route_remap(cudaStream_t st, const float* logits, int rows, int E, int k,
                                int S, long long Bw, long long Bs, const LayerDev& L, Plan* plan,
                                int all_resident) {
-  route_remap_kernel<<<1, kThreads, 0, st>>>(logits, rows, E, k, S, Bw, Bs, L, plan,
-                                             all_resident);
-  return cudaGetLastError();
+  const int kpl = (E + 31) / 32;
+#define RR(N)                                                                                   \
+  if (kpl <= N) {                                                                              \
+    route_remap_kernel<N><<<1, kThreads, 0, st>>>(logits, rows, E, k, S, Bw, Bs, L, plan,      \
+                                                  all_resident);                               \
+    return cudaGetLastError();                                                                 \
+  }
+  RR(1) RR(2) RR(4) RR(8) RR(16) RR(32)
+#undef RR
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe
