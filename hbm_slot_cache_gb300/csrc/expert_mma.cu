@@ -1,0 +1,376 @@
+// Grouped expert matmuls for multi-row steps on the 5th-generation tensor
+// cores: tcgen05.mma kind::mxf4nvf4 with block scaling (E2M1 x E2M1, one UE4M3
+// scale per 16 elements on both operands, fp32 accumulators in TMEM).
+//
+// Rows of a round are grouped by expert so each expert's bytes are read once
+// for every row that chose it ("TensorFold GLM-5.3 explained": the round
+// fetches the union of its rows' experts once and every row reads that copy).
+// The weights are the MMA's A operand exactly as stored in the slot (or in
+// host memory on a bypass): no decode on the CUDA cores.  The activations are
+// the B operand in residual multi-level NVFP4 (quantize.cu): the N = 32
+// columns of one MMA are 5 member rows x 6 levels, and the epilogue adds the
+// levels with their fp32 level scales.
+//
+// One CTA (4 warps, one per TMEM lane quadrant) computes a 128-row weight tile
+// for one job (5 members of one group) over the whole K:
+//   gate/up: tile = 64 gate rows + the 64 matching up rows, so the epilogue
+//            forms h = silu(gate) * up for those 64 rows directly;
+//   down:    tile = 128 rows of W2, y_p = W2 h_p per member pick p.
+// K is walked in chunks of up to 256 elements: A (128 x 128 B) and B
+// (32 x 128 B) are copied with cp.async into the no-swizzle K-major core-matrix
+// layout (8 rows x 16 B per core matrix; K-adjacent cores 128 B apart, 8-row
+// groups 1 KB apart), the chunk's scale factors go to TMEM with tcgen05.st, and
+// one thread issues the chunk's MMAs and commits them to an mbarrier.  Two
+// stages: chunk c+1 loads while chunk c's MMAs run.
+//
+// Scale-factor placement: each 32-bit TMEM word holds the four UE4M3 scales of
+// one row for one 64-element MMA step (byte b = elements 16b..16b+15).  Every
+// warp writes its own lane quadrant, and each step's word is written to four
+// adjacent columns, so the MMA finds the scales whichever of those columns its
+// quadrant reads.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTileM = 128;
+constexpr int kTileN = 32;
+constexpr int kMaxChunkBytes = 128;  // 256 FP4 elements per row per stage
+constexpr int kABytes = kTileM * kMaxChunkBytes;
+constexpr int kBBytes = kTileN * kMaxChunkBytes;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 128;
+constexpr int kColD = 0, kColSF = 32;  // SF stage s: A at 32 + 32 s, B at 48 + 32 s
+constexpr int kSmemBytes = 48 * 1024;  // 2 stages + epilogue exchange; <= 4 CTAs/SM = TMEM
+
+struct MmaArgs {
+  const GroupPlan* gp;
+  int K;        // inner dimension: H for gate/up, I for down
+  int H, I, k;  // layer shape, top_k
+  int gate_up;  // 1: gate/up + SwiGLU, 0: down
+  QuantBuf act; // gate/up: by token row; down: by pick
+  float* out;   // gate/up: h [P][I]; down: y [P][H]
+  uint32_t* flags;
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128u >> 4) << 16;   // K-adjacent core matrices: 128 B
+  d |= (uint64_t)(1024u >> 4) << 32;  // 8-row groups: 1 KB
+  d |= (uint64_t)1 << 46;             // sm_100-family descriptor version; no swizzle
+  return d;
+}
+
+// kind::mxf4nvf4 instruction descriptor: A, B = E2M1, UE4M3 scales, K-major,
+// M = 128, N = 32, dense.
+__host__ __device__ constexpr uint32_t umma_idesc() {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%2,%2,%2,%2,%3,%3,%3,%3,%4,%4,%4,%4};" ::"r"(
+          taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+      : "memory");
+}
+
+template <int P>  // 16-byte pieces per row per chunk (8: 256 elements, 4: 128)
+__global__ void __launch_bounds__(kThreads)
+grouped_mma_kernel(MmaArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_pick[kRowsPerJob], s_brow[kRowsPerJob];
+  __shared__ float s_gl[kRowsPerJob][kLevels];
+  __shared__ int s_fail;
+  const GroupPlan* gp = a.gp;
+  const int job = blockIdx.x;
+  if (job >= gp->n_jobs) return;  // uniform: before any TMEM or barrier use
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = blockIdx.y;
+  const int jv = gp->jobs[job];
+  const int g = jv >> 8, tile = jv & 255;
+  const int gstart = gp->g_start[g], gcount = gp->g_count[g];
+  const int m0 = tile * kRowsPerJob;
+  const int nmem = min(kRowsPerJob, gcount - m0);
+  const int K = a.K, H = a.H, I = a.I;
+  constexpr int CB = P * 16;             // bytes per row per chunk
+  constexpr int KSTEPS = CB / 32;        // 64-element MMA steps per chunk
+  const int nchunks = K / (2 * CB);
+
+  if (tid < kRowsPerJob) {
+    int p = -1, br = 0;
+    if (tid < nmem) {
+      p = gp->members[gstart + m0 + tid];
+      br = a.gate_up ? p / a.k : p;
+    }
+    s_pick[tid] = p;
+    s_brow[tid] = br;
+  }
+  if (tid == 0) s_fail = 0;
+  __syncthreads();
+  if (tid < kRowsPerJob * kLevels) {
+    const int s = tid / kLevels, l = tid - s * kLevels;
+    s_gl[s][l] = (s < nmem) ? a.act.gl[(size_t)s_brow[s] * kLevels + l] : 0.f;
+  }
+
+  // weight rows of this tile
+  const uint8_t* wbase = gp->g_wptr[g];
+  const uint8_t* sbase = gp->g_sptr[g];
+  size_t row_stride_w, row_stride_s;
+  if (a.gate_up) {
+    row_stride_w = H / 2;
+    row_stride_s = H / 16;
+  } else {
+    wbase += (size_t)I * H;
+    sbase += (size_t)I * H / 8;
+    row_stride_w = I / 2;
+    row_stride_s = I / 16;
+  }
+  auto src_row = [&](int r) -> size_t {  // tile row -> row index within the matrix block
+    if (a.gate_up) return r < 64 ? (size_t)(64 * mt + r) : (size_t)(I + 64 * mt + r - 64);
+    return (size_t)(kTileM * mt + r);
+  };
+
+  // this thread's cp.async pieces: A rows tid/P + (128/P) i, piece tid % P
+  constexpr int AR = kTileM * P / kThreads;  // A rows per thread
+  constexpr int BR = kTileN * P / kThreads;  // B rows per thread
+  const int kc = tid % P;
+  const uint8_t* a_src[AR];
+#pragma unroll
+  for (int i = 0; i < AR; ++i) a_src[i] = wbase + src_row(tid / P + (kThreads / P) * i) * row_stride_w + kc * 16;
+  const uint8_t* b_src[BR];
+  uint32_t b_ok[BR];
+#pragma unroll
+  for (int i = 0; i < BR; ++i) {
+    const int n = tid / P + (kThreads / P) * i;
+    const int s = n / kLevels, l = n - s * kLevels;
+    const bool ok = n < kRowsPerJob * kLevels && s < nmem;
+    b_ok[i] = ok ? 16u : 0u;
+    b_src[i] = ok ? a.act.codes + ((size_t)s_brow[s] * kLevels + l) * (K / 2) + kc * 16 : a.act.codes;
+  }
+  // this thread's scale rows: A row 32*warp + lane, B row lane
+  const uint8_t* sa_src = sbase + src_row(32 * warp + lane) * row_stride_s;
+  const uint8_t* sb_src = nullptr;
+  {
+    const int s = lane / kLevels, l = lane - s * kLevels;
+    if (lane < kRowsPerJob * kLevels && s < nmem)
+      sb_src = a.act.scales + ((size_t)s_brow[s] * kLevels + l) * (K / 16);
+  }
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&s_tmem)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+
+  auto load_chunk = [&](int c, int stage, uint32_t (&sfa)[4], uint32_t (&sfb)[4]) {
+    uint8_t* sA = smem + stage * kStageBytes;
+    uint8_t* sB = sA + kABytes;
+#pragma unroll
+    for (int i = 0; i < AR; ++i) {
+      const int r = tid / P + (kThreads / P) * i;
+      cp_async16(sA + (r >> 3) * 1024 + kc * 128 + (r & 7) * 16, a_src[i] + (size_t)c * CB, 16u);
+    }
+#pragma unroll
+    for (int i = 0; i < BR; ++i) {
+      const int n = tid / P + (kThreads / P) * i;
+      cp_async16(sB + (n >> 3) * 1024 + kc * 128 + (n & 7) * 16,
+                 b_ok[i] ? b_src[i] + (size_t)c * CB : b_src[i], b_ok[i]);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    // scales: CB/8 bytes per row per chunk (one 32-bit word per MMA step)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      sfa[q] = 0u;
+      sfb[q] = 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < KSTEPS; ++q) {
+      sfa[q] = __ldg(reinterpret_cast<const uint32_t*>(sa_src + (size_t)c * (CB / 8)) + q);
+      if (sb_src) sfb[q] = __ldg(reinterpret_cast<const uint32_t*>(sb_src + (size_t)c * (CB / 8)) + q);
+    }
+  };
+
+  uint32_t sfa[2][4], sfb[2][4];
+  load_chunk(0, 0, sfa[0], sfb[0]);
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c & 1;
+    if (c + 1 < nchunks) {
+      if (c >= 1) {  // chunk c-1's MMAs read the stage chunk c+1 is about to fill
+        if (!mbar_wait_bounded(&s_bar, (uint32_t)((c - 1) & 1), a.flags)) s_fail = 1;
+      }
+      load_chunk(c + 1, st ^ 1, sfa[st ^ 1], sfb[st ^ 1]);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    tmem_st16(tmem + lane_base + kColSF + 32 * st, sfa[st]);
+    tmem_st16(tmem + lane_base + kColSF + 32 * st + 16, sfb[st]);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (s_fail) {
+      ok = false;
+      break;
+    }
+    if (tid == 0) {
+      const uint32_t sA = smem_addr(smem + st * kStageBytes);
+      const uint32_t sB = sA + kABytes;
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const uint64_t da = umma_desc(sA + 256 * ks), db = umma_desc(sB + 256 * ks);
+        const uint32_t sfa_t = tmem + kColSF + 32 * st + 4 * ks;
+        const uint32_t sfb_t = tmem + kColSF + 32 * st + 16 + 4 * ks;
+        const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                tmem + kColD),
+            "l"(da), "l"(db), "r"(umma_idesc()), "r"(sfa_t), "r"(sfb_t), "r"(acc)
+            : "memory");
+      }
+      asm volatile(
+          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+              smem_addr(&s_bar))
+          : "memory");
+    }
+  }
+  if (ok && !mbar_wait_bounded(&s_bar, (uint32_t)((nchunks - 1) & 1), a.flags)) s_fail = 1;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing may land after exit
+  __syncthreads();
+  ok = s_fail == 0;  // uniform across the CTA
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+  if (ok) {
+    uint32_t v[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(tmem + lane_base + kColD));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    const int row = 32 * warp + lane;  // tile row
+    float val[kRowsPerJob];
+#pragma unroll
+    for (int s = 0; s < kRowsPerJob; ++s) {
+      float acc = 0.f;
+#pragma unroll
+      for (int l = 0; l < kLevels; ++l) acc = fmaf(s_gl[s][l], __uint_as_float(v[s * kLevels + l]), acc);
+      val[s] = acc;
+    }
+    const float* gsc = gp->g_gs + 3 * g;
+    if (a.gate_up) {
+      float* s_up = reinterpret_cast<float*>(smem);  // stages are idle now
+      if (row >= 64)
+#pragma unroll
+        for (int s = 0; s < kRowsPerJob; ++s) s_up[(row - 64) * kRowsPerJob + s] = val[s];
+      __syncthreads();
+      if (row < 64) {
+        for (int s = 0; s < nmem; ++s) {
+          const float gate = gsc[0] * val[s];
+          const float up = gsc[1] * s_up[row * kRowsPerJob + s];
+          a.out[(size_t)s_pick[s] * I + 64 * mt + row] = gate / (1.0f + expf(-gate)) * up;
+        }
+      }
+    } else {
+      for (int s = 0; s < nmem; ++s)
+        a.out[(size_t)s_pick[s] * H + kTileM * mt + row] = gsc[2] * val[s];
+    }
+  } else {
+    __syncthreads();
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols));
+}
+
+// out[m][o] = sum_j w[m*k + j] * y[m*k + j][o], j in rank order.
+__global__ void combine_kernel(const GroupPlan* __restrict__ gp, const float* __restrict__ y,
+                               float* __restrict__ out, int H, int k) {
+  const int m = blockIdx.y;
+  const int o = blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= H) return;
+  float acc = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int p = m * k + j;
+    acc = fmaf(gp->wts[p], y[(size_t)p * H + o], acc);
+  }
+  out[(size_t)m * H + o] = acc;
+}
+
+template <int P>
+cudaError_t run_mma(cudaStream_t st, const MmaArgs& a, int max_jobs, int m_tiles) {
+  auto kern = grouped_mma_kernel<P>;
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  kern<<<dim3(max_jobs, m_tiles), kThreads, kSmemBytes, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mma_supported(int H, int I) {
+  auto ok = [](int K) { return K % 64 == 0 && (K <= 256 ? (K == 128 || K == 256) : K % 256 == 0); };
+  return ok(H) && ok(I) && I % 64 == 0 && H % 128 == 0;
+}
+
+cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int max_jobs, bool gate_up,
+                               int H, int I, int k, const QuantBuf& act, float* out,
+                               uint32_t* flags) {
+  if (max_jobs <= 0) return cudaSuccess;
+  MmaArgs a;
+  a.gp = gp;
+  a.K = gate_up ? H : I;
+  a.H = H;
+  a.I = I;
+  a.k = k;
+  a.gate_up = gate_up ? 1 : 0;
+  a.act = act;
+  a.out = out;
+  a.flags = flags;
+  const int m_tiles = gate_up ? I / 64 : H / kTileM;
+  if (a.K >= 256) return run_mma<8>(st, a, max_jobs, m_tiles);
+  return run_mma<4>(st, a, max_jobs, m_tiles);
+}
+
+cudaError_t launch_combine(cudaStream_t st, const GroupPlan* gp, const float* y, float* out,
+                           int rows, int H, int k) {
+  dim3 grid((H + 255) / 256, rows);
+  combine_kernel<<<grid, 256, 0, st>>>(gp, y, out, H, k);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

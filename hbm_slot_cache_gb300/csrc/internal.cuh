@@ -51,12 +51,57 @@ struct Plan {
   float gs[MOE_MAX_PICKS][4];          // (gate, up, down, unused) global scales
 };
 
+// Multi-row steps: picks grouped by expert so each expert's bytes are read
+// once for all rows that chose it ("TensorFold GLM-5.3 explained": a round
+// fetches the union of its rows' experts once).  Groups are in ascending
+// expert id, members (pick indices p = row * k + rank) ascending within a
+// group, jobs = (group, tile of kRowsPerJob members).  Sized at create for the
+// largest step (P = max_rows * top_k picks).
+constexpr int kLevels = 6;       // residual NVFP4 levels of the activations
+constexpr int kRowsPerJob = 5;   // members per MMA N-tile (5 * 6 = 30 of 32 columns)
+struct GroupPlan {
+  int32_t n_groups, n_jobs, rows, npicks;
+  int32_t* g_expert;       // [G]
+  int32_t* g_start;        // [G] first member
+  int32_t* g_count;        // [G]
+  const uint8_t** g_wptr;  // [G] expert codes (slot, or host memory on a bypass)
+  const uint8_t** g_sptr;  // [G]
+  float* g_gs;             // [G][3]
+  int32_t* members;        // [P] pick indices grouped
+  int32_t* jobs;           // [J] (group << 8) | tile
+  float* wts;              // [P] router weights by pick
+};
+
+// Activations in residual NVFP4: codes [rows][kLevels][K/2], scales
+// [rows][kLevels][K/16] (UE4M3), level scales [rows][kLevels] (fp32).
+struct QuantBuf {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* gl;
+};
+
 // ------------------------------------------------------------ launchers
 
-// route + remap/LRU for rows <= MOE_MAX_CACHED_ROWS (one CTA).
+// route + remap/LRU for rows <= MOE_MAX_CACHED_ROWS (one CTA); gp != null
+// also emits the expert groups of a multi-row step.
 cudaError_t launch_route_remap(cudaStream_t st, const float* logits, int rows, int E, int k,
                                int S, long long Bw, long long Bs, const LayerDev& L, Plan* plan,
-                               int all_resident);
+                               int all_resident, GroupPlan* gp);
+// bypass steps: route every row, group picks by expert over host backing.
+cudaError_t launch_route_rows(cudaStream_t st, const float* logits, int rows, int E, int k,
+                              int32_t* ids, GroupPlan* gp, const LayerDev& L, long long Bw,
+                              long long Bs);
+// activations (bf16 or fp32 rows of K) -> residual NVFP4 levels.
+cudaError_t launch_quantize_rows(cudaStream_t st, const void* src, bool bf16_in, int rows, int K,
+                                 const QuantBuf& q);
+// grouped tcgen05 expert matmuls: gate/up + SwiGLU -> h [P][I], or down -> y [P][H].
+bool mma_supported(int H, int I);
+cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int max_jobs, bool gate_up,
+                               int H, int I, int k, const QuantBuf& act, float* out,
+                               uint32_t* flags);
+// out[m] = sum_j w[m,j] y[m*k+j], rank order.
+cudaError_t launch_combine(cudaStream_t st, const GroupPlan* gp, const float* y, float* out,
+                           int rows, int H, int k);
 
 // miss copy host -> slot, SM kernel; reads the miss list from the plan.
 cudaError_t launch_miss_copy(cudaStream_t st, const Plan* plan, const uint8_t* host_w,

@@ -13,6 +13,10 @@
 
 using namespace moe;
 
+namespace {
+constexpr int kDefaultMaxRows = 512;  // largest prefill chunk a handle takes by default
+}
+
 struct moe_cache {
   int L, E, S, H, I, k;
   long long Bw, Bs;
@@ -32,6 +36,12 @@ struct moe_cache {
   // per-step workspace
   Plan* plan = nullptr;
   GemvWorkspace gemv{};
+  // multi-row / bypass workspace (sized for max_rows)
+  int max_picks = 0;
+  GroupPlan* gp = nullptr;  // device copy of the header; arrays below
+  QuantBuf xq{}, hq{};      // residual NVFP4 activations: x by row, h by pick
+  int32_t* ids_ws = nullptr;
+  std::vector<void*> extra;  // further device allocations, freed with the handle
   // host backing (device-visible addresses)
   std::vector<const uint8_t*> host_w, host_s;
   // optional per-kernel timing events (caller-owned)
@@ -63,6 +73,49 @@ void free_all(moe_cache* h) {
   cudaFree(h->gemv.hbuf);
   cudaFree(h->gemv.ypart);
   cudaFree(h->gemv.tile_cnt);
+  for (void* p : h->extra) cudaFree(p);
+  h->extra.clear();
+}
+
+// Group plan, quantised-activation buffers and bypass ids for steps of up to
+// max_rows rows.
+bool alloc_multirow(moe_cache* h) {
+  const size_t P = (size_t)h->opts.max_rows * h->k;
+  const size_t G = P < (size_t)h->E ? P : (size_t)h->E;
+  const size_t J = P + G;
+  const size_t R = (size_t)h->opts.max_rows;
+  h->max_picks = (int)P;
+  auto get = [&](size_t bytes) -> void* {
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes ? bytes : 16) != cudaSuccess) return nullptr;
+    h->extra.push_back(p);
+    return p;
+  };
+  GroupPlan g{};
+  g.g_expert = static_cast<int32_t*>(get(4 * G));
+  g.g_start = static_cast<int32_t*>(get(4 * G));
+  g.g_count = static_cast<int32_t*>(get(4 * G));
+  g.g_wptr = static_cast<const uint8_t**>(get(sizeof(void*) * G));
+  g.g_sptr = static_cast<const uint8_t**>(get(sizeof(void*) * G));
+  g.g_gs = static_cast<float*>(get(4 * 3 * G));
+  g.members = static_cast<int32_t*>(get(4 * P));
+  g.jobs = static_cast<int32_t*>(get(4 * J));
+  g.wts = static_cast<float*>(get(4 * P));
+  h->gp = static_cast<GroupPlan*>(get(sizeof(GroupPlan)));
+  h->ids_ws = static_cast<int32_t*>(get(4 * P));
+  h->xq.codes = static_cast<uint8_t*>(get(R * kLevels * (h->H / 2)));
+  h->xq.scales = static_cast<uint8_t*>(get(R * kLevels * (h->H / 16)));
+  h->xq.gl = static_cast<float*>(get(4 * R * kLevels));
+  h->hq.codes = static_cast<uint8_t*>(get(P * kLevels * (h->I / 2)));
+  h->hq.scales = static_cast<uint8_t*>(get(P * kLevels * (h->I / 16)));
+  h->hq.gl = static_cast<float*>(get(4 * P * kLevels));
+  for (void* p : h->extra)
+    if (!p) return false;
+  if (!g.g_expert || !g.g_start || !g.g_count || !g.g_wptr || !g.g_sptr || !g.g_gs ||
+      !g.members || !g.jobs || !g.wts || !h->gp || !h->ids_ws || !h->xq.codes || !h->xq.scales ||
+      !h->xq.gl || !h->hq.codes || !h->hq.scales || !h->hq.gl)
+    return false;
+  return cudaMemcpy(h->gp, &g, sizeof g, cudaMemcpyHostToDevice) == cudaSuccess;
 }
 
 // Resolve a pinned host pointer to the address kernels use; -1 if not pinned.
@@ -137,11 +190,11 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
   moe_cache_opts_t o{};
   o.copy_backend = MOE_COPY_SM;
   o.bypass_rows = MOE_MAX_CACHED_ROWS;
-  o.max_rows = MOE_MAX_CACHED_ROWS;
+  o.max_rows = kDefaultMaxRows;
   if (opts) {
     o = *opts;
     if (o.bypass_rows <= 0) o.bypass_rows = MOE_MAX_CACHED_ROWS;
-    if (o.max_rows <= 0) o.max_rows = MOE_MAX_CACHED_ROWS;
+    if (o.max_rows <= 0) o.max_rows = kDefaultMaxRows;
   }
   if (layers < 1 || experts < 1 || top_k < 1 || hidden < 1 || inter < 1 || !host_backing)
     return MOE_ERR_ARG;
@@ -191,6 +244,8 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
     std::memcpy(gs.data() + (size_t)l * experts * 3, hl.gscale, sizeof(float) * experts * 3);
   }
   const size_t LS = (size_t)layers * slots, LE = (size_t)layers * experts;
+  size_t max_picks = (size_t)o.max_rows * top_k;
+  if (max_picks < (size_t)MOE_MAX_PICKS) max_picks = MOE_MAX_PICKS;
   const int cap = o.trace_capacity;
   bool ok = dalloc(&h->slot_w, LS * (size_t)h->Bw) == cudaSuccess &&
             dalloc(&h->slot_s, LS * (size_t)h->Bs) == cudaSuccess &&
@@ -201,10 +256,11 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
             dalloc(&h->trace, (size_t)layers * (cap ? cap : 1)) == cudaSuccess &&
             dalloc(&h->trace_head, (size_t)layers) == cudaSuccess &&
             dalloc(&h->plan, 1) == cudaSuccess &&
-            dalloc(&h->gemv.hbuf, (size_t)MOE_MAX_PICKS * inter) == cudaSuccess &&
-            dalloc(&h->gemv.ypart, (size_t)MOE_MAX_TOPK * hidden) == cudaSuccess &&
+            dalloc(&h->gemv.hbuf, (size_t)max_picks * inter) == cudaSuccess &&
+            dalloc(&h->gemv.ypart, (size_t)max_picks * hidden) == cudaSuccess &&
             dalloc(&h->gemv.tile_cnt, (size_t)(hidden / gemv_down_tile_rows(hidden, inter) + 1)) ==
                 cudaSuccess;
+  ok = ok && alloc_multirow(h);
   if (!ok) {
     cudaGetLastError();
     free_all(h);
@@ -236,7 +292,8 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     return MOE_ERR_ARG;
   if ((uintptr_t)x & 15) return MOE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (rows > h->opts.bypass_rows || rows > 1) return MOE_ERR_UNSUPPORTED;
+  if (rows > h->opts.bypass_rows && rows > h->opts.max_rows) return MOE_ERR_UNSUPPORTED;
+  if (rows > 1 && !mma_supported(h->H, h->I)) return MOE_ERR_UNSUPPORTED;
   const LayerDev L = layer_dev(h, layer);
   // inside a capture an event record must be an external node to be replayed
   auto mark = [&](int i) -> cudaError_t {
@@ -247,21 +304,51 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     return cudaEventRecordWithFlags(
         h->ev[i], st, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u);
   };
-  cudaError_t e = mark(0);
-  if (e == cudaSuccess)
-    e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
-                           h->opts.all_resident);
-  if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess && !h->opts.all_resident)
-    e = launch_miss_copy(st, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
-                         2 * h->num_sms);
-  if (e == cudaSuccess) e = mark(2);
   uint32_t* flags = &(h->stats + layer)->flags;
+  cudaError_t e = mark(0);
+  if (rows == 1) {
+    // one row: route/remap, miss copy, GEMV gate/up + SwiGLU, GEMV down + combine
+    if (e == cudaSuccess)
+      e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
+                             h->opts.all_resident, nullptr);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess && !h->opts.all_resident)
+      e = launch_miss_copy(st, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
+                           2 * h->num_sms);
+    if (e == cudaSuccess) e = mark(2);
+    if (e == cudaSuccess)
+      e = launch_gemv_gateup(st, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms);
+    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess)
+      e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, out, flags, h->num_sms);
+    if (e == cudaSuccess) e = mark(4);
+    return cuda_err(e);
+  }
+  // several rows: experts grouped, each read once for all its rows (tensor cores)
+  const int npicks = rows * h->k;
+  if (rows <= h->opts.bypass_rows) {
+    if (e == cudaSuccess)
+      e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
+                             h->opts.all_resident, h->gp);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess && !h->opts.all_resident)
+      e = launch_miss_copy(st, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
+                           2 * h->num_sms);
+  } else {
+    // prefill bypass: experts read from host memory, cache untouched
+    if (e == cudaSuccess)
+      e = launch_route_rows(st, router_logits, rows, h->E, h->k, h->ids_ws, h->gp, L, h->Bw, h->Bs);
+    if (e == cudaSuccess) e = mark(1);
+  }
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess) e = launch_quantize_rows(st, x, true, rows, h->H, h->xq);
   if (e == cudaSuccess)
-    e = launch_gemv_gateup(st, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms);
+    e = launch_grouped_mma(st, h->gp, npicks, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf, flags);
   if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess) e = launch_quantize_rows(st, h->gemv.hbuf, false, npicks, h->I, h->hq);
   if (e == cudaSuccess)
-    e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, out, flags, h->num_sms);
+    e = launch_grouped_mma(st, h->gp, npicks, false, h->H, h->I, h->k, h->hq, h->gemv.ypart, flags);
+  if (e == cudaSuccess) e = launch_combine(st, h->gp, h->gemv.ypart, out, rows, h->H, h->k);
   if (e == cudaSuccess) e = mark(4);
   return cuda_err(e);
 }

@@ -22,6 +22,7 @@
 // memory, state untouched).  The i-th miss gets the i-th smallest unused slot,
 // which equals filling the misses one at a time.
 #include "internal.cuh"
+#include "router.cuh"
 
 namespace moe {
 namespace {
@@ -29,21 +30,68 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWords = MOE_MAX_EXPERTS / 32;
 
-__device__ __forceinline__ uint32_t rank_key(float f) {
-  if (isnan(f)) return 0u;                              // below -inf
-  uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);  // -0 ranks as +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
-  return a > b ? a : b;
+// Multi-row steps: group the picks by expert for the grouped tensor-core pass.
+// Groups are the union's experts in ascending id (group = rank in the union),
+// members are pick indices in ascending order, jobs are tiles of kRowsPerJob
+// members.  Called by every thread of the CTA.
+__device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
+                            const int32_t* s_ids, const float* s_wts,
+                            const uint8_t* const* s_wp, const uint8_t* const* s_sp,
+                            const uint32_t* s_union, const int32_t* s_upre, int32_t* s_pgroup,
+                            int32_t* s_gcount, int32_t* s_gstart, int32_t* s_jstart,
+                            const float* gscale) {
+  const int tid = threadIdx.x;
+  for (int g = tid; g < n_union; g += kThreads) s_gcount[g] = 0;
+  __syncthreads();
+  for (int p = tid; p < npicks; p += kThreads) {
+    const int e = s_ids[p];
+    const int g = s_upre[e >> 5] + __popc(s_union[e >> 5] & ((1u << (e & 31)) - 1u));
+    s_pgroup[p] = g;
+    atomicAdd(&s_gcount[g], 1);
+    gp->wts[p] = s_wts[p];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int m = 0, j = 0;
+    for (int g = 0; g < n_union; ++g) {
+      s_gstart[g] = m;
+      s_jstart[g] = j;
+      m += s_gcount[g];
+      j += (s_gcount[g] + kRowsPerJob - 1) / kRowsPerJob;
+    }
+    gp->n_groups = n_union;
+    gp->n_jobs = j;
+    gp->rows = rows;
+    gp->npicks = npicks;
+  }
+  __syncthreads();
+  for (int g = tid; g < n_union; g += kThreads) {
+    int idx = 0, first = -1;
+    for (int p = 0; p < npicks; ++p) {
+      if (s_pgroup[p] != g) continue;
+      gp->members[s_gstart[g] + idx++] = p;
+      if (first < 0) first = p;
+    }
+    const int e = s_ids[first];
+    gp->g_expert[g] = e;
+    gp->g_start[g] = s_gstart[g];
+    gp->g_count[g] = s_gcount[g];
+    gp->g_wptr[g] = s_wp[first];
+    gp->g_sptr[g] = s_sp[first];
+    gp->g_gs[3 * g + 0] = gscale[3 * e + 0];
+    gp->g_gs[3 * g + 1] = gscale[3 * e + 1];
+    gp->g_gs[3 * g + 2] = gscale[3 * e + 2];
+    const int nj = (s_gcount[g] + kRowsPerJob - 1) / kRowsPerJob;
+    for (int t = 0; t < nj; ++t) gp->jobs[s_jstart[g] + t] = (g << 8) | t;
+  }
 }
 
 // KPL = keys per lane = ceil(E / 32) rounded up to a power of two.
 template <int KPL>
 __global__ void __launch_bounds__(kThreads, 1)
 route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int S, long long Bw,
-                   long long Bs, LayerDev L, Plan* __restrict__ plan, int all_resident) {
+                   long long Bs, LayerDev L, Plan* __restrict__ plan, int all_resident,
+                   GroupPlan* __restrict__ gp) {
   __shared__ int32_t s_ids[MOE_MAX_PICKS];
   __shared__ float s_wts[MOE_MAX_PICKS];
   __shared__ int32_t s_hit[MOE_MAX_PICKS];
@@ -55,6 +103,11 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   __shared__ unsigned long long s_key[MOE_MAX_EXPERTS];    // (stamp, slot); ~0 = used now
   __shared__ uint32_t s_union[kWords];
   __shared__ uint32_t s_missmask[kWords];
+  __shared__ int32_t s_upre[kWords];                   // union ranks before each word
+  __shared__ const uint8_t* s_wp[MOE_MAX_PICKS];       // bytes each pick reads
+  __shared__ const uint8_t* s_sp[MOE_MAX_PICKS];
+  __shared__ int32_t s_pgroup[MOE_MAX_PICKS], s_gcount[MOE_MAX_PICKS];
+  __shared__ int32_t s_gstart[MOE_MAX_PICKS], s_jstart[MOE_MAX_PICKS];
   __shared__ int32_t s_n_union, s_n_miss, s_n_hits, s_n_evict;
   __shared__ uint32_t s_flags, s_clock;
 
@@ -80,51 +133,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
 
   // ---- router: warp per row
   for (int m = warp; m < rows; m += kThreads / 32) {
-    const float* lr = logits + (size_t)m * E;
-    unsigned long long key[KPL];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      const int e = lane + 32 * i;
-      key[i] = 0ull;
-      if (e < E) {
-        const float f = lr[e];
-        bad |= !isfinite(f);
-        key[i] = ((unsigned long long)rank_key(f) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-      }
-    }
-    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(&s_flags, MOE_FLAG_NONFINITE_LOGIT);
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) best = umax64(best, key[i]);
-    float lsel = 0.f;  // lane j < k keeps the j-th selected logit
-    for (int j = 0; j < k; ++j) {
-      unsigned long long w = best;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) w = umax64(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
-      const int e = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
-      if ((e & 31) == lane) {  // the owning lane drops the winner and rescans
-        best = 0ull;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-          if (lane + 32 * i == e) key[i] = 0ull;
-          best = umax64(best, key[i]);
-        }
-      }
-      if (lane == 0) s_ids[m * k + j] = e;
-      if (lane == j) lsel = lr[e];
-    }
-    // softmax over the k selected logits; NaN counts as -inf; a logit equal to
-    // the maximum contributes exactly 1
-    float l = (lane < k) ? (isnan(lsel) ? -INFINITY : lsel) : -INFINITY;
-    float lmax = l;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
-    const float ej = (lane < k) ? ((l == lmax) ? 1.0f : expf(l - lmax)) : 0.0f;
-    // sum in rank order (lane 0 first) for a fixed rounding
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ej, j);
-    if (lane < k) s_wts[m * k + lane] = ej / sum;
+    const bool bad = route_row<KPL>(logits + (size_t)m * E, E, k, lane, s_ids + m * k, s_wts + m * k);
+    if (bad && lane == 0) atomicOr(&s_flags, MOE_FLAG_NONFINITE_LOGIT);
   }
   __syncthreads();
 
@@ -146,12 +156,17 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     const int nu = __popc(s_union[lane]);
     const uint32_t mm = s_missmask[lane];
     const int nm = __popc(mm);
-    int incl = nm, tot_u = nu;
+    int incl = nm, tot_u = nu, uincl = nu;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int a = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += a;
+      const int b = __shfl_up_sync(0xFFFFFFFFu, uincl, o);
+      if (lane >= o) {
+        incl += a;
+        uincl += b;
+      }
     }
+    s_upre[lane] = uincl - nu;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tot_u += __shfl_xor_sync(0xFFFFFFFFu, tot_u, o);
     int i = incl - nm;
@@ -177,6 +192,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       plan->wts[p] = s_wts[p];
       plan->wptr[p] = L.host_w + (long long)e * Bw;
       plan->sptr[p] = L.host_s + (long long)e * Bs;
+      s_wp[p] = plan->wptr[p];
+      s_sp[p] = plan->sptr[p];
       plan->gs[p][0] = L.gscale[3 * e + 0];
       plan->gs[p][1] = L.gscale[3 * e + 1];
       plan->gs[p][2] = L.gscale[3 * e + 2];
@@ -189,6 +206,9 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       }
     }
     __syncthreads();
+    if (gp)
+      emit_groups(gp, rows, npicks, n_union, s_ids, s_wts, s_wp, s_sp, s_union, s_upre, s_pgroup,
+                  s_gcount, s_gstart, s_jstart, L.gscale);
     if (tid == 0) {
       plan->rows = rows;
       plan->npicks = npicks;
@@ -254,6 +274,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     plan->wts[p] = s_wts[p];
     plan->wptr[p] = L.slot_w + (long long)v * Bw;
     plan->sptr[p] = L.slot_s + (long long)v * Bs;
+    s_wp[p] = plan->wptr[p];
+    s_sp[p] = plan->sptr[p];
     plan->gs[p][0] = L.gscale[3 * e + 0];
     plan->gs[p][1] = L.gscale[3 * e + 1];
     plan->gs[p][2] = L.gscale[3 * e + 2];
@@ -272,6 +294,9 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     }
   }
   __syncthreads();
+  if (gp)
+    emit_groups(gp, rows, npicks, n_union, s_ids, s_wts, s_wp, s_sp, s_union, s_upre, s_pgroup,
+                s_gcount, s_gstart, s_jstart, L.gscale);
   if (tid == 0) {
     plan->rows = rows;
     plan->npicks = npicks;
@@ -301,12 +326,12 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
 
 cudaError_t launch_route_remap(cudaStream_t st, const float* logits, int rows, int E, int k,
                                int S, long long Bw, long long Bs, const LayerDev& L, Plan* plan,
-                               int all_resident) {
+                               int all_resident, GroupPlan* gp) {
   const int kpl = (E + 31) / 32;
 #define RR(N)                                                                                   \
   if (kpl <= N) {                                                                              \
     route_remap_kernel<N><<<1, kThreads, 0, st>>>(logits, rows, E, k, S, Bw, Bs, L, plan,      \
-                                                  all_resident);                               \
+                                                  all_resident, gp);                           \
     return cudaGetLastError();                                                                 \
   }
   RR(1) RR(2) RR(4) RR(8) RR(16) RR(32)

@@ -1,0 +1,179 @@
+"""GPU parity for multi-row steps (grouped tcgen05 path) and the prefill bypass.
+
+Multi-row cached steps (2 <= M <= 16): every row's router ids equal the
+oracle's, the union's slot/hit/miss/eviction record equals the oracle LRU bit
+for bit (a union larger than S bypasses on the device), outputs are within the
+stated tolerance of the oracle, and a cached run is bit-identical to an
+all-resident run.  Bypass steps (M > 16): outputs within tolerance, the cache
+untouched (no fills, slot map unchanged).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workload
+from harness import (Banks, assert_within_tolerance, check_record_against_sim, make_cache,
+                     record_ids)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import hbm_slot_cache_gb300 as m
+    m.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def _dev(cfg, rows):
+    return (torch.empty((rows, cfg.experts), dtype=torch.float32, device="cuda"),
+            torch.empty((rows, cfg.hidden), dtype=torch.bfloat16, device="cuda"),
+            torch.empty((rows, cfg.hidden), dtype=torch.float32, device="cuda"))
+
+
+def _put(lg_d, x_d, lg, xb):
+    lg_d.copy_(torch.from_numpy(np.ascontiguousarray(lg)))
+    x_d.copy_(torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16))
+
+
+def _oracle_rows(orc, banks, cfg, lg, xb, rows):
+    w, s, g = banks.layer_arrays(0)
+    out = np.zeros((len(rows), cfg.hidden))
+    for i, m in enumerate(rows):
+        o, _, _, _ = orc.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
+                                  lg[m:m + 1], xb[m:m + 1])
+        out[i] = o[0]
+    return out
+
+
+def test_tiny_multirow_trace_outputs_and_device_bypass(lib, orc):
+    cfg = workload.CONFIGS["tiny"]
+    M, steps = 4, 40
+    banks = Banks(cfg)
+    cache = make_cache(cfg, banks, trace_capacity=steps)
+    rt = workload.Routing(cfg)
+    xs = workload.activations(cfg.seed, 0, steps, M, cfg.hidden)
+    sim = orc.LRUSim(cfg.experts, cfg.slots)
+    lg_d, x_d, out_d = _dev(cfg, M)
+    ids_ref, worst = [], {}
+    for t in range(steps):
+        lg = rt.step(M)
+        _put(lg_d, x_d, lg, xs[t])
+        cache.step(0, lg_d, x_d, out_d)
+        w, s, g = banks.layer_arrays(0)
+        ref, ids, _, _ = orc.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
+                                      lg, xs[t])
+        m = assert_within_tolerance(out_d.cpu().numpy(), ref, f"step {t}")
+        worst = {k: max(worst.get(k, 0.0), v) for k, v in m.items()}
+        ids_ref.append(ids)
+    print("tiny multirow worst", worst)
+    recs = cache.trace(0)
+    n_bypass = 0
+    for t, rec in enumerate(recs):
+        assert np.array_equal(record_ids(rec, M, cfg.top_k), ids_ref[t])
+        sr = sim.step(ids_ref[t].ravel())
+        check_record_against_sim(rec, sr, M, cfg.top_k)
+        n_bypass += sr["bypass"]
+    st = cache.stats(0)
+    assert st["misses"] == sim.stats["misses"] and st["hits"] == sim.stats["hits"]
+    assert st["bypass_calls"] == sim.stats["bypass"]
+    assert 0 < n_bypass < steps      # both the cached and the union > S path ran
+    cache.close()
+    banks.close()
+
+
+def test_glm_multirow_rounds(lib, orc):
+    """GLM shape, M = 16 rows per round (4 streams x 4 rows): trace on every step,
+    outputs on sampled rows, and cached == all-resident bitwise."""
+    cfg = workload.CONFIGS["multirow"]
+    M, steps = cfg.rows, 24
+    banks = Banks(cfg)
+    cache = make_cache(cfg, banks, layers=1, trace_capacity=steps)
+    rt = workload.Routing(cfg)
+    xs = workload.activations(cfg.seed, 0, steps, M, cfg.hidden)
+    sim = orc.LRUSim(cfg.experts, cfg.slots, check_list=False)
+    lg_d, x_d, out_d = _dev(cfg, M)
+    lgs, outs = [], []
+    for t in range(steps):
+        lg = rt.step()
+        lgs.append(lg)
+        _put(lg_d, x_d, lg, xs[t])
+        cache.step(0, lg_d, x_d, out_d)
+        outs.append(out_d.cpu().numpy().copy())
+        if t in (0, steps - 1):
+            rows = [0, 5, 15]
+            ref = _oracle_rows(orc, banks, cfg, lg, xs[t], rows)
+            m = assert_within_tolerance(outs[-1][rows], ref, f"step {t}")
+            print("glm multirow step", t, m)
+    recs = cache.trace(0)
+    unions = []
+    for t, rec in enumerate(recs):
+        ids = np.stack([orc.route(lgs[t][m], cfg.top_k)[0] for m in range(M)])
+        assert np.array_equal(record_ids(rec, M, cfg.top_k), ids)
+        check_record_against_sim(rec, sim.step(ids.ravel()), M, cfg.top_k)
+        unions.append(rec.n_union)
+    st = cache.stats(0)
+    assert st["picks"] == steps * M * cfg.top_k
+    # union fetch: far fewer experts than picks (shared draft ids, popular experts)
+    assert np.mean(unions) < 0.6 * M * cfg.top_k
+    cache.close()
+    # same steps, every expert resident: identical bits
+    full = make_cache(cfg, banks, layers=1, all_resident=True)
+    for t in range(steps):
+        _put(lg_d, x_d, lgs[t], xs[t])
+        full.step(0, lg_d, x_d, out_d)
+        got = out_d.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), outs[t].view(np.uint32)), f"step {t}"
+    full.close()
+    banks.close()
+
+
+@pytest.mark.parametrize("rows", [17, 64])
+def test_tiny_prefill_bypass(lib, orc, rows):
+    cfg = workload.CONFIGS["tiny"]
+    banks = Banks(cfg)
+    cache = make_cache(cfg, banks)
+    # warm the ring with a few decode steps, then bypass
+    lg1, x1, o1 = _dev(cfg, 1)
+    rt = workload.Routing(cfg)
+    xs = workload.activations(cfg.seed, 0, 6, 1, cfg.hidden)
+    for t in range(6):
+        _put(lg1, x1, rt.step(), xs[t])
+        cache.step(0, lg1, x1, o1)
+    before = cache.slot_map(0).copy()
+    st0 = cache.stats(0)
+    lg = workload.prefill_logits(cfg, 0, rows)
+    xb = workload.activations(cfg.seed, 1, 1, rows, cfg.hidden)[0]
+    lg_d, x_d, out_d = _dev(cfg, rows)
+    _put(lg_d, x_d, lg, xb)
+    cache.step(0, lg_d, x_d, out_d)
+    w, s, g = banks.layer_arrays(0)
+    ref, _, _, _ = orc.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, lg, xb)
+    print("tiny bypass", rows, assert_within_tolerance(out_d.cpu().numpy(), ref))
+    st1 = cache.stats(0)
+    assert st1["bypass_calls"] == st0["bypass_calls"] + 1
+    assert st1["misses"] == st0["misses"] and st1["bytes_copied"] == st0["bytes_copied"]
+    assert np.array_equal(cache.slot_map(0), before)
+    cache.close()
+    banks.close()
+
+
+def test_glm_prefill_bypass_sampled_rows(lib, orc):
+    cfg = workload.CONFIGS["prefill"]
+    rows = 64
+    banks = Banks(cfg)
+    cache = make_cache(cfg, banks, layers=1)
+    lg = workload.prefill_logits(cfg, 0, rows)
+    xb = workload.activations(cfg.seed, 0, 1, rows, cfg.hidden)[0]
+    lg_d, x_d, out_d = _dev(cfg, rows)
+    _put(lg_d, x_d, lg, xb)
+    cache.step(0, lg_d, x_d, out_d)
+    got = out_d.cpu().numpy()
+    sample = [0, 31, 63]
+    ref = _oracle_rows(orc, banks, cfg, lg, xb, sample)
+    print("glm bypass", assert_within_tolerance(got[sample], ref))
+    st = cache.stats(0)
+    assert st["bypass_calls"] == 1 and st["misses"] == 0
+    cache.close()
+    banks.close()
