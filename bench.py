@@ -213,7 +213,7 @@ def run_ours(args) -> None:
     cfg = workload.CONFIGS["glm"]
     E, H, k = cfg.experts, cfg.hidden, cfg.top_k
     banks = Banks(cfg)
-    cache = make_cache(cfg, banks, layers=1)
+    cache = make_cache(cfg, banks, layers=1, trace_capacity=200)
     prewarm = 64
     W, K = args.warmup, args.steps
     G = min(K, 200)  # steps in the final (event-instrumented) graph
@@ -234,7 +234,7 @@ def run_ours(args) -> None:
         steps_on(0, prewarm)                      # fill the ring to steady state (eager)
     stream.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(G)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(G)]
     for row in evs:
         for e in row:
             e.record(stream)                      # materialise the event handles
@@ -255,8 +255,13 @@ def run_ours(args) -> None:
     g_main = capture(t_w, t_w + K - G) if K > G else None
     g_ev = capture(t_w + K - G, t_w + K, with_events=True)
 
+    # Warm-up: the W-step graph, then one untimed pass of each timed graph (a
+    # graph's first launch uploads it; the timed replays are the second).
     with torch.cuda.stream(stream):
         g_warm.replay()
+        if g_main is not None:
+            g_main.replay()
+        g_ev.replay()
     stream.synchronize()
     s0 = cache.stats(0)
 
@@ -295,17 +300,25 @@ def run_ours(args) -> None:
     picks = s1["picks"] - s0["picks"]
     assert s1["error_flags"] == 0, s1
 
-    # per-kernel times over the instrumented graph (last G steps of the timed region)
-    names = ["route_remap", "miss_copy", "gemv_gateup", "gemv_down"]
-    per = {n: 0.0 for n in names}
-    for row in evs:
-        for i, n in enumerate(names):
-            per[n] += row[i].elapsed_time(row[i + 1])
-    per_launch_ms = {n: per[n] / G for n in names}
-    gap_ms = sum(evs[t][4].elapsed_time(evs[t + 1][0]) for t in range(G - 1)) / max(G - 1, 1)
+    # per-kernel times over the instrumented graph (last G steps of the timed
+    # region); per-step hit/miss counts from the cache's trace ring
+    recs = cache.trace(0)[-G:]
+    n_miss = np.array([r.n_miss for r in recs], np.float64)
+    n_hit = k - n_miss
+    ev_ms = np.array([[row[0].elapsed_time(row[i]) for i in range(8)] for row in evs])
+    t_route = ev_ms[:, 1]
+    t_copy = ev_ms[:, 2] - ev_ms[:, 1]
+    t_gu_miss = ev_ms[:, 3] - ev_ms[:, 2]
+    t_dn_miss = ev_ms[:, 4] - ev_ms[:, 3]
+    t_gu_hit = ev_ms[:, 5] - ev_ms[:, 1]
+    t_dn_hit = ev_ms[:, 6] - ev_ms[:, 5]
+    t_combine = ev_ms[:, 7] - np.maximum(ev_ms[:, 4], ev_ms[:, 6])
+    gap_ms = sum(evs[t][7].elapsed_time(evs[t + 1][0]) for t in range(G - 1)) / max(G - 1, 1)
     timing_split = {"ms_per_step_plain_graph": start.elapsed_time(mid) / (K - G) if K > G else None,
                     "ms_per_step_event_graph": mid.elapsed_time(end) / G,
-                    "ms_between_steps": gap_ms}
+                    "ms_between_steps": gap_ms,
+                    "ms_miss_path": float(np.mean(ev_ms[:, 4] - ev_ms[:, 1])),
+                    "ms_hit_path": float(np.mean(ev_ms[:, 6] - ev_ms[:, 1]))}
 
     # host-link bandwidth probed in the same session
     from hbm_slot_cache_gb300 import HostBank, moe_probe_host_link
@@ -329,35 +342,45 @@ def run_ours(args) -> None:
     t_roof_s = hbm_bytes / (hbm_peak * 1e9) + link_bytes / (link_peak * 1e9)
     path_frac = t_roof_s / (ms_step * 1e-3)
 
-    # kernel rooflines (per launch, averaged over the instrumented steps)
-    gemv_bytes_gu = k * (2 * cfg.inter * (H // 2 + H // 16))
-    gemv_bytes_dn = k * (H * (cfg.inter // 2 + cfg.inter // 16))
-    ev_misses = None
-    kern = {}
-    for n, nbytes, peak, unit, bound in (
-            ("gemv_gateup", gemv_bytes_gu, hbm_peak, "GB/s", "hbm"),
-            ("gemv_down", gemv_bytes_dn, hbm_peak, "GB/s", "hbm")):
-        t = per_launch_ms[n] * 1e-3
-        kern[n] = {"bound": bound, "achieved": nbytes / t / 1e9, "peak": peak, "unit": unit,
-                   "frac": nbytes / t / 1e9 / peak, "traffic": _traffic(n),
-                   "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": per_launch_ms[n]}
-    # the miss copy: bytes moved per launch over the link, against the link probe
-    copy_bytes = miss_per_step * Bexp
-    t = per_launch_ms["miss_copy"] * 1e-3
-    kern["miss_copy"] = {"bound": "host-link", "achieved": copy_bytes / t / 1e9 if t else None,
-                         "peak": link_peak, "unit": "GB/s",
-                         "frac": copy_bytes / t / 1e9 / link_peak if t else None,
-                         "traffic": _traffic("miss_copy"),
-                         "algorithmic_bytes_per_launch": copy_bytes,
-                         "ms_per_launch": per_launch_ms["miss_copy"],
-                         "note": "bytes = the timed region's mean miss bytes per step"}
-    kern["route_remap"] = {"ms_per_launch": per_launch_ms["route_remap"]}
-    dom = max(("gemv_gateup", "gemv_down", "miss_copy"), key=lambda n: per_launch_ms[n])
+    # kernel rooflines: algorithmic bytes of the launch / its measured time,
+    # summed over the instrumented steps
+    gu_pick = 2 * cfg.inter * (H // 2 + H // 16)   # gate/up bytes of one pick
+    dn_pick = H * (cfg.inter // 2 + cfg.inter // 16)
+    def entry(bytes_total, ms_total, peak, bound, launches):
+        ach = bytes_total / (ms_total * 1e-3) / 1e9 if ms_total > 0 else None
+        return {"bound": bound, "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak if ach else None,
+                "algorithmic_bytes_per_launch": bytes_total / launches,
+                "ms_per_launch": ms_total / launches}
+    hm = n_miss > 0
+    kern = {
+        "gemv_gateup[resident picks]": entry(float((n_hit * gu_pick).sum()), float(t_gu_hit.sum()),
+                                             hbm_peak, "hbm", G),
+        "gemv_down[resident picks]": entry(float((n_hit * dn_pick).sum()), float(t_dn_hit.sum()),
+                                           hbm_peak, "hbm", G),
+        "gemv_gateup[missed picks]": entry(float((n_miss * gu_pick).sum()),
+                                           float(t_gu_miss[hm].sum()), hbm_peak, "hbm",
+                                           max(int(hm.sum()), 1)),
+        "gemv_down[missed picks]": entry(float((n_miss * dn_pick).sum()),
+                                         float(t_dn_miss[hm].sum()), hbm_peak, "hbm",
+                                         max(int(hm.sum()), 1)),
+        "miss_copy": entry(float((n_miss * Bexp).sum()), float(t_copy[hm].sum()), link_peak,
+                           "host-link", max(int(hm.sum()), 1)),
+        "route_remap": {"ms_per_launch": float(t_route.mean())},
+        "combine": {"ms_per_launch": float(t_combine.mean())},
+    }
+    for n in kern:
+        if "gemv" in n:
+            kern[n]["traffic"] = _traffic(n.split("[")[0])
+    kern["miss_copy"]["traffic"] = None
+    kern["miss_copy"]["note"] = "steps with at least one miss; bytes over the host link"
+    share = {n: v["ms_per_launch"] * (G if "resident" in n or n in ("route_remap", "combine")
+                                      else max(int(hm.sum()), 1)) for n, v in kern.items()}
+    dom = max(share, key=share.get)
     roofline = dict(kern[dom])
     roofline["kernel"] = dom
-    roofline["peak_source"] = (hbm_src if roofline["bound"] == "hbm"
+    roofline["peak_source"] = (hbm_src if roofline.get("bound") == "hbm"
                                else "moe_probe_host_link, same session (best of SM copy / cudaMemcpyAsync)")
-    del ev_misses
 
     # end to end through the public API: pinned host inputs -> step -> host output
     Ke = min(K, 1000)
@@ -411,7 +434,7 @@ def run_ours(args) -> None:
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": E * 4 + H * 2,
                     "d2h_bytes_per_step": H * 4, "steps": Ke},
-            "gpu_launches": K * 4, "clocks": clocks,
+            "gpu_launches": K * 7, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     cache.close()

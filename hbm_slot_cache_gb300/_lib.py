@@ -180,12 +180,17 @@ def moe_cache_destroy(h: int) -> None:
     _check(lib().moe_cache_destroy(h), "moe_cache_destroy")
 
 
+MOE_TIMING_EVENTS = 8
+
+
 def moe_cache_set_timing_events(h: int, events) -> None:
-    """events: 5 cudaEvent_t handles (ints), or None to stop recording."""
+    """events: MOE_TIMING_EVENTS cudaEvent_t handles (ints), or None to stop recording."""
     if events is None:
         _check(lib().moe_cache_set_timing_events(h, None), "moe_cache_set_timing_events")
         return
-    arr = (ctypes.c_void_p * 5)(*[int(e) for e in events])
+    if len(events) != MOE_TIMING_EVENTS:
+        raise ValueError(f"need {MOE_TIMING_EVENTS} events")
+    arr = (ctypes.c_void_p * MOE_TIMING_EVENTS)(*[int(e) for e in events])
     _check(lib().moe_cache_set_timing_events(h, ctypes.cast(arr, ctypes.c_void_p)),
            "moe_cache_set_timing_events")
 

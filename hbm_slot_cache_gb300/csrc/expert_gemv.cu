@@ -21,13 +21,17 @@
 // sums: reduce-scatter butterfly of shuffles, then a fixed-order sum across
 // warps.  The epilogue writes h = silu(gate) * up in fp32.
 //
-// down + combine: persistent grid, 1 CTA per SM.  A thread owns one
-// (pick j, 32-element block of I) pair and keeps gscale_j * w_j * h_j for it in
-// registers for the whole kernel; a unit is R2 output rows of all k picks, so
-// out[row] = sum over all threads of their partial dot products -- the router
-// weights are applied before the down matvec, the combine is the fixed-order
-// reduction, and nothing else is written.  Every order is fixed, so a cached
-// step and an all-resident step give the same bits.
+// down: persistent grid, 1 CTA per SM.  A thread owns one (pick j, 32-element
+// block of I) pair and keeps gscale_j * w_j * h_j for it in registers for the
+// whole kernel; a unit is R2 output rows of the launch's picks, reduced per
+// pick (shuffles within the pick's lanes, then its warps) into the weighted
+// output y'_j.  combine: out = sum_j y'_j in rank order.
+//
+// Both GEMVs take a subset of the step's picks (the resident ones, the missed
+// ones, or all), so a step can run the resident picks while the missed picks'
+// bytes are still being copied.  A pick's computation and reduction order do
+// not depend on the subset it runs in, so a cached step and an all-resident
+// step give the same bits.
 #include "internal.cuh"
 
 namespace moe {
@@ -176,7 +180,8 @@ __device__ __forceinline__ int units_of_block(int nunits) {
 template <int RPT, bool WARP_RED>
 __global__ void __launch_bounds__(kGateUpThreads, 2)
 gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
-                   float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags) {
+                   float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
+                   int subset) {
   constexpr int V = 2 * RPT;
   constexpr int R = kGateUpRows;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -188,12 +193,21 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   const int stage_bytes = 2 * cb + 2 * sb;
   Stages S = carve(smem, NS, stage_bytes);
 
+  // the picks this launch covers
+  int pbeg = 0, pcnt = plan->npicks;
+  if (subset == kPicksHit) pcnt = plan->n_hit;
+  if (subset == kPicksMiss) {
+    pbeg = plan->n_hit;
+    pcnt = plan->npicks - plan->n_hit;
+  }
+  auto pick_of = [&](int jl) { return subset == kPicksAll ? jl : plan->order[pbeg + jl]; };
   const int upp = I / R;  // units per pick
-  const int nunits = plan->npicks * upp;
+  const int nunits = pcnt * upp;
   const int my_units = units_of_block(nunits);
 
   auto issue = [&](int unit, int stage) {
-    const int j = unit / upp, rb = unit - j * upp;
+    const int jl = unit / upp, rb = unit - jl * upp;
+    const int j = pick_of(jl);
     const uint8_t* w = plan->wptr[j];
     const uint8_t* s = plan->sptr[j];
     uint8_t* dst = S.base + (size_t)stage * stage_bytes;
@@ -270,7 +284,8 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
     if (tid < RL * RPT) {
       const int gg = tid / RPT, q = tid - gg * RPT;
-      const int j = unit / upp, rb = unit - j * upp;
+      const int jl = unit / upp, rb = unit - jl * upp;
+      const int j = pick_of(jl);
       const float gate = plan->gs[j][0] * xup * sum_partial<V, WARP_RED>(S.red, gg, q, C);
       const float up = plan->gs[j][1] * xup * sum_partial<V, WARP_RED>(S.red, gg, RPT + q, C);
       const float h = gate / (1.0f + expf(-gate)) * up;
@@ -284,28 +299,47 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
 template <int R2>
 __global__ void __launch_bounds__(kDownThreads, 1)
 gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
-                 float* __restrict__ out, int H, int I, int NS, uint32_t* flags) {
+                 float* __restrict__ ypart, int H, int I, int NS, uint32_t* flags, int subset) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int C = I / 32;
-  const int k = plan->npicks;
+  const int C = I / 32;  // 32-element blocks per h row; C divides 32 or is a multiple of it
+  const int kmax = plan->npicks;
+  int pbeg = 0, pcnt = kmax;
+  if (subset == kPicksHit) pcnt = plan->n_hit;
+  if (subset == kPicksMiss) {
+    pbeg = plan->n_hit;
+    pcnt = kmax - plan->n_hit;
+  }
+  auto pick_of = [&](int jl) { return subset == kPicksAll ? jl : plan->order[pbeg + jl]; };
+  // Few picks: spread each unit's rows over RL row groups so the CTA stays
+  // busy (thread = (row group g, pick jl, 32-block c)); RL * pcnt <= kmax keeps
+  // a stage within the room sized for all picks.
+  int RL = 1;
+  while (pcnt > 0 && 2 * RL * pcnt <= kmax && 2 * RL * pcnt * C <= (int)blockDim.x) RL *= 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool active = tid < k * C;
-  const int j = active ? tid / C : 0, c = active ? tid - j * C : 0;
-  const int cb = R2 * I / 2, sb = R2 * I / 16;  // per pick
-  const int stage_bytes = k * (cb + sb);
-  Stages S = carve(smem, NS, stage_bytes);
+  const int per_g = pcnt * C;
+  const bool active = tid < RL * per_g;
+  const int g = active ? tid / per_g : 0;
+  const int rem = tid - g * per_g;
+  const int jl = active ? rem / C : 0, c = active ? rem - jl * C : 0;
+  const int j = active ? pick_of(jl) : 0;
+  const int UR = R2 * RL;                           // rows per unit
+  const int cb = UR * I / 2, sb = UR * I / 16;      // per pick
+  const int stage_stride = kmax * R2 * (I / 2 + I / 16);
+  const int stage_bytes = pcnt * (cb + sb);
+  Stages S = carve(smem, NS, stage_stride);
 
-  const int nunits = H / R2;
+  const int nunits = pcnt > 0 ? H / UR : 0;
   const int my_units = units_of_block(nunits);
   const size_t w2_codes = (size_t)I * H;        // 2I rows of H/2 bytes precede W2
   const size_t w2_scales = (size_t)I * H / 8;   // 2I rows of H/16 bytes
 
   auto issue = [&](int unit, int stage) {
-    uint8_t* dst = S.base + (size_t)stage * stage_bytes;
+    uint8_t* dst = S.base + (size_t)stage * stage_stride;
     mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
-    for (int jj = 0; jj < k; ++jj) {
-      bulk_g2s(dst + jj * cb, plan->wptr[jj] + w2_codes + (size_t)unit * cb, cb, &S.full[stage]);
-      bulk_g2s(dst + k * cb + jj * sb, plan->sptr[jj] + w2_scales + (size_t)unit * sb, sb,
+    for (int q = 0; q < pcnt; ++q) {
+      const int jj = pick_of(q);
+      bulk_g2s(dst + q * cb, plan->wptr[jj] + w2_codes + (size_t)unit * cb, cb, &S.full[stage]);
+      bulk_g2s(dst + pcnt * cb + q * sb, plan->sptr[jj] + w2_scales + (size_t)unit * sb, sb,
                &S.full[stage]);
     }
   };
@@ -343,30 +377,56 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
       drain_fills(S, i, NS, my_units, flags);
       return;
     }
-    const uint8_t* st = S.base + (size_t)stage * stage_bytes;
+    const uint8_t* st = S.base + (size_t)stage * stage_stride;
     float a[R2];
 #pragma unroll
     for (int r = 0; r < R2; ++r) {
       a[r] = 0.f;
       if (active) {
-        const uint4 cw = *reinterpret_cast<const uint4*>(st + j * cb + r * (I / 2) + c * 16);
-        const uint32_t s2 = *reinterpret_cast<const uint16_t*>(st + k * cb + j * sb +
-                                                               r * (I / 16) + c * 2);
+        const int row = g + RL * r;
+        const uint4 cw = *reinterpret_cast<const uint4*>(st + jl * cb + row * (I / 2) + c * 16);
+        const uint32_t s2 = *reinterpret_cast<const uint16_t*>(st + pcnt * cb + jl * sb +
+                                                               row * (I / 16) + c * 2);
         const float2 sc = e4m3x2_to_float2(s2);
         a[r] = dot16_f32(cw.x, cw.y, hv) * sc.x + dot16_f32(cw.z, cw.w, hv + 16) * sc.y;
       }
     }
-    const float s = warp_reduce_scatter<R2>(a, lane);
-    constexpr int sh = 5 - ilog2(R2);
-    if ((lane & ((1 << sh) - 1)) == 0) S.red[warp * R2 + (lane >> sh)] = s;
-    __syncthreads();
-    if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
-    if (tid < R2) {
-      float acc = 0.f;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) acc += S.red[w * R2 + tid];
-      out[unit * R2 + tid] = acc;
+    if (C >= 32) {
+      // a (row group, pick) spans C/32 whole warps: butterfly per warp, then its warps
+      const float s = warp_reduce_scatter<R2>(a, lane);
+      constexpr int sh = 5 - ilog2(R2);
+      if ((lane & ((1 << sh) - 1)) == 0) S.red[warp * R2 + (lane >> sh)] = s;
+      __syncthreads();
+      if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
+      if (tid < RL * pcnt * R2) {
+        const int gq = tid / R2, r = tid - gq * R2;  // gq = g * pcnt + q
+        const int gg = gq / pcnt, q = gq - gg * pcnt, wp = C / 32;
+        float y = 0.f;
+        for (int w = 0; w < wp; ++w) y += S.red[(gq * wp + w) * R2 + r];
+        ypart[(size_t)pick_of(q) * H + unit * UR + gg + RL * r] = y;
+      }
+    } else {
+      // several (row group, pick) pairs per warp: reduce within each aligned group of C lanes
+#pragma unroll
+      for (int r = 0; r < R2; ++r)
+        for (int o = C / 2; o > 0; o >>= 1) a[r] += __shfl_xor_sync(0xFFFFFFFFu, a[r], o);
+      if (active && c == 0)
+#pragma unroll
+        for (int r = 0; r < R2; ++r) ypart[(size_t)j * H + unit * UR + g + RL * r] = a[r];
+      __syncthreads();
+      if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
     }
   }
+}
+
+// out[o] = sum_j y'_j[o], j in rank order.
+__global__ void gemv_combine_kernel(const float* __restrict__ ypart, float* __restrict__ out, int H,
+                                    int k) {
+  const int o = blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= H) return;
+  float acc = 0.f;
+  for (int j = 0; j < k; ++j) acc += ypart[(size_t)j * H + o];
+  out[o] = acc;
 }
 
 // ------------------------------------------------------------- dispatch
@@ -406,23 +466,27 @@ GateUpShape gateup_shape(int H) {
 
 template <int RPT, bool WR>
 cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
-                       const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags) {
+                       const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
+                       int subset) {
   auto kern = gemv_gateup_kernel<RPT, WR>;
   static int smem_set = 0;  // raise the opt-in limit once per size (not a stream operation)
   if (s.smem > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
+    if (e == cudaSuccess) e = prefer_max_shared(kern);
     if (e != cudaSuccess) return e;
     smem_set = s.smem;
   }
-  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags);
+  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool gemv_supported(int H, int I, int k) {
+  const int C = I / 32;  // a pick's threads in the down kernel: whole warps or part of one
   return H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM &&
-         k * (I / 32) <= kDownThreads && H / 16 <= kGateUpThreads * kGateUpRows;
+         k * C <= kDownThreads && (C % 32 == 0 || 32 % C == 0) &&
+         H / 16 <= kGateUpThreads * kGateUpRows;
 }
 
 int gemv_down_tile_rows(int H, int I) {
@@ -432,22 +496,23 @@ int gemv_down_tile_rows(int H, int I) {
 }
 
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
-                               int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms) {
+                               int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
+                               int subset) {
   const GateUpShape s = gateup_shape(H);
   if (s.NS < 2 || s.NT > kGateUpThreads) return cudaErrorInvalidConfiguration;
   const int nunits = k * (I / kGateUpRows);
   const int grid = nunits < 2 * num_sms ? nunits : 2 * num_sms;
-#define GU(N)                                                                            \
-  if (s.RPT == N)                                                                        \
-    return s.warp_red ? run_gateup<N, true>(st, grid, s, plan, x, ws.hbuf, H, I, flags) \
-                      : run_gateup<N, false>(st, grid, s, plan, x, ws.hbuf, H, I, flags);
+#define GU(N)                                                                                    \
+  if (s.RPT == N)                                                                                \
+    return s.warp_red ? run_gateup<N, true>(st, grid, s, plan, x, ws.hbuf, H, I, flags, subset) \
+                      : run_gateup<N, false>(st, grid, s, plan, x, ws.hbuf, H, I, flags, subset);
   GU(1) GU(2) GU(4)
 #undef GU
   return cudaErrorInvalidConfiguration;
 }
 
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
-                             const GemvWorkspace& ws, float* out, uint32_t* flags, int num_sms) {
+                             const GemvWorkspace& ws, uint32_t* flags, int num_sms, int subset) {
   constexpr int R2 = kDownRows;
   if (k * (I / 32) > kDownThreads) return cudaErrorInvalidConfiguration;
   const int stage = k * (R2 * I / 2 + R2 * I / 16);
@@ -463,10 +528,22 @@ cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, in
   static int smem_set = 0;
   if (smem > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = prefer_max_shared(kern);
     if (e != cudaSuccess) return e;
     smem_set = smem;
   }
-  kern<<<grid, nt, smem, st>>>(plan, ws.hbuf, out, H, I, ns, flags);
+  kern<<<grid, nt, smem, st>>>(plan, ws.hbuf, ws.ypart, H, I, ns, flags, subset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_combine(cudaStream_t st, const float* ypart, float* out, int H, int k) {
+  static bool once = false;
+  if (!once) {
+    cudaError_t e = prefer_max_shared(gemv_combine_kernel);
+    if (e != cudaSuccess) return e;
+    once = true;
+  }
+  gemv_combine_kernel<<<(H + 255) / 256, 256, 0, st>>>(ypart, out, H, k);
   return cudaGetLastError();
 }
 

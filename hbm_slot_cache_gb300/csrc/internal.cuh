@@ -41,7 +41,10 @@ struct LayerDev {
 // The per-step plan written by the remap kernel and read by the copy and
 // expert kernels.  One per handle: steps run in order on one stream.
 struct Plan {
-  int32_t rows, npicks, n_union, n_miss, bypass, pad[3];
+  int32_t rows, npicks, n_union, n_miss, bypass;
+  int32_t n_hit;   // picks resident at step start (one-row steps)
+  int32_t pad[2];
+  int32_t order[MOE_MAX_PICKS];  // picks, hits first, each part in rank order
   int32_t ids[MOE_MAX_PICKS];
   float wts[MOE_MAX_PICKS];
   int32_t miss_e[MOE_MAX_PICKS];
@@ -117,13 +120,30 @@ struct GemvWorkspace {
   uint32_t* tile_cnt; // [H / down rows per tile]
   uint32_t* flags;    // error flags word for waits (per layer stats flags)
 };
+// Pick subsets of a one-row step: the picks resident at step start, the
+// missed picks (after their copy), or all picks.
+enum PickSubset { kPicksHit = 0, kPicksMiss = 1, kPicksAll = 2 };
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
-                               int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms);
+                               int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
+                               int subset);
+// y'_j = gscale_j * w_j * (W2_j h_j) for the subset's picks -> ws.ypart [k][H]
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
-                             const GemvWorkspace& ws, float* out, uint32_t* flags, int num_sms);
+                             const GemvWorkspace& ws, uint32_t* flags, int num_sms, int subset);
+// out[o] = sum_j y'_j[o], j in rank order
+cudaError_t launch_gemv_combine(cudaStream_t st, const float* ypart, float* out, int H, int k);
 int gemv_down_tile_rows(int H, int I);
 // Shapes the M = 1 expert kernels handle (top_k * inter <= 16384, dims % 128 == 0).
 bool gemv_supported(int H, int I, int k);
+
+// Every kernel of a step asks for the maximum shared-memory carveout, so an SM
+// never has to drain to re-partition L1/shared memory between kernels, and the
+// step's concurrent kernels (miss copy beside the resident picks' GEMVs) can
+// share SMs.  Call once per kernel function before its first launch.
+template <class F>
+inline cudaError_t prefer_max_shared(F* func) {
+  return cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
 
 // ------------------------------------------------------- device helpers
 

@@ -6,16 +6,18 @@
 // One launch covers all of a step's misses (the pages used four launches per
 // layer: w13 rows, w2 rows and two scale tensors).  The grid is fixed, so the
 // launch is graph-capturable; the miss count is read on the device and a step
-// without misses exits at once.  Work is cut into 16 KB chunks (256 threads x
-// 4 x 16 B); each thread keeps 4 independent 16-byte host loads in flight
-// before storing them.
+// without misses exits at once.  Work is cut into 32 KB chunks (256 threads x
+// 8 x 16 B); each thread keeps 8 independent 16-byte host loads in flight
+// before storing them, so a grid of about a quarter of the SMs keeps ~1 MB in
+// flight, enough to fill the host link, and leaves the other SMs to the
+// resident experts' kernels that run beside it.
 #include "internal.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 constexpr long long kChunk = (long long)kThreads * kUnroll * 16;
 
 __device__ __forceinline__ void copy_chunk(const uint8_t* __restrict__ src,
@@ -65,6 +67,12 @@ link_probe_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, lo
 cudaError_t launch_miss_copy(cudaStream_t st, const Plan* plan, const uint8_t* host_w,
                              const uint8_t* host_s, uint8_t* slot_w, uint8_t* slot_s,
                              long long Bw, long long Bs, int grid) {
+  static bool once = false;
+  if (!once) {
+    cudaError_t e = prefer_max_shared(miss_copy_kernel);
+    if (e != cudaSuccess) return e;
+    once = true;
+  }
   miss_copy_kernel<<<grid, kThreads, 0, st>>>(plan, host_w, host_s, slot_w, slot_s, Bw, Bs);
   return cudaGetLastError();
 }

@@ -44,8 +44,11 @@ struct moe_cache {
   std::vector<void*> extra;  // further device allocations, freed with the handle
   // host backing (device-visible addresses)
   std::vector<const uint8_t*> host_w, host_s;
+  // one-row steps fork the miss path onto a second stream
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
   // optional per-kernel timing events (caller-owned)
-  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t ev[MOE_TIMING_EVENTS] = {};
   bool timing = false;
 };
 
@@ -75,6 +78,11 @@ void free_all(moe_cache* h) {
   cudaFree(h->gemv.tile_cnt);
   for (void* p : h->extra) cudaFree(p);
   h->extra.clear();
+  if (h->fork) cudaEventDestroy(h->fork);
+  if (h->join) cudaEventDestroy(h->join);
+  if (h->side) cudaStreamDestroy(h->side);
+  h->fork = h->join = nullptr;
+  h->side = nullptr;
 }
 
 // Group plan, quantised-activation buffers and bypass ids for steps of up to
@@ -261,6 +269,9 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
             dalloc(&h->gemv.tile_cnt, (size_t)(hidden / gemv_down_tile_rows(hidden, inter) + 1)) ==
                 cudaSuccess;
   ok = ok && alloc_multirow(h);
+  ok = ok && cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_all(h);
@@ -296,32 +307,52 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   if (rows > 1 && !mma_supported(h->H, h->I)) return MOE_ERR_UNSUPPORTED;
   const LayerDev L = layer_dev(h, layer);
   // inside a capture an event record must be an external node to be replayed
-  auto mark = [&](int i) -> cudaError_t {
+  auto mark = [&](int i, cudaStream_t s) -> cudaError_t {
     if (!h->timing) return cudaSuccess;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
     if (e != cudaSuccess) return e;
     return cudaEventRecordWithFlags(
-        h->ev[i], st, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u);
+        h->ev[i], s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u);
   };
   uint32_t* flags = &(h->stats + layer)->flags;
-  cudaError_t e = mark(0);
+  cudaError_t e = mark(0, st);
   if (rows == 1) {
-    // one row: route/remap, miss copy, GEMV gate/up + SwiGLU, GEMV down + combine
+    // One row.  After route/remap the missed picks take a second stream: copy
+    // host -> slot, then their gate/up and down; meanwhile the resident picks'
+    // gate/up and down run on the caller's stream, so the hit experts' HBM
+    // reads overlap the host-link copy.  Each pick's weighted output y'_j is
+    // computed the same way whichever path it takes, and the combine adds them
+    // in rank order, so the result does not depend on the hit/miss split.
     if (e == cudaSuccess)
       e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, nullptr);
-    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = mark(1, st);
+    if (e == cudaSuccess) e = cudaEventRecord(h->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork, 0);
     if (e == cudaSuccess && !h->opts.all_resident)
-      e = launch_miss_copy(st, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
-                           2 * h->num_sms);
-    if (e == cudaSuccess) e = mark(2);
+      e = launch_miss_copy(h->side, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw,
+                           h->Bs, h->num_sms / 4 > 8 ? h->num_sms / 4 : 8);
+    if (e == cudaSuccess) e = mark(2, h->side);
     if (e == cudaSuccess)
-      e = launch_gemv_gateup(st, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms);
-    if (e == cudaSuccess) e = mark(3);
+      e = launch_gemv_gateup(h->side, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
+                             kPicksMiss);
+    if (e == cudaSuccess) e = mark(3, h->side);
     if (e == cudaSuccess)
-      e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, out, flags, h->num_sms);
-    if (e == cudaSuccess) e = mark(4);
+      e = launch_gemv_down(h->side, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
+                           kPicksMiss);
+    if (e == cudaSuccess) e = mark(4, h->side);
+    if (e == cudaSuccess) e = cudaEventRecord(h->join, h->side);
+    if (e == cudaSuccess)
+      e = launch_gemv_gateup(st, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
+                             kPicksHit);
+    if (e == cudaSuccess) e = mark(5, st);
+    if (e == cudaSuccess)
+      e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms, kPicksHit);
+    if (e == cudaSuccess) e = mark(6, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->join, 0);
+    if (e == cudaSuccess) e = launch_gemv_combine(st, h->gemv.ypart, out, h->H, h->k);
+    if (e == cudaSuccess) e = mark(7, st);
     return cuda_err(e);
   }
   // several rows: experts grouped, each read once for all its rows (tensor cores)
@@ -330,7 +361,7 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     if (e == cudaSuccess)
       e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, h->gp);
-    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess && !h->opts.all_resident)
       e = launch_miss_copy(st, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
                            2 * h->num_sms);
@@ -338,18 +369,21 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     // prefill bypass: experts read from host memory, cache untouched
     if (e == cudaSuccess)
       e = launch_route_rows(st, router_logits, rows, h->E, h->k, h->ids_ws, h->gp, L, h->Bw, h->Bs);
-    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = mark(1, st);
   }
-  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess) e = mark(2, st);
   if (e == cudaSuccess) e = launch_quantize_rows(st, x, true, rows, h->H, h->xq);
   if (e == cudaSuccess)
     e = launch_grouped_mma(st, h->gp, npicks, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf, flags);
-  if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess) e = mark(3, st);
+  if (e == cudaSuccess) e = mark(5, st);
   if (e == cudaSuccess) e = launch_quantize_rows(st, h->gemv.hbuf, false, npicks, h->I, h->hq);
   if (e == cudaSuccess)
     e = launch_grouped_mma(st, h->gp, npicks, false, h->H, h->I, h->k, h->hq, h->gemv.ypart, flags);
+  if (e == cudaSuccess) e = mark(4, st);
+  if (e == cudaSuccess) e = mark(6, st);
   if (e == cudaSuccess) e = launch_combine(st, h->gp, h->gemv.ypart, out, rows, h->H, h->k);
-  if (e == cudaSuccess) e = mark(4);
+  if (e == cudaSuccess) e = mark(7, st);
   return cuda_err(e);
 }
 
@@ -437,7 +471,7 @@ int moe_cache_set_timing_events(moe_cache_t* h, void* const* events) {
     h->timing = false;
     return MOE_OK;
   }
-  for (int i = 0; i < 5; ++i) {
+  for (int i = 0; i < MOE_TIMING_EVENTS; ++i) {
     if (!events[i]) return MOE_ERR_ARG;
     h->ev[i] = static_cast<cudaEvent_t>(events[i]);
   }

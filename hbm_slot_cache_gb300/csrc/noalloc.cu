@@ -146,8 +146,9 @@ extern "C" int moe_expert_pass_noalloc(int k, int hidden, int inter, const void*
   noalloc_plan_kernel<<<1, 64, 0, st>>>(a, plan, ws.tile_cnt, (int)kTileWords);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = launch_gemv_gateup(st, plan, x, hidden, inter, k, ws, flags, d->num_sms);
+    e = launch_gemv_gateup(st, plan, x, hidden, inter, k, ws, flags, d->num_sms, kPicksAll);
   if (e == cudaSuccess)
-    e = launch_gemv_down(st, plan, hidden, inter, k, ws, out, flags, d->num_sms);
+    e = launch_gemv_down(st, plan, hidden, inter, k, ws, flags, d->num_sms, kPicksAll);
+  if (e == cudaSuccess) e = launch_gemv_combine(st, ws.ypart, out, hidden, k);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

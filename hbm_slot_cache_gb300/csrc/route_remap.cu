@@ -303,6 +303,14 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     plan->n_union = n_union;
     plan->n_miss = n_miss;
     plan->bypass = 0;
+    if (rows == 1) {  // hits first, then misses, each in rank order
+      int nh = 0;
+      for (int p = 0; p < npicks; ++p)
+        if (s_hit[p]) plan->order[nh++] = p;
+      plan->n_hit = nh;
+      for (int p = 0; p < npicks; ++p)
+        if (!s_hit[p]) plan->order[nh++] = p;
+    }
     *L.clock = t;
     st->steps += 1;
     st->picks += (unsigned long long)npicks;
@@ -330,6 +338,12 @@ cudaError_t launch_route_remap(cudaStream_t st, const float* logits, int rows, i
   const int kpl = (E + 31) / 32;
 #define RR(N)                                                                                   \
   if (kpl <= N) {                                                                              \
+    static bool once = false;                                                                  \
+    if (!once) {                                                                               \
+      cudaError_t e = prefer_max_shared(route_remap_kernel<N>);                                \
+      if (e != cudaSuccess) return e;                                                          \
+      once = true;                                                                             \
+    }                                                                                          \
     route_remap_kernel<N><<<1, kThreads, 0, st>>>(logits, rows, E, k, S, Bw, Bs, L, plan,      \
                                                   all_resident, gp);                           \
     return cudaGetLastError();                                                                 \

@@ -198,12 +198,19 @@ int moe_host_free(void* p);
 int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int method,
                         int iters, double* best_gbps);
 
-/* Per-kernel timing hook: events points at 5 cudaEvent_t (created by the
- * caller).  While set, every moe_cache_step records events[0] before its first
- * kernel and events[1..4] after route/remap, miss copy, gate/up and
- * down/combine, on the step's stream (also inside a CUDA-graph capture, where
- * they become event-record nodes).  NULL stops recording.  The library does
- * not own the events. */
+/* Per-kernel timing hook: events points at MOE_TIMING_EVENTS cudaEvent_t
+ * (created by the caller, timing enabled).  While set, every moe_cache_step
+ * records them (also inside a CUDA-graph capture, where they become
+ * event-record nodes):
+ *   0 before route/remap, 1 after it (caller's stream);
+ *   2 after the miss copy, 3 after the missed picks' gate/up, 4 after their
+ *     down (one-row steps: the library's second stream; multi-row steps: 3 and
+ *     4 after the grouped gate/up and down on the caller's stream);
+ *   5 after the resident picks' gate/up, 6 after their down (one-row steps;
+ *     multi-row: same points as 3 and 4);
+ *   7 end of the step (after the combine).
+ * NULL stops recording.  The library does not own the events. */
+#define MOE_TIMING_EVENTS 8
 int moe_cache_set_timing_events(moe_cache_t* h, void* const* events);
 
 /* ------------------------------------------------------ no-allocation pass */
