@@ -1,6 +1,5 @@
 // Decode expert kernels for one row (M = 1): the grouped NVFP4
-// gate/up -> SwiGLU -> down pass over the k routed experts, reading only the
-// bytes the plan points at (a slot, or host memory on a bypassed step).
+// gate/up -> SwiGLU -> down pass over the k routed experts.
 // ("GLM 5.3 Testing: HBM Expert Allocation", "What the slot cache is": the
 // expert kernel reads the same bytes as in the all-HBM case, only the index
 // changes; "A correction first": 0.041 ms for the all-HBM layer under graphs.)
@@ -10,10 +9,9 @@
 // are built around the cheapest exact decode: the hardware E2M1x2 -> f16x2
 // conversion, then products into fp32 accumulators.
 //
-// gate/up + SwiGLU: persistent grid, 2 CTAs per SM.  A unit is R row pairs of
-// one pick (gate rows r.., up rows I+r..), contiguous in the slot; its code
-// and scale rows are staged into shared memory by 1-D TMA bulk copies
-// (cp.async.bulk on an mbarrier), NS units in flight per CTA.  A thread owns a
+// gate/up + SwiGLU: persistent grid.  A unit is R row pairs of one pick (gate
+// rows r.., up rows I+r..), contiguous in the expert's bytes; its code and
+// scale rows are staged into shared memory NS units ahead.  A thread owns a
 // 16-element block of every row it touches and keeps the matching 16
 // activations in registers as f16 (the row is prescaled by a power of two so
 // no activation overflows f16; bf16 -> f16 is then exact apart from f16
@@ -21,17 +19,32 @@
 // sums: reduce-scatter butterfly of shuffles, then a fixed-order sum across
 // warps.  The epilogue writes h = silu(gate) * up in fp32.
 //
-// down: persistent grid, 1 CTA per SM.  A thread owns one (pick j, 32-element
-// block of I) pair and keeps gscale_j * w_j * h_j for it in registers for the
-// whole kernel; a unit is R2 output rows of the launch's picks, reduced per
-// pick (shuffles within the pick's lanes, then its warps) into the weighted
-// output y'_j.  combine: out = sum_j y'_j in rank order.
+// down: persistent grid.  A thread owns one (pick j, 32-element block of I)
+// pair and keeps gscale_j * w_j * h_j for it in registers for the whole
+// kernel; a unit is a few output rows of the launch's picks, reduced per pick
+// (shuffles within the pick's lanes, then its warps) into the weighted output
+// y'_j.  The last CTA of the step's down launches to finish adds
+// out = sum_j y'_j in rank order.
 //
-// Both GEMVs take a subset of the step's picks (the resident ones, the missed
-// ones, or all), so a step can run the resident picks while the missed picks'
-// bytes are still being copied.  A pick's computation and reduction order do
-// not depend on the subset it runs in, so a cached step and an all-resident
-// step give the same bits.
+// Both GEMVs run on a subset of the step's picks (the resident ones, the
+// missed ones, or all) and stage slot bytes from HBM with 1-D TMA bulk copies
+// (cp.async.bulk) on an mbarrier.
+//
+// read-through: the missed picks take one launch that reads each missed
+// expert once over the host link and uses it on the way in.  Every thread
+// stages 16-byte pieces from host memory with cp.async, an mbarrier counts
+// the threads' completions, and after use each stage is written through to
+// the pick's victim slot.  Phase A is the gate/up kernel above on the W13
+// rows; each finished unit is counted per pick.  Phase B takes the pick's W2
+// rows (prefetched from the launch's start, so the link never idles): once
+// the pick's count shows all its h is written, a warp per row computes y'_j,
+// with the per-thread blocks and reduction tree of the down kernel.
+//
+// A pick's computation and reduction order do not depend on the subset, the
+// source or the kernel it runs in, so a cached step and an all-resident step
+// give the same bits.  Every launch that writes y'_j counts its CTAs in a
+// step counter; the CTA that completes the count adds out = sum_j y'_j in
+// rank order and resets the counters.
 #include "internal.cuh"
 
 namespace moe {
@@ -39,7 +52,7 @@ namespace {
 
 constexpr int kGateUpRows = 4;     // row pairs per gate/up unit
 constexpr int kGateUpThreads = 512;
-constexpr int kDownRows = 4;       // output rows per down unit
+constexpr int kDownRows = 4;       // output rows per down unit (per row group)
 constexpr int kDownThreads = 512;
 constexpr int kSmemPerSm = 227 * 1024;
 
@@ -78,8 +91,9 @@ __device__ __forceinline__ float dot16_f16(uint2 codes, const uint32_t* __restri
   return s0 + s1;
 }
 
-// 16 codes (8 bytes) times 16 fp32 values.
-__device__ __forceinline__ float dot16_f32(uint32_t lo, uint32_t hi, const float* __restrict__ v) {
+// 16 codes (8 bytes) times 16 fp32 values v(0..15).
+template <class Get>
+__device__ __forceinline__ float dot16_f32(uint32_t lo, uint32_t hi, Get v) {
   uint32_t h[8];
   e2m1x8_to_f16x8(lo, h[0], h[1], h[2], h[3]);
   e2m1x8_to_f16x8(hi, h[4], h[5], h[6], h[7]);
@@ -87,10 +101,21 @@ __device__ __forceinline__ float dot16_f32(uint32_t lo, uint32_t hi, const float
 #pragma unroll
   for (int b = 0; b < 8; ++b) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
-    s0 = fmaf(f.x, v[2 * b], s0);
-    s1 = fmaf(f.y, v[2 * b + 1], s1);
+    s0 = fmaf(f.x, v(2 * b), s0);
+    s1 = fmaf(f.y, v(2 * b + 1), s1);
   }
   return s0 + s1;
+}
+
+// One 32-element block of a W2 row: 16 code bytes, 2 scale bytes, and the 32
+// values v(0..31) of gscale * w * h.  Roundings are pinned so every kernel
+// gets the same bits.
+template <class Get>
+__device__ __forceinline__ float w2_block(uint4 cw, uint32_t s2, Get v) {
+  const float2 sc = e4m3x2_to_float2(s2);
+  const float d0 = dot16_f32(cw.x, cw.y, v);
+  const float d1 = dot16_f32(cw.z, cw.w, [&](int i) { return v(16 + i); });
+  return __fmaf_rn(d0, sc.x, __fmul_rn(d1, sc.y));
 }
 
 __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
@@ -164,28 +189,150 @@ __device__ __forceinline__ Stages carve(uint8_t* smem, int NS, int stage_bytes) 
 }
 
 // After a timed-out wait: wait (bounded) for the fills still in flight into
-// this CTA's shared memory, so none lands after the CTA exits.
+// this CTA's shared memory, so none lands after the CTA is done with it.
+template <bool FROM_HOST>
 __device__ void drain_fills(const Stages& S, int i, int NS, int my_units, uint32_t* flags) {
-  if (threadIdx.x != 0) return;
-  for (int ii = i; ii < i + NS && ii < my_units; ++ii)
-    if (!mbar_wait_bounded(&S.full[ii % NS], (uint32_t)((ii / NS) & 1), flags)) return;
+  if constexpr (FROM_HOST) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    if (threadIdx.x != 0) return;
+    for (int ii = i; ii < i + NS && ii < my_units; ++ii)
+      if (!mbar_wait_bounded(&S.full[ii % NS], (uint32_t)((ii / NS) & 1), flags)) return;
+  }
 }
 
 __device__ __forceinline__ int units_of_block(int nunits) {
   return nunits > (int)blockIdx.x ? (nunits - 1 - (int)blockIdx.x) / gridDim.x + 1 : 0;
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
+// The mbarrier receives one arrival when all of this thread's earlier
+// cp.async copies have landed (its expected count is the thread count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// A stage made of consecutive byte segments: segment i is n[i] bytes copied
+// from src[i] (and, on write-through, to dst[i]).  Sizes are multiples of 16.
+template <int NSEG>
+struct Segs {
+  const uint8_t* src[NSEG];
+  uint8_t* dst[NSEG];
+  int n[NSEG];
+};
+
+// All threads: stage the segments piece by piece (16 B) with cp.async.
+template <int NSEG>
+__device__ __forceinline__ void stage_from_host(uint8_t* stage, const Segs<NSEG>& sg, int nseg,
+                                                uint64_t* bar) {
+  int base = 0;
+  for (int s = 0; s < nseg; ++s) {
+    for (int off = threadIdx.x * 16; off < sg.n[s]; off += blockDim.x * 16)
+      cp_async16(stage + base + off, sg.src[s] + off);
+    base += sg.n[s];
+  }
+  cp_async_arrive(bar);
+}
+
+// All threads: write the staged segments through to their destinations.
+template <int NSEG>
+__device__ __forceinline__ void write_through(const uint8_t* stage, const Segs<NSEG>& sg, int nseg) {
+  int base = 0;
+  for (int s = 0; s < nseg; ++s) {
+    for (int off = threadIdx.x * 16; off < sg.n[s]; off += blockDim.x * 16)
+      *reinterpret_cast<uint4*>(sg.dst[s] + off) =
+          *reinterpret_cast<const uint4*>(stage + base + off);
+    base += sg.n[s];
+  }
+}
+
+// Counters of one step (a small array, zero between steps):
+//   [0]            CTAs of the step's y'_j launches that have finished
+//   [kPickCtr + jl] gate/up units done for pick jl of the read-through launch
+constexpr int kPickCtr = 2;
+
+// Tail of every launch that writes y'_j: count this CTA; the CTA that brings
+// the count to total_ctas adds out = sum_j y'_j in rank order and resets the
+// counters for the next step.
+__device__ void finish_step(const Plan* __restrict__ plan, const float* __restrict__ ypart,
+                            float* __restrict__ out, int H, uint32_t* ctr, int total_ctas,
+                            int* s_last) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_last = atomicAdd(ctr, 1u) == (uint32_t)(total_ctas - 1);
+  __syncthreads();
+  if (*s_last) {
+    __threadfence();
+    const int kmax = plan->npicks;
+    for (int o = threadIdx.x; o < H; o += blockDim.x) {
+      float acc = 0.f;
+      for (int jj = 0; jj < kmax; ++jj) acc += __ldcg(ypart + (size_t)jj * H + o);
+      out[o] = acc;
+    }
+    if (threadIdx.x == 0) {
+      ctr[0] = 0u;
+      for (int jj = 0; jj < kmax; ++jj) ctr[kPickCtr + jj] = 0u;
+    }
+  }
+}
+
+// One W2 row, one warp: y = sum over the row's 32-element blocks c, each the
+// partial a thread of the down kernel computes, reduced in that kernel's
+// order (a butterfly over 32 consecutive blocks, then those sums in order; or
+// a butterfly within groups of I/32 < 32 lanes).
+__device__ __forceinline__ float w2_row_warp(const uint8_t* __restrict__ cw,
+                                             const uint8_t* __restrict__ sc,
+                                             const float* __restrict__ hs, int I, int lane) {
+  const int C = I / 32;
+  if (C >= 32) {
+    float y = 0.f;
+    for (int c = lane; c < C; c += 32) {
+      float p = w2_block(*reinterpret_cast<const uint4*>(cw + c * 16),
+                         *reinterpret_cast<const uint16_t*>(sc + c * 2),
+                         [&](int i) { return hs[i * C + c]; });
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xFFFFFFFFu, p, o);
+      y += p;
+    }
+    return y;
+  }
+  float p = 0.f;
+  if (lane < C)
+    p = w2_block(*reinterpret_cast<const uint4*>(cw + lane * 16),
+                 *reinterpret_cast<const uint16_t*>(sc + lane * 2),
+                 [&](int i) { return hs[i * C + lane]; });
+  for (int o = C / 2; o > 0; o >>= 1) p += __shfl_xor_sync(0xFFFFFFFFu, p, o);
+  return p;
+}
+
+// Extra arguments of the read-through launch.
+struct RtArgs {
+  float* ypart;     // [k][H] weighted outputs y'_j
+  float* out;       // [H]
+  uint32_t* ctr;    // step counters (see kPickCtr)
+  int total_ctas;   // CTAs of all the step's y'_j launches
+  int URB;          // W2 rows per phase-B unit
+  int NSB;          // phase-B stages
+  int b_off;        // byte offset of the phase-B region in dynamic shared memory
+};
+
 // ----------------------------------------------------------- gate / up
 
-template <int RPT, bool WARP_RED>
+template <int RPT, bool WARP_RED, bool FROM_HOST>
 __global__ void __launch_bounds__(kGateUpThreads, 2)
 gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
                    float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
-                   int subset) {
+                   int subset, RtArgs rt) {
   constexpr int V = 2 * RPT;
   constexpr int R = kGateUpRows;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_xmax[kGateUpThreads / 32];
+  __shared__ int s_last;
   const int C = H / 16;
   const int tid = threadIdx.x, lane = tid & 31;
   const int g = tid / C, c = tid - g * C;
@@ -205,27 +352,78 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   const int nunits = pcnt * upp;
   const int my_units = units_of_block(nunits);
 
-  auto issue = [&](int unit, int stage) {
+  // a unit's four segments: gate codes, up codes, gate scales, up scales
+  auto segs = [&](int unit) {
     const int jl = unit / upp, rb = unit - jl * upp;
     const int j = pick_of(jl);
-    const uint8_t* w = plan->wptr[j];
-    const uint8_t* s = plan->sptr[j];
+    const uint8_t* w = FROM_HOST ? plan->hwptr[j] : plan->wptr[j];
+    const uint8_t* s = FROM_HOST ? plan->hsptr[j] : plan->sptr[j];
+    const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
+    Segs<4> sg;
+    sg.src[0] = w + og * (H / 2);
+    sg.src[1] = w + ou * (H / 2);
+    sg.src[2] = s + og * (H / 16);
+    sg.src[3] = s + ou * (H / 16);
+    uint8_t* dw = const_cast<uint8_t*>(plan->wptr[j]);
+    uint8_t* ds = const_cast<uint8_t*>(plan->sptr[j]);
+    sg.dst[0] = dw + og * (H / 2);
+    sg.dst[1] = dw + ou * (H / 2);
+    sg.dst[2] = ds + og * (H / 16);
+    sg.dst[3] = ds + ou * (H / 16);
+    sg.n[0] = sg.n[1] = cb;
+    sg.n[2] = sg.n[3] = sb;
+    return sg;
+  };
+  auto issue = [&](int unit, int stage) {  // FROM_HOST: every thread; else thread 0
     uint8_t* dst = S.base + (size_t)stage * stage_bytes;
-    mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
-    bulk_g2s(dst, w + (size_t)rb * R * (H / 2), cb, &S.full[stage]);
-    bulk_g2s(dst + cb, w + (size_t)(I + rb * R) * (H / 2), cb, &S.full[stage]);
-    bulk_g2s(dst + 2 * cb, s + (size_t)rb * R * (H / 16), sb, &S.full[stage]);
-    bulk_g2s(dst + 2 * cb + sb, s + (size_t)(I + rb * R) * (H / 16), sb, &S.full[stage]);
+    const Segs<4> sg = segs(unit);
+    if constexpr (FROM_HOST) {
+      stage_from_host(dst, sg, 4, &S.full[stage]);
+    } else {
+      mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
+      int base = 0;
+      for (int q = 0; q < 4; ++q) {
+        bulk_g2s(dst + base, sg.src[q], sg.n[q], &S.full[stage]);
+        base += sg.n[q];
+      }
+    }
+  };
+
+  // phase B (read-through only): W2 rows of the missed picks, URB rows a unit
+  const int URB = FROM_HOST ? rt.URB : 1, NSB = FROM_HOST ? rt.NSB : 0;
+  const int stage_b = URB * (I / 2 + I / 16);
+  uint8_t* stB = smem + rt.b_off;
+  uint64_t* barB = reinterpret_cast<uint64_t*>(stB + (size_t)NSB * stage_b);
+  float* hs = reinterpret_cast<float*>(barB + NSB);
+  const int uppb = H / URB;
+  const int my_b = FROM_HOST ? units_of_block(pcnt * uppb) : 0;
+  auto segs_b = [&](int unit) {
+    const int jl = unit / uppb, rb = unit - jl * uppb;
+    const int j = pick_of(jl);
+    const size_t oc = (size_t)I * H + (size_t)rb * URB * (I / 2);
+    const size_t os = (size_t)I * H / 8 + (size_t)rb * URB * (I / 16);
+    Segs<2> sg;
+    sg.src[0] = plan->hwptr[j] + oc;
+    sg.src[1] = plan->hsptr[j] + os;
+    sg.dst[0] = const_cast<uint8_t*>(plan->wptr[j]) + oc;
+    sg.dst[1] = const_cast<uint8_t*>(plan->sptr[j]) + os;
+    sg.n[0] = URB * (I / 2);
+    sg.n[1] = URB * (I / 16);
+    return sg;
   };
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], FROM_HOST ? blockDim.x : 1);
+    for (int s = 0; s < NSB; ++s) mbar_init(&barB[s], blockDim.x);
     fence_mbar_init();
     *S.abort_flag = 0;
   }
   __syncthreads();
-  if (tid == 0)
+  if (FROM_HOST || tid == 0)
     for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
+  if constexpr (FROM_HOST)
+    for (int s = 0; s < NSB && s < my_b; ++s)
+      stage_from_host(stB + (size_t)s * stage_b, segs_b(blockIdx.x + s * gridDim.x), 2, &barB[s]);
 
   // this thread's 16 activations, as f16 after a power-of-two prescale of the
   // whole row that keeps max |x| below 2^15
@@ -258,14 +456,21 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     xh[i] = *reinterpret_cast<const uint32_t*>(&p);
   }
 
+  // ---- phase A: gate/up + SwiGLU
+  bool failed = false;
   for (int i = 0; i < my_units; ++i) {
     const int unit = blockIdx.x + i * gridDim.x;
     const int stage = i % NS;
     if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
     __syncthreads();
+    // read-through: the previous unit's h is written and fenced; count it for its pick
+    if (FROM_HOST && tid == 0 && i > 0)
+      atomicAdd(&rt.ctr[kPickCtr + (unit - gridDim.x) / upp], 1u);
     if (*S.abort_flag) {
-      drain_fills(S, i, NS, my_units, flags);
-      return;
+      drain_fills<FROM_HOST>(S, i, NS, my_units, flags);
+      if constexpr (!FROM_HOST) return;
+      failed = true;
+      break;
     }
     const uint8_t* st = S.base + (size_t)stage * stage_bytes;
     float a[V];
@@ -279,9 +484,10 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
       a[q] = dot16_f16(cg, xh) * e4m3_to_float(sg);
       a[RPT + q] = dot16_f16(cu, xh) * e4m3_to_float(su);
     }
+    if constexpr (FROM_HOST) write_through(st, segs(unit), 4);
     stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
     __syncthreads();
-    if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
+    if ((FROM_HOST || tid == 0) && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
     if (tid < RL * RPT) {
       const int gg = tid / RPT, q = tid - gg * RPT;
       const int jl = unit / upp, rb = unit - jl * upp;
@@ -290,17 +496,71 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
       const float up = plan->gs[j][1] * xup * sum_partial<V, WARP_RED>(S.red, gg, RPT + q, C);
       const float h = gate / (1.0f + expf(-gate)) * up;
       hbuf[(size_t)j * I + rb * R + gg + q * RL] = h;
+      if constexpr (FROM_HOST) __threadfence();
     }
+  }
+  if constexpr (FROM_HOST) {
+  // ---- phase B (read-through): the missed picks' W2 rows -> y'_j
+  __syncthreads();
+  if (tid == 0 && !failed && my_units > 0)
+    atomicAdd(&rt.ctr[kPickCtr + (blockIdx.x + (my_units - 1) * gridDim.x) / upp], 1u);
+  if (failed) {
+    // let the other CTAs' phase B run (on garbage, flagged) instead of timing out
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (tid == 0)
+      for (int jl = 0; jl < pcnt; ++jl) atomicAdd(&rt.ctr[kPickCtr + jl], (uint32_t)upp);
+  } else {
+    const int warp = tid >> 5, nwarps = blockDim.x >> 5;
+    int cur = -1;
+    for (int i = 0; i < my_b; ++i) {
+      const int unit = blockIdx.x + i * gridDim.x;
+      const int stage = i % NSB;
+      const int jl = unit / uppb, rb = unit - jl * uppb;
+      const int j = pick_of(jl);
+      if (j != cur) {  // wait until all of h_j is written, then stage gscale * w * h_j
+        if (tid == 0 && !count_wait_bounded(&rt.ctr[kPickCtr + jl], (uint32_t)upp, flags))
+          *S.abort_flag = 1;
+        __syncthreads();
+        if (*S.abort_flag) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          break;
+        }
+        const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
+        for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
+          hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
+        cur = j;
+      }
+      if (!mbar_wait_bounded(&barB[stage], (uint32_t)((i / NSB) & 1), flags)) *S.abort_flag = 1;
+      __syncthreads();
+      if (*S.abort_flag) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        break;
+      }
+      const uint8_t* st = stB + (size_t)stage * stage_b;
+      for (int r = warp; r < URB; r += nwarps) {
+        const float y = w2_row_warp(st + r * (I / 2), st + URB * (I / 2) + r * (I / 16), hs, I, lane);
+        if (lane == 0) rt.ypart[(size_t)j * H + rb * URB + r] = y;
+      }
+      write_through(st, segs_b(unit), 2);
+      __syncthreads();
+      if (i + NSB < my_b)
+        stage_from_host(stB + (size_t)stage * stage_b, segs_b(unit + NSB * gridDim.x), 2,
+                        &barB[stage]);
+    }
+  }
+  finish_step(plan, rt.ypart, rt.out, H, rt.ctr, rt.total_ctas, &s_last);
   }
 }
 
-// ---------------------------------------------------------- down + combine
+// ---------------------------------------------------------------- down
 
 template <int R2>
 __global__ void __launch_bounds__(kDownThreads, 1)
 gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
-                 float* __restrict__ ypart, int H, int I, int NS, uint32_t* flags, int subset) {
+                 float* __restrict__ ypart, int H, int I, int NS, uint32_t* flags, int subset,
+                 float* __restrict__ out, uint32_t* __restrict__ done, int total_ctas) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_last;
   const int C = I / 32;  // 32-element blocks per h row; C divides 32 or is a multiple of it
   const int kmax = plan->npicks;
   int pbeg = 0, pcnt = kmax;
@@ -333,7 +593,8 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
   const size_t w2_codes = (size_t)I * H;        // 2I rows of H/2 bytes precede W2
   const size_t w2_scales = (size_t)I * H / 8;   // 2I rows of H/16 bytes
 
-  auto issue = [&](int unit, int stage) {
+  // stage layout: every pick's codes, then every pick's scales
+  auto issue = [&](int unit, int stage) {  // thread 0
     uint8_t* dst = S.base + (size_t)stage * stage_stride;
     mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
     for (int q = 0; q < pcnt; ++q) {
@@ -348,23 +609,22 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
     for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], 1);
     fence_mbar_init();
     *S.abort_flag = 0;
+    for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
   }
   __syncthreads();
-  if (tid == 0)
-    for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
 
   // gscale_j * w_j * h_j for this thread's 32 inputs, for the whole kernel
   float hv[32];
   {
-    const float f = active ? plan->gs[j][2] * plan->wts[j] : 0.f;
+    const float f = active ? __fmul_rn(plan->gs[j][2], plan->wts[j]) : 0.f;
     const float4* hp = reinterpret_cast<const float4*>(hbuf + (size_t)j * I + c * 32);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const float4 v = active ? __ldg(hp + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-      hv[4 * q] = f * v.x;
-      hv[4 * q + 1] = f * v.y;
-      hv[4 * q + 2] = f * v.z;
-      hv[4 * q + 3] = f * v.w;
+      hv[4 * q] = __fmul_rn(f, v.x);
+      hv[4 * q + 1] = __fmul_rn(f, v.y);
+      hv[4 * q + 2] = __fmul_rn(f, v.z);
+      hv[4 * q + 3] = __fmul_rn(f, v.w);
     }
   }
 
@@ -374,8 +634,8 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
     if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
     __syncthreads();
     if (*S.abort_flag) {
-      drain_fills(S, i, NS, my_units, flags);
-      return;
+      drain_fills<false>(S, i, NS, my_units, flags);
+      break;  // still counted below, so the step's combine happens
     }
     const uint8_t* st = S.base + (size_t)stage * stage_stride;
     float a[R2];
@@ -387,8 +647,7 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
         const uint4 cw = *reinterpret_cast<const uint4*>(st + jl * cb + row * (I / 2) + c * 16);
         const uint32_t s2 = *reinterpret_cast<const uint16_t*>(st + pcnt * cb + jl * sb +
                                                                row * (I / 16) + c * 2);
-        const float2 sc = e4m3x2_to_float2(s2);
-        a[r] = dot16_f32(cw.x, cw.y, hv) * sc.x + dot16_f32(cw.z, cw.w, hv + 16) * sc.y;
+        a[r] = w2_block(cw, s2, [&](int i) { return hv[i]; });
       }
     }
     if (C >= 32) {
@@ -417,16 +676,8 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
       if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
     }
   }
-}
 
-// out[o] = sum_j y'_j[o], j in rank order.
-__global__ void gemv_combine_kernel(const float* __restrict__ ypart, float* __restrict__ out, int H,
-                                    int k) {
-  const int o = blockIdx.x * blockDim.x + threadIdx.x;
-  if (o >= H) return;
-  float acc = 0.f;
-  for (int j = 0; j < k; ++j) acc += ypart[(size_t)j * H + o];
-  out[o] = acc;
+  finish_step(plan, ypart, out, H, done, total_ctas, &s_last);
 }
 
 // ------------------------------------------------------------- dispatch
@@ -442,7 +693,7 @@ struct GateUpShape {
   bool warp_red;
 };
 
-GateUpShape gateup_shape(int H) {
+GateUpShape gateup_shape(int H, int stages) {
   GateUpShape s;
   const int R = kGateUpRows;
   s.C = H / 16;
@@ -459,24 +710,96 @@ GateUpShape gateup_shape(int H) {
   const int per_cta = kSmemPerSm / 2 - 1024;  // two CTAs per SM
   int ns = (per_cta - 16 - red_floats * 4) / stage;
   if (ns > 6) ns = 6;
+  if (stages > 0 && stages < ns) ns = stages;
   s.NS = ns;
   s.smem = ns * stage + 8 * ns + 8 + red_floats * 4;
   return s;
 }
 
-template <int RPT, bool WR>
-cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
+// Phase-B shape of the read-through launch: W2 rows per unit (about 20 KB a
+// stage), two stages, then gscale * w * h of one pick in shared memory.
+struct RtShape {
+  int URB, NSB, b_off, smem;
+};
+
+RtShape rt_shape(const GateUpShape& s, int I) {
+  RtShape r;
+  const int row = I / 2 + I / 16;
+  int urb = 16;
+  while (urb > 4 && urb * row > 20 * 1024) urb /= 2;
+  r.URB = urb;
+  r.NSB = 2;
+  r.b_off = (s.smem + 127) / 128 * 128;
+  r.smem = r.b_off + r.NSB * urb * row + 8 * r.NSB + I * 4;
+  return r;
+}
+
+template <int RPT, bool WR, bool FH>
+cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, int smem, const Plan* plan,
                        const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
-                       int subset) {
-  auto kern = gemv_gateup_kernel<RPT, WR>;
+                       int subset, const RtArgs& rt) {
+  auto kern = gemv_gateup_kernel<RPT, WR, FH>;
   static int smem_set = 0;  // raise the opt-in limit once per size (not a stream operation)
-  if (s.smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = prefer_max_shared(kern);
     if (e != cudaSuccess) return e;
-    smem_set = s.smem;
+    smem_set = smem;
   }
-  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset);
+  kern<<<grid, s.NT, smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset, rt);
+  return cudaGetLastError();
+}
+
+int gateup_grid(int I, int k, int num_sms, const GemvLaunch& how) {
+  const int nunits = k * (I / kGateUpRows);
+  const int grid = how.grid > 0 ? how.grid : 2 * num_sms;
+  return grid < nunits ? grid : nunits;
+}
+
+template <bool FH>
+cudaError_t dispatch_gateup(cudaStream_t st, int grid, const GateUpShape& s, int smem,
+                            const Plan* plan, const uint16_t* x, float* hbuf, int H, int I,
+                            uint32_t* flags, int subset, const RtArgs& rt) {
+#define GU(N)                                                                                   \
+  if (s.RPT == N)                                                                               \
+    return s.warp_red                                                                           \
+               ? run_gateup<N, true, FH>(st, grid, s, smem, plan, x, hbuf, H, I, flags, subset, rt) \
+               : run_gateup<N, false, FH>(st, grid, s, smem, plan, x, hbuf, H, I, flags, subset, rt);
+  GU(1) GU(2) GU(4)
+#undef GU
+  return cudaErrorInvalidConfiguration;
+}
+
+struct DownShape {
+  int NS, smem, stage;
+};
+
+DownShape down_shape(int I, int k, int stages) {
+  DownShape d;
+  constexpr int R2 = kDownRows;
+  d.stage = k * (R2 * I / 2 + R2 * I / 16);
+  const int red_floats = (kDownThreads / 32) * R2;
+  int ns = (kSmemPerSm - 1024 - 16 - red_floats * 4) / d.stage;
+  if (ns > 8) ns = 8;
+  if (stages > 0 && stages < ns) ns = stages;
+  d.NS = ns;
+  d.smem = ns * d.stage + 8 * ns + 8 + red_floats * 4;
+  return d;
+}
+
+cudaError_t run_down(cudaStream_t st, int grid, int nt, const DownShape& d, const Plan* plan,
+                     const GemvWorkspace& ws, int H, int I, uint32_t* flags, int subset,
+                     float* out, uint32_t* done, int total_ctas) {
+  auto kern = gemv_down_kernel<kDownRows>;
+  static int smem_set = 0;
+  if (d.smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem);
+    if (e == cudaSuccess) e = prefer_max_shared(kern);
+    if (e != cudaSuccess) return e;
+    smem_set = d.smem;
+  }
+  kern<<<grid, nt, d.smem, st>>>(plan, ws.hbuf, ws.ypart, H, I, d.NS, flags, subset, out, done,
+                                 total_ctas);
   return cudaGetLastError();
 }
 
@@ -486,7 +809,7 @@ bool gemv_supported(int H, int I, int k) {
   const int C = I / 32;  // a pick's threads in the down kernel: whole warps or part of one
   return H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM &&
          k * C <= kDownThreads && (C % 32 == 0 || 32 % C == 0) &&
-         H / 16 <= kGateUpThreads * kGateUpRows;
+         H / 16 <= kGateUpThreads * kGateUpRows && gateup_shape(H, 0).NT % 32 == 0;
 }
 
 int gemv_down_tile_rows(int H, int I) {
@@ -497,54 +820,53 @@ int gemv_down_tile_rows(int H, int I) {
 
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
                                int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
-                               int subset) {
-  const GateUpShape s = gateup_shape(H);
-  if (s.NS < 2 || s.NT > kGateUpThreads) return cudaErrorInvalidConfiguration;
-  const int nunits = k * (I / kGateUpRows);
-  const int grid = nunits < 2 * num_sms ? nunits : 2 * num_sms;
-#define GU(N)                                                                                    \
-  if (s.RPT == N)                                                                                \
-    return s.warp_red ? run_gateup<N, true>(st, grid, s, plan, x, ws.hbuf, H, I, flags, subset) \
-                      : run_gateup<N, false>(st, grid, s, plan, x, ws.hbuf, H, I, flags, subset);
-  GU(1) GU(2) GU(4)
-#undef GU
-  return cudaErrorInvalidConfiguration;
+                               const GemvLaunch& how) {
+  const GateUpShape s = gateup_shape(H, how.stages);
+  if (s.NS < 1 || s.NT > kGateUpThreads || how.from_host) return cudaErrorInvalidConfiguration;
+  return dispatch_gateup<false>(st, gateup_grid(I, k, num_sms, how), s, s.smem, plan, x, ws.hbuf,
+                                H, I, flags, how.subset, RtArgs{});
+}
+
+int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how) {
+  return gateup_grid(I, k, num_sms, how);
+}
+
+cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uint16_t* x, int H,
+                                    int I, int k, const GemvWorkspace& ws, uint32_t* flags,
+                                    int num_sms, const GemvLaunch& how, float* out, uint32_t* ctr,
+                                    int total_ctas) {
+  const GateUpShape s = gateup_shape(H, how.stages);
+  if (s.NS < 1 || s.NT > kGateUpThreads || !how.from_host || how.subset != kPicksMiss)
+    return cudaErrorInvalidConfiguration;
+  const RtShape r = rt_shape(s, I);
+  RtArgs rt;
+  rt.ypart = ws.ypart;
+  rt.out = out;
+  rt.ctr = ctr;
+  rt.total_ctas = total_ctas;
+  rt.URB = r.URB;
+  rt.NSB = r.NSB;
+  rt.b_off = r.b_off;
+  return dispatch_gateup<true>(st, gemv_readthrough_grid(I, k, num_sms, how), s, r.smem, plan, x,
+                               ws.hbuf, H, I, flags, how.subset, rt);
+}
+
+int gemv_down_grid(int H, int num_sms, const GemvLaunch& how) {
+  const int nunits = H / kDownRows;
+  int grid = how.grid > 0 ? how.grid : num_sms;
+  return grid < nunits ? grid : nunits;
 }
 
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
-                             const GemvWorkspace& ws, uint32_t* flags, int num_sms, int subset) {
-  constexpr int R2 = kDownRows;
+                             const GemvWorkspace& ws, uint32_t* flags, int num_sms,
+                             const GemvLaunch& how, float* out, uint32_t* done, int total_ctas) {
   if (k * (I / 32) > kDownThreads) return cudaErrorInvalidConfiguration;
-  const int stage = k * (R2 * I / 2 + R2 * I / 16);
-  const int red_floats = (kDownThreads / 32) * R2;
-  int ns = (kSmemPerSm - 1024 - 16 - red_floats * 4) / stage;
-  if (ns > 8) ns = 8;
-  if (ns < 2) return cudaErrorInvalidConfiguration;
-  const int smem = ns * stage + 8 * ns + 8 + red_floats * 4;
-  const int nunits = H / R2;
-  const int grid = nunits < num_sms ? nunits : num_sms;
-  int nt = ((k * (I / 32) + 31) / 32) * 32;
-  auto kern = gemv_down_kernel<R2>;
-  static int smem_set = 0;
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) e = prefer_max_shared(kern);
-    if (e != cudaSuccess) return e;
-    smem_set = smem;
-  }
-  kern<<<grid, nt, smem, st>>>(plan, ws.hbuf, ws.ypart, H, I, ns, flags, subset);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gemv_combine(cudaStream_t st, const float* ypart, float* out, int H, int k) {
-  static bool once = false;
-  if (!once) {
-    cudaError_t e = prefer_max_shared(gemv_combine_kernel);
-    if (e != cudaSuccess) return e;
-    once = true;
-  }
-  gemv_combine_kernel<<<(H + 255) / 256, 256, 0, st>>>(ypart, out, H, k);
-  return cudaGetLastError();
+  const DownShape d = down_shape(I, k, how.stages);
+  if (d.NS < 1) return cudaErrorInvalidConfiguration;
+  const int grid = gemv_down_grid(H, num_sms, how);
+  const int nt = ((k * (I / 32) + 31) / 32) * 32;
+  if (how.from_host) return cudaErrorInvalidValue;  // reads slot bytes only
+  return run_down(st, grid, nt, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
 }
 
 }  // namespace moe

@@ -51,6 +51,8 @@ struct Plan {
   int32_t miss_v[MOE_MAX_PICKS];
   const uint8_t* wptr[MOE_MAX_PICKS];  // expert codes this pick reads (slot or host)
   const uint8_t* sptr[MOE_MAX_PICKS];  // expert scales
+  const uint8_t* hwptr[MOE_MAX_PICKS]; // the expert's host backing (read-through of a miss)
+  const uint8_t* hsptr[MOE_MAX_PICKS];
   float gs[MOE_MAX_PICKS][4];          // (gate, up, down, unused) global scales
 };
 
@@ -121,16 +123,34 @@ struct GemvWorkspace {
   uint32_t* flags;    // error flags word for waits (per layer stats flags)
 };
 // Pick subsets of a one-row step: the picks resident at step start, the
-// missed picks (after their copy), or all picks.
+// missed picks, or all picks.
 enum PickSubset { kPicksHit = 0, kPicksMiss = 1, kPicksAll = 2 };
+struct GemvLaunch {
+  int subset;      // PickSubset
+  bool from_host;  // read-through launch only: the picks come from host memory
+  int grid;        // CTAs (0: the kernel's default, a full persistent grid)
+  int stages;      // units in flight per CTA (0: as many as fit)
+};
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
                                int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
-                               int subset);
-// y'_j = gscale_j * w_j * (W2_j h_j) for the subset's picks -> ws.ypart [k][H]
+                               const GemvLaunch& how);
+// The missed picks end to end (subset kPicksMiss, from_host): each missed
+// expert read once from host memory and written through to its slot, gate/up
+// + SwiGLU on the W13 rows, then y'_j = gscale_j * w_j * (W2_j h_j) on the W2
+// rows -> ws.ypart.  Counts its CTAs in ctr[0] like launch_gemv_down.
+cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uint16_t* x, int H,
+                                    int I, int k, const GemvWorkspace& ws, uint32_t* flags,
+                                    int num_sms, const GemvLaunch& how, float* out, uint32_t* ctr,
+                                    int total_ctas);
+int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how);
+// y'_j = gscale_j * w_j * (W2_j h_j) for the subset's picks -> ws.ypart [k][H].  Every CTA
+// of the step's y'_j launches counts itself in done[0] when it finishes; the one that brings
+// the count to total_ctas adds out = sum_j y'_j in rank order and resets done[0] and the
+// read-through launch's per-pick counters done[2 .. 2 + k).  done: >= 2 + k words, zero.
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
-                             const GemvWorkspace& ws, uint32_t* flags, int num_sms, int subset);
-// out[o] = sum_j y'_j[o], j in rank order
-cudaError_t launch_gemv_combine(cudaStream_t st, const float* ypart, float* out, int H, int k);
+                             const GemvWorkspace& ws, uint32_t* flags, int num_sms,
+                             const GemvLaunch& how, float* out, uint32_t* done, int total_ctas);
+int gemv_down_grid(int H, int num_sms, const GemvLaunch& how);
 int gemv_down_tile_rows(int H, int I);
 // Shapes the M = 1 expert kernels handle (top_k * inter <= 16384, dims % 128 == 0).
 bool gemv_supported(int H, int I, int k);
@@ -201,6 +221,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       return false;
     }
     __nanosleep(64);
+  }
+}
+
+// Waits (acquire, at most ~2 s) until the global counter *ctr reaches target;
+// on timeout sets MOE_FLAG_WAIT_TIMEOUT in *flags and returns false.
+__device__ __forceinline__ bool count_wait_bounded(const uint32_t* ctr, uint32_t target,
+                                                   uint32_t* flags) {
+  const uint64_t t0 = global_ns();
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(flags, MOE_FLAG_WAIT_TIMEOUT);
+      return false;
+    }
+    __nanosleep(128);
   }
 }
 

@@ -269,7 +269,14 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
             dalloc(&h->gemv.tile_cnt, (size_t)(hidden / gemv_down_tile_rows(hidden, inter) + 1)) ==
                 cudaSuccess;
   ok = ok && alloc_multirow(h);
-  ok = ok && cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess &&
+  // The second stream carries the missed picks' read-through pass, the step's
+  // critical path: highest priority, so its CTAs are placed before the
+  // resident picks' persistent grids fill the SMs.
+  int prio_least = 0, prio_greatest = 0;
+  ok = ok && cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest) == cudaSuccess;
+  ok = ok &&
+       cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_greatest) ==
+           cudaSuccess &&
        cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
@@ -318,40 +325,45 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   uint32_t* flags = &(h->stats + layer)->flags;
   cudaError_t e = mark(0, st);
   if (rows == 1) {
-    // One row.  After route/remap the missed picks take a second stream: copy
-    // host -> slot, then their gate/up and down; meanwhile the resident picks'
-    // gate/up and down run on the caller's stream, so the hit experts' HBM
-    // reads overlap the host-link copy.  Each pick's weighted output y'_j is
-    // computed the same way whichever path it takes, and the combine adds them
-    // in rank order, so the result does not depend on the hit/miss split.
+    // One row.  After route/remap the missed picks take a second stream: one
+    // read-through launch reads each missed expert once over the host link,
+    // computes its gate/up and down on the way in and writes it through to the
+    // victim slot.  Meanwhile the resident picks' gate/up and down run on the
+    // caller's stream, so the hit experts' HBM reads overlap the host-link
+    // transfer.  Each pick's weighted output y'_j is computed the same way
+    // whichever path it takes, and the last CTA of the step's y'_j launches
+    // adds them in rank order, so the result does not depend on the hit/miss
+    // split.
     if (e == cudaSuccess)
       e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, nullptr);
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess) e = cudaEventRecord(h->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork, 0);
-    if (e == cudaSuccess && !h->opts.all_resident)
-      e = launch_miss_copy(h->side, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw,
-                           h->Bs, h->num_sms / 4 > 8 ? h->num_sms / 4 : 8);
+    // missed picks: a small grid keeps the host link saturated without taking
+    // many SMs from the resident picks
+    const int rt_grid = h->num_sms / 4 > 8 ? h->num_sms / 4 : 8;
+    const GemvLaunch miss{kPicksMiss, true, rt_grid, 2};
+    // resident picks: slot bytes from HBM
+    const GemvLaunch hit_gu{kPicksHit, false, 0, 3}, hit_dn{kPicksHit, false, 0, 4};
+    const int total = gemv_readthrough_grid(h->I, h->k, h->num_sms, miss) +
+                      gemv_down_grid(h->H, h->num_sms, hit_dn);
     if (e == cudaSuccess) e = mark(2, h->side);
     if (e == cudaSuccess)
-      e = launch_gemv_gateup(h->side, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
-                             kPicksMiss);
+      e = launch_gemv_readthrough(h->side, h->plan, x, h->H, h->I, h->k, h->gemv, flags,
+                                  h->num_sms, miss, out, h->gemv.tile_cnt, total);
     if (e == cudaSuccess) e = mark(3, h->side);
-    if (e == cudaSuccess)
-      e = launch_gemv_down(h->side, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
-                           kPicksMiss);
     if (e == cudaSuccess) e = mark(4, h->side);
     if (e == cudaSuccess) e = cudaEventRecord(h->join, h->side);
     if (e == cudaSuccess)
       e = launch_gemv_gateup(st, h->plan, x, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
-                             kPicksHit);
+                             hit_gu);
     if (e == cudaSuccess) e = mark(5, st);
     if (e == cudaSuccess)
-      e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms, kPicksHit);
+      e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms, hit_dn,
+                           out, h->gemv.tile_cnt, total);
     if (e == cudaSuccess) e = mark(6, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->join, 0);
-    if (e == cudaSuccess) e = launch_gemv_combine(st, h->gemv.ypart, out, h->H, h->k);
     if (e == cudaSuccess) e = mark(7, st);
     return cuda_err(e);
   }

@@ -145,10 +145,11 @@ extern "C" int moe_expert_pass_noalloc(int k, int hidden, int inter, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   noalloc_plan_kernel<<<1, 64, 0, st>>>(a, plan, ws.tile_cnt, (int)kTileWords);
   cudaError_t e = cudaGetLastError();
+  const GemvLaunch all{kPicksAll, false, 0, 0};
   if (e == cudaSuccess)
-    e = launch_gemv_gateup(st, plan, x, hidden, inter, k, ws, flags, d->num_sms, kPicksAll);
+    e = launch_gemv_gateup(st, plan, x, hidden, inter, k, ws, flags, d->num_sms, all);
   if (e == cudaSuccess)
-    e = launch_gemv_down(st, plan, hidden, inter, k, ws, flags, d->num_sms, kPicksAll);
-  if (e == cudaSuccess) e = launch_gemv_combine(st, ws.ypart, out, hidden, k);
+    e = launch_gemv_down(st, plan, hidden, inter, k, ws, flags, d->num_sms, all, out, ws.tile_cnt,
+                         gemv_down_grid(hidden, d->num_sms, all));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

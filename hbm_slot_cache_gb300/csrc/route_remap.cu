@@ -274,6 +274,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     plan->wts[p] = s_wts[p];
     plan->wptr[p] = L.slot_w + (long long)v * Bw;
     plan->sptr[p] = L.slot_s + (long long)v * Bs;
+    plan->hwptr[p] = L.host_w + (long long)e * Bw;
+    plan->hsptr[p] = L.host_s + (long long)e * Bs;
     s_wp[p] = plan->wptr[p];
     s_sp[p] = plan->sptr[p];
     plan->gs[p][0] = L.gscale[3 * e + 0];
