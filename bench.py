@@ -316,7 +316,10 @@ def run_ours(args) -> None:
                     "ms_between_steps": gap_ms,
                     "ms_miss_path": float(np.mean(ev_ms[:, 4] - ev_ms[:, 1])),
                     "ms_hit_path": float(np.mean(ev_ms[:, 6] - ev_ms[:, 1])),
-                    "ms_route": float(np.mean(t_route))}
+                    "ms_route": float(np.mean(t_route)),
+                    "ms_step_with_miss": float(np.mean(ev_ms[n_miss > 0, 7])) if (n_miss > 0).any() else None,
+                    "ms_step_no_miss": float(np.mean(ev_ms[n_miss == 0, 7])) if (n_miss == 0).any() else None,
+                    "frac_steps_with_miss": float(np.mean(n_miss > 0))}
 
     # host-link bandwidth probed in the same session
     from hbm_slot_cache_gb300 import HostBank, moe_probe_host_link

@@ -252,9 +252,12 @@ __device__ __forceinline__ void write_through(const uint8_t* stage, const Segs<N
 }
 
 // Counters of one step (a small array, zero between steps):
-//   [0]            CTAs of the step's y'_j launches that have finished
+//   [0]             CTAs of the step's y'_j launches that have finished
+//   [kWorkCtr]      W2 units taken by the read-through launch
 //   [kPickCtr + jl] gate/up units done for pick jl of the read-through launch
+constexpr int kWorkCtr = 1;   // phase-B units taken by the read-through launch
 constexpr int kPickCtr = 2;
+constexpr int kMaxStagesB = 8;
 
 // Tail of every launch that writes y'_j: count this CTA; the CTA that brings
 // the count to total_ctas adds out = sum_j y'_j in rank order and resets the
@@ -268,14 +271,31 @@ __device__ void finish_step(const Plan* __restrict__ plan, const float* __restri
   __syncthreads();
   if (*s_last) {
     __threadfence();
+    // four outputs a thread, eight picks' loads in flight at once
     const int kmax = plan->npicks;
-    for (int o = threadIdx.x; o < H; o += blockDim.x) {
-      float acc = 0.f;
-      for (int jj = 0; jj < kmax; ++jj) acc += __ldcg(ypart + (size_t)jj * H + o);
-      out[o] = acc;
+    const int H4 = H / 4;
+    const float4* __restrict__ y4 = reinterpret_cast<const float4*>(ypart);
+    for (int o = threadIdx.x; o < H4; o += blockDim.x) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j0 = 0; j0 < kmax; j0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (j0 + q < kmax) v[q] = __ldcg(y4 + (size_t)(j0 + q) * H4 + o);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (j0 + q < kmax) {
+            acc.x += v[q].x;
+            acc.y += v[q].y;
+            acc.z += v[q].z;
+            acc.w += v[q].w;
+          }
+      }
+      reinterpret_cast<float4*>(out)[o] = acc;
     }
     if (threadIdx.x == 0) {
       ctr[0] = 0u;
+      ctr[kWorkCtr] = 0u;
       for (int jj = 0; jj < kmax; ++jj) ctr[kPickCtr + jj] = 0u;
     }
   }
@@ -389,14 +409,24 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     }
   };
 
-  // phase B (read-through only): W2 rows of the missed picks, URB rows a unit
+  // phase B (read-through only): W2 rows of the missed picks, URB rows a unit.
+  // Units are taken in ascending order from the step's work counter, so CTAs
+  // that finish phase A early take more.  Stages: NSB of its own from the
+  // start, then NSA more in the phase-A stage memory once phase A is done.
   const int URB = FROM_HOST ? rt.URB : 1, NSB = FROM_HOST ? rt.NSB : 0;
   const int stage_b = URB * (I / 2 + I / 16);
+  const int NSA = FROM_HOST ? min(kMaxStagesB - NSB, NS * stage_bytes / stage_b) : 0;
+  const int NST = NSB + NSA;
   uint8_t* stB = smem + rt.b_off;
   uint64_t* barB = reinterpret_cast<uint64_t*>(stB + (size_t)NSB * stage_b);
-  float* hs = reinterpret_cast<float*>(barB + NSB);
+  float* hs = reinterpret_cast<float*>(barB + kMaxStagesB);
   const int uppb = H / URB;
-  const int my_b = FROM_HOST ? units_of_block(pcnt * uppb) : 0;
+  const int nb = FROM_HOST ? pcnt * uppb : 0;
+  auto stage_ptr = [&](int s) {
+    return s < NSB ? stB + (size_t)s * stage_b : S.base + (size_t)(s - NSB) * stage_b;
+  };
+  __shared__ int s_unitB[kMaxStagesB];  // unit staged in each phase-B stage, -1: none
+  __shared__ int s_nextB[2];            // by iteration parity: read after the writer moved on
   auto segs_b = [&](int unit) {
     const int jl = unit / uppb, rb = unit - jl * uppb;
     const int j = pick_of(jl);
@@ -414,16 +444,20 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], FROM_HOST ? blockDim.x : 1);
-    for (int s = 0; s < NSB; ++s) mbar_init(&barB[s], blockDim.x);
+    for (int s = 0; s < NST; ++s) mbar_init(&barB[s], blockDim.x);
     fence_mbar_init();
     *S.abort_flag = 0;
+    if (FROM_HOST) {  // this CTA's first phase-B units
+      const int u0 = (int)atomicAdd(&rt.ctr[kWorkCtr], (uint32_t)NSB);
+      for (int s = 0; s < kMaxStagesB; ++s) s_unitB[s] = (s < NSB && u0 + s < nb) ? u0 + s : -1;
+    }
   }
   __syncthreads();
   if (FROM_HOST || tid == 0)
     for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
   if constexpr (FROM_HOST)
-    for (int s = 0; s < NSB && s < my_b; ++s)
-      stage_from_host(stB + (size_t)s * stage_b, segs_b(blockIdx.x + s * gridDim.x), 2, &barB[s]);
+    for (int s = 0; s < NSB; ++s)
+      if (s_unitB[s] >= 0) stage_from_host(stage_ptr(s), segs_b(s_unitB[s]), 2, &barB[s]);
 
   // this thread's 16 activations, as f16 after a power-of-two prescale of the
   // whole row that keeps max |x| below 2^15
@@ -510,11 +544,22 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     if (tid == 0)
       for (int jl = 0; jl < pcnt; ++jl) atomicAdd(&rt.ctr[kPickCtr + jl], (uint32_t)upp);
   } else {
+    // phase-A stage memory is free now: stage NSA more units there
+    if (tid == 0 && NSA > 0) {
+      const int u0 = (int)atomicAdd(&rt.ctr[kWorkCtr], (uint32_t)NSA);
+      for (int s = NSB; s < NST; ++s) s_unitB[s] = u0 + (s - NSB) < nb ? u0 + (s - NSB) : -1;
+    }
+    __syncthreads();
+    for (int s = NSB; s < NST; ++s)
+      if (s_unitB[s] >= 0) stage_from_host(stage_ptr(s), segs_b(s_unitB[s]), 2, &barB[s]);
     const int warp = tid >> 5, nwarps = blockDim.x >> 5;
     int cur = -1;
-    for (int i = 0; i < my_b; ++i) {
-      const int unit = blockIdx.x + i * gridDim.x;
-      const int stage = i % NSB;
+    for (int i = 0;; ++i) {
+      const int stage = i % NST;
+      const int unit = s_unitB[stage];
+      if (unit < 0) break;  // units are taken in order: none left for this CTA
+      // the unit that refills this stage: taken now, its value used at the end
+      const int taken = tid == 0 ? (int)atomicAdd(&rt.ctr[kWorkCtr], 1u) : 0;
       const int jl = unit / uppb, rb = unit - jl * uppb;
       const int j = pick_of(jl);
       if (j != cur) {  // wait until all of h_j is written, then stage gscale * w * h_j
@@ -530,22 +575,23 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
           hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
         cur = j;
       }
-      if (!mbar_wait_bounded(&barB[stage], (uint32_t)((i / NSB) & 1), flags)) *S.abort_flag = 1;
+      if (!mbar_wait_bounded(&barB[stage], (uint32_t)((i / NST) & 1), flags)) *S.abort_flag = 1;
       __syncthreads();
       if (*S.abort_flag) {
         asm volatile("cp.async.wait_all;" ::: "memory");
         break;
       }
-      const uint8_t* st = stB + (size_t)stage * stage_b;
+      const uint8_t* st = stage_ptr(stage);
       for (int r = warp; r < URB; r += nwarps) {
         const float y = w2_row_warp(st + r * (I / 2), st + URB * (I / 2) + r * (I / 16), hs, I, lane);
         if (lane == 0) rt.ypart[(size_t)j * H + rb * URB + r] = y;
       }
       write_through(st, segs_b(unit), 2);
+      if (tid == 0) s_nextB[i & 1] = taken < nb ? taken : -1;
       __syncthreads();
-      if (i + NSB < my_b)
-        stage_from_host(stB + (size_t)stage * stage_b, segs_b(unit + NSB * gridDim.x), 2,
-                        &barB[stage]);
+      const int nxt = s_nextB[i & 1];
+      if (tid == 0) s_unitB[stage] = nxt;
+      if (nxt >= 0) stage_from_host(stage_ptr(stage), segs_b(nxt), 2, &barB[stage]);
     }
   }
   finish_step(plan, rt.ypart, rt.out, H, rt.ctr, rt.total_ctas, &s_last);
@@ -730,7 +776,7 @@ RtShape rt_shape(const GateUpShape& s, int I) {
   r.URB = urb;
   r.NSB = 2;
   r.b_off = (s.smem + 127) / 128 * 128;
-  r.smem = r.b_off + r.NSB * urb * row + 8 * r.NSB + I * 4;
+  r.smem = r.b_off + r.NSB * urb * row + 8 * kMaxStagesB + I * 4;
   return r;
 }
 

@@ -308,7 +308,7 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
                    const uint16_t* x, float* out, void* stream) {
   if (!h || layer < 0 || layer >= h->L || rows < 1 || !router_logits || !x || !out)
     return MOE_ERR_ARG;
-  if ((uintptr_t)x & 15) return MOE_ERR_ARG;
+  if (((uintptr_t)x & 15) || ((uintptr_t)out & 15)) return MOE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (rows > h->opts.bypass_rows && rows > h->opts.max_rows) return MOE_ERR_UNSUPPORTED;
   if (rows > 1 && !mma_supported(h->H, h->I)) return MOE_ERR_UNSUPPORTED;
@@ -342,7 +342,7 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork, 0);
     // missed picks: a small grid keeps the host link saturated without taking
     // many SMs from the resident picks
-    const int rt_grid = h->num_sms / 4 > 8 ? h->num_sms / 4 : 8;
+    const int rt_grid = h->num_sms / 2 > 8 ? h->num_sms / 2 : 8;
     const GemvLaunch miss{kPicksMiss, true, rt_grid, 2};
     // resident picks: slot bytes from HBM
     const GemvLaunch hit_gu{kPicksHit, false, 0, 3}, hit_dn{kPicksHit, false, 0, 4};

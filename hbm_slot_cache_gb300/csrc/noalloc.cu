@@ -108,7 +108,7 @@ extern "C" int moe_expert_pass_noalloc(int k, int hidden, int inter, const void*
                                        const float* weights, const uint16_t* x, float* out,
                                        void* stream) {
   if (k < 1 || hidden < 1 || inter < 1 || !expert_w || !expert_s || !gscale || !weights || !x ||
-      !out || ((uintptr_t)x & 15) || ((uintptr_t)out & 3))
+      !out || ((uintptr_t)x & 15) || ((uintptr_t)out & 15))
     return MOE_ERR_ARG;
   if (k > kMaxK || hidden > kMaxDim || inter > kMaxDim || hidden % 128 || inter % 128 ||
       !gemv_supported(hidden, inter, k))

@@ -3,15 +3,21 @@
 // One CTA does the whole step (the pages fuse all bookkeeping into a single
 // kernel: "GLM 5.3 Testing: HBM Expert Allocation", "The build, measured ...":
 // remap, miss detection and LRU in one launch instead of a dozen tiny ops).
-// The layer's map, owners and last-use stamps are read into shared memory in
-// one coalesced pass, all decisions are taken there, and only what changed is
-// written back, so the kernel costs about one global round trip.
+// The layer's map, owners, last-use stamps, clock and trace head are read in
+// one coalesced pass at the start (the picks' global scales as soon as the
+// picks are known), all decisions are taken in shared memory, only what
+// changed is written back and the counters take fire-and-forget atomics, so
+// the kernel costs about one global round trip.
 //
 // Router ("What the slot cache is": the router chooses top-8 expert ids before
 // the expert kernel; "TensorFold GLM-5.3 explained": ties break by a stable
-// expert order): one warp per row ranks the E logits by (logit desc, id asc)
-// with NaN below every number, in k rounds of a warp max over 64-bit keys.
-// Weights are the softmax over the k selected logits.
+// expert order): the E logits are ranked by (logit desc, id asc) with NaN below
+// every number, as distinct 64-bit keys.  Several rows: one warp per row, k
+// rounds of a warp max.  One row: the whole CTA; the k-th largest of the
+// warps' maxima is a lower bound T of the k-th largest key (those maxima are k
+// distinct keys), so only keys >= T can be selected, and each candidate's rank
+// is its count of larger candidates.  Weights are the softmax over the k
+// selected logits, the same code either way.
 //
 // Remap/LRU ("What the slot cache is": a miss fills an LRU-victim slot, then
 // the map is updated; "TensorFold GLM-5.3 explained": the union of a round's
@@ -109,7 +115,13 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   __shared__ int32_t s_pgroup[MOE_MAX_PICKS], s_gcount[MOE_MAX_PICKS];
   __shared__ int32_t s_gstart[MOE_MAX_PICKS], s_jstart[MOE_MAX_PICKS];
   __shared__ int32_t s_n_union, s_n_miss, s_n_hits, s_n_evict;
-  __shared__ uint32_t s_flags, s_clock;
+  __shared__ uint32_t s_flags, s_clock, s_trace_head;
+  // one-row router
+  __shared__ float s_logit[MOE_MAX_EXPERTS];
+  __shared__ unsigned long long s_cand[MOE_MAX_EXPERTS];
+  __shared__ unsigned long long s_gmax[kThreads / 32], s_T;
+  __shared__ float s_lsel[MOE_MAX_TOPK];
+  __shared__ int32_t s_ncand;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int npicks = rows * k;
@@ -123,7 +135,9 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     s_flags = 0;
     s_n_hits = 0;
     s_n_evict = 0;
+    s_ncand = 0;
     s_clock = *L.clock;
+    s_trace_head = L.trace_cap ? *L.trace_head : 0u;
   }
   for (int e = tid; e < E; e += kThreads) s_map[e] = L.map[e];
   for (int v = tid; v < S; v += kThreads) {
@@ -131,12 +145,72 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     s_key[v] = ((unsigned long long)L.stamp[v] << 32) | (unsigned)v;
   }
 
-  // ---- router: warp per row
-  for (int m = warp; m < rows; m += kThreads / 32) {
-    const bool bad = route_row<KPL>(logits + (size_t)m * E, E, k, lane, s_ids + m * k, s_wts + m * k);
-    if (bad && lane == 0) atomicOr(&s_flags, MOE_FLAG_NONFINITE_LOGIT);
+  // ---- router
+  if (rows == 1) {
+    constexpr int KPT = (MOE_MAX_EXPERTS + kThreads - 1) / kThreads;
+    unsigned long long key[KPT];
+    bool bad = false;
+#pragma unroll
+    for (int q = 0; q < KPT; ++q) {
+      const int e = tid + q * kThreads;
+      key[q] = 0ull;
+      if (e < E) {
+        const float f = logits[e];
+        bad |= !isfinite(f);
+        key[q] = route_key(f, e);
+        s_logit[e] = f;
+      }
+    }
+    unsigned long long m = key[0];
+#pragma unroll
+    for (int q = 1; q < KPT; ++q) m = umax64(m, key[q]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = umax64(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) s_gmax[warp] = m;
+    if (__syncthreads_or(bad) && tid == 0) s_flags |= MOE_FLAG_NONFINITE_LOGIT;
+    if (warp == 0) {  // T = k-th largest warp maximum (1: every key, if fewer warps have keys)
+      const int G = min(kThreads / 32, (E + 31) / 32);
+      const unsigned long long g = lane < G ? s_gmax[lane] : 0ull;
+      int r = 0;
+      for (int u = 0; u < G; ++u) r += s_gmax[u] > g;
+      if (lane < G && r == k - 1) s_T = g;
+      if (lane == 0 && G < k) s_T = 1ull;
+    }
+    __syncthreads();
+    const unsigned long long T = s_T;
+#pragma unroll
+    for (int q = 0; q < KPT; ++q)
+      if (key[q] >= T) s_cand[atomicAdd(&s_ncand, 1)] = key[q];
+    __syncthreads();
+    const int nc = s_ncand;
+    for (int i = tid; i < nc; i += kThreads) {
+      const unsigned long long kk = s_cand[i];
+      int r = 0;
+      for (int u = 0; u < nc; ++u) r += s_cand[u] > kk;
+      if (r < k) {
+        const int e = (int)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull));
+        s_ids[r] = e;
+        s_lsel[r] = s_logit[e];
+      }
+    }
+    __syncthreads();
+    if (warp == 0) route_weights(lane < k ? s_lsel[lane] : 0.f, k, lane, s_wts);
+  } else {  // warp per row
+    for (int m = warp; m < rows; m += kThreads / 32) {
+      const bool bad =
+          route_row<KPL>(logits + (size_t)m * E, E, k, lane, s_ids + m * k, s_wts + m * k);
+      if (bad && lane == 0) atomicOr(&s_flags, MOE_FLAG_NONFINITE_LOGIT);
+    }
   }
   __syncthreads();
+  // the picks' global scales, in flight while the remap decisions are taken
+  float gs0 = 0.f, gs1 = 0.f, gs2 = 0.f;
+  if (tid < npicks) {
+    const int e = s_ids[tid];
+    gs0 = L.gscale[3 * e + 0];
+    gs1 = L.gscale[3 * e + 1];
+    gs2 = L.gscale[3 * e + 2];
+  }
 
   // ---- union, hits (slot marked used), missing ids
   for (int p = tid; p < npicks; p += kThreads) {
@@ -194,11 +268,11 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       plan->sptr[p] = L.host_s + (long long)e * Bs;
       s_wp[p] = plan->wptr[p];
       s_sp[p] = plan->sptr[p];
-      plan->gs[p][0] = L.gscale[3 * e + 0];
-      plan->gs[p][1] = L.gscale[3 * e + 1];
-      plan->gs[p][2] = L.gscale[3 * e + 2];
+      plan->gs[p][0] = gs0;  // p == tid: npicks <= kThreads
+      plan->gs[p][1] = gs1;
+      plan->gs[p][2] = gs2;
       if (L.trace_cap) {
-        moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
+        moe_step_record_t* r = L.trace + (s_trace_head % L.trace_cap);
         r->ids[p] = e;
         r->weights[p] = s_wts[p];
         r->slot[p] = -1;
@@ -215,17 +289,17 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       plan->n_union = n_union;
       plan->n_miss = 0;
       plan->bypass = 1;
-      st->steps += 1;
-      st->bypass_calls += 1;
+      atomicAdd(&st->steps, 1ull);
+      atomicAdd(&st->bypass_calls, 1ull);
       if (s_flags) atomicOr(&st->flags, s_flags);
       if (L.trace_cap) {
-        moe_step_record_t* r = L.trace + (*L.trace_head % L.trace_cap);
+        moe_step_record_t* r = L.trace + (s_trace_head % L.trace_cap);
         r->clock = s_clock;
         r->rows = rows;
         r->n_union = n_union;
         r->n_miss = 0;
         r->bypass = 1;
-        *L.trace_head += 1;
+        *L.trace_head = s_trace_head + 1u;
       }
     }
     return;
@@ -266,7 +340,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   __syncthreads();
 
   // ---- per pick: the slot it reads
-  moe_step_record_t* r = L.trace_cap ? L.trace + (*L.trace_head % L.trace_cap) : nullptr;
+  moe_step_record_t* r = L.trace_cap ? L.trace + (s_trace_head % L.trace_cap) : nullptr;
   for (int p = tid; p < npicks; p += kThreads) {
     const int e = s_ids[p];
     const int v = s_map[e];
@@ -278,9 +352,9 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     plan->hsptr[p] = L.host_s + (long long)e * Bs;
     s_wp[p] = plan->wptr[p];
     s_sp[p] = plan->sptr[p];
-    plan->gs[p][0] = L.gscale[3 * e + 0];
-    plan->gs[p][1] = L.gscale[3 * e + 1];
-    plan->gs[p][2] = L.gscale[3 * e + 2];
+    plan->gs[p][0] = gs0;  // p == tid: npicks <= kThreads
+    plan->gs[p][1] = gs1;
+    plan->gs[p][2] = gs2;
     if (r) {
       r->ids[p] = e;
       r->weights[p] = s_wts[p];
@@ -299,27 +373,29 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   if (gp)
     emit_groups(gp, rows, npicks, n_union, s_ids, s_wts, s_wp, s_sp, s_union, s_upre, s_pgroup,
                 s_gcount, s_gstart, s_jstart, L.gscale);
+  if (rows == 1 && warp == 0) {  // hits first, then misses, each in rank order (npicks <= 32)
+    const bool in = lane < npicks;
+    const bool hit = in && s_hit[lane];
+    const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hit);
+    const uint32_t mb = __ballot_sync(0xFFFFFFFFu, in && !hit);
+    const uint32_t below = (1u << lane) - 1u;
+    if (hit) plan->order[__popc(hb & below)] = lane;
+    if (in && !hit) plan->order[__popc(hb) + __popc(mb & below)] = lane;
+    if (lane == 0) plan->n_hit = __popc(hb);
+  }
   if (tid == 0) {
     plan->rows = rows;
     plan->npicks = npicks;
     plan->n_union = n_union;
     plan->n_miss = n_miss;
     plan->bypass = 0;
-    if (rows == 1) {  // hits first, then misses, each in rank order
-      int nh = 0;
-      for (int p = 0; p < npicks; ++p)
-        if (s_hit[p]) plan->order[nh++] = p;
-      plan->n_hit = nh;
-      for (int p = 0; p < npicks; ++p)
-        if (!s_hit[p]) plan->order[nh++] = p;
-    }
     *L.clock = t;
-    st->steps += 1;
-    st->picks += (unsigned long long)npicks;
-    st->hits += (unsigned long long)s_n_hits;
-    st->misses += (unsigned long long)n_miss;
-    st->evictions += (unsigned long long)s_n_evict;
-    st->bytes_copied += (unsigned long long)n_miss * (unsigned long long)(Bw + Bs);
+    atomicAdd(&st->steps, 1ull);
+    atomicAdd(&st->picks, (unsigned long long)npicks);
+    atomicAdd(&st->hits, (unsigned long long)s_n_hits);
+    atomicAdd(&st->misses, (unsigned long long)n_miss);
+    atomicAdd(&st->evictions, (unsigned long long)s_n_evict);
+    atomicAdd(&st->bytes_copied, (unsigned long long)n_miss * (unsigned long long)(Bw + Bs));
     if (s_flags) atomicOr(&st->flags, s_flags);
     if (r) {
       r->clock = t;
@@ -327,7 +403,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       r->n_union = n_union;
       r->n_miss = n_miss;
       r->bypass = 0;
-      *L.trace_head += 1;
+      *L.trace_head = s_trace_head + 1u;
     }
   }
 }

@@ -22,6 +22,24 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
   return a > b ? a : b;
 }
 
+// Softmax over the k selected logits; all 32 lanes call it, lane j < k holding
+// the j-th selected logit, and lane j writes wts[j].
+__device__ __forceinline__ void route_weights(float lsel, int k, int lane, float* wts) {
+  const float l = (lane < k) ? (isnan(lsel) ? -INFINITY : lsel) : -INFINITY;
+  float lmax = l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+  const float ej = (lane < k) ? ((l == lmax) ? 1.0f : expf(l - lmax)) : 0.0f;
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ej, j);
+  if (lane < k) wts[lane] = ej / sum;
+}
+
+// Ranking key of logit f for expert e: larger key = earlier rank; never 0.
+__device__ __forceinline__ unsigned long long route_key(float f, int e) {
+  return ((unsigned long long)rank_key(f) << 32) | (0xFFFFFFFFu - (uint32_t)e);
+}
+
 // All 32 lanes call it.  ids[j] / wts[j] (j < k) are written by lanes 0 and j;
 // returns true (on every lane) if any of the row's logits is NaN or infinite.
 // KPL = keys per lane >= ceil(E / 32).
@@ -37,7 +55,7 @@ __device__ __forceinline__ bool route_row(const float* __restrict__ lr, int E, i
     if (e < E) {
       const float f = lr[e];
       bad |= !isfinite(f);
-      key[i] = ((unsigned long long)rank_key(f) << 32) | (0xFFFFFFFFu - (uint32_t)e);
+      key[i] = route_key(f, e);
     }
   }
   unsigned long long best = 0ull;
@@ -60,14 +78,7 @@ __device__ __forceinline__ bool route_row(const float* __restrict__ lr, int E, i
     if (lane == 0) ids[j] = e;
     if (lane == j) lsel = lr[e];
   }
-  const float l = (lane < k) ? (isnan(lsel) ? -INFINITY : lsel) : -INFINITY;
-  float lmax = l;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
-  const float ej = (lane < k) ? ((l == lmax) ? 1.0f : expf(l - lmax)) : 0.0f;
-  float sum = 0.f;
-  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ej, j);
-  if (lane < k) wts[lane] = ej / sum;
+  route_weights(lsel, k, lane, wts);
   return __any_sync(0xFFFFFFFFu, bad) != 0;
 }
 

@@ -136,8 +136,9 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
 
 /* One layer-step for `rows` tokens:
  *   router_logits: device fp32 [rows][experts]
- *   x:             device bf16 bits [rows][hidden]
- *   out:           device fp32 [rows][hidden] (written, not accumulated)
+ *   x:             device bf16 bits [rows][hidden], 16-byte aligned
+ *   out:           device fp32 [rows][hidden] (written, not accumulated),
+ *                  16-byte aligned
  *   stream:        cudaStream_t (NULL = legacy default stream)
  * rows <= bypass_rows: route (top-k by logit, ties to the lower id; weights =
  * softmax of the k selected logits), map ids to slots, copy misses host->slot,
@@ -227,7 +228,8 @@ int moe_cache_set_timing_events(moe_cache_t* h, void* const* events);
  *     codes (Bw bytes) and scales (Bs bytes), storage layout as in
  *     moe_host_layer_t, 16-byte aligned;
  *   gscale: host [k][3]; weights: host [k] (router weights, rank order);
- *   x: device bf16 [hidden]; out: device fp32 [hidden] (written).
+ *   x: device bf16 [hidden]; out: device fp32 [hidden] (written); both
+ *     16-byte aligned.
  * Allocates nothing: its scratch (about 1.1 MB: plan, h, per-expert partial
  * outputs, tile tickets) is one file-scope device array, fixed in size for
  * k <= MOE_MAX_TOPK and hidden, inter <= MOE_MAX_DIM, held by every GPU that

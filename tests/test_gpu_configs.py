@@ -165,6 +165,9 @@ def test_host_side_errors(lib):
     with pytest.raises(L.MoeError) as e:   # misaligned activations
         L.moe_cache_step(cache.h, 0, 1, lg_d.data_ptr(), x_d.data_ptr() + 2, out_d.data_ptr(), 0)
     assert e.value.code == L.MOE_ERR_ARG
+    with pytest.raises(L.MoeError) as e:   # misaligned output
+        L.moe_cache_step(cache.h, 0, 1, lg_d.data_ptr(), x_d.data_ptr(), out_d.data_ptr() + 4, 0)
+    assert e.value.code == L.MOE_ERR_ARG
     assert cache.stats(0)["steps"] == 0
     cache.close()
     banks.close()
