@@ -449,6 +449,131 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
+# ------------------------------------------------- multi-row / prefill rounds
+
+def run_rows(args) -> None:
+    """Multi-row rounds (M = 16, cached, tcgen05) or prefill (M = 512, bypass):
+    one JSON line for that workload.  Not the headline line; the default run
+    measures the one-row decode step."""
+    import torch
+
+    import workload
+    from harness import Banks, make_cache
+    import hbm_slot_cache_gb300 as hsc
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    hsc.build()
+    cfg = workload.CONFIGS[args.workload]
+    E, H, I, k, M = cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, cfg.rows
+    L = args.layers or cfg.layers
+    W, K = args.warmup, args.steps
+    if K * L > 4096:
+        raise SystemExit("--workload multirow/prefill: steps x layers must be <= 4096 (one graph)")
+    T = W + K
+    banks = Banks(cfg)
+    prefill = args.workload == "prefill"
+    cache = make_cache(cfg, banks, layers=L, trace_capacity=0 if prefill else T,
+                       max_rows=max(M, 16))
+    Bexp = banks.Bw + banks.Bs
+    # inputs: per (step, layer) logits; activations per step, shared by the layers
+    if prefill:
+        lgs = np.stack([np.stack([workload.prefill_logits(cfg, l, M) for l in range(L)])] * T)
+    else:
+        rts = [workload.Routing(cfg, layer=l) for l in range(L)]
+        lgs = np.stack([np.stack([rts[l].step() for l in range(L)]) for _ in range(T)])
+    xs = workload.activations(cfg.seed, 0, T, M, H)
+    lg_d = torch.from_numpy(lgs.astype(np.float32)).cuda()               # [T, L, M, E]
+    x_d = torch.from_numpy(xs.view(np.int16)).cuda().view(torch.bfloat16)  # [T, M, H]
+    out_d = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def run(t0, t1):
+        for t in range(t0, t1):
+            for l in range(L):
+                cache.step(l, lg_d[t, l], x_d[t], out_d)
+
+    with torch.cuda.stream(stream):
+        run(0, W)                                  # eager warm-up (fills the rings)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run(W, T)
+    with torch.cuda.stream(stream):
+        g.replay()                                 # upload; the rings move on, steady state
+    stream.synchronize()
+    s0 = cache.stats(-1)
+    sampler = ClockSampler(None)
+    time.sleep(0.15)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    s1 = cache.stats(-1)
+    layer_steps = K * L
+    misses = s1["misses"] - s0["misses"]
+    # experts each layer-step reads: the union of its rows' picks
+    if prefill:
+        ids = np.argsort(-lgs[0], axis=-1, kind="stable")[..., :k]        # [L, M, k]
+        union = float(np.mean([len(np.unique(ids[l])) for l in range(L)]))
+    else:
+        unions = []
+        for l in range(L):
+            recs = cache.trace(l)[-K:]
+            unions += [r.n_union for r in recs]
+        union = float(np.mean(unions))
+    hbm_peak, hbm_src = _peaks()
+    link_peak = None
+    hb = hsc.HostBank(1 << 30)
+    try:
+        dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+        link_peak = max(hsc.moe_probe_host_link(hb.ptr, dst.data_ptr(), 1 << 30, m, 5)
+                        for m in (0, 1))
+    finally:
+        hb.close()
+    s_layer = ms * 1e-3 / layer_steps
+    useful_flop = 2.0 * M * k * 3 * H * I                  # per layer-step
+    fp4_peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"] * 6.0 \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0 * 6.0
+    if prefill:
+        link_bytes = union * Bexp                          # every expert read over the link
+        t_roof = link_bytes / (link_peak * 1e9)
+        roof = {"bound": "host-link", "bytes_per_layer_step": link_bytes,
+                "t_roofline_ms": t_roof * 1e3, "frac": t_roof / s_layer, "peak_gbs": link_peak}
+        metric = "GLM-shape MoE prefill bypass rows/s (M=512, 8 layers, experts read from host)"
+    else:
+        hbm_bytes = union * Bexp
+        link_bytes = misses / layer_steps * Bexp
+        t_roof = hbm_bytes / (hbm_peak * 1e9) + link_bytes / (link_peak * 1e9)
+        roof = {"bound": "hbm+host-link", "hbm_bytes_per_layer_step": hbm_bytes,
+                "link_bytes_per_layer_step": link_bytes, "t_roofline_ms": t_roof * 1e3,
+                "frac": t_roof / s_layer, "hbm_peak_gbs": hbm_peak, "hbm_peak_source": hbm_src,
+                "link_peak_gbs": link_peak}
+        metric = "GLM-shape MoE multi-row round rows/s (M=16, 16 layers, S=128, tcgen05)"
+    line = {"metric": metric, "value": M * layer_steps / (ms * 1e-3), "unit": "rows/s",
+            "n_gpus": 1, "steps": K, "warmup": W, "ms_per_layer_step": s_layer * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 weights x residual nvfp4 activations, fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}: hidden {H}, inter {I}, {E} experts, top-{k}, "
+                                   f"M={M} rows, {L} layers, S={cfg.slots}",
+                       "graph": "one CUDA graph over the timed steps"},
+            "layer_steps_per_s": layer_steps / (ms * 1e-3),
+            "experts_read_per_layer_step": union, "misses_per_layer_step": misses / layer_steps,
+            "roofline": roof,
+            "tensor": {"useful_tflops": useful_flop / s_layer / 1e12,
+                       "fp4_peak_tflops": fp4_peak,
+                       "note": "useful = 2*M*k*3*H*I per layer-step; the MMA issues 6 "
+                               "activation levels in N=32 columns per 5 rows"},
+            "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    cache.close()
+    banks.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,11 +581,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="glm", choices=["glm", "multirow", "prefill"],
+                    help="glm: the one-row decode step (the headline line); multirow / "
+                         "prefill: M=16 rounds or M=512 bypass, their own line")
+    ap.add_argument("--layers", type=int, default=0, help="multirow/prefill: layers (0: config)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "glm":
+        run_rows(args)
     else:
         run_ours(args)
 

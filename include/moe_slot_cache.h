@@ -87,7 +87,7 @@ typedef struct {
   int all_resident;   /* 1: every expert lives in HBM (S = experts, loaded at create);
                          same kernels, used to check that caching changes no output bit */
   int trace_capacity; /* per-layer ring of moe_step_record_t for cached steps (0 = off) */
-  int max_rows;       /* largest rows of any step (sizes the bypass workspace); default 16 */
+  int max_rows;       /* largest rows of any step (sizes the bypass workspace); default 512 */
 } moe_cache_opts_t;
 
 typedef struct {
