@@ -54,8 +54,9 @@ def _src_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if taken on this source."""
+def _traffic(kernel: str, picks: float):
+    """dram bytes per launch of `picks` picks, from the committed ncu summary's bytes
+    per pick, if that summary was taken on this source (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -63,7 +64,7 @@ def _traffic(kernel: str):
     if d.get("src_sha") != _src_sha():
         return None
     k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("dram_bytes_per_launch")
+    return None if k is None else k["dram_bytes_per_pick"] * picks
 
 
 class ClockSampler:
@@ -370,7 +371,7 @@ def run_ours(args) -> None:
     }
     for n in kern:
         if "resident" in n:
-            kern[n]["traffic"] = _traffic(n.split("[")[0])
+            kern[n]["traffic"] = _traffic(n.split("[")[0], float(n_hit.mean()))
         elif "missed" in n:
             kern[n]["traffic"] = None
             kern[n]["note"] = "steps with at least one miss"
