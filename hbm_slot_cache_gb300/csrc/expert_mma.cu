@@ -19,9 +19,11 @@
 // K is walked in chunks of up to 256 elements: A (128 x 128 B) and B
 // (32 x 128 B) are copied with cp.async into the no-swizzle K-major core-matrix
 // layout (8 rows x 16 B per core matrix; K-adjacent cores 128 B apart, 8-row
-// groups 1 KB apart), the chunk's scale factors go to TMEM with tcgen05.st, and
-// one thread issues the chunk's MMAs and commits them to an mbarrier.  Two
-// stages: chunk c+1 loads while chunk c's MMAs run.
+// groups 1 KB apart), and each row's scale words for the chunk land beside
+// them.  Four stages: three chunks load while one computes.  Per chunk the
+// scale factors go from shared memory to TMEM with tcgen05.st (two slots, by
+// chunk parity), and one thread issues the chunk's MMAs and commits them to
+// the mbarrier of that parity.
 //
 // Scale-factor placement: each 32-bit TMEM word holds the four UE4M3 scales of
 // one row for one 64-element MMA step (byte b = elements 16b..16b+15).  Every
@@ -39,10 +41,13 @@ constexpr int kTileN = 32;
 constexpr int kMaxChunkBytes = 128;  // 256 FP4 elements per row per stage
 constexpr int kABytes = kTileM * kMaxChunkBytes;
 constexpr int kBBytes = kTileN * kMaxChunkBytes;
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSfaBytes = kTileM * 16;  // the chunk's scale words, 16 B a row
+constexpr int kSfbBytes = kTileN * 16;
+constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 22 KB
+constexpr int kStages = 4;
 constexpr int kTmemCols = 128;
 constexpr int kColD = 0, kColSF = 32;  // SF stage s: A at 32 + 32 s, B at 48 + 32 s
-constexpr int kSmemBytes = 48 * 1024;  // 2 stages + epilogue exchange; <= 4 CTAs/SM = TMEM
+constexpr int kSmemBytes = kStages * kStageBytes;  // 88 KB: two CTAs per SM
 
 struct MmaArgs {
   const GroupPlan* gp;
@@ -56,6 +61,13 @@ struct MmaArgs {
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// 8-byte piece (scale words of a 128-element chunk)
+__device__ __forceinline__ void cp_async8(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src),
                "r"(src_bytes)
                : "memory");
 }
@@ -87,7 +99,7 @@ template <int P>  // 16-byte pieces per row per chunk (8: 256 elements, 4: 128)
 __global__ void __launch_bounds__(kThreads)
 grouped_mma_kernel(MmaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_bar[2];  // MMA commits of even / odd chunks
   __shared__ uint32_t s_tmem;
   __shared__ int s_pick[kRowsPerJob], s_brow[kRowsPerJob];
   __shared__ float s_gl[kRowsPerJob][kLevels];
@@ -174,7 +186,8 @@ grouped_mma_kernel(MmaArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    mbar_init(&s_bar, 1);
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
     fence_mbar_init();
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -183,50 +196,59 @@ grouped_mma_kernel(MmaArgs a) {
   const uint32_t tmem = s_tmem;
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
-  auto load_chunk = [&](int c, int stage, uint32_t (&sfa)[4], uint32_t (&sfb)[4]) {
-    uint8_t* sA = smem + stage * kStageBytes;
-    uint8_t* sB = sA + kABytes;
+  // Chunk c goes to stage c % kStages: A and B codes in the core-matrix layout,
+  // then each row's scale words (A: this thread's row; B: warp 0, row = lane).
+  // Every thread commits one cp.async group per chunk (empty past the end), so
+  // "chunk c landed" is a fixed wait_group count.
+  auto load_chunk = [&](int c) {
+    if (c < nchunks) {
+      uint8_t* sA = smem + (c % kStages) * kStageBytes;
+      uint8_t* sB = sA + kABytes;
+      uint8_t* sSa = sB + kBBytes;
+      uint8_t* sSb = sSa + kSfaBytes;
 #pragma unroll
-    for (int i = 0; i < AR; ++i) {
-      const int r = tid / P + (kThreads / P) * i;
-      cp_async16(sA + (r >> 3) * 1024 + kc * 128 + (r & 7) * 16, a_src[i] + (size_t)c * CB, 16u);
-    }
+      for (int i = 0; i < AR; ++i) {
+        const int r = tid / P + (kThreads / P) * i;
+        cp_async16(sA + (r >> 3) * 1024 + kc * 128 + (r & 7) * 16, a_src[i] + (size_t)c * CB, 16u);
+      }
 #pragma unroll
-    for (int i = 0; i < BR; ++i) {
-      const int n = tid / P + (kThreads / P) * i;
-      cp_async16(sB + (n >> 3) * 1024 + kc * 128 + (n & 7) * 16,
-                 b_ok[i] ? b_src[i] + (size_t)c * CB : b_src[i], b_ok[i]);
+      for (int i = 0; i < BR; ++i) {
+        const int n = tid / P + (kThreads / P) * i;
+        cp_async16(sB + (n >> 3) * 1024 + kc * 128 + (n & 7) * 16,
+                   b_ok[i] ? b_src[i] + (size_t)c * CB : b_src[i], b_ok[i]);
+      }
+      constexpr int SW = CB / 8;  // scale bytes per row per chunk: 16 or 8
+      if constexpr (SW == 16) {
+        cp_async16(sSa + 16 * tid, sa_src + (size_t)c * SW, 16u);
+        if (warp == 0) cp_async16(sSb + 16 * lane, sb_src ? sb_src + (size_t)c * SW : sa_src, sb_src ? 16u : 0u);
+      } else {
+        cp_async8(sSa + 16 * tid, sa_src + (size_t)c * SW, 8u);
+        if (warp == 0) cp_async8(sSb + 16 * lane, sb_src ? sb_src + (size_t)c * SW : sa_src, sb_src ? 8u : 0u);
+      }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    // scales: CB/8 bytes per row per chunk (one 32-bit word per MMA step)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      sfa[q] = 0u;
-      sfb[q] = 0u;
-    }
-#pragma unroll
-    for (int q = 0; q < KSTEPS; ++q) {
-      sfa[q] = __ldg(reinterpret_cast<const uint32_t*>(sa_src + (size_t)c * (CB / 8)) + q);
-      if (sb_src) sfb[q] = __ldg(reinterpret_cast<const uint32_t*>(sb_src + (size_t)c * (CB / 8)) + q);
-    }
   };
 
-  uint32_t sfa[2][4], sfb[2][4];
-  load_chunk(0, 0, sfa[0], sfb[0]);
+#pragma unroll
+  for (int c = 0; c < kStages - 1; ++c) load_chunk(c);
   bool ok = true;
   for (int c = 0; c < nchunks; ++c) {
-    const int st = c & 1;
-    if (c + 1 < nchunks) {
-      if (c >= 1) {  // chunk c-1's MMAs read the stage chunk c+1 is about to fill
-        if (!mbar_wait_bounded(&s_bar, (uint32_t)((c - 1) & 1), a.flags)) s_fail = 1;
-      }
-      load_chunk(c + 1, st ^ 1, sfa[st ^ 1], sfb[st ^ 1]);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    const int st = c % kStages, sf = c & 1;
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 2) : "memory");  // chunk c landed
+    __syncthreads();
+    // MMA(c-1) done => its stage may refill, and SF slot c & 1 (last read by MMA(c-2)) is free
+    if (c >= 1 && !mbar_wait_bounded(&s_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1), a.flags))
+      s_fail = 1;
+    load_chunk(c + kStages - 1);
+    const uint8_t* sSa = smem + st * kStageBytes + kABytes + kBBytes;
+    uint32_t w[4], wb[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      w[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + 16 * tid)[q] : 0u;
+      wb[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + kSfaBytes + 16 * lane)[q] : 0u;
     }
-    tmem_st16(tmem + lane_base + kColSF + 32 * st, sfa[st]);
-    tmem_st16(tmem + lane_base + kColSF + 32 * st + 16, sfb[st]);
+    tmem_st16(tmem + lane_base + kColSF + 32 * sf, w);
+    tmem_st16(tmem + lane_base + kColSF + 32 * sf + 16, wb);
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -242,8 +264,8 @@ grouped_mma_kernel(MmaArgs a) {
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
         const uint64_t da = umma_desc(sA + 256 * ks), db = umma_desc(sB + 256 * ks);
-        const uint32_t sfa_t = tmem + kColSF + 32 * st + 4 * ks;
-        const uint32_t sfb_t = tmem + kColSF + 32 * st + 16 + 4 * ks;
+        const uint32_t sfa_t = tmem + kColSF + 32 * sf + 4 * ks;
+        const uint32_t sfb_t = tmem + kColSF + 32 * sf + 16 + 4 * ks;
         const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
@@ -254,11 +276,13 @@ grouped_mma_kernel(MmaArgs a) {
       }
       asm volatile(
           "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-              smem_addr(&s_bar))
+              smem_addr(&s_bar[sf]))
           : "memory");
     }
   }
-  if (ok && !mbar_wait_bounded(&s_bar, (uint32_t)((nchunks - 1) & 1), a.flags)) s_fail = 1;
+  if (ok && !mbar_wait_bounded(&s_bar[(nchunks - 1) & 1], (uint32_t)(((nchunks - 1) >> 1) & 1),
+                               a.flags))
+    s_fail = 1;
   asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing may land after exit
   __syncthreads();
   ok = s_fail == 0;  // uniform across the CTA
@@ -333,6 +357,7 @@ cudaError_t run_mma(cudaStream_t st, const MmaArgs& a, int max_jobs, int m_tiles
   static bool set = false;
   if (!set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess) e = prefer_max_shared(kern);
     if (e != cudaSuccess) return e;
     set = true;
   }
