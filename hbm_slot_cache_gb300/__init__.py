@@ -60,7 +60,8 @@ class MoeCache:
     (or pinned torch CPU uint8 tensors) and gscale a float32 array [E, 3]."""
 
     def __init__(self, layers, experts, slots, hidden, inter, top_k, host_layers, *,
-                 all_resident=False, trace_capacity=0, bypass_rows=0, max_rows=0):
+                 all_resident=False, trace_capacity=0, bypass_rows=0, max_rows=0,
+                 prefill_chunk=0):
         self.layers, self.experts, self.hidden, self.inter, self.top_k = (
             layers, experts, hidden, inter, top_k)
         self.slots = experts if all_resident else slots
@@ -73,7 +74,8 @@ class MoeCache:
             ptrs.append((self._host_ptr(w), self._host_ptr(s), g.ctypes.data))
         self.h = moe_cache_create(layers, experts, slots, hidden, inter, top_k, ptrs,
                                   all_resident=all_resident, trace_capacity=trace_capacity,
-                                  bypass_rows=bypass_rows, max_rows=max_rows)
+                                  bypass_rows=bypass_rows, max_rows=max_rows,
+                                  prefill_chunk=prefill_chunk)
         self.trace_capacity = trace_capacity
 
     @staticmethod

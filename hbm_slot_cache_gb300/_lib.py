@@ -47,7 +47,7 @@ class HostLayer(ctypes.Structure):
 class Opts(ctypes.Structure):
     _fields_ = [("copy_backend", ctypes.c_int), ("bypass_rows", ctypes.c_int),
                 ("all_resident", ctypes.c_int), ("trace_capacity", ctypes.c_int),
-                ("max_rows", ctypes.c_int)]
+                ("max_rows", ctypes.c_int), ("prefill_chunk", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):
@@ -128,10 +128,10 @@ def moe_expert_bytes(hidden: int, inter: int) -> tuple[int, int]:
 def moe_cache_create(layers: int, experts: int, slots: int, hidden: int, inter: int, top_k: int,
                      host_layers, copy_backend: int = MOE_COPY_SM, bypass_rows: int = 0,
                      all_resident: bool = False, trace_capacity: int = 0,
-                     max_rows: int = 0) -> int:
+                     max_rows: int = 0, prefill_chunk: int = 0) -> int:
     """host_layers: sequence of (w_ptr, s_ptr, gscale_ptr) per layer. Returns the handle."""
     arr = (HostLayer * layers)(*[HostLayer(int(w), int(s), int(g)) for (w, s, g) in host_layers])
-    o = Opts(copy_backend, bypass_rows, int(all_resident), trace_capacity, max_rows)
+    o = Opts(copy_backend, bypass_rows, int(all_resident), trace_capacity, max_rows, prefill_chunk)
     h = ctypes.c_void_p()
     _check(lib().moe_cache_create(ctypes.byref(h), layers, experts, slots, hidden, inter, top_k,
                                   ctypes.cast(arr, ctypes.c_void_p), ctypes.byref(o)),

@@ -57,6 +57,7 @@ struct MmaArgs {
   QuantBuf act; // gate/up: by token row; down: by pick
   float* out;   // gate/up: h [P][I]; down: y [P][H]
   uint32_t* flags;
+  int g0, g1;   // the launch's groups [g0, g1)
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
@@ -105,79 +106,20 @@ grouped_mma_kernel(MmaArgs a) {
   __shared__ float s_gl[kRowsPerJob][kLevels];
   __shared__ int s_fail;
   const GroupPlan* gp = a.gp;
-  const int job = blockIdx.x;
-  if (job >= gp->n_jobs) return;  // uniform: before any TMEM or barrier use
+  // this launch's jobs: those of groups [g0, g1)
+  const int ng = gp->n_groups;
+  const int jbeg = a.g0 < ng ? gp->g_job[a.g0] : gp->n_jobs;
+  const int jend = gp->g_job[a.g1 < ng ? a.g1 : ng];
+  if (jbeg + (int)blockIdx.x >= jend) return;  // uniform: before any TMEM or barrier use
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.y;
-  const int jv = gp->jobs[job];
-  const int g = jv >> 8, tile = jv & 255;
-  const int gstart = gp->g_start[g], gcount = gp->g_count[g];
-  const int m0 = tile * kRowsPerJob;
-  const int nmem = min(kRowsPerJob, gcount - m0);
   const int K = a.K, H = a.H, I = a.I;
   constexpr int CB = P * 16;             // bytes per row per chunk
   constexpr int KSTEPS = CB / 32;        // 64-element MMA steps per chunk
   const int nchunks = K / (2 * CB);
-
-  if (tid < kRowsPerJob) {
-    int p = -1, br = 0;
-    if (tid < nmem) {
-      p = gp->members[gstart + m0 + tid];
-      br = a.gate_up ? p / a.k : p;
-    }
-    s_pick[tid] = p;
-    s_brow[tid] = br;
-  }
-  if (tid == 0) s_fail = 0;
-  __syncthreads();
-  if (tid < kRowsPerJob * kLevels) {
-    const int s = tid / kLevels, l = tid - s * kLevels;
-    s_gl[s][l] = (s < nmem) ? a.act.gl[(size_t)s_brow[s] * kLevels + l] : 0.f;
-  }
-
-  // weight rows of this tile
-  const uint8_t* wbase = gp->g_wptr[g];
-  const uint8_t* sbase = gp->g_sptr[g];
-  size_t row_stride_w, row_stride_s;
-  if (a.gate_up) {
-    row_stride_w = H / 2;
-    row_stride_s = H / 16;
-  } else {
-    wbase += (size_t)I * H;
-    sbase += (size_t)I * H / 8;
-    row_stride_w = I / 2;
-    row_stride_s = I / 16;
-  }
-  auto src_row = [&](int r) -> size_t {  // tile row -> row index within the matrix block
-    if (a.gate_up) return r < 64 ? (size_t)(64 * mt + r) : (size_t)(I + 64 * mt + r - 64);
-    return (size_t)(kTileM * mt + r);
-  };
-
-  // this thread's cp.async pieces: A rows tid/P + (128/P) i, piece tid % P
   constexpr int AR = kTileM * P / kThreads;  // A rows per thread
   constexpr int BR = kTileN * P / kThreads;  // B rows per thread
   const int kc = tid % P;
-  const uint8_t* a_src[AR];
-#pragma unroll
-  for (int i = 0; i < AR; ++i) a_src[i] = wbase + src_row(tid / P + (kThreads / P) * i) * row_stride_w + kc * 16;
-  const uint8_t* b_src[BR];
-  uint32_t b_ok[BR];
-#pragma unroll
-  for (int i = 0; i < BR; ++i) {
-    const int n = tid / P + (kThreads / P) * i;
-    const int s = n / kLevels, l = n - s * kLevels;
-    const bool ok = n < kRowsPerJob * kLevels && s < nmem;
-    b_ok[i] = ok ? 16u : 0u;
-    b_src[i] = ok ? a.act.codes + ((size_t)s_brow[s] * kLevels + l) * (K / 2) + kc * 16 : a.act.codes;
-  }
-  // this thread's scale rows: A row 32*warp + lane, B row lane
-  const uint8_t* sa_src = sbase + src_row(32 * warp + lane) * row_stride_s;
-  const uint8_t* sb_src = nullptr;
-  {
-    const int s = lane / kLevels, l = lane - s * kLevels;
-    if (lane < kRowsPerJob * kLevels && s < nmem)
-      sb_src = a.act.scales + ((size_t)s_brow[s] * kLevels + l) * (K / 16);
-  }
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -189,106 +131,176 @@ grouped_mma_kernel(MmaArgs a) {
     mbar_init(&s_bar[0], 1);
     mbar_init(&s_bar[1], 1);
     fence_mbar_init();
+    s_fail = 0;
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
   const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  int gc = 0;  // chunks this CTA has committed: barrier phases continue across jobs
 
-  // Chunk c goes to stage c % kStages: A and B codes in the core-matrix layout,
-  // then each row's scale words (A: this thread's row; B: warp 0, row = lane).
-  // Every thread commits one cp.async group per chunk (empty past the end), so
-  // "chunk c landed" is a fixed wait_group count.
-  auto load_chunk = [&](int c) {
-    if (c < nchunks) {
-      uint8_t* sA = smem + (c % kStages) * kStageBytes;
-      uint8_t* sB = sA + kABytes;
-      uint8_t* sSa = sB + kBBytes;
-      uint8_t* sSb = sSa + kSfaBytes;
-#pragma unroll
-      for (int i = 0; i < AR; ++i) {
-        const int r = tid / P + (kThreads / P) * i;
-        cp_async16(sA + (r >> 3) * 1024 + kc * 128 + (r & 7) * 16, a_src[i] + (size_t)c * CB, 16u);
+  for (int job = jbeg + blockIdx.x; job < jend; job += gridDim.x) {
+    const int jv = gp->jobs[job];
+    const int g = jv >> 8, tile = jv & 255;
+    const int gstart = gp->g_start[g], gcount = gp->g_count[g];
+    const int m0 = tile * kRowsPerJob;
+    const int nmem = min(kRowsPerJob, gcount - m0);
+    if (tid < kRowsPerJob) {
+      int p = -1, br = 0;
+      if (tid < nmem) {
+        p = gp->members[gstart + m0 + tid];
+        br = a.gate_up ? p / a.k : p;
       }
-#pragma unroll
-      for (int i = 0; i < BR; ++i) {
-        const int n = tid / P + (kThreads / P) * i;
-        cp_async16(sB + (n >> 3) * 1024 + kc * 128 + (n & 7) * 16,
-                   b_ok[i] ? b_src[i] + (size_t)c * CB : b_src[i], b_ok[i]);
-      }
-      constexpr int SW = CB / 8;  // scale bytes per row per chunk: 16 or 8
-      if constexpr (SW == 16) {
-        cp_async16(sSa + 16 * tid, sa_src + (size_t)c * SW, 16u);
-        if (warp == 0) cp_async16(sSb + 16 * lane, sb_src ? sb_src + (size_t)c * SW : sa_src, sb_src ? 16u : 0u);
-      } else {
-        cp_async8(sSa + 16 * tid, sa_src + (size_t)c * SW, 8u);
-        if (warp == 0) cp_async8(sSb + 16 * lane, sb_src ? sb_src + (size_t)c * SW : sa_src, sb_src ? 8u : 0u);
-      }
+      s_pick[tid] = p;
+      s_brow[tid] = br;
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
+    __syncthreads();
+    if (tid < kRowsPerJob * kLevels) {
+      const int s = tid / kLevels, l = tid - s * kLevels;
+      s_gl[s][l] = (s < nmem) ? a.act.gl[(size_t)s_brow[s] * kLevels + l] : 0.f;
+    }
+
+    // weight rows of this tile
+    const uint8_t* wbase = gp->g_wptr[g];
+    const uint8_t* sbase = gp->g_sptr[g];
+    size_t row_stride_w, row_stride_s;
+    if (a.gate_up) {
+      row_stride_w = H / 2;
+      row_stride_s = H / 16;
+    } else {
+      wbase += (size_t)I * H;
+      sbase += (size_t)I * H / 8;
+      row_stride_w = I / 2;
+      row_stride_s = I / 16;
+    }
+    auto src_row = [&](int r) -> size_t {  // tile row -> row index within the matrix block
+      if (a.gate_up) return r < 64 ? (size_t)(64 * mt + r) : (size_t)(I + 64 * mt + r - 64);
+      return (size_t)(kTileM * mt + r);
+    };
+    // this thread's cp.async pieces: A rows tid/P + (128/P) i, piece tid % P
+    const uint8_t* a_src[AR];
+#pragma unroll
+    for (int i = 0; i < AR; ++i)
+      a_src[i] = wbase + src_row(tid / P + (kThreads / P) * i) * row_stride_w + kc * 16;
+    const uint8_t* b_src[BR];
+    uint32_t b_ok[BR];
+#pragma unroll
+    for (int i = 0; i < BR; ++i) {
+      const int n = tid / P + (kThreads / P) * i;
+      const int s = n / kLevels, l = n - s * kLevels;
+      const bool ok = n < kRowsPerJob * kLevels && s < nmem;
+      b_ok[i] = ok ? 16u : 0u;
+      b_src[i] = ok ? a.act.codes + ((size_t)s_brow[s] * kLevels + l) * (K / 2) + kc * 16 : a.act.codes;
+    }
+    // this thread's scale rows: A row 32*warp + lane, B row lane
+    const uint8_t* sa_src = sbase + src_row(32 * warp + lane) * row_stride_s;
+    const uint8_t* sb_src = nullptr;
+    {
+      const int s = lane / kLevels, l = lane - s * kLevels;
+      if (lane < kRowsPerJob * kLevels && s < nmem)
+        sb_src = a.act.scales + ((size_t)s_brow[s] * kLevels + l) * (K / 16);
+    }
+
+    // Chunk c goes to stage c % kStages: A and B codes in the core-matrix layout,
+    // then each row's scale words (A: this thread's row; B: warp 0, row = lane).
+    // Every thread commits one cp.async group per chunk (empty past the end), so
+    // "chunk c landed" is a fixed wait_group count.
+    auto load_chunk = [&](int c) {
+      if (c < nchunks) {
+        uint8_t* sA = smem + (c % kStages) * kStageBytes;
+        uint8_t* sB = sA + kABytes;
+        uint8_t* sSa = sB + kBBytes;
+        uint8_t* sSb = sSa + kSfaBytes;
+#pragma unroll
+        for (int i = 0; i < AR; ++i) {
+          const int r = tid / P + (kThreads / P) * i;
+          cp_async16(sA + (r >> 3) * 1024 + kc * 128 + (r & 7) * 16, a_src[i] + (size_t)c * CB, 16u);
+        }
+#pragma unroll
+        for (int i = 0; i < BR; ++i) {
+          const int n = tid / P + (kThreads / P) * i;
+          cp_async16(sB + (n >> 3) * 1024 + kc * 128 + (n & 7) * 16,
+                     b_ok[i] ? b_src[i] + (size_t)c * CB : b_src[i], b_ok[i]);
+        }
+        constexpr int SW = CB / 8;  // scale bytes per row per chunk: 16 or 8
+        if constexpr (SW == 16) {
+          cp_async16(sSa + 16 * tid, sa_src + (size_t)c * SW, 16u);
+          if (warp == 0)
+            cp_async16(sSb + 16 * lane, sb_src ? sb_src + (size_t)c * SW : sa_src, sb_src ? 16u : 0u);
+        } else {
+          cp_async8(sSa + 16 * tid, sa_src + (size_t)c * SW, 8u);
+          if (warp == 0)
+            cp_async8(sSb + 16 * lane, sb_src ? sb_src + (size_t)c * SW : sa_src, sb_src ? 8u : 0u);
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
 
 #pragma unroll
-  for (int c = 0; c < kStages - 1; ++c) load_chunk(c);
-  bool ok = true;
-  for (int c = 0; c < nchunks; ++c) {
-    const int st = c % kStages, sf = c & 1;
-    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 2) : "memory");  // chunk c landed
-    __syncthreads();
-    // MMA(c-1) done => its stage may refill, and SF slot c & 1 (last read by MMA(c-2)) is free
-    if (c >= 1 && !mbar_wait_bounded(&s_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1), a.flags))
-      s_fail = 1;
-    load_chunk(c + kStages - 1);
-    const uint8_t* sSa = smem + st * kStageBytes + kABytes + kBBytes;
-    uint32_t w[4], wb[4];
+    for (int c = 0; c < kStages - 1; ++c) load_chunk(c);
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % kStages, sf = (gc + c) & 1;
+      asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 2) : "memory");  // chunk c landed
+      __syncthreads();
+      // MMA(c-1) done => its stage may refill, and SF slot sf (last read by MMA(c-2)) is free
+      if (c >= 1) {
+        const int pc = gc + c - 1;
+        if (!mbar_wait_bounded(&s_bar[pc & 1], (uint32_t)((pc >> 1) & 1), a.flags)) s_fail = 1;
+      }
+      load_chunk(c + kStages - 1);
+      const uint8_t* sSa = smem + st * kStageBytes + kABytes + kBBytes;
+      uint32_t w[4], wb[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      w[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + 16 * tid)[q] : 0u;
-      wb[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + kSfaBytes + 16 * lane)[q] : 0u;
-    }
-    tmem_st16(tmem + lane_base + kColSF + 32 * sf, w);
-    tmem_st16(tmem + lane_base + kColSF + 32 * sf + 16, wb);
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (s_fail) {
-      ok = false;
-      break;
-    }
-    if (tid == 0) {
-      const uint32_t sA = smem_addr(smem + st * kStageBytes);
-      const uint32_t sB = sA + kABytes;
+      for (int q = 0; q < 4; ++q) {
+        w[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + 16 * tid)[q] : 0u;
+        wb[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + kSfaBytes + 16 * lane)[q] : 0u;
+      }
+      tmem_st16(tmem + lane_base + kColSF + 32 * sf, w);
+      tmem_st16(tmem + lane_base + kColSF + 32 * sf + 16, wb);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncthreads();
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (s_fail) {
+        ok = false;
+        break;
+      }
+      if (tid == 0) {
+        const uint32_t sA = smem_addr(smem + st * kStageBytes);
+        const uint32_t sB = sA + kABytes;
 #pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        const uint64_t da = umma_desc(sA + 256 * ks), db = umma_desc(sB + 256 * ks);
-        const uint32_t sfa_t = tmem + kColSF + 32 * sf + 4 * ks;
-        const uint32_t sfb_t = tmem + kColSF + 32 * sf + 16 + 4 * ks;
-        const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const uint64_t da = umma_desc(sA + 256 * ks), db = umma_desc(sB + 256 * ks);
+          const uint32_t sfa_t = tmem + kColSF + 32 * sf + 4 * ks;
+          const uint32_t sfb_t = tmem + kColSF + 32 * sf + 16 + 4 * ks;
+          const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                  tmem + kColD),
+              "l"(da), "l"(db), "r"(umma_idesc()), "r"(sfa_t), "r"(sfb_t), "r"(acc)
+              : "memory");
+        }
         asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                tmem + kColD),
-            "l"(da), "l"(db), "r"(umma_idesc()), "r"(sfa_t), "r"(sfb_t), "r"(acc)
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                smem_addr(&s_bar[sf]))
             : "memory");
       }
-      asm volatile(
-          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-              smem_addr(&s_bar[sf]))
-          : "memory");
     }
-  }
-  if (ok && !mbar_wait_bounded(&s_bar[(nchunks - 1) & 1], (uint32_t)(((nchunks - 1) >> 1) & 1),
-                               a.flags))
-    s_fail = 1;
-  asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing may land after exit
-  __syncthreads();
-  ok = s_fail == 0;  // uniform across the CTA
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (ok) {
+      const int pc = gc + nchunks - 1;
+      if (!mbar_wait_bounded(&s_bar[pc & 1], (uint32_t)((pc >> 1) & 1), a.flags)) s_fail = 1;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing may land after exit
+    __syncthreads();
+    ok = s_fail == 0;  // uniform across the CTA
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!ok) break;  // a timed-out wait leaves the barrier phases unknown: stop here
+    gc += nchunks;
 
-  if (ok) {
     uint32_t v[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -327,8 +339,10 @@ grouped_mma_kernel(MmaArgs a) {
       for (int s = 0; s < nmem; ++s)
         a.out[(size_t)s_pick[s] * H + kTileM * mt + row] = gsc[2] * val[s];
     }
-  } else {
+    // the next job rewrites s_pick / s_gl and the stages; TMEM reads are done
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -352,7 +366,7 @@ __global__ void combine_kernel(const GroupPlan* __restrict__ gp, const float* __
 }
 
 template <int P>
-cudaError_t run_mma(cudaStream_t st, const MmaArgs& a, int max_jobs, int m_tiles) {
+cudaError_t run_mma(cudaStream_t st, const MmaArgs& a, int grid_x, int m_tiles) {
   auto kern = grouped_mma_kernel<P>;
   static bool set = false;
   if (!set) {
@@ -361,7 +375,7 @@ cudaError_t run_mma(cudaStream_t st, const MmaArgs& a, int max_jobs, int m_tiles
     if (e != cudaSuccess) return e;
     set = true;
   }
-  kern<<<dim3(max_jobs, m_tiles), kThreads, kSmemBytes, st>>>(a);
+  kern<<<dim3(grid_x, m_tiles), kThreads, kSmemBytes, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -372,10 +386,10 @@ bool mma_supported(int H, int I) {
   return ok(H) && ok(I) && I % 64 == 0 && H % 128 == 0;
 }
 
-cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int max_jobs, bool gate_up,
+cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int grid_x, bool gate_up,
                                int H, int I, int k, const QuantBuf& act, float* out,
-                               uint32_t* flags) {
-  if (max_jobs <= 0) return cudaSuccess;
+                               uint32_t* flags, int g0, int g1) {
+  if (grid_x <= 0) return cudaSuccess;
   MmaArgs a;
   a.gp = gp;
   a.K = gate_up ? H : I;
@@ -386,9 +400,11 @@ cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int max_job
   a.act = act;
   a.out = out;
   a.flags = flags;
+  a.g0 = g0;
+  a.g1 = g1;
   const int m_tiles = gate_up ? I / 64 : H / kTileM;
-  if (a.K >= 256) return run_mma<8>(st, a, max_jobs, m_tiles);
-  return run_mma<4>(st, a, max_jobs, m_tiles);
+  if (a.K >= 256) return run_mma<8>(st, a, grid_x, m_tiles);
+  return run_mma<4>(st, a, grid_x, m_tiles);
 }
 
 cudaError_t launch_combine(cudaStream_t st, const GroupPlan* gp, const float* y, float* out,

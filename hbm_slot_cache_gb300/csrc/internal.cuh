@@ -75,6 +75,7 @@ struct GroupPlan {
   int32_t* members;        // [P] pick indices grouped
   int32_t* jobs;           // [J] (group << 8) | tile
   float* wts;              // [P] router weights by pick
+  int32_t* g_job;          // [G + 1] first job of each group; [n_groups] = n_jobs
 };
 
 // Activations in residual NVFP4: codes [rows][kLevels][K/2], scales
@@ -100,10 +101,20 @@ cudaError_t launch_route_rows(cudaStream_t st, const float* logits, int rows, in
 cudaError_t launch_quantize_rows(cudaStream_t st, const void* src, bool bf16_in, int rows, int K,
                                  const QuantBuf& q);
 // grouped tcgen05 expert matmuls: gate/up + SwiGLU -> h [P][I], or down -> y [P][H].
+// Jobs of groups [g0, g1) (all groups: g0 = 0, g1 = INT_MAX); grid_x CTAs per weight tile
+// loop over them.
 bool mma_supported(int H, int I);
-cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int max_jobs, bool gate_up,
+cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int grid_x, bool gate_up,
                                int H, int I, int k, const QuantBuf& act, float* out,
-                               uint32_t* flags);
+                               uint32_t* flags, int g0 = 0, int g1 = 0x7FFFFFFF);
+// residual-NVFP4 quantisation of the rows of src named by the members of groups [g0, g1)
+cudaError_t launch_quantize_members(cudaStream_t st, const float* src, int K, const GroupPlan* gp,
+                                    int g0, int g1, const QuantBuf& q, int grid);
+// staged prefill: copy the experts of groups [q*C, q*C + C) host -> staging half (q & 1) and
+// point the groups' weight pointers at the staged bytes
+cudaError_t launch_stage_copy(cudaStream_t st, GroupPlan* gp, int q, int C, const LayerDev& L,
+                              uint8_t* stage_w, uint8_t* stage_s, long long Bw, long long Bs,
+                              int grid);
 // out[m] = sum_j w[m,j] y[m*k+j], rank order.
 cudaError_t launch_combine(cudaStream_t st, const GroupPlan* gp, const float* y, float* out,
                            int rows, int H, int k);

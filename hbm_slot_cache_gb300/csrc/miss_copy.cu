@@ -56,6 +56,38 @@ miss_copy_kernel(const Plan* __restrict__ plan, const uint8_t* __restrict__ host
   }
 }
 
+// Staged prefill ("GB300 GLM 5.3 Testing": stage a prefill's experts into HBM
+// by DMA, up to 64 at a time, and run the grouped kernel from there): the
+// experts of groups [q*C, q*C + C) go host -> staging half (q & 1), each read
+// once over the host link, and those groups' pointers are set to the staged
+// bytes for the grouped MMAs that follow.
+__global__ void __launch_bounds__(kThreads)
+stage_copy_kernel(GroupPlan* __restrict__ gp, int q, int C, LayerDev L, uint8_t* __restrict__ stage_w,
+                  uint8_t* __restrict__ stage_s, long long Bw, long long Bs) {
+  const int ng = gp->n_groups;
+  const int g0 = q * C;
+  if (g0 >= ng) return;
+  const int n = min(C, ng - g0);
+  const int half = (q & 1) * C;
+  const long long ncw = (Bw + kChunk - 1) / kChunk;
+  const long long ncs = (Bs + kChunk - 1) / kChunk;
+  const long long nc = ncw + ncs;
+  for (long long c = blockIdx.x; c < (long long)n * nc; c += gridDim.x) {
+    const int i = (int)(c / nc);
+    const long long r = c - (long long)i * nc;
+    const long long e = gp->g_expert[g0 + i], b = half + i;
+    if (r < ncw)
+      copy_chunk(L.host_w + e * Bw, stage_w + b * Bw, r * kChunk, Bw);
+    else
+      copy_chunk(L.host_s + e * Bs, stage_s + b * Bs, (r - ncw) * kChunk, Bs);
+  }
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      gp->g_wptr[g0 + i] = stage_w + (long long)(half + i) * Bw;
+      gp->g_sptr[g0 + i] = stage_s + (long long)(half + i) * Bs;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads)
 link_probe_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, long long bytes) {
   const long long nc = (bytes + kChunk - 1) / kChunk;
@@ -74,6 +106,19 @@ cudaError_t launch_miss_copy(cudaStream_t st, const Plan* plan, const uint8_t* h
     once = true;
   }
   miss_copy_kernel<<<grid, kThreads, 0, st>>>(plan, host_w, host_s, slot_w, slot_s, Bw, Bs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stage_copy(cudaStream_t st, GroupPlan* gp, int q, int C, const LayerDev& L,
+                              uint8_t* stage_w, uint8_t* stage_s, long long Bw, long long Bs,
+                              int grid) {
+  static bool once = false;
+  if (!once) {
+    cudaError_t e = prefer_max_shared(stage_copy_kernel);
+    if (e != cudaSuccess) return e;
+    once = true;
+  }
+  stage_copy_kernel<<<grid, kThreads, 0, st>>>(gp, q, C, L, stage_w, stage_s, Bw, Bs);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <algorithm>
 #include <vector>
 
 #include "internal.cuh"
@@ -15,6 +16,7 @@ using namespace moe;
 
 namespace {
 constexpr int kDefaultMaxRows = 512;  // largest prefill chunk a handle takes by default
+constexpr int kDefaultPrefillChunk = 32;  // experts staged per prefill chunk (two chunks held)
 }
 
 struct moe_cache {
@@ -47,6 +49,11 @@ struct moe_cache {
   // one-row steps fork the miss path onto a second stream
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  // staged prefill: two halves of `chunk` expert slots, events per chunk
+  int chunk = 0, nchunks = 0;
+  uint8_t* stage_w = nullptr;  // [2 * chunk][Bw]
+  uint8_t* stage_s = nullptr;  // [2 * chunk][Bs]
+  std::vector<cudaEvent_t> ev_staged, ev_used;  // [nchunks]
   // optional per-kernel timing events (caller-owned)
   cudaEvent_t ev[MOE_TIMING_EVENTS] = {};
   bool timing = false;
@@ -78,6 +85,10 @@ void free_all(moe_cache* h) {
   cudaFree(h->gemv.tile_cnt);
   for (void* p : h->extra) cudaFree(p);
   h->extra.clear();
+  for (cudaEvent_t e : h->ev_staged) cudaEventDestroy(e);
+  for (cudaEvent_t e : h->ev_used) cudaEventDestroy(e);
+  h->ev_staged.clear();
+  h->ev_used.clear();
   if (h->fork) cudaEventDestroy(h->fork);
   if (h->join) cudaEventDestroy(h->join);
   if (h->side) cudaStreamDestroy(h->side);
@@ -109,6 +120,7 @@ bool alloc_multirow(moe_cache* h) {
   g.members = static_cast<int32_t*>(get(4 * P));
   g.jobs = static_cast<int32_t*>(get(4 * J));
   g.wts = static_cast<float*>(get(4 * P));
+  g.g_job = static_cast<int32_t*>(get(4 * (G + 1)));
   h->gp = static_cast<GroupPlan*>(get(sizeof(GroupPlan)));
   h->ids_ws = static_cast<int32_t*>(get(4 * P));
   h->xq.codes = static_cast<uint8_t*>(get(R * kLevels * (h->H / 2)));
@@ -120,7 +132,7 @@ bool alloc_multirow(moe_cache* h) {
   for (void* p : h->extra)
     if (!p) return false;
   if (!g.g_expert || !g.g_start || !g.g_count || !g.g_wptr || !g.g_sptr || !g.g_gs ||
-      !g.members || !g.jobs || !g.wts || !h->gp || !h->ids_ws || !h->xq.codes || !h->xq.scales ||
+      !g.members || !g.jobs || !g.wts || !g.g_job || !h->gp || !h->ids_ws || !h->xq.codes || !h->xq.scales ||
       !h->xq.gl || !h->hq.codes || !h->hq.scales || !h->hq.gl)
     return false;
   return cudaMemcpy(h->gp, &g, sizeof g, cudaMemcpyHostToDevice) == cudaSuccess;
@@ -203,7 +215,11 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
     o = *opts;
     if (o.bypass_rows <= 0) o.bypass_rows = MOE_MAX_CACHED_ROWS;
     if (o.max_rows <= 0) o.max_rows = kDefaultMaxRows;
+    if (o.prefill_chunk == 0) o.prefill_chunk = kDefaultPrefillChunk;
+  } else {
+    o.prefill_chunk = kDefaultPrefillChunk;
   }
+  if (o.prefill_chunk < -1) return MOE_ERR_ARG;
   if (layers < 1 || experts < 1 || top_k < 1 || hidden < 1 || inter < 1 || !host_backing)
     return MOE_ERR_ARG;
   if (o.trace_capacity < 0 || o.copy_backend != MOE_COPY_SM) return MOE_ERR_ARG;
@@ -269,6 +285,26 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
             dalloc(&h->gemv.tile_cnt, (size_t)(hidden / gemv_down_tile_rows(hidden, inter) + 1)) ==
                 cudaSuccess;
   ok = ok && alloc_multirow(h);
+  if (ok && o.max_rows > o.bypass_rows && o.prefill_chunk > 0) {
+    // staged prefill: two halves of `chunk` expert slots, two events per chunk
+    h->chunk = o.prefill_chunk < experts ? o.prefill_chunk : experts;
+    h->nchunks = (experts + h->chunk - 1) / h->chunk;
+    void* w = nullptr;
+    void* sc = nullptr;
+    ok = cudaMalloc(&w, (size_t)2 * h->chunk * h->Bw) == cudaSuccess;
+    if (w) h->extra.push_back(w);
+    ok = ok && cudaMalloc(&sc, (size_t)2 * h->chunk * h->Bs) == cudaSuccess;
+    if (sc) h->extra.push_back(sc);
+    h->stage_w = static_cast<uint8_t*>(w);
+    h->stage_s = static_cast<uint8_t*>(sc);
+    for (int q = 0; ok && q < h->nchunks; ++q) {
+      cudaEvent_t a = nullptr, b = nullptr;
+      ok = cudaEventCreateWithFlags(&a, cudaEventDisableTiming) == cudaSuccess;
+      if (a) h->ev_staged.push_back(a);
+      ok = ok && cudaEventCreateWithFlags(&b, cudaEventDisableTiming) == cudaSuccess;
+      if (b) h->ev_used.push_back(b);
+    }
+  }
   // The second stream carries the missed picks' read-through pass, the step's
   // critical path: highest priority, so its CTAs are placed before the
   // resident picks' persistent grids fill the SMs.
@@ -385,15 +421,51 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   }
   if (e == cudaSuccess) e = mark(2, st);
   if (e == cudaSuccess) e = launch_quantize_rows(st, x, true, rows, h->H, h->xq);
-  if (e == cudaSuccess)
-    e = launch_grouped_mma(st, h->gp, npicks, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf, flags);
-  if (e == cudaSuccess) e = mark(3, st);
-  if (e == cudaSuccess) e = mark(5, st);
-  if (e == cudaSuccess) e = launch_quantize_rows(st, h->gemv.hbuf, false, npicks, h->I, h->hq);
-  if (e == cudaSuccess)
-    e = launch_grouped_mma(st, h->gp, npicks, false, h->H, h->I, h->k, h->hq, h->gemv.ypart, flags);
-  if (e == cudaSuccess) e = mark(4, st);
-  if (e == cudaSuccess) e = mark(6, st);
+  if (rows > h->opts.bypass_rows && h->chunk > 0) {
+    // Staged prefill: chunk q's experts go host -> HBM staging on the second
+    // stream while the caller's stream runs chunk q-1's grouped MMAs from the
+    // staged bytes; a staging half is refilled only after the MMAs that read it.
+    // Every chunk is launched (graph-safe); chunks past the step's groups exit.
+    const int C = h->chunk;
+    const int gx_gu = std::max(1, 2 * h->num_sms / (h->I / 64));
+    const int gx_dn = std::max(1, 2 * h->num_sms / (h->H / 128));
+    if (e == cudaSuccess) e = cudaEventRecord(h->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork, 0);
+    for (int q = 0; q < h->nchunks && e == cudaSuccess; ++q) {
+      const int g0 = q * C, g1 = g0 + C;
+      if (q >= 2) e = cudaStreamWaitEvent(h->side, h->ev_used[q - 2], 0);
+      if (e == cudaSuccess)
+        e = launch_stage_copy(h->side, h->gp, q, C, L, h->stage_w, h->stage_s, h->Bw, h->Bs,
+                              std::max(8, h->num_sms / 2));
+      if (e == cudaSuccess) e = cudaEventRecord(h->ev_staged[q], h->side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_staged[q], 0);
+      if (e == cudaSuccess)
+        e = launch_grouped_mma(st, h->gp, gx_gu, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf,
+                               flags, g0, g1);
+      if (e == cudaSuccess)
+        e = launch_quantize_members(st, h->gemv.hbuf, h->I, h->gp, g0, g1, h->hq, h->num_sms);
+      if (e == cudaSuccess)
+        e = launch_grouped_mma(st, h->gp, gx_dn, false, h->H, h->I, h->k, h->hq, h->gemv.ypart,
+                               flags, g0, g1);
+      if (e == cudaSuccess) e = cudaEventRecord(h->ev_used[q], st);
+    }
+    if (e == cudaSuccess) e = mark(3, st);
+    if (e == cudaSuccess) e = mark(5, st);
+    if (e == cudaSuccess) e = mark(4, st);
+    if (e == cudaSuccess) e = mark(6, st);
+  } else {
+    if (e == cudaSuccess)
+      e = launch_grouped_mma(st, h->gp, npicks, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf,
+                             flags);
+    if (e == cudaSuccess) e = mark(3, st);
+    if (e == cudaSuccess) e = mark(5, st);
+    if (e == cudaSuccess) e = launch_quantize_rows(st, h->gemv.hbuf, false, npicks, h->I, h->hq);
+    if (e == cudaSuccess)
+      e = launch_grouped_mma(st, h->gp, npicks, false, h->H, h->I, h->k, h->hq, h->gemv.ypart,
+                             flags);
+    if (e == cudaSuccess) e = mark(4, st);
+    if (e == cudaSuccess) e = mark(6, st);
+  }
   if (e == cudaSuccess) e = launch_combine(st, h->gp, h->gemv.ypart, out, rows, h->H, h->k);
   if (e == cudaSuccess) e = mark(7, st);
   return cuda_err(e);

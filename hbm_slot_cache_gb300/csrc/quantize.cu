@@ -50,10 +50,9 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
 }
 
 template <bool BF16_IN>
-__global__ void __launch_bounds__(1024)
-quantize_rows_kernel(const void* __restrict__ src, int K, QuantBuf q) {
-  __shared__ float red[32];
-  const int row = blockIdx.x, t = threadIdx.x;
+__device__ void quantize_row(const void* __restrict__ src, int K, const QuantBuf& q, int row,
+                             float* red) {
+  const int t = threadIdx.x;
   const int nblk = K / 16;
   float r[16];
   if (t < nblk) {
@@ -119,7 +118,39 @@ quantize_rows_kernel(const void* __restrict__ src, int K, QuantBuf q) {
   }
 }
 
+template <bool BF16_IN>
+__global__ void __launch_bounds__(1024)
+quantize_rows_kernel(const void* __restrict__ src, int K, QuantBuf q) {
+  __shared__ float red[32];
+  quantize_row<BF16_IN>(src, K, q, blockIdx.x, red);
+}
+
+// The rows named by the members of groups [g0, g1) (members are stored group
+// after group, so they are one contiguous range).
+__global__ void __launch_bounds__(1024)
+quantize_members_kernel(const float* __restrict__ src, int K, const GroupPlan* __restrict__ gp,
+                        int g0, int g1, QuantBuf q) {
+  __shared__ float red[32];
+  const int ng = gp->n_groups;
+  if (g0 >= ng) return;
+  const int mbeg = gp->g_start[g0];
+  const int mend = g1 < ng ? gp->g_start[g1] : gp->npicks;
+  for (int i = mbeg + blockIdx.x; i < mend; i += gridDim.x) {
+    quantize_row<false>(src, K, q, gp->members[i], red);
+    __syncthreads();  // red is reused by the next row
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_members(cudaStream_t st, const float* src, int K, const GroupPlan* gp,
+                                    int g0, int g1, const QuantBuf& q, int grid) {
+  const int nblk = K / 16;
+  const int threads = ((nblk + 31) / 32) * 32;
+  if (threads > 1024 || grid <= 0) return cudaErrorInvalidValue;
+  quantize_members_kernel<<<grid, threads, 0, st>>>(src, K, gp, g0, g1, q);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_rows(cudaStream_t st, const void* src, bool bf16_in, int rows, int K,
                                  const QuantBuf& q) {

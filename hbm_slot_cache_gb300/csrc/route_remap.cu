@@ -89,7 +89,9 @@ __device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
     gp->g_gs[3 * g + 2] = gscale[3 * e + 2];
     const int nj = (s_gcount[g] + kRowsPerJob - 1) / kRowsPerJob;
     for (int t = 0; t < nj; ++t) gp->jobs[s_jstart[g] + t] = (g << 8) | t;
+    gp->g_job[g] = s_jstart[g];
   }
+  if (tid == 0) gp->g_job[n_union] = gp->n_jobs;
 }
 
 // KPL = keys per lane = ceil(E / 32) rounded up to a power of two.

@@ -97,8 +97,10 @@ group_rows_kernel(const int32_t* __restrict__ ids, int rows, int E, int k, long 
     gp->g_gs[3 * gidx + 1] = L.gscale[3 * e + 1];
     gp->g_gs[3 * gidx + 2] = L.gscale[3 * e + 2];
     for (int t = 0; t < nj; ++t) gp->jobs[jstart + t] = (gidx << 8) | t;
+    gp->g_job[gidx] = jstart;
   }
   if (tid == 0) {
+    gp->g_job[n_groups] = n_jobs;
     gp->n_groups = n_groups;
     gp->n_jobs = n_jobs;
     gp->rows = rows;

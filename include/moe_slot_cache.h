@@ -10,8 +10,9 @@
  * least-recently-used slot, then the map is updated; the expert kernel reads
  * the same bytes it would read if every expert were in HBM, only the index
  * changes.  Fixed addresses and fixed shapes make a decode round replayable as
- * a CUDA graph.  Steps with more than 16 rows (prefill) bypass the cache and
- * read experts zero-copy from host memory, so no expert is ever unreachable.
+ * a CUDA graph.  Steps with more than 16 rows (prefill) bypass the cache, so
+ * no expert is ever unreachable: each expert they use is read once from host
+ * memory, staged into HBM a chunk at a time (or read zero-copy, by option).
  *
  * Conventions
  *  - Every function returns MOE_OK (0) or a negative MOE_ERR_* code; nothing
@@ -88,6 +89,10 @@ typedef struct {
                          same kernels, used to check that caching changes no output bit */
   int trace_capacity; /* per-layer ring of moe_step_record_t for cached steps (0 = off) */
   int max_rows;       /* largest rows of any step (sizes the bypass workspace); default 512 */
+  int prefill_chunk;  /* bypass steps: experts staged into HBM per chunk, two chunks held at
+                         once (a 2 * prefill_chunk expert staging area, allocated at create
+                         when max_rows > bypass_rows); 0: default 32; -1: no staging, the
+                         grouped kernels read host memory directly */
 } moe_cache_opts_t;
 
 typedef struct {

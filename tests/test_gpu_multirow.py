@@ -177,3 +177,64 @@ def test_glm_prefill_bypass_sampled_rows(lib, orc):
     assert st["bypass_calls"] == 1 and st["misses"] == 0
     cache.close()
     banks.close()
+
+
+def test_tiny_prefill_staged_equals_zero_copy(lib, orc):
+    """Staged prefill (experts copied into HBM a chunk at a time, two chunks held)
+    gives the same bits as reading host memory directly, for chunk sizes that
+    cover the union in one chunk, in several, and with a ragged last chunk."""
+    cfg = workload.CONFIGS["tiny"]
+    rows = 64
+    banks = Banks(cfg)
+    lg = workload.prefill_logits(cfg, 0, rows)
+    xb = workload.activations(cfg.seed, 3, 1, rows, cfg.hidden)[0]
+    lg_d, x_d, out_d = _dev(cfg, rows)
+    _put(lg_d, x_d, lg, xb)
+    outs = {}
+    for chunk in (-1, 0, 4, 3, 1):
+        cache = make_cache(cfg, banks, prefill_chunk=chunk)
+        for _ in range(2):   # twice: the staging halves are reused across steps
+            cache.step(0, lg_d, x_d, out_d)
+        outs[chunk] = out_d.cpu().numpy().copy()
+        st = cache.stats(0)
+        assert st["bypass_calls"] == 2 and st["misses"] == 0 and st["error_flags"] == 0
+        cache.close()
+    w, s, g = banks.layer_arrays(0)
+    ref, _, _, _ = orc.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, lg, xb)
+    assert_within_tolerance(outs[-1], ref)
+    for chunk, o in outs.items():
+        assert np.array_equal(o.view(np.uint32), outs[-1].view(np.uint32)), f"chunk {chunk}"
+    banks.close()
+
+
+def test_glm_prefill_staged_graph_and_zero_copy(lib, orc):
+    """GLM prefill, 128 rows: the staged path (8 chunks of 32 experts) replayed
+    from a CUDA graph equals its eager run and the zero-copy path bit for bit."""
+    cfg = workload.CONFIGS["prefill"]
+    rows = 128
+    banks = Banks(cfg)
+    lg = workload.prefill_logits(cfg, 1, rows)
+    xb = workload.activations(cfg.seed, 4, 1, rows, cfg.hidden)[0]
+    lg_d, x_d, out_d = _dev(cfg, rows)
+    _put(lg_d, x_d, lg, xb)
+    zc = make_cache(cfg, banks, layers=1, prefill_chunk=-1)
+    zc.step(0, lg_d, x_d, out_d)
+    ref_bits = out_d.cpu().numpy().copy()
+    zc.close()
+    cache = make_cache(cfg, banks, layers=1)
+    cache.step(0, lg_d, x_d, out_d)
+    eager = out_d.cpu().numpy().copy()
+    assert np.array_equal(eager.view(np.uint32), ref_bits.view(np.uint32))
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    out_d.zero_()
+    with torch.cuda.graph(g, stream=s):
+        cache.step(0, lg_d, x_d, out_d)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(out_d.cpu().numpy().view(np.uint32), ref_bits.view(np.uint32))
+    sample = [0, 64, 127]
+    assert_within_tolerance(eager[sample], _oracle_rows(orc, banks, cfg, lg, xb, sample))
+    assert cache.stats(0)["error_flags"] == 0
+    cache.close()
+    banks.close()
