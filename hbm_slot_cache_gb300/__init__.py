@@ -61,7 +61,7 @@ class MoeCache:
 
     def __init__(self, layers, experts, slots, hidden, inter, top_k, host_layers, *,
                  all_resident=False, trace_capacity=0, bypass_rows=0, max_rows=0,
-                 prefill_chunk=0):
+                 prefill_chunk=0, batch_invariant=False):
         self.layers, self.experts, self.hidden, self.inter, self.top_k = (
             layers, experts, hidden, inter, top_k)
         self.slots = experts if all_resident else slots
@@ -75,7 +75,7 @@ class MoeCache:
         self.h = moe_cache_create(layers, experts, slots, hidden, inter, top_k, ptrs,
                                   all_resident=all_resident, trace_capacity=trace_capacity,
                                   bypass_rows=bypass_rows, max_rows=max_rows,
-                                  prefill_chunk=prefill_chunk)
+                                  prefill_chunk=prefill_chunk, batch_invariant=batch_invariant)
         self.trace_capacity = trace_capacity
 
     @staticmethod

@@ -21,6 +21,7 @@ MOE_ERR_CUDA = -4
 MOE_ERR_UNSUPPORTED = -5
 MOE_FLAG_NONFINITE_LOGIT = 0x1
 MOE_FLAG_WAIT_TIMEOUT = 0x2
+MOE_FLAG_BAD_PLAN = 0x4
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_TOPK = 16
 MOE_MAX_CACHED_ROWS = 16
@@ -47,7 +48,8 @@ class HostLayer(ctypes.Structure):
 class Opts(ctypes.Structure):
     _fields_ = [("copy_backend", ctypes.c_int), ("bypass_rows", ctypes.c_int),
                 ("all_resident", ctypes.c_int), ("trace_capacity", ctypes.c_int),
-                ("max_rows", ctypes.c_int), ("prefill_chunk", ctypes.c_int)]
+                ("max_rows", ctypes.c_int), ("prefill_chunk", ctypes.c_int),
+                ("batch_invariant", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):
@@ -128,10 +130,12 @@ def moe_expert_bytes(hidden: int, inter: int) -> tuple[int, int]:
 def moe_cache_create(layers: int, experts: int, slots: int, hidden: int, inter: int, top_k: int,
                      host_layers, copy_backend: int = MOE_COPY_SM, bypass_rows: int = 0,
                      all_resident: bool = False, trace_capacity: int = 0,
-                     max_rows: int = 0, prefill_chunk: int = 0) -> int:
+                     max_rows: int = 0, prefill_chunk: int = 0,
+                     batch_invariant: bool = False) -> int:
     """host_layers: sequence of (w_ptr, s_ptr, gscale_ptr) per layer. Returns the handle."""
     arr = (HostLayer * layers)(*[HostLayer(int(w), int(s), int(g)) for (w, s, g) in host_layers])
-    o = Opts(copy_backend, bypass_rows, int(all_resident), trace_capacity, max_rows, prefill_chunk)
+    o = Opts(copy_backend, bypass_rows, int(all_resident), trace_capacity, max_rows, prefill_chunk,
+             int(batch_invariant))
     h = ctypes.c_void_p()
     _check(lib().moe_cache_create(ctypes.byref(h), layers, experts, slots, hidden, inter, top_k,
                                   ctypes.cast(arr, ctypes.c_void_p), ctypes.byref(o)),

@@ -141,15 +141,24 @@ grouped_mma_kernel(MmaArgs a) {
   int gc = 0;  // chunks this CTA has committed: barrier phases continue across jobs
 
   for (int job = jbeg + blockIdx.x; job < jend; job += gridDim.x) {
-    const int jv = gp->jobs[job];
+    // the job's plan entries are checked before they address memory (uniform
+    // decision); a bad entry sets MOE_FLAG_BAD_PLAN and the job is skipped
+    bool good = plan_ok(job >= 0 && job < gp->n_jobs, a.flags);
+    const int jv = good ? gp->jobs[job] : 0;
     const int g = jv >> 8, tile = jv & 255;
-    const int gstart = gp->g_start[g], gcount = gp->g_count[g];
+    good = good && plan_ok(g >= 0 && g < ng, a.flags);
+    const int gstart = good ? gp->g_start[g] : 0, gcount = good ? gp->g_count[g] : 1;
+    good = good && plan_ok(gstart >= 0 && gcount >= 1 && gstart + gcount <= gp->npicks, a.flags);
     const int m0 = tile * kRowsPerJob;
+    good = good && plan_ok(m0 < gcount, a.flags);
+    good = __syncthreads_and(good);
+    if (!good) continue;
     const int nmem = min(kRowsPerJob, gcount - m0);
     if (tid < kRowsPerJob) {
       int p = -1, br = 0;
       if (tid < nmem) {
         p = gp->members[gstart + m0 + tid];
+        if (!plan_ok(p >= 0 && p < gp->npicks, a.flags)) p = 0;
         br = a.gate_up ? p / a.k : p;
       }
       s_pick[tid] = p;
@@ -257,6 +266,7 @@ grouped_mma_kernel(MmaArgs a) {
         w[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + 16 * tid)[q] : 0u;
         wb[q] = q < KSTEPS ? reinterpret_cast<const uint32_t*>(sSa + kSfaBytes + 16 * lane)[q] : 0u;
       }
+      __syncwarp();  // tcgen05.st is .sync.aligned: the warp reconverges after the wait
       tmem_st16(tmem + lane_base + kColSF + 32 * sf, w);
       tmem_st16(tmem + lane_base + kColSF + 32 * sf + 16, wb);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -302,6 +312,7 @@ grouped_mma_kernel(MmaArgs a) {
     gc += nchunks;
 
     uint32_t v[32];
+    __syncwarp();
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"

@@ -235,6 +235,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Index check on plan data one kernel hands to the next: false (and the sticky
+// MOE_FLAG_BAD_PLAN set in *flags) when cond fails, so the caller skips the
+// access instead of touching memory outside its buffers.
+__device__ __forceinline__ bool plan_ok(bool cond, uint32_t* flags) {
+  if (!cond) {
+    if (flags) atomicOr(flags, MOE_FLAG_BAD_PLAN);
+    __threadfence_system();
+  }
+  return cond;
+}
+
 // Waits (acquire, at most ~2 s) until the global counter *ctr reaches target;
 // on timeout sets MOE_FLAG_WAIT_TIMEOUT in *flags and returns false.
 __device__ __forceinline__ bool count_wait_bounded(const uint32_t* ctr, uint32_t target,

@@ -219,7 +219,8 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
   } else {
     o.prefill_chunk = kDefaultPrefillChunk;
   }
-  if (o.prefill_chunk < -1) return MOE_ERR_ARG;
+  if (o.prefill_chunk < -1 || o.batch_invariant < 0 || o.batch_invariant > 1) return MOE_ERR_ARG;
+  if (o.batch_invariant && !mma_supported(hidden, inter)) return MOE_ERR_UNSUPPORTED;
   if (layers < 1 || experts < 1 || top_k < 1 || hidden < 1 || inter < 1 || !host_backing)
     return MOE_ERR_ARG;
   if (o.trace_capacity < 0 || o.copy_backend != MOE_COPY_SM) return MOE_ERR_ARG;
@@ -347,7 +348,8 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   if (((uintptr_t)x & 15) || ((uintptr_t)out & 15)) return MOE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (rows > h->opts.bypass_rows && rows > h->opts.max_rows) return MOE_ERR_UNSUPPORTED;
-  if (rows > 1 && !mma_supported(h->H, h->I)) return MOE_ERR_UNSUPPORTED;
+  const bool one_row = rows == 1 && !h->opts.batch_invariant;
+  if (!one_row && !mma_supported(h->H, h->I)) return MOE_ERR_UNSUPPORTED;
   const LayerDev L = layer_dev(h, layer);
   // inside a capture an event record must be an external node to be replayed
   auto mark = [&](int i, cudaStream_t s) -> cudaError_t {
@@ -360,7 +362,7 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   };
   uint32_t* flags = &(h->stats + layer)->flags;
   cudaError_t e = mark(0, st);
-  if (rows == 1) {
+  if (one_row) {
     // One row.  After route/remap the missed picks take a second stream: one
     // read-through launch reads each missed expert once over the host link,
     // computes its gate/up and down on the way in and writes it through to the

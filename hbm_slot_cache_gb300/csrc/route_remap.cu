@@ -27,6 +27,10 @@
 // (stamp, slot id); |U| > S bypasses the cache (expert pointers go to host
 // memory, state untouched).  The i-th miss gets the i-th smallest unused slot,
 // which equals filling the misses one at a time.
+//
+// Indices derived from the step's own data (expert ids, group ranks, member
+// and job slots) are checked before they address memory; a failed check sets
+// MOE_FLAG_BAD_PLAN and skips the access.
 #include "internal.cuh"
 #include "router.cuh"
 
@@ -45,13 +49,15 @@ __device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
                             const uint8_t* const* s_wp, const uint8_t* const* s_sp,
                             const uint32_t* s_union, const int32_t* s_upre, int32_t* s_pgroup,
                             int32_t* s_gcount, int32_t* s_gstart, int32_t* s_jstart,
-                            const float* gscale) {
+                            const float* gscale, int E, uint32_t* fl) {
   const int tid = threadIdx.x;
   for (int g = tid; g < n_union; g += kThreads) s_gcount[g] = 0;
   __syncthreads();
   for (int p = tid; p < npicks; p += kThreads) {
     const int e = s_ids[p];
+    if (!plan_ok(e >= 0 && e < E, fl)) continue;
     const int g = s_upre[e >> 5] + __popc(s_union[e >> 5] & ((1u << (e & 31)) - 1u));
+    if (!plan_ok(g >= 0 && g < n_union, fl)) continue;
     s_pgroup[p] = g;
     atomicAdd(&s_gcount[g], 1);
     gp->wts[p] = s_wts[p];
@@ -75,10 +81,13 @@ __device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
     int idx = 0, first = -1;
     for (int p = 0; p < npicks; ++p) {
       if (s_pgroup[p] != g) continue;
-      gp->members[s_gstart[g] + idx++] = p;
+      if (plan_ok(s_gstart[g] + idx < npicks, fl)) gp->members[s_gstart[g] + idx] = p;
+      ++idx;
       if (first < 0) first = p;
     }
+    if (!plan_ok(first >= 0, fl)) continue;
     const int e = s_ids[first];
+    if (!plan_ok(e >= 0 && e < E, fl)) continue;
     gp->g_expert[g] = e;
     gp->g_start[g] = s_gstart[g];
     gp->g_count[g] = s_gcount[g];
@@ -88,10 +97,11 @@ __device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
     gp->g_gs[3 * g + 1] = gscale[3 * e + 1];
     gp->g_gs[3 * g + 2] = gscale[3 * e + 2];
     const int nj = (s_gcount[g] + kRowsPerJob - 1) / kRowsPerJob;
-    for (int t = 0; t < nj; ++t) gp->jobs[s_jstart[g] + t] = (g << 8) | t;
+    for (int t = 0; t < nj; ++t)
+      if (plan_ok(s_jstart[g] + t < npicks, fl)) gp->jobs[s_jstart[g] + t] = (g << 8) | t;
     gp->g_job[g] = s_jstart[g];
   }
-  if (tid == 0) gp->g_job[n_union] = gp->n_jobs;
+  if (tid == 0 && plan_ok(n_union <= npicks, fl)) gp->g_job[n_union] = gp->n_jobs;
 }
 
 // KPL = keys per lane = ceil(E / 32) rounded up to a power of two.
@@ -127,6 +137,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int npicks = rows * k;
+  uint32_t* const fl = &L.stats->flags;  // plan index checks report here
 
   // ---- state into shared memory (overlaps the router's logit loads)
   if (tid < kWords) {
@@ -200,14 +211,14 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   } else {  // warp per row
     for (int m = warp; m < rows; m += kThreads / 32) {
       const bool bad =
-          route_row<KPL>(logits + (size_t)m * E, E, k, lane, s_ids + m * k, s_wts + m * k);
+          route_row<KPL>(logits + (size_t)m * E, E, k, lane, s_ids + m * k, s_wts + m * k, fl);
       if (bad && lane == 0) atomicOr(&s_flags, MOE_FLAG_NONFINITE_LOGIT);
     }
   }
   __syncthreads();
   // the picks' global scales, in flight while the remap decisions are taken
   float gs0 = 0.f, gs1 = 0.f, gs2 = 0.f;
-  if (tid < npicks) {
+  if (tid < npicks && plan_ok(s_ids[tid] >= 0 && s_ids[tid] < E, fl)) {
     const int e = s_ids[tid];
     gs0 = L.gscale[3 * e + 0];
     gs1 = L.gscale[3 * e + 1];
@@ -217,9 +228,11 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   // ---- union, hits (slot marked used), missing ids
   for (int p = tid; p < npicks; p += kThreads) {
     const int e = s_ids[p];
+    if (!plan_ok(e >= 0 && e < E, fl)) continue;
     atomicOr(&s_union[e >> 5], 1u << (e & 31));
     const int v = s_map[e];
     s_hit[p] = v >= 0;
+    if (v >= 0 && !plan_ok(v < S, fl)) continue;
     if (v >= 0) {
       s_key[v] = ~0ull;
       atomicAdd(&s_n_hits, 1);
@@ -249,7 +262,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     uint32_t bits = mm;
     while (bits) {  // misses in ascending expert id
       const int b = __ffs(bits) - 1;
-      s_miss_e[i++] = 32 * lane + b;
+      if (plan_ok(i < MOE_MAX_PICKS, fl)) s_miss_e[i] = 32 * lane + b;
+      ++i;
       bits &= bits - 1;
     }
     if (lane == 31) s_n_miss = incl;
@@ -264,6 +278,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     // read every expert from host memory; cache state untouched
     for (int p = tid; p < npicks; p += kThreads) {
       const int e = s_ids[p];
+      if (!plan_ok(e >= 0 && e < E, fl)) continue;
       plan->ids[p] = e;
       plan->wts[p] = s_wts[p];
       plan->wptr[p] = L.host_w + (long long)e * Bw;
@@ -284,7 +299,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     __syncthreads();
     if (gp)
       emit_groups(gp, rows, npicks, n_union, s_ids, s_wts, s_wp, s_sp, s_union, s_upre, s_pgroup,
-                  s_gcount, s_gstart, s_jstart, L.gscale);
+                  s_gcount, s_gstart, s_jstart, L.gscale, E, fl);
     if (tid == 0) {
       plan->rows = rows;
       plan->npicks = npicks;
@@ -374,7 +389,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   __syncthreads();
   if (gp)
     emit_groups(gp, rows, npicks, n_union, s_ids, s_wts, s_wp, s_sp, s_union, s_upre, s_pgroup,
-                s_gcount, s_gstart, s_jstart, L.gscale);
+                s_gcount, s_gstart, s_jstart, L.gscale, E, fl);
   if (rows == 1 && warp == 0) {  // hits first, then misses, each in rank order (npicks <= 32)
     const bool in = lane < npicks;
     const bool hit = in && s_hit[lane];

@@ -26,7 +26,8 @@ route_rows_kernel(const float* __restrict__ logits, int rows, int E, int k,
   const int m = blockIdx.x * (kRouteThreads / 32) + (threadIdx.x >> 5);
   if (m >= rows) return;
   const bool bad =
-      route_row<KPL>(logits + (size_t)m * E, E, k, lane, ids + (size_t)m * k, gp->wts + (size_t)m * k);
+      route_row<KPL>(logits + (size_t)m * E, E, k, lane, ids + (size_t)m * k, gp->wts + (size_t)m * k,
+                     &st->flags);
   if (bad && lane == 0) atomicOr(&st->flags, MOE_FLAG_NONFINITE_LOGIT);
 }
 

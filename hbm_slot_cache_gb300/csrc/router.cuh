@@ -42,10 +42,10 @@ __device__ __forceinline__ unsigned long long route_key(float f, int e) {
 
 // All 32 lanes call it.  ids[j] / wts[j] (j < k) are written by lanes 0 and j;
 // returns true (on every lane) if any of the row's logits is NaN or infinite.
-// KPL = keys per lane >= ceil(E / 32).
+// KPL = keys per lane >= ceil(E / 32).  flags: the layer's error word.
 template <int KPL>
 __device__ __forceinline__ bool route_row(const float* __restrict__ lr, int E, int k, int lane,
-                                          int32_t* ids, float* wts) {
+                                          int32_t* ids, float* wts, uint32_t* flags) {
   unsigned long long key[KPL];
   bool bad = false;
 #pragma unroll
@@ -75,8 +75,8 @@ __device__ __forceinline__ bool route_row(const float* __restrict__ lr, int E, i
         best = umax64(best, key[i]);
       }
     }
-    if (lane == 0) ids[j] = e;
-    if (lane == j) lsel = lr[e];
+    if (lane == 0 && plan_ok(e >= 0 && e < E, flags)) ids[j] = e;
+    if (lane == j && plan_ok(e >= 0 && e < E, flags)) lsel = lr[e];
   }
   route_weights(lsel, k, lane, wts);
   return __any_sync(0xFFFFFFFFu, bad) != 0;

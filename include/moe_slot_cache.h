@@ -48,6 +48,8 @@ extern "C" {
 /* sticky device flags (moe_cache_stats_t.error_flags) */
 #define MOE_FLAG_NONFINITE_LOGIT 0x1u /* a router logit was NaN or +-inf */
 #define MOE_FLAG_WAIT_TIMEOUT 0x2u    /* a kernel's bounded wait on its own copies gave up */
+#define MOE_FLAG_BAD_PLAN 0x4u        /* a kernel found an out-of-range index in the step's plan
+                                         and skipped that access (output undefined) */
 
 /* limits */
 #define MOE_MAX_EXPERTS 1024
@@ -93,6 +95,11 @@ typedef struct {
                          once (a 2 * prefill_chunk expert staging area, allocated at create
                          when max_rows > bypass_rows); 0: default 32; -1: no staging, the
                          grouped kernels read host memory directly */
+  int batch_invariant; /* 1: one-row steps take the grouped tensor-core path of multi-row
+                          rounds, so every row's output is bit-identical whether it is
+                          stepped alone or inside a round of up to 16 rows (exact verify
+                          rows for speculative decoding); 0 (default): one-row steps take
+                          the faster CUDA-core decode path */
 } moe_cache_opts_t;
 
 typedef struct {
