@@ -13,7 +13,9 @@ from . import _lib
 from ._lib import (MoeError, moe_cache_create, moe_cache_destroy, moe_cache_reset,  # noqa: F401
                    moe_cache_slot_bytes, moe_cache_slot_map, moe_cache_stats, moe_cache_step,
                    moe_cache_trace, moe_expert_bytes, moe_host_alloc, moe_host_free,
-                   moe_probe_host_link, moe_cache_set_timing_events)
+                   moe_probe_host_link, moe_cache_set_timing_events, moe_policy_hybrid,
+                   moe_policy_lru, moe_policy_lru_curve, moe_policy_size_layers,
+                   moe_policy_static)
 
 __all__ = ["HostBank", "MoeCache", "MoeError", "build"]
 
@@ -61,7 +63,7 @@ class MoeCache:
 
     def __init__(self, layers, experts, slots, hidden, inter, top_k, host_layers, *,
                  all_resident=False, trace_capacity=0, bypass_rows=0, max_rows=0,
-                 prefill_chunk=0, batch_invariant=False):
+                 prefill_chunk=0, batch_invariant=False, slots_per_layer=None):
         self.layers, self.experts, self.hidden, self.inter, self.top_k = (
             layers, experts, hidden, inter, top_k)
         self.slots = experts if all_resident else slots
@@ -75,7 +77,8 @@ class MoeCache:
         self.h = moe_cache_create(layers, experts, slots, hidden, inter, top_k, ptrs,
                                   all_resident=all_resident, trace_capacity=trace_capacity,
                                   bypass_rows=bypass_rows, max_rows=max_rows,
-                                  prefill_chunk=prefill_chunk, batch_invariant=batch_invariant)
+                                  prefill_chunk=prefill_chunk, batch_invariant=batch_invariant,
+                                  slots_per_layer=slots_per_layer)
         self.trace_capacity = trace_capacity
 
     @staticmethod
@@ -104,7 +107,11 @@ class MoeCache:
         return moe_cache_stats(self.h, layer)
 
     def slot_map(self, layer: int) -> np.ndarray:
-        return moe_cache_slot_map(self.h, layer, self.slots)
+        """Expert in each slot of `layer`'s ring (-1: empty)."""
+        return moe_cache_slot_map(self.h, layer)
+
+    def layer_slots(self, layer: int) -> int:
+        return _lib.moe_cache_layer_slots(self.h, layer)
 
     def slot_bytes(self, layer: int, slot: int):
         return moe_cache_slot_bytes(self.h, layer, slot, self.Bw, self.Bs)

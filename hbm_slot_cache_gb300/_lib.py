@@ -32,7 +32,9 @@ MOE_COPY_SM = 0
 EXPORTS = ("moe_cache_create", "moe_cache_step", "moe_cache_stats", "moe_cache_slot_map",
            "moe_cache_slot_bytes", "moe_cache_trace", "moe_cache_reset", "moe_cache_destroy",
            "moe_cache_strerror", "moe_expert_bytes", "moe_host_alloc", "moe_host_free",
-           "moe_probe_host_link", "moe_cache_set_timing_events", "moe_expert_pass_noalloc")
+           "moe_probe_host_link", "moe_cache_set_timing_events", "moe_expert_pass_noalloc",
+           "moe_policy_lru", "moe_policy_static", "moe_policy_hybrid", "moe_policy_lru_curve",
+           "moe_policy_size_layers", "moe_cache_layer_slots")
 
 
 class MoeError(RuntimeError):
@@ -49,7 +51,15 @@ class Opts(ctypes.Structure):
     _fields_ = [("copy_backend", ctypes.c_int), ("bypass_rows", ctypes.c_int),
                 ("all_resident", ctypes.c_int), ("trace_capacity", ctypes.c_int),
                 ("max_rows", ctypes.c_int), ("prefill_chunk", ctypes.c_int),
-                ("batch_invariant", ctypes.c_int)]
+                ("batch_invariant", ctypes.c_int), ("slots_per_layer", ctypes.c_void_p)]
+
+
+class PolicyResult(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in ("steps", "picks", "hits", "misses", "evictions",
+                                               "bypass_steps", "host_experts")]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 class Stats(ctypes.Structure):
@@ -89,6 +99,7 @@ def lib() -> ctypes.CDLL:
         L.moe_cache_step.argtypes = [P, I, I, P, P, P, P]
         L.moe_cache_stats.argtypes = [P, I, ctypes.POINTER(Stats)]
         L.moe_cache_slot_map.argtypes = [P, I, P]
+        L.moe_cache_layer_slots.argtypes = [P, I, ctypes.POINTER(I)]
         L.moe_cache_slot_bytes.argtypes = [P, I, I, P, P]
         L.moe_cache_trace.argtypes = [P, I, P, I, ctypes.POINTER(ctypes.c_int)]
         L.moe_cache_reset.argtypes = [P]
@@ -102,6 +113,12 @@ def lib() -> ctypes.CDLL:
                                           ctypes.POINTER(ctypes.c_double)]
         L.moe_cache_set_timing_events.argtypes = [P, P]
         L.moe_expert_pass_noalloc.argtypes = [I, I, I, P, P, P, P, P, P, P]
+        PR = ctypes.POINTER(PolicyResult)
+        L.moe_policy_lru.argtypes = [P, I, I, I, I, PR]
+        L.moe_policy_static.argtypes = [P, I, I, I, I, PR]
+        L.moe_policy_hybrid.argtypes = [P, I, I, I, I, I, PR]
+        L.moe_policy_lru_curve.argtypes = [P, I, I, I, I, P]
+        L.moe_policy_size_layers.argtypes = [P, I, I, I, I, P]
         for name in EXPORTS:
             if name != "moe_cache_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -131,11 +148,16 @@ def moe_cache_create(layers: int, experts: int, slots: int, hidden: int, inter: 
                      host_layers, copy_backend: int = MOE_COPY_SM, bypass_rows: int = 0,
                      all_resident: bool = False, trace_capacity: int = 0,
                      max_rows: int = 0, prefill_chunk: int = 0,
-                     batch_invariant: bool = False) -> int:
+                     batch_invariant: bool = False, slots_per_layer=None) -> int:
     """host_layers: sequence of (w_ptr, s_ptr, gscale_ptr) per layer. Returns the handle."""
     arr = (HostLayer * layers)(*[HostLayer(int(w), int(s), int(g)) for (w, s, g) in host_layers])
+    spl = None
+    if slots_per_layer is not None:
+        spl = np.ascontiguousarray(slots_per_layer, np.int32)
+        if spl.shape != (layers,):
+            raise ValueError("slots_per_layer must have one entry per layer")
     o = Opts(copy_backend, bypass_rows, int(all_resident), trace_capacity, max_rows, prefill_chunk,
-             int(batch_invariant))
+             int(batch_invariant), spl.ctypes.data if spl is not None else None)
     h = ctypes.c_void_p()
     _check(lib().moe_cache_create(ctypes.byref(h), layers, experts, slots, hidden, inter, top_k,
                                   ctypes.cast(arr, ctypes.c_void_p), ctypes.byref(o)),
@@ -154,7 +176,15 @@ def moe_cache_stats(h: int, layer: int = -1) -> dict:
     return st.as_dict()
 
 
-def moe_cache_slot_map(h: int, layer: int, slots: int) -> np.ndarray:
+def moe_cache_layer_slots(h: int, layer: int) -> int:
+    n = ctypes.c_int()
+    _check(lib().moe_cache_layer_slots(h, layer, ctypes.byref(n)), "moe_cache_layer_slots")
+    return n.value
+
+
+def moe_cache_slot_map(h: int, layer: int, slots: int | None = None) -> np.ndarray:
+    if slots is None:
+        slots = moe_cache_layer_slots(h, layer)
     out = np.empty(slots, np.int32)
     _check(lib().moe_cache_slot_map(h, layer, out.ctypes.data), "moe_cache_slot_map")
     return out
@@ -230,3 +260,56 @@ def moe_probe_host_link(host_src: int, dev_dst: int, nbytes: int, method: int = 
     _check(lib().moe_probe_host_link(host_src, dev_dst, nbytes, method, iters, ctypes.byref(g)),
            "moe_probe_host_link")
     return g.value
+
+
+# ------------------------------------------------------------ offline slot policy
+
+def _trace(trace) -> tuple[np.ndarray, int, int]:
+    t = np.ascontiguousarray(trace, np.int32)
+    if t.ndim != 2:
+        raise ValueError("trace must be [steps, picks]")
+    return t, t.shape[0], t.shape[1]
+
+
+def moe_policy_lru(trace, experts: int, slots: int) -> dict:
+    """LRU ring of `slots` slots over one layer's trace [steps, picks] (see the header)."""
+    t, n, p = _trace(trace)
+    r = PolicyResult()
+    _check(lib().moe_policy_lru(t.ctypes.data, n, p, experts, slots, ctypes.byref(r)),
+           "moe_policy_lru")
+    return r.as_dict()
+
+
+def moe_policy_static(trace, experts: int, slots: int) -> dict:
+    t, n, p = _trace(trace)
+    r = PolicyResult()
+    _check(lib().moe_policy_static(t.ctypes.data, n, p, experts, slots, ctypes.byref(r)),
+           "moe_policy_static")
+    return r.as_dict()
+
+
+def moe_policy_hybrid(trace, experts: int, slots: int, pinned: int) -> dict:
+    t, n, p = _trace(trace)
+    r = PolicyResult()
+    _check(lib().moe_policy_hybrid(t.ctypes.data, n, p, experts, slots, pinned, ctypes.byref(r)),
+           "moe_policy_hybrid")
+    return r.as_dict()
+
+
+def moe_policy_lru_curve(trace, experts: int, max_slots: int) -> np.ndarray:
+    """host_experts of an S-slot LRU ring for S = 1 .. max_slots (uint64 [max_slots])."""
+    t, n, p = _trace(trace)
+    out = np.zeros(max_slots, np.uint64)
+    _check(lib().moe_policy_lru_curve(t.ctypes.data, n, p, experts, max_slots, out.ctypes.data),
+           "moe_policy_lru_curve")
+    return out
+
+
+def moe_policy_size_layers(curves, budget: int, min_slots: int = 1) -> np.ndarray:
+    """Per-layer ring sizes (int32 [layers]) minimising the summed host-link experts
+    of the layers' LRU curves (uint64 [layers, max_slots]) within a total budget."""
+    c = np.ascontiguousarray(curves, np.uint64)
+    out = np.zeros(c.shape[0], np.int32)
+    _check(lib().moe_policy_size_layers(c.ctypes.data, c.shape[0], c.shape[1], budget, min_slots,
+                                        out.ctypes.data), "moe_policy_size_layers")
+    return out

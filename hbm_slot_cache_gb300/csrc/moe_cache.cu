@@ -20,17 +20,19 @@ constexpr int kDefaultPrefillChunk = 32;  // experts staged per prefill chunk (t
 }
 
 struct moe_cache {
-  int L, E, S, H, I, k;
+  int L, E, S, H, I, k;          // S: the largest ring of any layer
+  std::vector<int> S_of;         // [L] ring size of each layer
+  std::vector<size_t> slot_off;  // [L + 1] first slot of each layer in the slot arrays
   long long Bw, Bs;
   moe_cache_opts_t opts;
   int device, num_sms;
   // device state, per layer blocks
-  uint8_t* slot_w = nullptr;   // [L][S][Bw]
-  uint8_t* slot_s = nullptr;   // [L][S][Bs]
+  uint8_t* slot_w = nullptr;   // [sum S_l][Bw], layer l from slot_off[l]
+  uint8_t* slot_s = nullptr;   // [sum S_l][Bs]
   float* gscale = nullptr;     // [L][E][3]
   int32_t* map = nullptr;      // [L][E]
-  int32_t* owner = nullptr;    // [L][S]
-  uint32_t* stamp = nullptr;   // [L][S]
+  int32_t* owner = nullptr;    // [sum S_l]
+  uint32_t* stamp = nullptr;   // [sum S_l]
   uint32_t* clock = nullptr;   // [L]
   DevStats* stats = nullptr;   // [L]
   moe_step_record_t* trace = nullptr;  // [L][cap]
@@ -151,13 +153,13 @@ int device_view(const void* p, const uint8_t** out) {
 }
 
 int init_state(moe_cache* h) {
-  const size_t LE = (size_t)h->L * h->E, LS = (size_t)h->L * h->S;
+  const size_t LE = (size_t)h->L * h->E, LS = h->slot_off[h->L];
   std::vector<int32_t> map(LE, -1), owner(LS, -1);
   if (h->opts.all_resident) {
     for (int l = 0; l < h->L; ++l)
       for (int e = 0; e < h->E; ++e) {
         map[(size_t)l * h->E + e] = e;
-        owner[(size_t)l * h->S + e] = e;
+        owner[h->slot_off[l] + e] = e;
       }
   }
   cudaError_t e = cudaMemcpy(h->map, map.data(), LE * 4, cudaMemcpyHostToDevice);
@@ -175,11 +177,11 @@ int init_state(moe_cache* h) {
 LayerDev layer_dev(moe_cache* h, int l) {
   LayerDev d;
   d.map = h->map + (size_t)l * h->E;
-  d.owner = h->owner + (size_t)l * h->S;
-  d.stamp = h->stamp + (size_t)l * h->S;
+  d.owner = h->owner + h->slot_off[l];
+  d.stamp = h->stamp + h->slot_off[l];
   d.clock = h->clock + l;
-  d.slot_w = h->slot_w + (size_t)l * h->S * h->Bw;
-  d.slot_s = h->slot_s + (size_t)l * h->S * h->Bs;
+  d.slot_w = h->slot_w + h->slot_off[l] * h->Bw;
+  d.slot_s = h->slot_s + h->slot_off[l] * h->Bs;
   d.host_w = h->host_w[l];
   d.host_s = h->host_s[l];
   d.gscale = h->gscale + (size_t)l * h->E * 3;
@@ -229,13 +231,21 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
       o.bypass_rows > MOE_MAX_CACHED_ROWS || !gemv_supported(hidden, inter, top_k))
     return MOE_ERR_UNSUPPORTED;
   if (o.all_resident) slots = experts;
-  if (slots < top_k || slots > experts) return MOE_ERR_ARG;
+  std::vector<int> S_of(layers, slots);
+  if (o.slots_per_layer && !o.all_resident)
+    for (int l = 0; l < layers; ++l) S_of[l] = o.slots_per_layer[l];
+  for (int l = 0; l < layers; ++l)
+    if (S_of[l] < top_k || S_of[l] > experts) return MOE_ERR_ARG;
+  o.slots_per_layer = nullptr;  // read here only
 
   moe_cache* h = new (std::nothrow) moe_cache();
   if (!h) return MOE_ERR_OOM;
   h->L = layers;
   h->E = experts;
-  h->S = slots;
+  h->S_of = S_of;
+  h->slot_off.assign(layers + 1, 0);
+  for (int l = 0; l < layers; ++l) h->slot_off[l + 1] = h->slot_off[l] + S_of[l];
+  h->S = *std::max_element(S_of.begin(), S_of.end());
   h->H = hidden;
   h->I = inter;
   h->k = top_k;
@@ -268,7 +278,7 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
     }
     std::memcpy(gs.data() + (size_t)l * experts * 3, hl.gscale, sizeof(float) * experts * 3);
   }
-  const size_t LS = (size_t)layers * slots, LE = (size_t)layers * experts;
+  const size_t LS = h->slot_off[layers], LE = (size_t)layers * experts;
   size_t max_picks = (size_t)o.max_rows * top_k;
   if (max_picks < (size_t)MOE_MAX_PICKS) max_picks = MOE_MAX_PICKS;
   const int cap = o.trace_capacity;
@@ -325,10 +335,10 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
   e = cudaMemcpy(h->gscale, gs.data(), gs.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess && o.all_resident) {
     for (int l = 0; l < layers && e == cudaSuccess; ++l) {
-      e = cudaMemcpy(h->slot_w + (size_t)l * slots * h->Bw, host_backing[l].w,
+      e = cudaMemcpy(h->slot_w + h->slot_off[l] * h->Bw, host_backing[l].w,
                      (size_t)experts * h->Bw, cudaMemcpyHostToDevice);
       if (e == cudaSuccess)
-        e = cudaMemcpy(h->slot_s + (size_t)l * slots * h->Bs, host_backing[l].s,
+        e = cudaMemcpy(h->slot_s + h->slot_off[l] * h->Bs, host_backing[l].s,
                        (size_t)experts * h->Bs, cudaMemcpyHostToDevice);
     }
   }
@@ -373,7 +383,7 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     // adds them in rank order, so the result does not depend on the hit/miss
     // split.
     if (e == cudaSuccess)
-      e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
+      e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S_of[layer], h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, nullptr);
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess) e = cudaEventRecord(h->fork, st);
@@ -409,7 +419,7 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   const int npicks = rows * h->k;
   if (rows <= h->opts.bypass_rows) {
     if (e == cudaSuccess)
-      e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S, h->Bw, h->Bs, L, h->plan,
+      e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S_of[layer], h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, h->gp);
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess && !h->opts.all_resident)
@@ -499,15 +509,21 @@ int moe_cache_slot_map(const moe_cache_t* h, int layer, int32_t* expert_of_slot)
   if (!h || !expert_of_slot || layer < 0 || layer >= h->L) return MOE_ERR_ARG;
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess)
-    e = cudaMemcpy(expert_of_slot, h->owner + (size_t)layer * h->S, sizeof(int32_t) * h->S,
-                   cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(expert_of_slot, h->owner + h->slot_off[layer],
+                   sizeof(int32_t) * h->S_of[layer], cudaMemcpyDeviceToHost);
   return cuda_err(e);
 }
 
+int moe_cache_layer_slots(const moe_cache_t* h, int layer, int* slots) {
+  if (!h || !slots || layer < 0 || layer >= h->L) return MOE_ERR_ARG;
+  *slots = h->S_of[layer];
+  return MOE_OK;
+}
+
 int moe_cache_slot_bytes(const moe_cache_t* h, int layer, int slot, void* w_dst, void* s_dst) {
-  if (!h || layer < 0 || layer >= h->L || slot < 0 || slot >= h->S) return MOE_ERR_ARG;
+  if (!h || layer < 0 || layer >= h->L || slot < 0 || slot >= h->S_of[layer]) return MOE_ERR_ARG;
   cudaError_t e = cudaDeviceSynchronize();
-  const size_t ls = (size_t)layer * h->S + slot;
+  const size_t ls = h->slot_off[layer] + slot;
   if (e == cudaSuccess && w_dst)
     e = cudaMemcpy(w_dst, h->slot_w + ls * h->Bw, h->Bw, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && s_dst)

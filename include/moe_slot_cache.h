@@ -100,6 +100,10 @@ typedef struct {
                           stepped alone or inside a round of up to 16 rows (exact verify
                           rows for speculative decoding); 0 (default): one-row steps take
                           the faster CUDA-core decode path */
+  const int32_t* slots_per_layer; /* NULL: every layer has `slots` slots; else host int32
+                                     [layers], layer l's ring size (top_k <= S_l <= experts,
+                                     e.g. from moe_policy_size_layers), read at create only;
+                                     ignored with all_resident */
 } moe_cache_opts_t;
 
 typedef struct {
@@ -167,8 +171,11 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
  * error_flags OR-ed).  Waits for all device work (device synchronize). */
 int moe_cache_stats(const moe_cache_t* h, int layer, moe_cache_stats_t* out);
 
-/* expert_of_slot: host int32 [slots]; -1 = empty.  Device synchronize. */
+/* expert_of_slot: host int32 [layer's ring size]; -1 = empty.  Device synchronize. */
 int moe_cache_slot_map(const moe_cache_t* h, int layer, int32_t* expert_of_slot);
+
+/* *slots = the ring size of `layer`. */
+int moe_cache_layer_slots(const moe_cache_t* h, int layer, int* slots);
 
 /* Copy one slot's resident bytes to host memory (w_dst: Bw bytes, s_dst: Bs
  * bytes; either may be NULL).  Device synchronize. */
@@ -227,6 +234,56 @@ int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int m
  * NULL stops recording.  The library does not own the events. */
 #define MOE_TIMING_EVENTS 8
 int moe_cache_set_timing_events(moe_cache_t* h, void* const* events);
+
+/* --------------------------------------------------- offline slot policy */
+
+/* Slot policies evaluated on a routing trace, host only (no GPU, no handle).
+ * The pages compare the cache's LRU with a hindsight-static pin of the
+ * hottest experts and with hybrids, on recorded routing traces, and size each
+ * layer's ring from its trace ("GB300 GLM 5.3 Testing", LRU vs static and
+ * hybrid hit rates; "GLM 5.3 Testing: HBM Expert Allocation", per-layer slot
+ * budgets).
+ *   trace: host int32 [steps][picks], one layer's expert ids per layer-step
+ *          (picks = rows * top_k, row-major), each in [0, experts).
+ * LRU follows the cache exactly: a pick hits if its expert was resident when
+ * the step began; each missing expert of the step's union is fetched once; a
+ * union larger than the ring bypasses it (read from host memory, ring and
+ * clock untouched).  Errors: MOE_ERR_ARG (bad sizes or an id out of range). */
+typedef struct {
+  uint64_t steps;        /* layer-steps in the trace */
+  uint64_t picks;        /* picks of the steps that did not bypass */
+  uint64_t hits;         /* of those, picks served from HBM (resident or pinned) */
+  uint64_t misses;       /* experts fetched into the ring */
+  uint64_t evictions;    /* fetches that replaced a resident expert */
+  uint64_t bypass_steps; /* steps whose (unpinned) union exceeded the ring */
+  uint64_t host_experts; /* experts read over the host link: fetches, bypassed
+                            unions, and unpinned experts under a static pin */
+} moe_policy_result_t;
+
+/* LRU ring of `slots` slots (1 <= slots <= experts). */
+int moe_policy_lru(const int32_t* trace, int steps, int picks, int experts, int slots,
+                   moe_policy_result_t* out);
+/* Hindsight static: the `slots` most picked experts of the whole trace (ties
+ * to the lower id) are always resident; every other expert a step uses is
+ * read from host memory each time (host_experts counts it once per step).
+ * 0 <= slots <= experts; misses and evictions are 0. */
+int moe_policy_static(const int32_t* trace, int steps, int picks, int experts, int slots,
+                      moe_policy_result_t* out);
+/* Hybrid: the `pinned` hottest experts are always resident and the other
+ * slots - pinned slots run LRU for the rest (pinned == 0: LRU; pinned ==
+ * slots: static).  0 <= pinned <= slots <= experts. */
+int moe_policy_hybrid(const int32_t* trace, int steps, int picks, int experts, int slots,
+                      int pinned, moe_policy_result_t* out);
+/* host_experts[S - 1] of an S-slot LRU ring for S = 1 .. max_slots. */
+int moe_policy_lru_curve(const int32_t* trace, int steps, int picks, int experts, int max_slots,
+                         uint64_t* host_experts);
+/* Per-layer ring sizes for a total slot budget: given each layer's LRU curve
+ * (host_experts: host [layers][max_slots], row l from moe_policy_lru_curve on
+ * layer l's trace), choose slots_out[l] in [min_slots, max_slots] with
+ * sum <= budget minimising the summed host-link experts (exact dynamic
+ * programme).  slots_out: host int32 [layers]. */
+int moe_policy_size_layers(const uint64_t* host_experts, int layers, int max_slots, int budget,
+                           int min_slots, int32_t* slots_out);
 
 /* ------------------------------------------------------ no-allocation pass */
 
