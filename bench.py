@@ -67,6 +67,15 @@ def _traffic(kernel: str, picks: float):
     return None if k is None else k["dram_bytes_per_pick"] * picks
 
 
+def _breakdown(ev):
+    """Mean event intervals of some one-row steps (events 0..7, see the header)."""
+    if len(ev) == 0:
+        return None
+    m = ev.mean(axis=0)
+    return {"route": m[1], "read_through": m[3] - m[2], "resident_gateup": m[5] - m[1],
+            "resident_down": m[6] - m[5], "join_to_end": m[7] - max(m[6], m[4]), "step": m[7]}
+
+
 class ClockSampler:
     def __init__(self, uuid: str | None):
         self.proc = None
@@ -320,7 +329,9 @@ def run_ours(args) -> None:
                     "ms_route": float(np.mean(t_route)),
                     "ms_step_with_miss": float(np.mean(ev_ms[n_miss > 0, 7])) if (n_miss > 0).any() else None,
                     "ms_step_no_miss": float(np.mean(ev_ms[n_miss == 0, 7])) if (n_miss == 0).any() else None,
-                    "frac_steps_with_miss": float(np.mean(n_miss > 0))}
+                    "frac_steps_with_miss": float(np.mean(n_miss > 0)),
+                    "no_miss_breakdown_ms": _breakdown(ev_ms[n_miss == 0]),
+                    "with_miss_breakdown_ms": _breakdown(ev_ms[n_miss > 0])}
 
     # host-link bandwidth probed in the same session
     from hbm_slot_cache_gb300 import HostBank, moe_probe_host_link

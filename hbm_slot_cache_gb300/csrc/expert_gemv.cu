@@ -52,7 +52,7 @@ namespace {
 
 constexpr int kGateUpRows = 4;     // row pairs per gate/up unit
 constexpr int kGateUpThreads = 512;
-constexpr int kDownRows = 4;       // output rows per down unit (per row group)
+constexpr int kDownUnitRows = 32;  // W2 rows per down unit (each warp takes two)
 constexpr int kDownThreads = 512;
 constexpr int kSmemPerSm = 227 * 1024;
 
@@ -91,19 +91,30 @@ __device__ __forceinline__ float dot16_f16(uint2 codes, const uint32_t* __restri
   return s0 + s1;
 }
 
-// 16 codes (8 bytes) times 16 fp32 values v(0..15).
+// 16 codes (8 bytes) times 16 fp32 values v(0..15): even elements into s0,
+// odd ones into s1 (both rn fp32 FMAs, done as one packed f32x2 FMA), then
+// s0 + s1.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
 template <class Get>
 __device__ __forceinline__ float dot16_f32(uint32_t lo, uint32_t hi, Get v) {
   uint32_t h[8];
   e2m1x8_to_f16x8(lo, h[0], h[1], h[2], h[3]);
   e2m1x8_to_f16x8(hi, h[4], h[5], h[6], h[7]);
-  float s0 = 0.f, s1 = 0.f;
+  uint64_t acc = 0ull;  // (s0, s1) = (+0, +0)
 #pragma unroll
   for (int b = 0; b < 8; ++b) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
-    s0 = fmaf(f.x, v(2 * b), s0);
-    s1 = fmaf(f.y, v(2 * b + 1), s1);
+    asm("fma.rn.f32x2 %0, %1, %2, %0;"
+        : "+l"(acc)
+        : "l"(pack_f32x2(f.x, f.y)), "l"(pack_f32x2(v(2 * b), v(2 * b + 1))));
   }
+  float s0, s1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(acc));
   return s0 + s1;
 }
 
@@ -302,19 +313,24 @@ __device__ void finish_step(const Plan* __restrict__ plan, const float* __restri
 }
 
 // One W2 row, one warp: y = sum over the row's 32-element blocks c, each the
-// partial a thread of the down kernel computes, reduced in that kernel's
-// order (a butterfly over 32 consecutive blocks, then those sums in order; or
-// a butterfly within groups of I/32 < 32 lanes).
-__device__ __forceinline__ float w2_row_warp(const uint8_t* __restrict__ cw,
-                                             const uint8_t* __restrict__ sc,
-                                             const float* __restrict__ hs, int I, int lane) {
-  const int C = I / 32;
+// partial w2_block computes, reduced in a fixed order: a butterfly over 32
+// consecutive blocks, then those sums in order (I/32 >= 32); or a butterfly
+// within groups of I/32 < 32 lanes.  get(m, i) returns element i of block
+// lane + 32 m of gscale * w * h (block lane when I/32 < 32); nb = blocks per
+// lane.  Every caller uses this function, so a pick gets the same bits in
+// every kernel.
+template <class Get>
+__device__ __forceinline__ float w2_row_warp_g(const uint8_t* __restrict__ cw,
+                                               const uint8_t* __restrict__ sc, int C, int nb,
+                                               int lane, Get get) {
   if (C >= 32) {
     float y = 0.f;
-    for (int c = lane; c < C; c += 32) {
+#pragma unroll
+    for (int m = 0; m < nb; ++m) {
+      const int c = lane + 32 * m;
       float p = w2_block(*reinterpret_cast<const uint4*>(cw + c * 16),
                          *reinterpret_cast<const uint16_t*>(sc + c * 2),
-                         [&](int i) { return hs[i * C + c]; });
+                         [&](int i) { return get(m, i); });
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xFFFFFFFFu, p, o);
       y += p;
@@ -325,9 +341,19 @@ __device__ __forceinline__ float w2_row_warp(const uint8_t* __restrict__ cw,
   if (lane < C)
     p = w2_block(*reinterpret_cast<const uint4*>(cw + lane * 16),
                  *reinterpret_cast<const uint16_t*>(sc + lane * 2),
-                 [&](int i) { return hs[i * C + lane]; });
+                 [&](int i) { return get(0, i); });
   for (int o = C / 2; o > 0; o >>= 1) p += __shfl_xor_sync(0xFFFFFFFFu, p, o);
   return p;
+}
+
+// The same with gscale * w * h transposed in shared memory (element c*32+i at
+// i*C + c, so a warp's lanes read distinct banks).
+__device__ __forceinline__ float w2_row_warp(const uint8_t* __restrict__ cw,
+                                             const uint8_t* __restrict__ sc,
+                                             const float* __restrict__ hs, int I, int lane) {
+  const int C = I / 32;
+  return w2_row_warp_g(cw, sc, C, C >= 32 ? C / 32 : 1, lane,
+                       [&](int m, int i) { return hs[i * C + lane + 32 * m]; });
 }
 
 // Extra arguments of the read-through launch.
@@ -412,7 +438,8 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   // phase B (read-through only): W2 rows of the missed picks, URB rows a unit.
   // Units are taken in ascending order from the step's work counter, so CTAs
   // that finish phase A early take more.  Stages: NSB of its own from the
-  // start, then NSA more in the phase-A stage memory once phase A is done.
+  // start (none by default: the link serves phase A first), then NSA more in
+  // the phase-A stage memory once phase A is done.
   const int URB = FROM_HOST ? rt.URB : 1, NSB = FROM_HOST ? rt.NSB : 0;
   const int stage_b = URB * (I / 2 + I / 16);
   const int NSA = FROM_HOST ? min(kMaxStagesB - NSB, NS * stage_bytes / stage_b) : 0;
@@ -600,129 +627,92 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
 
 // ---------------------------------------------------------------- down
 
-template <int R2>
+// Each CTA serves one pick (CTAs b, b + pcnt, ... share pick b % pcnt), keeps
+// gscale * w * h of that pick in shared memory (transposed), and walks units
+// of kDownUnitRows W2 rows, a warp per row with w2_row_warp.  A unit's code and
+// scale rows are contiguous in the slot and arrive by two 1-D TMA bulk copies.
+template <int MB>  // h blocks a lane keeps in registers (0: read them from shared memory)
 __global__ void __launch_bounds__(kDownThreads, 1)
 gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
                  float* __restrict__ ypart, int H, int I, int NS, uint32_t* flags, int subset,
                  float* __restrict__ out, uint32_t* __restrict__ done, int total_ctas) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_last;
-  const int C = I / 32;  // 32-element blocks per h row; C divides 32 or is a multiple of it
-  const int kmax = plan->npicks;
-  int pbeg = 0, pcnt = kmax;
+  __shared__ int s_last, s_abort;
+  constexpr int UR = kDownUnitRows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  int pbeg = 0, pcnt = plan->npicks;
   if (subset == kPicksHit) pcnt = plan->n_hit;
   if (subset == kPicksMiss) {
     pbeg = plan->n_hit;
-    pcnt = kmax - plan->n_hit;
+    pcnt = plan->npicks - plan->n_hit;
   }
-  auto pick_of = [&](int jl) { return subset == kPicksAll ? jl : plan->order[pbeg + jl]; };
-  // Few picks: spread each unit's rows over RL row groups so the CTA stays
-  // busy (thread = (row group g, pick jl, 32-block c)); RL * pcnt <= kmax keeps
-  // a stage within the room sized for all picks.
-  int RL = 1;
-  while (pcnt > 0 && 2 * RL * pcnt <= kmax && 2 * RL * pcnt * C <= (int)blockDim.x) RL *= 2;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per_g = pcnt * C;
-  const bool active = tid < RL * per_g;
-  const int g = active ? tid / per_g : 0;
-  const int rem = tid - g * per_g;
-  const int jl = active ? rem / C : 0, c = active ? rem - jl * C : 0;
-  const int j = active ? pick_of(jl) : 0;
-  const int UR = R2 * RL;                           // rows per unit
-  const int cb = UR * I / 2, sb = UR * I / 16;      // per pick
-  const int stage_stride = kmax * R2 * (I / 2 + I / 16);
-  const int stage_bytes = pcnt * (cb + sb);
-  Stages S = carve(smem, NS, stage_stride);
-
-  const int nunits = pcnt > 0 ? H / UR : 0;
-  const int my_units = units_of_block(nunits);
-  const size_t w2_codes = (size_t)I * H;        // 2I rows of H/2 bytes precede W2
-  const size_t w2_scales = (size_t)I * H / 8;   // 2I rows of H/16 bytes
-
-  // stage layout: every pick's codes, then every pick's scales
-  auto issue = [&](int unit, int stage) {  // thread 0
-    uint8_t* dst = S.base + (size_t)stage * stage_stride;
-    mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
-    for (int q = 0; q < pcnt; ++q) {
-      const int jj = pick_of(q);
-      bulk_g2s(dst + q * cb, plan->wptr[jj] + w2_codes + (size_t)unit * cb, cb, &S.full[stage]);
-      bulk_g2s(dst + pcnt * cb + q * sb, plan->sptr[jj] + w2_scales + (size_t)unit * sb, sb,
-               &S.full[stage]);
-    }
+  const int row_b = I / 2 + I / 16;
+  const int stage_b = UR * row_b;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_b);
+  float* hs = reinterpret_cast<float*>(full + NS);
+  // this CTA's pick and its share of the pick's row units
+  const int jl = pcnt > 0 ? (int)blockIdx.x % pcnt : 0;
+  const int q = pcnt > 0 ? (int)blockIdx.x / pcnt : 0;
+  const int nq = pcnt > 0 ? ((int)gridDim.x - jl + pcnt - 1) / pcnt : 0;
+  const int units = H / UR;
+  const int my_units = (pcnt > 0 && q < units) ? (units - 1 - q) / nq + 1 : 0;
+  const int j = pcnt > 0 ? (subset == kPicksAll ? jl : plan->order[pbeg + jl]) : 0;
+  const uint8_t* wsrc = plan->wptr[j] + (size_t)I * H;     // W2 codes
+  const uint8_t* ssrc = plan->sptr[j] + (size_t)I * H / 8; // W2 scales
+  auto issue = [&](int i, int stage) {  // thread 0
+    const int rb = q + i * nq;
+    uint8_t* dst = smem + (size_t)stage * stage_b;
+    mbar_arrive_expect_tx(&full[stage], (uint32_t)stage_b);
+    bulk_g2s(dst, wsrc + (size_t)rb * UR * (I / 2), UR * (I / 2), &full[stage]);
+    bulk_g2s(dst + UR * (I / 2), ssrc + (size_t)rb * UR * (I / 16), UR * (I / 16), &full[stage]);
   };
-
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
-    *S.abort_flag = 0;
-    for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
+    s_abort = 0;
+    for (int s = 0; s < NS && s < my_units; ++s) issue(s, s);
+  }
+  if (my_units > 0) {  // uniform
+    const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
+    for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
+      hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldg(hbuf + (size_t)j * I + e));
   }
   __syncthreads();
-
-  // gscale_j * w_j * h_j for this thread's 32 inputs, for the whole kernel
-  float hv[32];
-  {
-    const float f = active ? __fmul_rn(plan->gs[j][2], plan->wts[j]) : 0.f;
-    const float4* hp = reinterpret_cast<const float4*>(hbuf + (size_t)j * I + c * 32);
+  // this lane's blocks of the pick's h, kept in registers for the whole kernel
+  const int C = I / 32;
+  float hv[MB > 0 ? MB : 1][32];
+  if constexpr (MB > 0) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 v = active ? __ldg(hp + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-      hv[4 * q] = __fmul_rn(f, v.x);
-      hv[4 * q + 1] = __fmul_rn(f, v.y);
-      hv[4 * q + 2] = __fmul_rn(f, v.z);
-      hv[4 * q + 3] = __fmul_rn(f, v.w);
-    }
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int c = lane + 32 * m;
+        hv[m][e] = (my_units > 0 && c < C) ? hs[e * C + c] : 0.f;
+      }
   }
-
   for (int i = 0; i < my_units; ++i) {
-    const int unit = blockIdx.x + i * gridDim.x;
     const int stage = i % NS;
-    if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
+    if (!mbar_wait_bounded(&full[stage], (uint32_t)((i / NS) & 1), flags)) s_abort = 1;
     __syncthreads();
-    if (*S.abort_flag) {
-      drain_fills<false>(S, i, NS, my_units, flags);
+    if (s_abort) {
+      drain_fills<false>(Stages{smem, full, nullptr, nullptr}, i, NS, my_units, flags);
       break;  // still counted below, so the step's combine happens
     }
-    const uint8_t* st = S.base + (size_t)stage * stage_stride;
-    float a[R2];
-#pragma unroll
-    for (int r = 0; r < R2; ++r) {
-      a[r] = 0.f;
-      if (active) {
-        const int row = g + RL * r;
-        const uint4 cw = *reinterpret_cast<const uint4*>(st + jl * cb + row * (I / 2) + c * 16);
-        const uint32_t s2 = *reinterpret_cast<const uint16_t*>(st + pcnt * cb + jl * sb +
-                                                               row * (I / 16) + c * 2);
-        a[r] = w2_block(cw, s2, [&](int i) { return hv[i]; });
-      }
+    const uint8_t* st = smem + (size_t)stage * stage_b;
+    const int rb = q + i * nq;
+    for (int r = warp; r < UR; r += nwarps) {
+      const uint8_t* cw = st + r * (I / 2);
+      const uint8_t* sc = st + UR * (I / 2) + r * (I / 16);
+      float y;
+      if constexpr (MB > 0)
+        y = w2_row_warp_g(cw, sc, C, MB, lane, [&](int m, int e) { return hv[m][e]; });
+      else
+        y = w2_row_warp(cw, sc, hs, I, lane);
+      if (lane == 0) ypart[(size_t)j * H + rb * UR + r] = y;
     }
-    if (C >= 32) {
-      // a (row group, pick) spans C/32 whole warps: butterfly per warp, then its warps
-      const float s = warp_reduce_scatter<R2>(a, lane);
-      constexpr int sh = 5 - ilog2(R2);
-      if ((lane & ((1 << sh) - 1)) == 0) S.red[warp * R2 + (lane >> sh)] = s;
-      __syncthreads();
-      if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
-      if (tid < RL * pcnt * R2) {
-        const int gq = tid / R2, r = tid - gq * R2;  // gq = g * pcnt + q
-        const int gg = gq / pcnt, q = gq - gg * pcnt, wp = C / 32;
-        float y = 0.f;
-        for (int w = 0; w < wp; ++w) y += S.red[(gq * wp + w) * R2 + r];
-        ypart[(size_t)pick_of(q) * H + unit * UR + gg + RL * r] = y;
-      }
-    } else {
-      // several (row group, pick) pairs per warp: reduce within each aligned group of C lanes
-#pragma unroll
-      for (int r = 0; r < R2; ++r)
-        for (int o = C / 2; o > 0; o >>= 1) a[r] += __shfl_xor_sync(0xFFFFFFFFu, a[r], o);
-      if (active && c == 0)
-#pragma unroll
-        for (int r = 0; r < R2; ++r) ypart[(size_t)j * H + unit * UR + g + RL * r] = a[r];
-      __syncthreads();
-      if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
-    }
+    __syncthreads();
+    if (tid == 0 && i + NS < my_units) issue(i + NS, stage);
   }
-
   finish_step(plan, ypart, out, H, done, total_ctas, &s_last);
 }
 
@@ -763,7 +753,9 @@ GateUpShape gateup_shape(int H, int stages) {
 }
 
 // Phase-B shape of the read-through launch: W2 rows per unit (about 20 KB a
-// stage), two stages, then gscale * w * h of one pick in shared memory.
+// stage), no stages of its own (the W2 stages use phase A's stage memory once
+// phase A is done, so phase A has the host link to itself until then), then
+// gscale * w * h of one pick in shared memory.
 struct RtShape {
   int URB, NSB, b_off, smem;
 };
@@ -774,7 +766,7 @@ RtShape rt_shape(const GateUpShape& s, int I) {
   int urb = 16;
   while (urb > 4 && urb * row > 20 * 1024) urb /= 2;
   r.URB = urb;
-  r.NSB = 2;
+  r.NSB = 0;
   r.b_off = (s.smem + 127) / 128 * 128;
   r.smem = r.b_off + r.NSB * urb * row + 8 * kMaxStagesB + I * 4;
   return r;
@@ -820,23 +812,24 @@ struct DownShape {
   int NS, smem, stage;
 };
 
-DownShape down_shape(int I, int k, int stages) {
+DownShape down_shape(int I, int stages) {
   DownShape d;
-  constexpr int R2 = kDownRows;
-  d.stage = k * (R2 * I / 2 + R2 * I / 16);
-  const int red_floats = (kDownThreads / 32) * R2;
-  int ns = (kSmemPerSm - 1024 - 16 - red_floats * 4) / d.stage;
+  d.stage = kDownUnitRows * (I / 2 + I / 16);
+  const int per_cta = kSmemPerSm / 2 - 1024;  // room for one more CTA of another kernel
+  int ns = (per_cta - I * 4 - 8 * 8) / d.stage;
+  if (ns < 2) ns = (kSmemPerSm - 1024 - I * 4 - 8 * 8) / d.stage;  // large I
   if (ns > 8) ns = 8;
   if (stages > 0 && stages < ns) ns = stages;
   d.NS = ns;
-  d.smem = ns * d.stage + 8 * ns + 8 + red_floats * 4;
+  d.smem = ns * d.stage + 8 * ns + I * 4;
   return d;
 }
 
-cudaError_t run_down(cudaStream_t st, int grid, int nt, const DownShape& d, const Plan* plan,
+template <int MB>
+cudaError_t run_down(cudaStream_t st, int grid, const DownShape& d, const Plan* plan,
                      const GemvWorkspace& ws, int H, int I, uint32_t* flags, int subset,
                      float* out, uint32_t* done, int total_ctas) {
-  auto kern = gemv_down_kernel<kDownRows>;
+  auto kern = gemv_down_kernel<MB>;
   static int smem_set = 0;
   if (d.smem > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem);
@@ -844,24 +837,18 @@ cudaError_t run_down(cudaStream_t st, int grid, int nt, const DownShape& d, cons
     if (e != cudaSuccess) return e;
     smem_set = d.smem;
   }
-  kern<<<grid, nt, d.smem, st>>>(plan, ws.hbuf, ws.ypart, H, I, d.NS, flags, subset, out, done,
-                                 total_ctas);
+  kern<<<grid, kDownThreads, d.smem, st>>>(plan, ws.hbuf, ws.ypart, H, I, d.NS, flags, subset,
+                                           out, done, total_ctas);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool gemv_supported(int H, int I, int k) {
-  const int C = I / 32;  // a pick's threads in the down kernel: whole warps or part of one
-  return H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM &&
-         k * C <= kDownThreads && (C % 32 == 0 || 32 % C == 0) &&
-         H / 16 <= kGateUpThreads * kGateUpRows && gateup_shape(H, 0).NT % 32 == 0;
-}
-
-int gemv_down_tile_rows(int H, int I) {
-  (void)H;
-  (void)I;
-  return kDownRows;
+  const int C = I / 32;  // 32-element blocks of a W2 row: whole warps of them or part of one
+  return H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM && k >= 1 &&
+         (C % 32 == 0 || 32 % C == 0) && H / 16 <= kGateUpThreads * kGateUpRows &&
+         gateup_shape(H, 0).NT % 32 == 0 && down_shape(I, 0).NS >= 1;
 }
 
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
@@ -898,21 +885,24 @@ cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uin
 }
 
 int gemv_down_grid(int H, int num_sms, const GemvLaunch& how) {
-  const int nunits = H / kDownRows;
-  int grid = how.grid > 0 ? how.grid : num_sms;
-  return grid < nunits ? grid : nunits;
+  (void)H;
+  const int grid = how.grid > 0 ? how.grid : num_sms;
+  return grid > MOE_MAX_TOPK ? grid : MOE_MAX_TOPK;  // at least one CTA per pick
 }
 
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
                              const GemvWorkspace& ws, uint32_t* flags, int num_sms,
                              const GemvLaunch& how, float* out, uint32_t* done, int total_ctas) {
-  if (k * (I / 32) > kDownThreads) return cudaErrorInvalidConfiguration;
-  const DownShape d = down_shape(I, k, how.stages);
-  if (d.NS < 1) return cudaErrorInvalidConfiguration;
+  (void)k;
+  const DownShape d = down_shape(I, how.stages);
+  if (d.NS < 1 || how.from_host) return cudaErrorInvalidConfiguration;  // slot bytes only
   const int grid = gemv_down_grid(H, num_sms, how);
-  const int nt = ((k * (I / 32) + 31) / 32) * 32;
-  if (how.from_host) return cudaErrorInvalidValue;  // reads slot bytes only
-  return run_down(st, grid, nt, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
+  const int C = I / 32;  // h blocks per W2 row: in registers up to two per lane
+  if (C <= 32)
+    return run_down<1>(st, grid, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
+  if (C == 64)
+    return run_down<2>(st, grid, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
+  return run_down<0>(st, grid, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
 }
 
 }  // namespace moe

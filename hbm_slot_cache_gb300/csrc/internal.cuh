@@ -130,7 +130,7 @@ cudaError_t launch_link_probe(cudaStream_t st, const void* src, void* dst, size_
 struct GemvWorkspace {
   float* hbuf;        // [MOE_MAX_PICKS][I]
   float* ypart;       // [MOE_MAX_TOPK][H]
-  uint32_t* tile_cnt; // [H / down rows per tile]
+  uint32_t* tile_cnt; // step counters, >= 2 + MOE_MAX_TOPK words, zero between steps
   uint32_t* flags;    // error flags word for waits (per layer stats flags)
 };
 // Pick subsets of a one-row step: the picks resident at step start, the
@@ -162,8 +162,8 @@ cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, in
                              const GemvWorkspace& ws, uint32_t* flags, int num_sms,
                              const GemvLaunch& how, float* out, uint32_t* done, int total_ctas);
 int gemv_down_grid(int H, int num_sms, const GemvLaunch& how);
-int gemv_down_tile_rows(int H, int I);
-// Shapes the M = 1 expert kernels handle (top_k * inter <= 16384, dims % 128 == 0).
+// Shapes the M = 1 expert kernels handle (dims % 128 == 0, inter / 32 a multiple or a
+// divisor of 32).
 bool gemv_supported(int H, int I, int k);
 
 // Every kernel of a step asks for the maximum shared-memory carveout, so an SM

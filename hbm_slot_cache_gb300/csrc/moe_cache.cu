@@ -17,6 +17,7 @@ using namespace moe;
 namespace {
 constexpr int kDefaultMaxRows = 512;  // largest prefill chunk a handle takes by default
 constexpr int kDefaultPrefillChunk = 32;  // experts staged per prefill chunk (two chunks held)
+constexpr int kStepCounterWords = 64;     // one-row step counters (>= 2 + MOE_MAX_TOPK)
 }
 
 struct moe_cache {
@@ -169,7 +170,7 @@ int init_state(moe_cache* h) {
   if (e == cudaSuccess) e = cudaMemset(h->stats, 0, (size_t)h->L * sizeof(DevStats));
   if (e == cudaSuccess) e = cudaMemset(h->trace_head, 0, (size_t)h->L * 4);
   if (e == cudaSuccess)
-    e = cudaMemset(h->gemv.tile_cnt, 0, sizeof(uint32_t) * (size_t)(h->H / gemv_down_tile_rows(h->H, h->I) + 1));
+    e = cudaMemset(h->gemv.tile_cnt, 0, sizeof(uint32_t) * kStepCounterWords);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return cuda_err(e);
 }
@@ -293,8 +294,7 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
             dalloc(&h->plan, 1) == cudaSuccess &&
             dalloc(&h->gemv.hbuf, (size_t)max_picks * inter) == cudaSuccess &&
             dalloc(&h->gemv.ypart, (size_t)max_picks * hidden) == cudaSuccess &&
-            dalloc(&h->gemv.tile_cnt, (size_t)(hidden / gemv_down_tile_rows(hidden, inter) + 1)) ==
-                cudaSuccess;
+            dalloc(&h->gemv.tile_cnt, (size_t)kStepCounterWords) == cudaSuccess;
   ok = ok && alloc_multirow(h);
   if (ok && o.max_rows > o.bypass_rows && o.prefill_chunk > 0) {
     // staged prefill: two halves of `chunk` expert slots, two events per chunk

@@ -142,9 +142,9 @@ typedef struct {
  * change afterwards.  Caches start empty.  host_backing has `layers` entries.
  * opts may be NULL (defaults).  Limits: experts <= MOE_MAX_EXPERTS,
  * top_k <= min(experts, MOE_MAX_TOPK), top_k <= slots <= experts,
- * hidden and inter multiples of 128 and <= MOE_MAX_DIM, top_k * inter <= 16384
- * (the one-row down kernel keeps one 32-element block of h per thread).
- * Errors: MOE_ERR_ARG, MOE_ERR_NOT_PINNED, MOE_ERR_OOM, MOE_ERR_CUDA,
+ * hidden and inter multiples of 128 and <= MOE_MAX_DIM, inter / 32 a multiple
+ * or a divisor of 32 (the one-row down pass spreads a W2 row's 32-element
+ * blocks over a warp's lanes).  Errors: MOE_ERR_ARG, MOE_ERR_NOT_PINNED, MOE_ERR_OOM, MOE_ERR_CUDA,
  * MOE_ERR_UNSUPPORTED.  On error *out is NULL and nothing leaks. */
 int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int hidden,
                      int inter, int top_k, const moe_host_layer_t* host_backing,
