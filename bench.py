@@ -72,7 +72,8 @@ def _breakdown(ev):
     if len(ev) == 0:
         return None
     m = ev.mean(axis=0)
-    return {"route": m[1], "read_through": m[3] - m[2], "resident_gateup": m[5] - m[1],
+    return {"route": m[1], "read_through": m[3] - m[2], "missed_down": m[4] - m[3],
+            "resident_gateup": m[5] - m[1],
             "resident_down": m[6] - m[5], "join_to_end": m[7] - max(m[6], m[4]), "step": m[7]}
 
 
@@ -317,7 +318,8 @@ def run_ours(args) -> None:
     n_hit = k - n_miss
     ev_ms = np.array([[row[0].elapsed_time(row[i]) for i in range(8)] for row in evs])
     t_route = ev_ms[:, 1]
-    t_rt = ev_ms[:, 3] - ev_ms[:, 2]        # missed picks: read-through pass (gate/up + down)
+    t_rt = ev_ms[:, 3] - ev_ms[:, 2]        # missed picks: read-through pass (link + gate/up)
+    t_dn_miss = ev_ms[:, 4] - ev_ms[:, 3]   # missed picks: down from their slots
     t_gu_hit = ev_ms[:, 5] - ev_ms[:, 1]    # resident picks: gate/up from HBM slots
     t_dn_hit = ev_ms[:, 6] - ev_ms[:, 5]    # resident picks: down (+ combine if last)
     gap_ms = sum(evs[t][7].elapsed_time(evs[t + 1][0]) for t in range(G - 1)) / max(G - 1, 1)
@@ -378,6 +380,8 @@ def run_ours(args) -> None:
                                            hbm_peak, "hbm", G),
         "gemv_readthrough[missed picks]": entry(float((n_miss * Bexp).sum()),
                                                 float(t_rt[hm].sum()), link_peak, "host-link", nm),
+        "gemv_down[missed picks]": entry(float((n_miss * dn_pick).sum()), float(t_dn_miss[hm].sum()),
+                                         hbm_peak, "hbm", nm),
         "route_remap": {"ms_per_launch": float(t_route.mean())},
     }
     for n in kern:
@@ -387,8 +391,10 @@ def run_ours(args) -> None:
             kern[n]["traffic"] = None
             kern[n]["note"] = "steps with at least one miss"
     kern["gemv_readthrough[missed picks]"]["note"] += (
-        "; whole missed experts over the host link, gate/up and down computed on the way in, "
+        "; whole missed experts over the host link, gate/up computed on the way in, "
         "written to their slots")
+    kern["gemv_down[missed picks]"]["note"] += "; W2 rows read back from the slots just written"
+
     share = {n: v["ms_per_launch"] * (nm if "missed" in n else G) for n, v in kern.items()}
     dom = max(share, key=share.get)
     roofline = dict(kern[dom])
@@ -452,7 +458,7 @@ def run_ours(args) -> None:
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": E * 4 + H * 2,
                     "d2h_bytes_per_step": H * 4, "steps": Ke},
-            "gpu_launches": K * 4, "clocks": clocks,
+            "gpu_launches": K * 5, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     cache.close()

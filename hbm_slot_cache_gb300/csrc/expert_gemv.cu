@@ -52,7 +52,7 @@ namespace {
 
 constexpr int kGateUpRows = 4;     // row pairs per gate/up unit
 constexpr int kGateUpThreads = 512;
-constexpr int kDownUnitRows = 32;  // W2 rows per down unit (each warp takes two)
+constexpr int kDownUnitRows = kOutBlockRows;  // W2 rows per down unit (each warp takes two)
 constexpr int kDownThreads = 512;
 constexpr int kSmemPerSm = 227 * 1024;
 
@@ -262,53 +262,49 @@ __device__ __forceinline__ void write_through(const uint8_t* stage, const Segs<N
   }
 }
 
-// Counters of one step (a small array, zero between steps):
-//   [0]             CTAs of the step's y'_j launches that have finished
-//   [kWorkCtr]      W2 units taken by the read-through launch
-//   [kPickCtr + jl] gate/up units done for pick jl of the read-through launch
-constexpr int kWorkCtr = 1;   // phase-B units taken by the read-through launch
-constexpr int kPickCtr = 2;
-constexpr int kMaxStagesB = 8;
+// Step counters (see kStepCounterWords).
+constexpr int kRtDoneCtr = 0;  // read-through CTAs finished
+constexpr int kWorkCtr = 1;    // read-through units taken
+constexpr int kBlockCtr = 2;   // + b: picks done for output block b
+constexpr int kMaxStages = 8;  // gate/up stages at most
 
-// Tail of every launch that writes y'_j: count this CTA; the CTA that brings
-// the count to total_ctas adds out = sum_j y'_j in rank order and resets the
-// counters for the next step.
-__device__ void finish_step(const Plan* __restrict__ plan, const float* __restrict__ ypart,
-                            float* __restrict__ out, int H, uint32_t* ctr, int total_ctas,
-                            int* s_last) {
+// Every thread of a down CTA, once all its units' rows are written: count
+// each unit (this CTA's pick, output blocks b0, b0 + db, ...) for its block;
+// for every block whose count this CTA completes over the step's npicks
+// picks, one warp adds out = sum_j y'_j over the block's rows in rank order
+// and resets the count.  s_lastb: room for nunits ints.
+__device__ __forceinline__ void count_blocks(const Plan* __restrict__ plan,
+                                             const float* __restrict__ ypart,
+                                             float* __restrict__ out, int H, uint32_t* ctr,
+                                             int b0, int db, int nunits, int* s_lastb,
+                                             int* s_nlast) {
+  const int npicks = plan->npicks;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   __threadfence();
+  if (threadIdx.x == 0) *s_nlast = 0;
   __syncthreads();
-  if (threadIdx.x == 0) *s_last = atomicAdd(ctr, 1u) == (uint32_t)(total_ctas - 1);
+  for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
+    const int b = b0 + u * db;
+    if (atomicAdd(&ctr[kBlockCtr + b], 1u) == (uint32_t)(npicks - 1))
+      s_lastb[atomicAdd(s_nlast, 1)] = b;
+  }
   __syncthreads();
-  if (*s_last) {
-    __threadfence();
-    // four outputs a thread, eight picks' loads in flight at once
-    const int kmax = plan->npicks;
-    const int H4 = H / 4;
-    const float4* __restrict__ y4 = reinterpret_cast<const float4*>(ypart);
-    for (int o = threadIdx.x; o < H4; o += blockDim.x) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j0 = 0; j0 < kmax; j0 += 8) {
-        float4 v[8];
+  const int nl = *s_nlast;
+  if (nl == 0) return;
+  __threadfence();
+  for (int t = warp; t < nl; t += nwarps) {  // a lane per row of the block
+    const int b = s_lastb[t];
+    const int row = b * kOutBlockRows + lane;
+    float v[MOE_MAX_TOPK];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (j0 + q < kmax) v[q] = __ldcg(y4 + (size_t)(j0 + q) * H4 + o);
+    for (int j = 0; j < MOE_MAX_TOPK; ++j)
+      if (j < npicks) v[j] = __ldcg(ypart + (size_t)j * H + row);
+    float acc = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (j0 + q < kmax) {
-            acc.x += v[q].x;
-            acc.y += v[q].y;
-            acc.z += v[q].z;
-            acc.w += v[q].w;
-          }
-      }
-      reinterpret_cast<float4*>(out)[o] = acc;
-    }
-    if (threadIdx.x == 0) {
-      ctr[0] = 0u;
-      ctr[kWorkCtr] = 0u;
-      for (int jj = 0; jj < kmax; ++jj) ctr[kPickCtr + jj] = 0u;
-    }
+    for (int j = 0; j < MOE_MAX_TOPK; ++j)
+      if (j < npicks) acc += v[j];
+    out[row] = acc;
+    if (lane == 0) ctr[kBlockCtr + b] = 0u;
   }
 }
 
@@ -356,138 +352,15 @@ __device__ __forceinline__ float w2_row_warp(const uint8_t* __restrict__ cw,
                        [&](int m, int i) { return hs[i * C + lane + 32 * m]; });
 }
 
-// Extra arguments of the read-through launch.
-struct RtArgs {
-  float* ypart;     // [k][H] weighted outputs y'_j
-  float* out;       // [H]
-  uint32_t* ctr;    // step counters (see kPickCtr)
-  int total_ctas;   // CTAs of all the step's y'_j launches
-  int URB;          // W2 rows per phase-B unit
-  int NSB;          // phase-B stages
-  int b_off;        // byte offset of the phase-B region in dynamic shared memory
-};
-
 // ----------------------------------------------------------- gate / up
 
-template <int RPT, bool WARP_RED, bool FROM_HOST>
-__global__ void __launch_bounds__(kGateUpThreads, 2)
-gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
-                   float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
-                   int subset, RtArgs rt) {
-  constexpr int V = 2 * RPT;
-  constexpr int R = kGateUpRows;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_xmax[kGateUpThreads / 32];
-  __shared__ int s_last;
-  const int C = H / 16;
+// This thread's 16 activations (block c of the row) as f16, after a
+// power-of-two prescale of the whole row that keeps max |x| below 2^15;
+// returns the factor that undoes the prescale.  Every thread of the CTA
+// calls it (one barrier); the CTA's threads cover every block of the row.
+__device__ __forceinline__ float load_x_f16(const uint16_t* __restrict__ x, int c, float* s_xmax,
+                                            uint32_t (&xh)[8]) {
   const int tid = threadIdx.x, lane = tid & 31;
-  const int g = tid / C, c = tid - g * C;
-  const int cb = R * H / 2, sb = R * H / 16;
-  const int stage_bytes = 2 * cb + 2 * sb;
-  Stages S = carve(smem, NS, stage_bytes);
-
-  // the picks this launch covers
-  int pbeg = 0, pcnt = plan->npicks;
-  if (subset == kPicksHit) pcnt = plan->n_hit;
-  if (subset == kPicksMiss) {
-    pbeg = plan->n_hit;
-    pcnt = plan->npicks - plan->n_hit;
-  }
-  auto pick_of = [&](int jl) { return subset == kPicksAll ? jl : plan->order[pbeg + jl]; };
-  const int upp = I / R;  // units per pick
-  const int nunits = pcnt * upp;
-  const int my_units = units_of_block(nunits);
-
-  // a unit's four segments: gate codes, up codes, gate scales, up scales
-  auto segs = [&](int unit) {
-    const int jl = unit / upp, rb = unit - jl * upp;
-    const int j = pick_of(jl);
-    const uint8_t* w = FROM_HOST ? plan->hwptr[j] : plan->wptr[j];
-    const uint8_t* s = FROM_HOST ? plan->hsptr[j] : plan->sptr[j];
-    const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
-    Segs<4> sg;
-    sg.src[0] = w + og * (H / 2);
-    sg.src[1] = w + ou * (H / 2);
-    sg.src[2] = s + og * (H / 16);
-    sg.src[3] = s + ou * (H / 16);
-    uint8_t* dw = const_cast<uint8_t*>(plan->wptr[j]);
-    uint8_t* ds = const_cast<uint8_t*>(plan->sptr[j]);
-    sg.dst[0] = dw + og * (H / 2);
-    sg.dst[1] = dw + ou * (H / 2);
-    sg.dst[2] = ds + og * (H / 16);
-    sg.dst[3] = ds + ou * (H / 16);
-    sg.n[0] = sg.n[1] = cb;
-    sg.n[2] = sg.n[3] = sb;
-    return sg;
-  };
-  auto issue = [&](int unit, int stage) {  // FROM_HOST: every thread; else thread 0
-    uint8_t* dst = S.base + (size_t)stage * stage_bytes;
-    const Segs<4> sg = segs(unit);
-    if constexpr (FROM_HOST) {
-      stage_from_host(dst, sg, 4, &S.full[stage]);
-    } else {
-      mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
-      int base = 0;
-      for (int q = 0; q < 4; ++q) {
-        bulk_g2s(dst + base, sg.src[q], sg.n[q], &S.full[stage]);
-        base += sg.n[q];
-      }
-    }
-  };
-
-  // phase B (read-through only): W2 rows of the missed picks, URB rows a unit.
-  // Units are taken in ascending order from the step's work counter, so CTAs
-  // that finish phase A early take more.  Stages: NSB of its own from the
-  // start (none by default: the link serves phase A first), then NSA more in
-  // the phase-A stage memory once phase A is done.
-  const int URB = FROM_HOST ? rt.URB : 1, NSB = FROM_HOST ? rt.NSB : 0;
-  const int stage_b = URB * (I / 2 + I / 16);
-  const int NSA = FROM_HOST ? min(kMaxStagesB - NSB, NS * stage_bytes / stage_b) : 0;
-  const int NST = NSB + NSA;
-  uint8_t* stB = smem + rt.b_off;
-  uint64_t* barB = reinterpret_cast<uint64_t*>(stB + (size_t)NSB * stage_b);
-  float* hs = reinterpret_cast<float*>(barB + kMaxStagesB);
-  const int uppb = H / URB;
-  const int nb = FROM_HOST ? pcnt * uppb : 0;
-  auto stage_ptr = [&](int s) {
-    return s < NSB ? stB + (size_t)s * stage_b : S.base + (size_t)(s - NSB) * stage_b;
-  };
-  __shared__ int s_unitB[kMaxStagesB];  // unit staged in each phase-B stage, -1: none
-  __shared__ int s_nextB[2];            // by iteration parity: read after the writer moved on
-  auto segs_b = [&](int unit) {
-    const int jl = unit / uppb, rb = unit - jl * uppb;
-    const int j = pick_of(jl);
-    const size_t oc = (size_t)I * H + (size_t)rb * URB * (I / 2);
-    const size_t os = (size_t)I * H / 8 + (size_t)rb * URB * (I / 16);
-    Segs<2> sg;
-    sg.src[0] = plan->hwptr[j] + oc;
-    sg.src[1] = plan->hsptr[j] + os;
-    sg.dst[0] = const_cast<uint8_t*>(plan->wptr[j]) + oc;
-    sg.dst[1] = const_cast<uint8_t*>(plan->sptr[j]) + os;
-    sg.n[0] = URB * (I / 2);
-    sg.n[1] = URB * (I / 16);
-    return sg;
-  };
-
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], FROM_HOST ? blockDim.x : 1);
-    for (int s = 0; s < NST; ++s) mbar_init(&barB[s], blockDim.x);
-    fence_mbar_init();
-    *S.abort_flag = 0;
-    if (FROM_HOST) {  // this CTA's first phase-B units
-      const int u0 = (int)atomicAdd(&rt.ctr[kWorkCtr], (uint32_t)NSB);
-      for (int s = 0; s < kMaxStagesB; ++s) s_unitB[s] = (s < NSB && u0 + s < nb) ? u0 + s : -1;
-    }
-  }
-  __syncthreads();
-  if (FROM_HOST || tid == 0)
-    for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
-  if constexpr (FROM_HOST)
-    for (int s = 0; s < NSB; ++s)
-      if (s_unitB[s] >= 0) stage_from_host(stage_ptr(s), segs_b(s_unitB[s]), 2, &barB[s]);
-
-  // this thread's 16 activations, as f16 after a power-of-two prescale of the
-  // whole row that keeps max |x| below 2^15
   float xf[16];
   float amax = 0.f;
   {
@@ -507,121 +380,257 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   __syncthreads();
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, s_xmax[w]);
   int e2 = 0;
-  frexpf(amax, &e2);                    // amax < 2^e2
+  frexpf(amax, &e2);  // amax < 2^e2
   const int xshift = e2 > 15 ? e2 - 15 : 0;
-  const float xdown = ldexpf(1.0f, -xshift), xup = ldexpf(1.0f, xshift);
-  uint32_t xh[8];
+  const float xdown = ldexpf(1.0f, -xshift);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const __half2 p = __floats2half2_rn(xf[2 * i] * xdown, xf[2 * i + 1] * xdown);
     xh[i] = *reinterpret_cast<const uint32_t*>(&p);
   }
+  return ldexpf(1.0f, xshift);
+}
 
-  // ---- phase A: gate/up + SwiGLU
-  bool failed = false;
+// Partial dot products of one staged gate/up unit (kGateUpRows row pairs laid
+// out as gate codes, up codes, gate scales, up scales) for this thread's
+// block c of rows g, g + RL, ...: a[q] gate rows, a[RPT + q] up rows.
+template <int RPT>
+__device__ __forceinline__ void gateup_partials(const uint8_t* __restrict__ st, int H, int RL,
+                                                int g, int c, const uint32_t (&xh)[8],
+                                                float (&a)[2 * RPT]) {
+  const int cb = kGateUpRows * H / 2, sb = kGateUpRows * H / 16;
+#pragma unroll
+  for (int q = 0; q < RPT; ++q) {
+    const int r = g + q * RL;
+    const uint2 cg = *reinterpret_cast<const uint2*>(st + r * (H / 2) + c * 8);
+    const uint2 cu = *reinterpret_cast<const uint2*>(st + cb + r * (H / 2) + c * 8);
+    const uint32_t sg = st[2 * cb + r * (H / 16) + c];
+    const uint32_t su = st[2 * cb + sb + r * (H / 16) + c];
+    a[q] = dot16_f16(cg, xh) * e4m3_to_float(sg);
+    a[RPT + q] = dot16_f16(cu, xh) * e4m3_to_float(su);
+  }
+}
+
+// h = silu(gate) * up of the unit's row pair handled by this thread (threads
+// tid < RL * RPT), from the partials stashed by every thread.
+template <int RPT, bool WARP_RED>
+__device__ __forceinline__ void gateup_epilogue(const float* red, int RL, int C,
+                                                const Plan* __restrict__ plan, int j, int rb,
+                                                float xup, float* __restrict__ hbuf, int I) {
+  constexpr int V = 2 * RPT;
+  const int tid = threadIdx.x;
+  const int gg = tid / RPT, q = tid - gg * RPT;
+  const float gate = plan->gs[j][0] * xup * sum_partial<V, WARP_RED>(red, gg, q, C);
+  const float up = plan->gs[j][1] * xup * sum_partial<V, WARP_RED>(red, gg, RPT + q, C);
+  hbuf[(size_t)j * I + rb * kGateUpRows + gg + q * RL] = gate / (1.0f + expf(-gate)) * up;
+}
+
+// Resident picks: slot bytes from HBM, a unit's four segments by 1-D TMA bulk
+// copies, units assigned round-robin over the persistent grid.
+template <int RPT, bool WARP_RED>
+__global__ void __launch_bounds__(kGateUpThreads, 2)
+gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
+                   float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
+                   int subset) {
+  constexpr int V = 2 * RPT;
+  constexpr int R = kGateUpRows;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_xmax[kGateUpThreads / 32];
+  const int C = H / 16;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int g = tid / C, c = tid - g * C;
+  const int cb = R * H / 2, sb = R * H / 16;
+  const int stage_bytes = 2 * cb + 2 * sb;
+  Stages S = carve(smem, NS, stage_bytes);
+
+  // the picks this launch covers
+  int pbeg = 0, pcnt = plan->npicks;
+  if (subset == kPicksHit) pcnt = plan->n_hit;
+  if (subset == kPicksMiss) {
+    pbeg = plan->n_hit;
+    pcnt = plan->npicks - plan->n_hit;
+  }
+  auto pick_of = [&](int jl) { return subset == kPicksAll ? jl : plan->order[pbeg + jl]; };
+  const int upp = I / R;  // units per pick
+  const int nunits = pcnt * upp;
+  const int my_units = units_of_block(nunits);
+
+  auto issue = [&](int unit, int stage) {  // thread 0
+    const int jl = unit / upp, rb = unit - jl * upp;
+    const int j = pick_of(jl);
+    const uint8_t* w = plan->wptr[j];
+    const uint8_t* sc = plan->sptr[j];
+    const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
+    uint8_t* dst = S.base + (size_t)stage * stage_bytes;
+    mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
+    bulk_g2s(dst, w + og * (H / 2), cb, &S.full[stage]);
+    bulk_g2s(dst + cb, w + ou * (H / 2), cb, &S.full[stage]);
+    bulk_g2s(dst + 2 * cb, sc + og * (H / 16), sb, &S.full[stage]);
+    bulk_g2s(dst + 2 * cb + sb, sc + ou * (H / 16), sb, &S.full[stage]);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], 1);
+    fence_mbar_init();
+    *S.abort_flag = 0;
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
+  uint32_t xh[8];
+  const float xup = load_x_f16(x, c, s_xmax, xh);
+
   for (int i = 0; i < my_units; ++i) {
     const int unit = blockIdx.x + i * gridDim.x;
     const int stage = i % NS;
     if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
     __syncthreads();
-    // read-through: the previous unit's h is written and fenced; count it for its pick
-    if (FROM_HOST && tid == 0 && i > 0)
-      atomicAdd(&rt.ctr[kPickCtr + (unit - gridDim.x) / upp], 1u);
     if (*S.abort_flag) {
-      drain_fills<FROM_HOST>(S, i, NS, my_units, flags);
-      if constexpr (!FROM_HOST) return;
-      failed = true;
-      break;
+      drain_fills<false>(S, i, NS, my_units, flags);
+      return;
     }
-    const uint8_t* st = S.base + (size_t)stage * stage_bytes;
     float a[V];
-#pragma unroll
-    for (int q = 0; q < RPT; ++q) {
-      const int r = g + q * RL;
-      const uint2 cg = *reinterpret_cast<const uint2*>(st + r * (H / 2) + c * 8);
-      const uint2 cu = *reinterpret_cast<const uint2*>(st + cb + r * (H / 2) + c * 8);
-      const uint32_t sg = st[2 * cb + r * (H / 16) + c];
-      const uint32_t su = st[2 * cb + sb + r * (H / 16) + c];
-      a[q] = dot16_f16(cg, xh) * e4m3_to_float(sg);
-      a[RPT + q] = dot16_f16(cu, xh) * e4m3_to_float(su);
-    }
-    if constexpr (FROM_HOST) write_through(st, segs(unit), 4);
+    gateup_partials<RPT>(S.base + (size_t)stage * stage_bytes, H, RL, g, c, xh, a);
     stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
     __syncthreads();
-    if ((FROM_HOST || tid == 0) && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
+    if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
     if (tid < RL * RPT) {
-      const int gg = tid / RPT, q = tid - gg * RPT;
-      const int jl = unit / upp, rb = unit - jl * upp;
-      const int j = pick_of(jl);
-      const float gate = plan->gs[j][0] * xup * sum_partial<V, WARP_RED>(S.red, gg, q, C);
-      const float up = plan->gs[j][1] * xup * sum_partial<V, WARP_RED>(S.red, gg, RPT + q, C);
-      const float h = gate / (1.0f + expf(-gate)) * up;
-      hbuf[(size_t)j * I + rb * R + gg + q * RL] = h;
-      if constexpr (FROM_HOST) __threadfence();
+      const int jl = unit / upp;
+      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan, pick_of(jl), unit - jl * upp, xup, hbuf,
+                                     I);
     }
   }
-  if constexpr (FROM_HOST) {
-  // ---- phase B (read-through): the missed picks' W2 rows -> y'_j
+}
+
+// ---------------------------------------------------------- read-through
+
+// The missed picks' host-link pass, one launch.  Its work list holds, for
+// each missed pick in rank order, the pick's gate/up units (computed on
+// arrival with the functions above, then written through to the victim slot)
+// followed by its W2 bytes in stage-sized copy units (written through only).
+// Units are taken one at a time from a step counter, so CTAs that get more of
+// the link take more, and the link streams without waiting for any h.  The
+// missed picks' down pass is the resident down kernel, launched after this
+// one on the same stream: it reads W2 from the slot (just written, so mostly
+// from L2) with the same row routine, hence the same bits.
+template <int RPT, bool WARP_RED>
+__global__ void __launch_bounds__(kGateUpThreads, 2)
+gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
+                        float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
+                        uint32_t* ctr) {
+  constexpr int V = 2 * RPT;
+  constexpr int R = kGateUpRows;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_xmax[kGateUpThreads / 32];
+  __shared__ int s_unit[kMaxStages];  // link unit staged in each stage, -1: none
+  __shared__ int s_next[2];           // by iteration parity: read after the writer moved on
+  const int C = H / 16;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int g = tid / C, c = tid - g * C;
+  const int cb = R * H / 2, sb = R * H / 16;
+  const int SB = 2 * cb + 2 * sb;  // stage bytes
+  Stages S = carve(smem, NS, SB);
+
+  const int pbeg = plan->n_hit, pcnt = plan->npicks - plan->n_hit;
+  auto pick_of = [&](int jl) { return plan->order[pbeg + jl]; };
+  const int upp = I / R;                                   // gate/up units per pick
+  const size_t w2c = (size_t)H * (I / 2), w2s = (size_t)H * (I / 16);
+  const int ncc = (int)((w2c + SB - 1) / SB), ncs = (int)((w2s + SB - 1) / SB);
+  const int upk = upp + ncc + ncs;                         // link units per pick
+  const int NL = pcnt * upk;
+
+  // link unit u: its byte segments in host memory and in the pick's slot
+  auto segs = [&](int u, int& nseg) {
+    const int jl = u / upk, r = u - jl * upk;
+    const int j = pick_of(jl);
+    const uint8_t* hw = plan->hwptr[j];
+    const uint8_t* hsc = plan->hsptr[j];
+    uint8_t* dw = const_cast<uint8_t*>(plan->wptr[j]);
+    uint8_t* ds = const_cast<uint8_t*>(plan->sptr[j]);
+    Segs<4> sg;
+    if (r < upp) {
+      const size_t og = (size_t)r * R, ou = (size_t)I + (size_t)r * R;
+      sg.src[0] = hw + og * (H / 2);
+      sg.src[1] = hw + ou * (H / 2);
+      sg.src[2] = hsc + og * (H / 16);
+      sg.src[3] = hsc + ou * (H / 16);
+      sg.dst[0] = dw + og * (H / 2);
+      sg.dst[1] = dw + ou * (H / 2);
+      sg.dst[2] = ds + og * (H / 16);
+      sg.dst[3] = ds + ou * (H / 16);
+      sg.n[0] = sg.n[1] = cb;
+      sg.n[2] = sg.n[3] = sb;
+      nseg = 4;
+    } else if (r < upp + ncc) {  // W2 codes follow the 2I W13 code rows
+      const size_t k0 = (size_t)(r - upp) * SB;
+      const size_t off = (size_t)I * H + k0;
+      sg.src[0] = hw + off;
+      sg.dst[0] = dw + off;
+      sg.n[0] = (int)(w2c - k0 < (size_t)SB ? w2c - k0 : (size_t)SB);
+      nseg = 1;
+    } else {  // W2 scales follow the 2I W13 scale rows
+      const size_t k0 = (size_t)(r - upp - ncc) * SB;
+      const size_t off = (size_t)I * H / 8 + k0;
+      sg.src[0] = hsc + off;
+      sg.dst[0] = ds + off;
+      sg.n[0] = (int)(w2s - k0 < (size_t)SB ? w2s - k0 : (size_t)SB);
+      nseg = 1;
+    }
+    return sg;
+  };
+  auto fill = [&](int u, int stage) {  // every thread
+    int n = 0;
+    const Segs<4> sg = segs(u, n);
+    stage_from_host(S.base + (size_t)stage * SB, sg, n, &S.full[stage]);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], blockDim.x);
+    fence_mbar_init();
+    *S.abort_flag = 0;
+    const int u0 = (int)atomicAdd(&ctr[kWorkCtr], (uint32_t)NS);
+    for (int s = 0; s < kMaxStages; ++s) s_unit[s] = (s < NS && u0 + s < NL) ? u0 + s : -1;
+  }
   __syncthreads();
-  if (tid == 0 && !failed && my_units > 0)
-    atomicAdd(&rt.ctr[kPickCtr + (blockIdx.x + (my_units - 1) * gridDim.x) / upp], 1u);
-  if (failed) {
-    // let the other CTAs' phase B run (on garbage, flagged) instead of timing out
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    if (tid == 0)
-      for (int jl = 0; jl < pcnt; ++jl) atomicAdd(&rt.ctr[kPickCtr + jl], (uint32_t)upp);
-  } else {
-    // phase-A stage memory is free now: stage NSA more units there
-    if (tid == 0 && NSA > 0) {
-      const int u0 = (int)atomicAdd(&rt.ctr[kWorkCtr], (uint32_t)NSA);
-      for (int s = NSB; s < NST; ++s) s_unitB[s] = u0 + (s - NSB) < nb ? u0 + (s - NSB) : -1;
-    }
+  for (int s = 0; s < NS; ++s)
+    if (s_unit[s] >= 0) fill(s_unit[s], s);
+  uint32_t xh[8];
+  const float xup = load_x_f16(x, c, s_xmax, xh);
+
+  for (int i = 0;; ++i) {
+    const int stage = i % NS;
+    const int unit = s_unit[stage];
+    if (unit < 0) break;  // units are taken in order: none left for this CTA
+    // the unit that refills this stage: taken now, used at the end
+    const int taken = tid == 0 ? (int)atomicAdd(&ctr[kWorkCtr], 1u) : 0;
+    if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
     __syncthreads();
-    for (int s = NSB; s < NST; ++s)
-      if (s_unitB[s] >= 0) stage_from_host(stage_ptr(s), segs_b(s_unitB[s]), 2, &barB[s]);
-    const int warp = tid >> 5, nwarps = blockDim.x >> 5;
-    int cur = -1;
-    for (int i = 0;; ++i) {
-      const int stage = i % NST;
-      const int unit = s_unitB[stage];
-      if (unit < 0) break;  // units are taken in order: none left for this CTA
-      // the unit that refills this stage: taken now, its value used at the end
-      const int taken = tid == 0 ? (int)atomicAdd(&rt.ctr[kWorkCtr], 1u) : 0;
-      const int jl = unit / uppb, rb = unit - jl * uppb;
-      const int j = pick_of(jl);
-      if (j != cur) {  // wait until all of h_j is written, then stage gscale * w * h_j
-        if (tid == 0 && !count_wait_bounded(&rt.ctr[kPickCtr + jl], (uint32_t)upp, flags))
-          *S.abort_flag = 1;
-        __syncthreads();
-        if (*S.abort_flag) {
-          asm volatile("cp.async.wait_all;" ::: "memory");
-          break;
-        }
-        const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
-        for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
-          hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
-        cur = j;
-      }
-      if (!mbar_wait_bounded(&barB[stage], (uint32_t)((i / NST) & 1), flags)) *S.abort_flag = 1;
-      __syncthreads();
-      if (*S.abort_flag) {
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        break;
-      }
-      const uint8_t* st = stage_ptr(stage);
-      for (int r = warp; r < URB; r += nwarps) {
-        const float y = w2_row_warp(st + r * (I / 2), st + URB * (I / 2) + r * (I / 16), hs, I, lane);
-        if (lane == 0) rt.ypart[(size_t)j * H + rb * URB + r] = y;
-      }
-      write_through(st, segs_b(unit), 2);
-      if (tid == 0) s_nextB[i & 1] = taken < nb ? taken : -1;
-      __syncthreads();
-      const int nxt = s_nextB[i & 1];
-      if (tid == 0) s_unitB[stage] = nxt;
-      if (nxt >= 0) stage_from_host(stage_ptr(stage), segs_b(nxt), 2, &barB[stage]);
+    if (*S.abort_flag) break;  // flagged; the copies in flight are drained below
+    const int jl = unit / upk, r = unit - jl * upk;
+    const uint8_t* st = S.base + (size_t)stage * SB;
+    int nseg = 0;
+    const Segs<4> sg = segs(unit, nseg);
+    if (r < upp) {  // uniform over the CTA
+      float a[V];
+      gateup_partials<RPT>(st, H, RL, g, c, xh, a);
+      write_through(st, sg, nseg);
+      stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
+    } else {
+      write_through(st, sg, nseg);
     }
+    if (tid == 0) s_next[i & 1] = taken < NL ? taken : -1;
+    __syncthreads();
+    if (r < upp && tid < RL * RPT)
+      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan, pick_of(jl), r, xup, hbuf, I);
+    const int nxt = s_next[i & 1];
+    if (tid == 0) s_unit[stage] = nxt;
+    if (nxt >= 0) fill(nxt, stage);
   }
-  finish_step(plan, rt.ypart, rt.out, H, rt.ctr, rt.total_ctas, &s_last);
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  // the last CTA out (no unit is taken after it) resets the launch's counters
+  if (tid == 0 && atomicAdd(&ctr[kRtDoneCtr], 1u) == gridDim.x - 1) {
+    ctr[kWorkCtr] = 0u;
+    ctr[kRtDoneCtr] = 0u;
   }
 }
 
@@ -635,10 +644,12 @@ template <int MB>  // h blocks a lane keeps in registers (0: read them from shar
 __global__ void __launch_bounds__(kDownThreads, 1)
 gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
                  float* __restrict__ ypart, int H, int I, int NS, uint32_t* flags, int subset,
-                 float* __restrict__ out, uint32_t* __restrict__ done, int total_ctas) {
+                 float* __restrict__ out, uint32_t* __restrict__ ctr) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_last, s_abort;
+  __shared__ int s_abort, s_nlast;
+  __shared__ int s_lastb[MOE_MAX_DIM / kDownUnitRows];
   constexpr int UR = kDownUnitRows;
+  pdl_wait();  // h and the slots may come from the kernel before this one
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   int pbeg = 0, pcnt = plan->npicks;
   if (subset == kPicksHit) pcnt = plan->n_hit;
@@ -656,7 +667,8 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
   const int nq = pcnt > 0 ? ((int)gridDim.x - jl + pcnt - 1) / pcnt : 0;
   const int units = H / UR;
   const int my_units = (pcnt > 0 && q < units) ? (units - 1 - q) / nq + 1 : 0;
-  const int j = pcnt > 0 ? (subset == kPicksAll ? jl : plan->order[pbeg + jl]) : 0;
+  if (my_units == 0) return;  // uniform
+  const int j = subset == kPicksAll ? jl : plan->order[pbeg + jl];
   const uint8_t* wsrc = plan->wptr[j] + (size_t)I * H;     // W2 codes
   const uint8_t* ssrc = plan->sptr[j] + (size_t)I * H / 8; // W2 scales
   auto issue = [&](int i, int stage) {  // thread 0
@@ -672,10 +684,10 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
     s_abort = 0;
     for (int s = 0; s < NS && s < my_units; ++s) issue(s, s);
   }
-  if (my_units > 0) {  // uniform
+  {
     const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
     for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
-      hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldg(hbuf + (size_t)j * I + e));
+      hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
   }
   __syncthreads();
   // this lane's blocks of the pick's h, kept in registers for the whole kernel
@@ -687,16 +699,16 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int c = lane + 32 * m;
-        hv[m][e] = (my_units > 0 && c < C) ? hs[e * C + c] : 0.f;
+        hv[m][e] = c < C ? hs[e * C + c] : 0.f;
       }
   }
   for (int i = 0; i < my_units; ++i) {
     const int stage = i % NS;
     if (!mbar_wait_bounded(&full[stage], (uint32_t)((i / NS) & 1), flags)) s_abort = 1;
     __syncthreads();
-    if (s_abort) {
+    if (s_abort) {  // flagged; the units are still counted below, so the combine happens
       drain_fills<false>(Stages{smem, full, nullptr, nullptr}, i, NS, my_units, flags);
-      break;  // still counted below, so the step's combine happens
+      break;
     }
     const uint8_t* st = smem + (size_t)stage * stage_b;
     const int rb = q + i * nq;
@@ -713,7 +725,7 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
     __syncthreads();
     if (tid == 0 && i + NS < my_units) issue(i + NS, stage);
   }
-  finish_step(plan, ypart, out, H, done, total_ctas, &s_last);
+  count_blocks(plan, ypart, out, H, ctr, q, nq, my_units, s_lastb, &s_nlast);
 }
 
 // ------------------------------------------------------------- dispatch
@@ -745,46 +757,42 @@ GateUpShape gateup_shape(int H, int stages) {
   const int stage = 2 * R * H / 2 + 2 * R * H / 16;
   const int per_cta = kSmemPerSm / 2 - 1024;  // two CTAs per SM
   int ns = (per_cta - 16 - red_floats * 4) / stage;
-  if (ns > 6) ns = 6;
+  if (ns > 6) ns = 6;  // <= kMaxStages
   if (stages > 0 && stages < ns) ns = stages;
   s.NS = ns;
   s.smem = ns * stage + 8 * ns + 8 + red_floats * 4;
   return s;
 }
 
-// Phase-B shape of the read-through launch: W2 rows per unit (about 20 KB a
-// stage), no stages of its own (the W2 stages use phase A's stage memory once
-// phase A is done, so phase A has the host link to itself until then), then
-// gscale * w * h of one pick in shared memory.
-struct RtShape {
-  int URB, NSB, b_off, smem;
-};
-
-RtShape rt_shape(const GateUpShape& s, int I) {
-  RtShape r;
-  const int row = I / 2 + I / 16;
-  int urb = 16;
-  while (urb > 4 && urb * row > 20 * 1024) urb /= 2;
-  r.URB = urb;
-  r.NSB = 0;
-  r.b_off = (s.smem + 127) / 128 * 128;
-  r.smem = r.b_off + r.NSB * urb * row + 8 * kMaxStagesB + I * 4;
-  return r;
-}
-
-template <int RPT, bool WR, bool FH>
-cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, int smem, const Plan* plan,
+template <int RPT, bool WR>
+cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
                        const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
-                       int subset, const RtArgs& rt) {
-  auto kern = gemv_gateup_kernel<RPT, WR, FH>;
+                       int subset) {
+  auto kern = gemv_gateup_kernel<RPT, WR>;
   static int smem_set = 0;  // raise the opt-in limit once per size (not a stream operation)
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (s.smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e == cudaSuccess) e = prefer_max_shared(kern);
     if (e != cudaSuccess) return e;
-    smem_set = smem;
+    smem_set = s.smem;
   }
-  kern<<<grid, s.NT, smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset, rt);
+  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset);
+  return cudaGetLastError();
+}
+
+template <int RPT, bool WR>
+cudaError_t run_readthrough(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
+                            const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
+                            uint32_t* ctr) {
+  auto kern = gemv_readthrough_kernel<RPT, WR>;
+  static int smem_set = 0;
+  if (s.smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
+    if (e == cudaSuccess) e = prefer_max_shared(kern);
+    if (e != cudaSuccess) return e;
+    smem_set = s.smem;
+  }
+  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, ctr);
   return cudaGetLastError();
 }
 
@@ -792,20 +800,6 @@ int gateup_grid(int I, int k, int num_sms, const GemvLaunch& how) {
   const int nunits = k * (I / kGateUpRows);
   const int grid = how.grid > 0 ? how.grid : 2 * num_sms;
   return grid < nunits ? grid : nunits;
-}
-
-template <bool FH>
-cudaError_t dispatch_gateup(cudaStream_t st, int grid, const GateUpShape& s, int smem,
-                            const Plan* plan, const uint16_t* x, float* hbuf, int H, int I,
-                            uint32_t* flags, int subset, const RtArgs& rt) {
-#define GU(N)                                                                                   \
-  if (s.RPT == N)                                                                               \
-    return s.warp_red                                                                           \
-               ? run_gateup<N, true, FH>(st, grid, s, smem, plan, x, hbuf, H, I, flags, subset, rt) \
-               : run_gateup<N, false, FH>(st, grid, s, smem, plan, x, hbuf, H, I, flags, subset, rt);
-  GU(1) GU(2) GU(4)
-#undef GU
-  return cudaErrorInvalidConfiguration;
 }
 
 struct DownShape {
@@ -828,7 +822,7 @@ DownShape down_shape(int I, int stages) {
 template <int MB>
 cudaError_t run_down(cudaStream_t st, int grid, const DownShape& d, const Plan* plan,
                      const GemvWorkspace& ws, int H, int I, uint32_t* flags, int subset,
-                     float* out, uint32_t* done, int total_ctas) {
+                     float* out, uint32_t* ctr, bool pdl) {
   auto kern = gemv_down_kernel<MB>;
   static int smem_set = 0;
   if (d.smem > smem_set) {
@@ -837,8 +831,11 @@ cudaError_t run_down(cudaStream_t st, int grid, const DownShape& d, const Plan* 
     if (e != cudaSuccess) return e;
     smem_set = d.smem;
   }
+  if (pdl)
+    return launch_pdl(kern, dim3(grid), dim3(kDownThreads), d.smem, st, plan, ws.hbuf, ws.ypart,
+                      H, I, d.NS, flags, subset, out, ctr);
   kern<<<grid, kDownThreads, d.smem, st>>>(plan, ws.hbuf, ws.ypart, H, I, d.NS, flags, subset,
-                                           out, done, total_ctas);
+                                           out, ctr);
   return cudaGetLastError();
 }
 
@@ -846,18 +843,31 @@ cudaError_t run_down(cudaStream_t st, int grid, const DownShape& d, const Plan* 
 
 bool gemv_supported(int H, int I, int k) {
   const int C = I / 32;  // 32-element blocks of a W2 row: whole warps of them or part of one
-  return H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM && k >= 1 &&
-         (C % 32 == 0 || 32 % C == 0) && H / 16 <= kGateUpThreads * kGateUpRows &&
-         gateup_shape(H, 0).NT % 32 == 0 && down_shape(I, 0).NS >= 1;
+  if (!(H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM && k >= 1 &&
+        (C % 32 == 0 || 32 % C == 0) && H / 16 <= kGateUpThreads * kGateUpRows))
+    return false;
+  const GateUpShape s = gateup_shape(H, 0);
+  return s.NT % 32 == 0 && s.NS >= 1 && down_shape(I, 0).NS >= 1;
 }
+
+#define GATEUP_DISPATCH(RUN, ...)                                  \
+  switch (s.RPT * 2 + (s.warp_red ? 1 : 0)) {                      \
+    case 2: return RUN<1, false>(__VA_ARGS__);                     \
+    case 3: return RUN<1, true>(__VA_ARGS__);                      \
+    case 4: return RUN<2, false>(__VA_ARGS__);                     \
+    case 5: return RUN<2, true>(__VA_ARGS__);                      \
+    case 8: return RUN<4, false>(__VA_ARGS__);                     \
+    case 9: return RUN<4, true>(__VA_ARGS__);                      \
+    default: return cudaErrorInvalidConfiguration;                 \
+  }
 
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
                                int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
                                const GemvLaunch& how) {
   const GateUpShape s = gateup_shape(H, how.stages);
   if (s.NS < 1 || s.NT > kGateUpThreads || how.from_host) return cudaErrorInvalidConfiguration;
-  return dispatch_gateup<false>(st, gateup_grid(I, k, num_sms, how), s, s.smem, plan, x, ws.hbuf,
-                                H, I, flags, how.subset, RtArgs{});
+  const int grid = gateup_grid(I, k, num_sms, how);
+  GATEUP_DISPATCH(run_gateup, st, grid, s, plan, x, ws.hbuf, H, I, flags, how.subset)
 }
 
 int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how) {
@@ -866,23 +876,14 @@ int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how) {
 
 cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uint16_t* x, int H,
                                     int I, int k, const GemvWorkspace& ws, uint32_t* flags,
-                                    int num_sms, const GemvLaunch& how, float* out, uint32_t* ctr,
-                                    int total_ctas) {
+                                    int num_sms, const GemvLaunch& how, uint32_t* ctr) {
   const GateUpShape s = gateup_shape(H, how.stages);
   if (s.NS < 1 || s.NT > kGateUpThreads || !how.from_host || how.subset != kPicksMiss)
     return cudaErrorInvalidConfiguration;
-  const RtShape r = rt_shape(s, I);
-  RtArgs rt;
-  rt.ypart = ws.ypart;
-  rt.out = out;
-  rt.ctr = ctr;
-  rt.total_ctas = total_ctas;
-  rt.URB = r.URB;
-  rt.NSB = r.NSB;
-  rt.b_off = r.b_off;
-  return dispatch_gateup<true>(st, gemv_readthrough_grid(I, k, num_sms, how), s, r.smem, plan, x,
-                               ws.hbuf, H, I, flags, how.subset, rt);
+  const int grid = gemv_readthrough_grid(I, k, num_sms, how);
+  GATEUP_DISPATCH(run_readthrough, st, grid, s, plan, x, ws.hbuf, H, I, flags, ctr)
 }
+#undef GATEUP_DISPATCH
 
 int gemv_down_grid(int H, int num_sms, const GemvLaunch& how) {
   (void)H;
@@ -892,17 +893,15 @@ int gemv_down_grid(int H, int num_sms, const GemvLaunch& how) {
 
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
                              const GemvWorkspace& ws, uint32_t* flags, int num_sms,
-                             const GemvLaunch& how, float* out, uint32_t* done, int total_ctas) {
+                             const GemvLaunch& how, float* out, uint32_t* ctr) {
   (void)k;
   const DownShape d = down_shape(I, how.stages);
   if (d.NS < 1 || how.from_host) return cudaErrorInvalidConfiguration;  // slot bytes only
   const int grid = gemv_down_grid(H, num_sms, how);
   const int C = I / 32;  // h blocks per W2 row: in registers up to two per lane
-  if (C <= 32)
-    return run_down<1>(st, grid, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
-  if (C == 64)
-    return run_down<2>(st, grid, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
-  return run_down<0>(st, grid, d, plan, ws, H, I, flags, how.subset, out, done, total_ctas);
+  if (C <= 32) return run_down<1>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl);
+  if (C == 64) return run_down<2>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl);
+  return run_down<0>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl);
 }
 
 }  // namespace moe

@@ -130,7 +130,7 @@ cudaError_t launch_link_probe(cudaStream_t st, const void* src, void* dst, size_
 struct GemvWorkspace {
   float* hbuf;        // [MOE_MAX_PICKS][I]
   float* ypart;       // [MOE_MAX_TOPK][H]
-  uint32_t* tile_cnt; // step counters, >= 2 + MOE_MAX_TOPK words, zero between steps
+  uint32_t* tile_cnt; // step counters (kStepCounterWords words), zero between steps
   uint32_t* flags;    // error flags word for waits (per layer stats flags)
 };
 // Pick subsets of a one-row step: the picks resident at step start, the
@@ -141,26 +141,34 @@ struct GemvLaunch {
   bool from_host;  // read-through launch only: the picks come from host memory
   int grid;        // CTAs (0: the kernel's default, a full persistent grid)
   int stages;      // units in flight per CTA (0: as many as fit)
+  bool pdl = false;  // down launch only: programmatic dependent launch on the
+                     // previous kernel of its stream (see pdl_wait)
 };
+// Counters of a one-row step (zero between steps; each user resets its own):
+//   [0] read-through CTAs that have finished, [1] read-through units taken,
+//   [2 + b] picks whose y'_j rows of output block b (kOutBlockRows rows) are written.
+constexpr int kOutBlockRows = 32;
+constexpr int kStepCounterWords = 2 + MOE_MAX_DIM / kOutBlockRows;
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
                                int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
                                const GemvLaunch& how);
-// The missed picks end to end (subset kPicksMiss, from_host): each missed
-// expert read once from host memory and written through to its slot, gate/up
-// + SwiGLU on the W13 rows, then y'_j = gscale_j * w_j * (W2_j h_j) on the W2
-// rows -> ws.ypart.  Counts its CTAs in ctr[0] like launch_gemv_down.
+// The missed picks' host-link pass (subset kPicksMiss, from_host): each
+// missed expert read once from host memory and written through to its slot,
+// gate/up + SwiGLU computed on its W13 rows on the way in -> ws.hbuf.  Takes
+// its work from ctr[1]; its last CTA resets ctr[0..1].  Their down pass is
+// launch_gemv_down with subset kPicksMiss, after this launch on its stream.
 cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uint16_t* x, int H,
                                     int I, int k, const GemvWorkspace& ws, uint32_t* flags,
-                                    int num_sms, const GemvLaunch& how, float* out, uint32_t* ctr,
-                                    int total_ctas);
+                                    int num_sms, const GemvLaunch& how, uint32_t* ctr);
 int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how);
-// y'_j = gscale_j * w_j * (W2_j h_j) for the subset's picks -> ws.ypart [k][H].  Every CTA
-// of the step's y'_j launches counts itself in done[0] when it finishes; the one that brings
-// the count to total_ctas adds out = sum_j y'_j in rank order and resets done[0] and the
-// read-through launch's per-pick counters done[2 .. 2 + k).  done: >= 2 + k words, zero.
+// y'_j = gscale_j * w_j * (W2_j h_j) for the subset's picks -> ws.ypart [k][H], a unit
+// being kOutBlockRows rows of one pick.  Each finished unit is counted in ctr[2 + b] for
+// its output block b; the CTA that completes a block's count (all the step's picks, from
+// this launch or the step's other down launch) adds out = sum_j y'_j over the block's rows
+// in rank order and resets the count.  ctr: kStepCounterWords words, zero.
 cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, int k,
                              const GemvWorkspace& ws, uint32_t* flags, int num_sms,
-                             const GemvLaunch& how, float* out, uint32_t* done, int total_ctas);
+                             const GemvLaunch& how, float* out, uint32_t* ctr);
 int gemv_down_grid(int H, int num_sms, const GemvLaunch& how);
 // Shapes the M = 1 expert kernels handle (dims % 128 == 0, inter / 32 a multiple or a
 // divisor of 32).
@@ -176,9 +184,34 @@ inline cudaError_t prefer_max_shared(F* func) {
                               cudaSharedmemCarveoutMaxShared);
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel of the stream finishes; it must call pdl_wait()
+// before touching anything that kernel writes.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------- device helpers
 
 #ifdef __CUDACC__
+
+// Waits until the grid this one depends on (launch_pdl) has completed and its
+// writes are visible; returns at once for a normal launch.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -17,7 +17,6 @@ using namespace moe;
 namespace {
 constexpr int kDefaultMaxRows = 512;  // largest prefill chunk a handle takes by default
 constexpr int kDefaultPrefillChunk = 32;  // experts staged per prefill chunk (two chunks held)
-constexpr int kStepCounterWords = 64;     // one-row step counters (>= 2 + MOE_MAX_TOPK)
 }
 
 struct moe_cache {
@@ -375,13 +374,13 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   if (one_row) {
     // One row.  After route/remap the missed picks take a second stream: one
     // read-through launch reads each missed expert once over the host link,
-    // computes its gate/up and down on the way in and writes it through to the
-    // victim slot.  Meanwhile the resident picks' gate/up and down run on the
-    // caller's stream, so the hit experts' HBM reads overlap the host-link
-    // transfer.  Each pick's weighted output y'_j is computed the same way
-    // whichever path it takes, and the last CTA of the step's y'_j launches
-    // adds them in rank order, so the result does not depend on the hit/miss
-    // split.
+    // computes its gate/up on the way in and writes it through to the victim
+    // slot; then their down pass reads W2 back from the slot.  Meanwhile the
+    // resident picks' gate/up and down run on the caller's stream, so the hit
+    // experts' HBM reads overlap the host-link transfer.  Each pick's weighted
+    // output y'_j is computed the same way whichever path it takes, and the
+    // last CTA of the step's two down launches adds them in rank order, so the
+    // result does not depend on the hit/miss split.
     if (e == cudaSuccess)
       e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S_of[layer], h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, nullptr);
@@ -392,15 +391,18 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     // many SMs from the resident picks
     const int rt_grid = h->num_sms / 2 > 8 ? h->num_sms / 2 : 8;
     const GemvLaunch miss{kPicksMiss, true, rt_grid, 2};
+    // their down pass starts as the read-through launch drains (not across a timing event)
+    const GemvLaunch miss_dn{kPicksMiss, false, 0, 4, !h->timing};
     // resident picks: slot bytes from HBM
     const GemvLaunch hit_gu{kPicksHit, false, 0, 3}, hit_dn{kPicksHit, false, 0, 4};
-    const int total = gemv_readthrough_grid(h->I, h->k, h->num_sms, miss) +
-                      gemv_down_grid(h->H, h->num_sms, hit_dn);
     if (e == cudaSuccess) e = mark(2, h->side);
     if (e == cudaSuccess)
       e = launch_gemv_readthrough(h->side, h->plan, x, h->H, h->I, h->k, h->gemv, flags,
-                                  h->num_sms, miss, out, h->gemv.tile_cnt, total);
+                                  h->num_sms, miss, h->gemv.tile_cnt);
     if (e == cudaSuccess) e = mark(3, h->side);
+    if (e == cudaSuccess)
+      e = launch_gemv_down(h->side, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
+                           miss_dn, out, h->gemv.tile_cnt);
     if (e == cudaSuccess) e = mark(4, h->side);
     if (e == cudaSuccess) e = cudaEventRecord(h->join, h->side);
     if (e == cudaSuccess)
@@ -409,7 +411,7 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     if (e == cudaSuccess) e = mark(5, st);
     if (e == cudaSuccess)
       e = launch_gemv_down(st, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms, hit_dn,
-                           out, h->gemv.tile_cnt, total);
+                           out, h->gemv.tile_cnt);
     if (e == cudaSuccess) e = mark(6, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->join, 0);
     if (e == cudaSuccess) e = mark(7, st);

@@ -29,7 +29,7 @@ constexpr int kMaxDim = MOE_MAX_DIM;
 constexpr size_t kPlanBytes = (sizeof(Plan) + 255) / 256 * 256;
 constexpr size_t kHBytes = sizeof(float) * kMaxK * kMaxDim;     // h [k][inter]
 constexpr size_t kYBytes = sizeof(float) * kMaxK * kMaxDim;     // y_j [k][hidden]
-constexpr size_t kTileWords = kMaxDim / 32 + 1;                  // down tiles of 32 rows
+constexpr size_t kTileWords = kStepCounterWords;                 // step counters
 constexpr size_t kTileBytes = (sizeof(uint32_t) * kTileWords + 255) / 256 * 256;
 constexpr size_t kFlagBytes = 256;
 constexpr size_t kScratchBytes = kPlanBytes + kHBytes + kYBytes + kTileBytes + kFlagBytes;
@@ -149,7 +149,6 @@ extern "C" int moe_expert_pass_noalloc(int k, int hidden, int inter, const void*
   if (e == cudaSuccess)
     e = launch_gemv_gateup(st, plan, x, hidden, inter, k, ws, flags, d->num_sms, all);
   if (e == cudaSuccess)
-    e = launch_gemv_down(st, plan, hidden, inter, k, ws, flags, d->num_sms, all, out, ws.tile_cnt,
-                         gemv_down_grid(hidden, d->num_sms, all));
+    e = launch_gemv_down(st, plan, hidden, inter, k, ws, flags, d->num_sms, all, out, ws.tile_cnt);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -224,8 +224,8 @@ int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int m
  * event-record nodes):
  *   0 before route/remap, 1 after it (caller's stream);
  *   one-row steps, the library's second stream: 2 before the missed picks'
- *     read-through pass (host -> slot with gate/up and down on the way in),
- *     3 and 4 both after it;
+ *     read-through pass (host -> slot with gate/up on the way in), 3 after
+ *     it, 4 after the missed picks' down pass;
  *   multi-row steps, the caller's stream: 2 after the miss copy, 3 after the
  *     grouped gate/up, 4 after the grouped down;
  *   5 after the resident picks' gate/up, 6 after their down (one-row steps;
