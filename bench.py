@@ -388,7 +388,8 @@ def run_ours(args) -> None:
         if "resident" in n:
             kern[n]["traffic"] = _traffic(n.split("[")[0], float(n_hit.mean()))
         elif "missed" in n:
-            kern[n]["traffic"] = None
+            kern[n]["traffic"] = _traffic(n.split("[")[0] + ("_missed" if "down" in n else ""),
+                                          float(n_miss[hm].mean()) if hm.any() else 0.0)
             kern[n]["note"] = "steps with at least one miss"
     kern["gemv_readthrough[missed picks]"]["note"] += (
         "; whole missed experts over the host link, gate/up computed on the way in, "

@@ -52,7 +52,8 @@ namespace {
 
 constexpr int kGateUpRows = 4;     // row pairs per gate/up unit
 constexpr int kGateUpThreads = 512;
-constexpr int kDownUnitRows = kOutBlockRows;  // W2 rows per down unit (each warp takes two)
+constexpr int kDownUnitRows = kOutBlockRows;  // W2 rows per down unit
+constexpr int kDownItemRows = 2;              // W2 rows a down warp takes at a time
 constexpr int kDownThreads = 512;
 constexpr int kSmemPerSm = 227 * 1024;
 
@@ -442,6 +443,14 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   const int cb = R * H / 2, sb = R * H / 16;
   const int stage_bytes = 2 * cb + 2 * sb;
   Stages S = carve(smem, NS, stage_bytes);
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], 1);
+    fence_mbar_init();
+    *S.abort_flag = 0;
+  }
+  uint32_t xh[8];
+  const float xup = load_x_f16(x, c, s_xmax, xh);  // x is the step's input, not route's output
+  pdl_wait();  // the plan comes from the kernel before this one
 
   // the picks this launch covers
   int pbeg = 0, pcnt = plan->npicks;
@@ -469,16 +478,8 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     bulk_g2s(dst + 2 * cb + sb, sc + ou * (H / 16), sb, &S.full[stage]);
   };
 
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], 1);
-    fence_mbar_init();
-    *S.abort_flag = 0;
-  }
-  __syncthreads();
   if (tid == 0)
     for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
-  uint32_t xh[8];
-  const float xup = load_x_f16(x, c, s_xmax, xh);
 
   for (int i = 0; i < my_units; ++i) {
     const int unit = blockIdx.x + i * gridDim.x;
@@ -636,19 +637,24 @@ gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restric
 
 // ---------------------------------------------------------------- down
 
-// Each CTA serves one pick (CTAs b, b + pcnt, ... share pick b % pcnt), keeps
-// gscale * w * h of that pick in shared memory (transposed), and walks units
-// of kDownUnitRows W2 rows, a warp per row with w2_row_warp.  A unit's code and
-// scale rows are contiguous in the slot and arrive by two 1-D TMA bulk copies.
+// Each CTA serves one pick (CTAs b, b + pcnt, ... share pick b % pcnt) and
+// takes units of kDownUnitRows W2 rows (output blocks) of it.  Its warps work
+// independently: warp w takes rows kDownItemRows * w .. of every unit of the
+// CTA, through a ring of its own (stages of kDownItemRows code and scale rows,
+// each filled by two 1-D TMA bulk copies on the stage's mbarrier), and
+// reduces each row with w2_row_warp_g against gscale * w * h of the pick held
+// in registers (or, for large I, in shared memory, transposed).  No barrier
+// between warps until the CTA's exit, where its units are counted for the
+// per-block combine.
 template <int MB>  // h blocks a lane keeps in registers (0: read them from shared memory)
 __global__ void __launch_bounds__(kDownThreads, 1)
 gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
-                 float* __restrict__ ypart, int H, int I, int NS, uint32_t* flags, int subset,
+                 float* __restrict__ ypart, int H, int I, int NSW, uint32_t* flags, int subset,
                  float* __restrict__ out, uint32_t* __restrict__ ctr) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_abort, s_nlast;
+  __shared__ int s_nlast;
   __shared__ int s_lastb[MOE_MAX_DIM / kDownUnitRows];
-  constexpr int UR = kDownUnitRows;
+  constexpr int UR = kDownUnitRows, IR = kDownItemRows;
   pdl_wait();  // h and the slots may come from the kernel before this one
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   int pbeg = 0, pcnt = plan->npicks;
@@ -657,11 +663,7 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
     pbeg = plan->n_hit;
     pcnt = plan->npicks - plan->n_hit;
   }
-  const int row_b = I / 2 + I / 16;
-  const int stage_b = UR * row_b;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_b);
-  float* hs = reinterpret_cast<float*>(full + NS);
-  // this CTA's pick and its share of the pick's row units
+  // this CTA's pick and its share of the pick's units
   const int jl = pcnt > 0 ? (int)blockIdx.x % pcnt : 0;
   const int q = pcnt > 0 ? (int)blockIdx.x / pcnt : 0;
   const int nq = pcnt > 0 ? ((int)gridDim.x - jl + pcnt - 1) / pcnt : 0;
@@ -671,18 +673,31 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
   const int j = subset == kPicksAll ? jl : plan->order[pbeg + jl];
   const uint8_t* wsrc = plan->wptr[j] + (size_t)I * H;     // W2 codes
   const uint8_t* ssrc = plan->sptr[j] + (size_t)I * H / 8; // W2 scales
-  auto issue = [&](int i, int stage) {  // thread 0
-    const int rb = q + i * nq;
-    uint8_t* dst = smem + (size_t)stage * stage_b;
-    mbar_arrive_expect_tx(&full[stage], (uint32_t)stage_b);
-    bulk_g2s(dst, wsrc + (size_t)rb * UR * (I / 2), UR * (I / 2), &full[stage]);
-    bulk_g2s(dst + UR * (I / 2), ssrc + (size_t)rb * UR * (I / 16), UR * (I / 16), &full[stage]);
+
+  // this warp's ring and its items: item n is rows row0(n) .. + IR
+  const int item_b = IR * (I / 2 + I / 16);
+  uint8_t* ring = smem + (size_t)warp * NSW * item_b;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)nwarps * NSW * item_b) + warp * NSW;
+  float* hs = reinterpret_cast<float*>(smem + (size_t)nwarps * NSW * (item_b + 8));
+  const int ipu = UR / IR;  // items per unit
+  const int nitems = my_units * ipu;
+  const int my_items = nitems > warp ? (nitems - 1 - warp) / nwarps + 1 : 0;
+  auto row0 = [&](int n) {
+    const int g = warp + n * nwarps;
+    const int i = g / ipu;
+    return (q + i * nq) * UR + (g - i * ipu) * IR;
   };
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+  auto issue = [&](int n, int s) {  // lane 0
+    const int r0 = row0(n);
+    uint8_t* dst = ring + (size_t)s * item_b;
+    mbar_arrive_expect_tx(&bars[s], (uint32_t)item_b);
+    bulk_g2s(dst, wsrc + (size_t)r0 * (I / 2), IR * (I / 2), &bars[s]);
+    bulk_g2s(dst + IR * (I / 2), ssrc + (size_t)r0 * (I / 16), IR * (I / 16), &bars[s]);
+  };
+  if (lane == 0) {
+    for (int s = 0; s < NSW; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
-    s_abort = 0;
-    for (int s = 0; s < NS && s < my_units; ++s) issue(s, s);
+    for (int s = 0; s < NSW && s < my_items; ++s) issue(s, s);
   }
   {
     const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
@@ -702,29 +717,30 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
         hv[m][e] = c < C ? hs[e * C + c] : 0.f;
       }
   }
-  for (int i = 0; i < my_units; ++i) {
-    const int stage = i % NS;
-    if (!mbar_wait_bounded(&full[stage], (uint32_t)((i / NS) & 1), flags)) s_abort = 1;
-    __syncthreads();
-    if (s_abort) {  // flagged; the units are still counted below, so the combine happens
-      drain_fills<false>(Stages{smem, full, nullptr, nullptr}, i, NS, my_units, flags);
-      break;
-    }
-    const uint8_t* st = smem + (size_t)stage * stage_b;
-    const int rb = q + i * nq;
-    for (int r = warp; r < UR; r += nwarps) {
+  int n = 0;
+  for (; n < my_items; ++n) {
+    const int s = n % NSW;
+    const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((n / NSW) & 1), flags);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;  // flagged; this warp's rows stay unwritten
+    const uint8_t* st = ring + (size_t)s * item_b;
+    const int r0 = row0(n);
+#pragma unroll
+    for (int r = 0; r < IR; ++r) {
       const uint8_t* cw = st + r * (I / 2);
-      const uint8_t* sc = st + UR * (I / 2) + r * (I / 16);
+      const uint8_t* sc = st + IR * (I / 2) + r * (I / 16);
       float y;
       if constexpr (MB > 0)
         y = w2_row_warp_g(cw, sc, C, MB, lane, [&](int m, int e) { return hv[m][e]; });
       else
         y = w2_row_warp(cw, sc, hs, I, lane);
-      if (lane == 0) ypart[(size_t)j * H + rb * UR + r] = y;
+      if (lane == 0) ypart[(size_t)j * H + r0 + r] = y;
     }
-    __syncthreads();
-    if (tid == 0 && i + NS < my_units) issue(i + NS, stage);
+    __syncwarp();  // every lane is done with the stage
+    if (lane == 0 && n + NSW < my_items) issue(n + NSW, s);
   }
+  if (n < my_items && lane == 0)  // after a timeout: let the copies in flight land (bounded)
+    for (int m = n; m < n + NSW && m < my_items; ++m)
+      if (!mbar_wait_bounded(&bars[m % NSW], (uint32_t)((m / NSW) & 1), flags)) break;
   count_blocks(plan, ypart, out, H, ctr, q, nq, my_units, s_lastb, &s_nlast);
 }
 
@@ -767,7 +783,7 @@ GateUpShape gateup_shape(int H, int stages) {
 template <int RPT, bool WR>
 cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
                        const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
-                       int subset) {
+                       int subset, bool pdl) {
   auto kern = gemv_gateup_kernel<RPT, WR>;
   static int smem_set = 0;  // raise the opt-in limit once per size (not a stream operation)
   if (s.smem > smem_set) {
@@ -776,6 +792,9 @@ cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Pl
     if (e != cudaSuccess) return e;
     smem_set = s.smem;
   }
+  if (pdl)
+    return launch_pdl(kern, dim3(grid), dim3(s.NT), s.smem, st, plan, x, hbuf, H, I, s.RL, s.NS,
+                      flags, subset);
   kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset);
   return cudaGetLastError();
 }
@@ -803,19 +822,21 @@ int gateup_grid(int I, int k, int num_sms, const GemvLaunch& how) {
 }
 
 struct DownShape {
-  int NS, smem, stage;
+  int NS, smem, stage;  // NS: stages per warp ring, stage: bytes of one
 };
 
 DownShape down_shape(int I, int stages) {
   DownShape d;
-  d.stage = kDownUnitRows * (I / 2 + I / 16);
-  const int per_cta = kSmemPerSm / 2 - 1024;  // room for one more CTA of another kernel
-  int ns = (per_cta - I * 4 - 8 * 8) / d.stage;
-  if (ns < 2) ns = (kSmemPerSm - 1024 - I * 4 - 8 * 8) / d.stage;  // large I
+  const int nwarps = kDownThreads / 32;
+  d.stage = kDownItemRows * (I / 2 + I / 16);
+  // leave room on the SM for one CTA of the step's other kernels
+  const int per_cta = 140 * 1024;
+  int ns = (per_cta - I * 4) / (nwarps * (d.stage + 8));
+  if (ns < 2) ns = (kSmemPerSm - 1024 - I * 4) / (nwarps * (d.stage + 8));  // large I
   if (ns > 8) ns = 8;
   if (stages > 0 && stages < ns) ns = stages;
   d.NS = ns;
-  d.smem = ns * d.stage + 8 * ns + I * 4;
+  d.smem = nwarps * ns * (d.stage + 8) + I * 4;
   return d;
 }
 
@@ -867,7 +888,7 @@ cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t
   const GateUpShape s = gateup_shape(H, how.stages);
   if (s.NS < 1 || s.NT > kGateUpThreads || how.from_host) return cudaErrorInvalidConfiguration;
   const int grid = gateup_grid(I, k, num_sms, how);
-  GATEUP_DISPATCH(run_gateup, st, grid, s, plan, x, ws.hbuf, H, I, flags, how.subset)
+  GATEUP_DISPATCH(run_gateup, st, grid, s, plan, x, ws.hbuf, H, I, flags, how.subset, how.pdl)
 }
 
 int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how) {

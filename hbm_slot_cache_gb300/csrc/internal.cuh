@@ -141,8 +141,8 @@ struct GemvLaunch {
   bool from_host;  // read-through launch only: the picks come from host memory
   int grid;        // CTAs (0: the kernel's default, a full persistent grid)
   int stages;      // units in flight per CTA (0: as many as fit)
-  bool pdl = false;  // down launch only: programmatic dependent launch on the
-                     // previous kernel of its stream (see pdl_wait)
+  bool pdl = false;  // gate/up and down launches: programmatic dependent launch
+                     // on the previous kernel of their stream (see pdl_wait)
 };
 // Counters of a one-row step (zero between steps; each user resets its own):
 //   [0] read-through CTAs that have finished, [1] read-through units taken,

@@ -394,7 +394,9 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     // their down pass starts as the read-through launch drains (not across a timing event)
     const GemvLaunch miss_dn{kPicksMiss, false, 0, 4, !h->timing};
     // resident picks: slot bytes from HBM
-    const GemvLaunch hit_gu{kPicksHit, false, 0, 3}, hit_dn{kPicksHit, false, 0, 4};
+    // (on the caller's stream each starts as the kernel before it drains; not across timing events)
+    const GemvLaunch hit_gu{kPicksHit, false, 0, 3, !h->timing},
+        hit_dn{kPicksHit, false, 0, 4, !h->timing};
     if (e == cudaSuccess) e = mark(2, h->side);
     if (e == cudaSuccess)
       e = launch_gemv_readthrough(h->side, h->plan, x, h->H, h->I, h->k, h->gemv, flags,

@@ -139,7 +139,24 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   const int npicks = rows * k;
   uint32_t* const fl = &L.stats->flags;  // plan index checks report here
 
-  // ---- state into shared memory (overlaps the router's logit loads)
+  // the next kernel of the stream may be scheduled now (it waits for this one)
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // ---- state into shared memory: every global load in flight at once
+  constexpr int KPT = (MOE_MAX_EXPERTS + kThreads - 1) / kThreads;
+  int32_t r_map[KPT], r_owner[KPT];
+  uint32_t r_stamp[KPT];
+  float r_logit[KPT];
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int e = tid + q * kThreads;
+    r_map[q] = e < E ? L.map[e] : -1;
+    r_owner[q] = e < S ? L.owner[e] : -1;
+    r_stamp[q] = e < S ? L.stamp[e] : 0u;
+    r_logit[q] = (rows == 1 && e < E) ? logits[e] : 0.f;
+  }
+  const uint32_t r_clock = tid == 0 ? *L.clock : 0u;
+  const uint32_t r_head = (tid == 0 && L.trace_cap) ? *L.trace_head : 0u;
   if (tid < kWords) {
     s_union[tid] = 0;
     s_missmask[tid] = 0;
@@ -149,18 +166,21 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     s_n_hits = 0;
     s_n_evict = 0;
     s_ncand = 0;
-    s_clock = *L.clock;
-    s_trace_head = L.trace_cap ? *L.trace_head : 0u;
+    s_clock = r_clock;
+    s_trace_head = r_head;
   }
-  for (int e = tid; e < E; e += kThreads) s_map[e] = L.map[e];
-  for (int v = tid; v < S; v += kThreads) {
-    s_owner[v] = L.owner[v];
-    s_key[v] = ((unsigned long long)L.stamp[v] << 32) | (unsigned)v;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) {
+    const int e = tid + q * kThreads;
+    if (e < E) s_map[e] = r_map[q];
+    if (e < S) {
+      s_owner[e] = r_owner[q];
+      s_key[e] = ((unsigned long long)r_stamp[q] << 32) | (unsigned)e;
+    }
   }
 
   // ---- router
   if (rows == 1) {
-    constexpr int KPT = (MOE_MAX_EXPERTS + kThreads - 1) / kThreads;
     unsigned long long key[KPT];
     bool bad = false;
 #pragma unroll
@@ -168,7 +188,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       const int e = tid + q * kThreads;
       key[q] = 0ull;
       if (e < E) {
-        const float f = logits[e];
+        const float f = r_logit[q];
         bad |= !isfinite(f);
         key[q] = route_key(f, e);
         s_logit[e] = f;
@@ -329,8 +349,16 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     for (int v = tid; v < S; v += kThreads) {
       const unsigned long long kv = s_key[v];
       if (kv == ~0ull) continue;
-      int r = 0;
-      for (int u = 0; u < S; ++u) r += s_key[u] < kv;
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+      int u = 0;
+      for (; u + 4 <= S; u += 4) {
+        r0 += s_key[u] < kv;
+        r1 += s_key[u + 1] < kv;
+        r2 += s_key[u + 2] < kv;
+        r3 += s_key[u + 3] < kv;
+      }
+      for (; u < S; ++u) r0 += s_key[u] < kv;
+      const int r = r0 + r1 + r2 + r3;
       if (r < n_miss) s_victim[r] = v;
     }
   }
@@ -400,6 +428,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     if (in && !hit) plan->order[__popc(hb) + __popc(mb & below)] = lane;
     if (lane == 0) plan->n_hit = __popc(hb);
   }
+  // bookkeeping spread over warps so no thread carries a serial tail
   if (tid == 0) {
     plan->rows = rows;
     plan->npicks = npicks;
@@ -407,21 +436,22 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     plan->n_miss = n_miss;
     plan->bypass = 0;
     *L.clock = t;
-    atomicAdd(&st->steps, 1ull);
-    atomicAdd(&st->picks, (unsigned long long)npicks);
-    atomicAdd(&st->hits, (unsigned long long)s_n_hits);
-    atomicAdd(&st->misses, (unsigned long long)n_miss);
-    atomicAdd(&st->evictions, (unsigned long long)s_n_evict);
-    atomicAdd(&st->bytes_copied, (unsigned long long)n_miss * (unsigned long long)(Bw + Bs));
-    if (s_flags) atomicOr(&st->flags, s_flags);
-    if (r) {
-      r->clock = t;
-      r->rows = rows;
-      r->n_union = n_union;
-      r->n_miss = n_miss;
-      r->bypass = 0;
-      *L.trace_head = s_trace_head + 1u;
-    }
+  } else if (tid >= 32 && tid < 39) {
+    const int c = tid - 32;
+    if (c == 0) atomicAdd(&st->steps, 1ull);
+    if (c == 1) atomicAdd(&st->picks, (unsigned long long)npicks);
+    if (c == 2) atomicAdd(&st->hits, (unsigned long long)s_n_hits);
+    if (c == 3) atomicAdd(&st->misses, (unsigned long long)n_miss);
+    if (c == 4) atomicAdd(&st->evictions, (unsigned long long)s_n_evict);
+    if (c == 5) atomicAdd(&st->bytes_copied, (unsigned long long)n_miss * (unsigned long long)(Bw + Bs));
+    if (c == 6 && s_flags) atomicOr(&st->flags, s_flags);
+  } else if (tid == 64 && r) {
+    r->clock = t;
+    r->rows = rows;
+    r->n_union = n_union;
+    r->n_miss = n_miss;
+    r->bypass = 0;
+    *L.trace_head = s_trace_head + 1u;
   }
 }
 
