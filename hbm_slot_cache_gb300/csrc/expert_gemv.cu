@@ -355,24 +355,27 @@ __device__ __forceinline__ float w2_row_warp(const uint8_t* __restrict__ cw,
 
 // ----------------------------------------------------------- gate / up
 
-// This thread's 16 activations (block c of the row) as f16, after a
-// power-of-two prescale of the whole row that keeps max |x| below 2^15;
-// returns the factor that undoes the prescale.  Every thread of the CTA
-// calls it (one barrier); the CTA's threads cover every block of the row.
+// This thread's 32 activations (elements 32c .. 32c + 31 of the row) as
+// f16, after a power-of-two prescale of the whole row that keeps max |x|
+// below 2^15; returns the factor that undoes the prescale.  Every thread of
+// the CTA calls it (one barrier); the CTA's threads cover the whole row.
 __device__ __forceinline__ float load_x_f16(const uint16_t* __restrict__ x, int c, float* s_xmax,
-                                            uint32_t (&xh)[8]) {
+                                            uint32_t (&xh)[16]) {
   const int tid = threadIdx.x, lane = tid & 31;
-  float xf[16];
+  float xf[32];
   float amax = 0.f;
   {
-    const uint4* xp = reinterpret_cast<const uint4*>(x + c * 16);
-    const uint4 a = __ldg(xp), b = __ldg(xp + 1);
-    const uint32_t wds[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint4* xp = reinterpret_cast<const uint4*>(x + c * 32);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      xf[2 * i] = bf16_bits_to_float(wds[i] & 0xFFFFu);
-      xf[2 * i + 1] = bf16_bits_to_float(wds[i] >> 16);
-      amax = fmaxf(amax, fmaxf(fabsf(xf[2 * i]), fabsf(xf[2 * i + 1])));
+    for (int v = 0; v < 4; ++v) {
+      const uint4 a = __ldg(xp + v);
+      const uint32_t wds[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xf[8 * v + 2 * i] = bf16_bits_to_float(wds[i] & 0xFFFFu);
+        xf[8 * v + 2 * i + 1] = bf16_bits_to_float(wds[i] >> 16);
+        amax = fmaxf(amax, fmaxf(fabsf(xf[8 * v + 2 * i]), fabsf(xf[8 * v + 2 * i + 1])));
+      }
     }
   }
 #pragma unroll
@@ -385,7 +388,7 @@ __device__ __forceinline__ float load_x_f16(const uint16_t* __restrict__ x, int 
   const int xshift = e2 > 15 ? e2 - 15 : 0;
   const float xdown = ldexpf(1.0f, -xshift);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 16; ++i) {
     const __half2 p = __floats2half2_rn(xf[2 * i] * xdown, xf[2 * i + 1] * xdown);
     xh[i] = *reinterpret_cast<const uint32_t*>(&p);
   }
@@ -393,63 +396,84 @@ __device__ __forceinline__ float load_x_f16(const uint16_t* __restrict__ x, int 
 }
 
 // Partial dot products of one staged gate/up unit (kGateUpRows row pairs laid
-// out as gate codes, up codes, gate scales, up scales) for this thread's
-// block c of rows g, g + RL, ...: a[q] gate rows, a[RPT + q] up rows.
+// out as gate codes, up codes, gate scales, up scales) over this thread's 32
+// columns 32c .. 32c + 31 (two 16-element scale blocks) of rows g, g + RL, ...:
+// a[q] gate rows, a[RPT + q] up rows.
 template <int RPT>
 __device__ __forceinline__ void gateup_partials(const uint8_t* __restrict__ st, int H, int RL,
-                                                int g, int c, const uint32_t (&xh)[8],
+                                                int g, int c, const uint32_t (&xh)[16],
                                                 float (&a)[2 * RPT]) {
   const int cb = kGateUpRows * H / 2, sb = kGateUpRows * H / 16;
 #pragma unroll
   for (int q = 0; q < RPT; ++q) {
     const int r = g + q * RL;
-    const uint2 cg = *reinterpret_cast<const uint2*>(st + r * (H / 2) + c * 8);
-    const uint2 cu = *reinterpret_cast<const uint2*>(st + cb + r * (H / 2) + c * 8);
-    const uint32_t sg = st[2 * cb + r * (H / 16) + c];
-    const uint32_t su = st[2 * cb + sb + r * (H / 16) + c];
-    a[q] = dot16_f16(cg, xh) * e4m3_to_float(sg);
-    a[RPT + q] = dot16_f16(cu, xh) * e4m3_to_float(su);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {  // gate, up
+      const uint4 cw = *reinterpret_cast<const uint4*>(st + u * cb + r * (H / 2) + c * 16);
+      const float2 sc = e4m3x2_to_float2(
+          *reinterpret_cast<const uint16_t*>(st + 2 * cb + u * sb + r * (H / 16) + c * 2));
+      const float d0 = dot16_f16(make_uint2(cw.x, cw.y), &xh[0]);
+      const float d1 = dot16_f16(make_uint2(cw.z, cw.w), &xh[8]);
+      a[u * RPT + q] = __fmaf_rn(d0, sc.x, __fmul_rn(d1, sc.y));
+    }
   }
 }
 
-// h = silu(gate) * up of the unit's row pair handled by this thread (threads
-// tid < RL * RPT), from the partials stashed by every thread.
+// h = silu(gate) * up of the unit's row pair t (t < RL * RPT), from the
+// partials stashed by every compute thread.
 template <int RPT, bool WARP_RED>
 __device__ __forceinline__ void gateup_epilogue(const float* red, int RL, int C,
                                                 const Plan* __restrict__ plan, int j, int rb,
-                                                float xup, float* __restrict__ hbuf, int I) {
+                                                float xup, float* __restrict__ hbuf, int I,
+                                                int t) {
   constexpr int V = 2 * RPT;
-  const int tid = threadIdx.x;
-  const int gg = tid / RPT, q = tid - gg * RPT;
+  const int gg = t / RPT, q = t - gg * RPT;
   const float gate = plan->gs[j][0] * xup * sum_partial<V, WARP_RED>(red, gg, q, C);
   const float up = plan->gs[j][1] * xup * sum_partial<V, WARP_RED>(red, gg, RPT + q, C);
   hbuf[(size_t)j * I + rb * kGateUpRows + gg + q * RL] = gate / (1.0f + expf(-gate)) * up;
 }
 
-// Resident picks: slot bytes from HBM, a unit's four segments by 1-D TMA bulk
-// copies, units assigned round-robin over the persistent grid.
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Resident picks: slot bytes from HBM, units assigned round-robin over the
+// persistent grid.  Warp-specialised: the C * RL compute threads wait only for
+// their unit's bytes (an mbarrier per stage), stash their partial sums and
+// signal the stage's named barrier without waiting; one control warp (the
+// CTA's last) waits on that barrier, forms h for the unit's rows and refills
+// the stage with the unit's four segments by 1-D TMA bulk copies.  No compute
+// warp ever waits for another.
 template <int RPT, bool WARP_RED>
-__global__ void __launch_bounds__(kGateUpThreads, 2)
+__global__ void __launch_bounds__(kGateUpThreads + 32, 2)
 gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
                    float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
                    int subset) {
   constexpr int V = 2 * RPT;
   constexpr int R = kGateUpRows;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_xmax[kGateUpThreads / 32];
-  const int C = H / 16;
+  __shared__ float s_xmax[kGateUpThreads / 32 + 1];
+  const int C = H / 32;
+  const int NC = C * RL;  // compute threads; the control warp follows them
   const int tid = threadIdx.x, lane = tid & 31;
   const int g = tid / C, c = tid - g * C;
   const int cb = R * H / 2, sb = R * H / 16;
   const int stage_bytes = 2 * cb + 2 * sb;
-  Stages S = carve(smem, NS, stage_bytes);
+  const int red_floats = WARP_RED ? RL * (C / 32) * V : NC * V;  // per stage
+  uint8_t* base = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
+  volatile int* abort_flag = reinterpret_cast<int*>(full + NS);
+  float* red0 = reinterpret_cast<float*>(full + NS + 1);
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
-    *S.abort_flag = 0;
+    *abort_flag = 0;
   }
-  uint32_t xh[8];
-  const float xup = load_x_f16(x, c, s_xmax, xh);  // x is the step's input, not route's output
+  uint32_t xh[16];
+  const float xup = load_x_f16(x, c < C ? c : 0, s_xmax, xh);  // x is the step's input
   pdl_wait();  // the plan comes from the kernel before this one
 
   // the picks this launch covers
@@ -464,42 +488,52 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   const int nunits = pcnt * upp;
   const int my_units = units_of_block(nunits);
 
-  auto issue = [&](int unit, int stage) {  // thread 0
-    const int jl = unit / upp, rb = unit - jl * upp;
-    const int j = pick_of(jl);
-    const uint8_t* w = plan->wptr[j];
-    const uint8_t* sc = plan->sptr[j];
-    const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
-    uint8_t* dst = S.base + (size_t)stage * stage_bytes;
-    mbar_arrive_expect_tx(&S.full[stage], (uint32_t)stage_bytes);
-    bulk_g2s(dst, w + og * (H / 2), cb, &S.full[stage]);
-    bulk_g2s(dst + cb, w + ou * (H / 2), cb, &S.full[stage]);
-    bulk_g2s(dst + 2 * cb, sc + og * (H / 16), sb, &S.full[stage]);
-    bulk_g2s(dst + 2 * cb + sb, sc + ou * (H / 16), sb, &S.full[stage]);
-  };
-
-  if (tid == 0)
-    for (int s = 0; s < NS && s < my_units; ++s) issue(blockIdx.x + s * gridDim.x, s);
-
+  if (tid >= NC) {  // ---- control warp
+    auto issue = [&](int unit, int stage) {  // lane 0
+      const int jl = unit / upp, rb = unit - jl * upp;
+      const int j = pick_of(jl);
+      const uint8_t* w = plan->wptr[j];
+      const uint8_t* sc = plan->sptr[j];
+      const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
+      uint8_t* dst = base + (size_t)stage * stage_bytes;
+      mbar_arrive_expect_tx(&full[stage], (uint32_t)stage_bytes);
+      bulk_g2s(dst, w + og * (H / 2), cb, &full[stage]);
+      bulk_g2s(dst + cb, w + ou * (H / 2), cb, &full[stage]);
+      bulk_g2s(dst + 2 * cb, sc + og * (H / 16), sb, &full[stage]);
+      bulk_g2s(dst + 2 * cb + sb, sc + ou * (H / 16), sb, &full[stage]);
+    };
+    int issued = 0;
+    if (lane == 0)
+      for (; issued < NS && issued < my_units; ++issued) issue(blockIdx.x + issued * gridDim.x, issued);
+    for (int i = 0; i < my_units; ++i) {
+      const int s = i % NS;
+      named_sync(1 + s, NC + 32);  // every compute thread has stashed unit i
+      const int unit = blockIdx.x + i * gridDim.x;
+      if (lane < RL * RPT) {
+        const int jl = unit / upp;
+        gateup_epilogue<RPT, WARP_RED>(red0 + s * red_floats, RL, C, plan, pick_of(jl),
+                                       unit - jl * upp, xup, hbuf, I, lane);
+      }
+      __syncwarp();
+      if (lane == 0 && i + NS < my_units && !*abort_flag) {
+        issue(unit + NS * gridDim.x, s);
+        ++issued;
+      }
+    }
+    if (lane == 0 && *abort_flag)  // let the copies in flight land (bounded)
+      for (int m = issued - NS > 0 ? issued - NS : 0; m < issued; ++m)
+        if (!mbar_wait_bounded(&full[m % NS], (uint32_t)((m / NS) & 1), flags)) break;
+    return;
+  }
+  // ---- compute threads
   for (int i = 0; i < my_units; ++i) {
-    const int unit = blockIdx.x + i * gridDim.x;
-    const int stage = i % NS;
-    if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
-    __syncthreads();
-    if (*S.abort_flag) {
-      drain_fills<false>(S, i, NS, my_units, flags);
-      return;
-    }
+    const int s = i % NS;
+    if (!*abort_flag && !mbar_wait_bounded(&full[s], (uint32_t)((i / NS) & 1), flags))
+      *abort_flag = 1;  // flagged; the remaining units are computed on whatever is staged
     float a[V];
-    gateup_partials<RPT>(S.base + (size_t)stage * stage_bytes, H, RL, g, c, xh, a);
-    stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
-    __syncthreads();
-    if (tid == 0 && i + NS < my_units) issue(unit + NS * gridDim.x, stage);
-    if (tid < RL * RPT) {
-      const int jl = unit / upp;
-      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan, pick_of(jl), unit - jl * upp, xup, hbuf,
-                                     I);
-    }
+    gateup_partials<RPT>(base + (size_t)s * stage_bytes, H, RL, g, c, xh, a);
+    stash_partials<V, WARP_RED>(a, red0 + s * red_floats, g, c, C, lane);
+    named_arrive(1 + s, NC + 32);
   }
 }
 
@@ -525,7 +559,7 @@ gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restric
   __shared__ float s_xmax[kGateUpThreads / 32];
   __shared__ int s_unit[kMaxStages];  // link unit staged in each stage, -1: none
   __shared__ int s_next[2];           // by iteration parity: read after the writer moved on
-  const int C = H / 16;
+  const int C = H / 32;
   const int tid = threadIdx.x, lane = tid & 31;
   const int g = tid / C, c = tid - g * C;
   const int cb = R * H / 2, sb = R * H / 16;
@@ -595,7 +629,7 @@ gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restric
   __syncthreads();
   for (int s = 0; s < NS; ++s)
     if (s_unit[s] >= 0) fill(s_unit[s], s);
-  uint32_t xh[8];
+  uint32_t xh[16];
   const float xup = load_x_f16(x, c, s_xmax, xh);
 
   for (int i = 0;; ++i) {
@@ -622,7 +656,7 @@ gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restric
     if (tid == 0) s_next[i & 1] = taken < NL ? taken : -1;
     __syncthreads();
     if (r < upp && tid < RL * RPT)
-      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan, pick_of(jl), r, xup, hbuf, I);
+      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan, pick_of(jl), r, xup, hbuf, I, tid);
     const int nxt = s_next[i & 1];
     if (tid == 0) s_unit[stage] = nxt;
     if (nxt >= 0) fill(nxt, stage);
@@ -760,7 +794,7 @@ struct GateUpShape {
 GateUpShape gateup_shape(int H, int stages) {
   GateUpShape s;
   const int R = kGateUpRows;
-  s.C = H / 16;
+  s.C = H / 32;  // threads across a row, 32 columns each
   int lim = kGateUpThreads / s.C;
   if (lim < 1) lim = 1;
   if (lim > R) lim = R;
@@ -772,11 +806,12 @@ GateUpShape gateup_shape(int H, int stages) {
   const int red_floats = s.warp_red ? s.RL * (s.C / 32) * V : s.NT * V;
   const int stage = 2 * R * H / 2 + 2 * R * H / 16;
   const int per_cta = kSmemPerSm / 2 - 1024;  // two CTAs per SM
-  int ns = (per_cta - 16 - red_floats * 4) / stage;
-  if (ns > 6) ns = 6;  // <= kMaxStages
+  // stages, their mbarriers and partial sums, the abort word
+  int ns = (per_cta - 16) / (stage + 8 + red_floats * 4);
+  if (ns > 6) ns = 6;  // <= kMaxStages, and named barriers 1 .. 6
   if (stages > 0 && stages < ns) ns = stages;
   s.NS = ns;
-  s.smem = ns * stage + 8 * ns + 8 + red_floats * 4;
+  s.smem = ns * stage + 8 * ns + 8 + ns * red_floats * 4;
   return s;
 }
 
@@ -793,9 +828,9 @@ cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Pl
     smem_set = s.smem;
   }
   if (pdl)
-    return launch_pdl(kern, dim3(grid), dim3(s.NT), s.smem, st, plan, x, hbuf, H, I, s.RL, s.NS,
-                      flags, subset);
-  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset);
+    return launch_pdl(kern, dim3(grid), dim3(s.NT + 32), s.smem, st, plan, x, hbuf, H, I, s.RL,
+                      s.NS, flags, subset);
+  kern<<<grid, s.NT + 32, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset);
   return cudaGetLastError();
 }
 
@@ -865,7 +900,7 @@ cudaError_t run_down(cudaStream_t st, int grid, const DownShape& d, const Plan* 
 bool gemv_supported(int H, int I, int k) {
   const int C = I / 32;  // 32-element blocks of a W2 row: whole warps of them or part of one
   if (!(H % 128 == 0 && I % 128 == 0 && H <= MOE_MAX_DIM && I <= MOE_MAX_DIM && k >= 1 &&
-        (C % 32 == 0 || 32 % C == 0) && H / 16 <= kGateUpThreads * kGateUpRows))
+        (C % 32 == 0 || 32 % C == 0) && H / 32 <= kGateUpThreads))
     return false;
   const GateUpShape s = gateup_shape(H, 0);
   return s.NT % 32 == 0 && s.NS >= 1 && down_shape(I, 0).NS >= 1;

@@ -394,8 +394,11 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     // their down pass starts as the read-through launch drains (not across a timing event)
     const GemvLaunch miss_dn{kPicksMiss, false, 0, 4, !h->timing};
     // resident picks: slot bytes from HBM
-    // (on the caller's stream each starts as the kernel before it drains; not across timing events)
-    const GemvLaunch hit_gu{kPicksHit, false, 0, 3, !h->timing},
+    // Gate/up is launched normally, after route/remap, so the second stream's
+    // higher priority places the read-through CTAs first (two gate/up CTAs
+    // fill an SM's registers); the down pass starts as gate/up drains
+    // (programmatic launch, not across timing events).
+    const GemvLaunch hit_gu{kPicksHit, false, 0, 3, false},
         hit_dn{kPicksHit, false, 0, 4, !h->timing};
     if (e == cudaSuccess) e = mark(2, h->side);
     if (e == cudaSuccess)
