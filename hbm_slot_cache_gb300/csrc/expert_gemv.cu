@@ -419,17 +419,16 @@ __device__ __forceinline__ void gateup_partials(const uint8_t* __restrict__ st, 
   }
 }
 
-// h = silu(gate) * up of the unit's row pair t (t < RL * RPT), from the
-// partials stashed by every compute thread.
+// h = silu(gate) * up of the unit's row pair t (t < RL * RPT) of pick j, from
+// the partials stashed by every compute thread; gs_*: the pick's global scales.
 template <int RPT, bool WARP_RED>
-__device__ __forceinline__ void gateup_epilogue(const float* red, int RL, int C,
-                                                const Plan* __restrict__ plan, int j, int rb,
-                                                float xup, float* __restrict__ hbuf, int I,
-                                                int t) {
+__device__ __forceinline__ void gateup_epilogue(const float* red, int RL, int C, float gs_gate,
+                                                float gs_up, int j, int rb, float xup,
+                                                float* __restrict__ hbuf, int I, int t) {
   constexpr int V = 2 * RPT;
   const int gg = t / RPT, q = t - gg * RPT;
-  const float gate = plan->gs[j][0] * xup * sum_partial<V, WARP_RED>(red, gg, q, C);
-  const float up = plan->gs[j][1] * xup * sum_partial<V, WARP_RED>(red, gg, RPT + q, C);
+  const float gate = gs_gate * xup * sum_partial<V, WARP_RED>(red, gg, q, C);
+  const float up = gs_up * xup * sum_partial<V, WARP_RED>(red, gg, RPT + q, C);
   hbuf[(size_t)j * I + rb * kGateUpRows + gg + q * RL] = gate / (1.0f + expf(-gate)) * up;
 }
 
@@ -483,17 +482,29 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     pbeg = plan->n_hit;
     pcnt = plan->npicks - plan->n_hit;
   }
-  auto pick_of = [&](int jl) { return subset == kPicksAll ? jl : plan->order[pbeg + jl]; };
   const int upp = I / R;  // units per pick
   const int nunits = pcnt * upp;
   const int my_units = units_of_block(nunits);
+  // the launch's picks, once: no global round trip on the refill path
+  __shared__ int s_j[MOE_MAX_TOPK];
+  __shared__ const uint8_t* s_w[MOE_MAX_TOPK];
+  __shared__ const uint8_t* s_s[MOE_MAX_TOPK];
+  __shared__ float s_gs[MOE_MAX_TOPK][2];
+  if (tid < pcnt && tid < MOE_MAX_TOPK) {
+    const int j = subset == kPicksAll ? tid : plan->order[pbeg + tid];
+    s_j[tid] = j;
+    s_w[tid] = plan->wptr[j];
+    s_s[tid] = plan->sptr[j];
+    s_gs[tid][0] = plan->gs[j][0];
+    s_gs[tid][1] = plan->gs[j][1];
+  }
+  __syncthreads();
 
   if (tid >= NC) {  // ---- control warp
     auto issue = [&](int unit, int stage) {  // lane 0
       const int jl = unit / upp, rb = unit - jl * upp;
-      const int j = pick_of(jl);
-      const uint8_t* w = plan->wptr[j];
-      const uint8_t* sc = plan->sptr[j];
+      const uint8_t* w = s_w[jl];
+      const uint8_t* sc = s_s[jl];
       const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
       uint8_t* dst = base + (size_t)stage * stage_bytes;
       mbar_arrive_expect_tx(&full[stage], (uint32_t)stage_bytes);
@@ -509,16 +520,19 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
       const int s = i % NS;
       named_sync(1 + s, NC + 32);  // every compute thread has stashed unit i
       const int unit = blockIdx.x + i * gridDim.x;
-      if (lane < RL * RPT) {
-        const int jl = unit / upp;
-        gateup_epilogue<RPT, WARP_RED>(red0 + s * red_floats, RL, C, plan, pick_of(jl),
-                                       unit - jl * upp, xup, hbuf, I, lane);
-      }
-      __syncwarp();
-      if (lane == 0 && i + NS < my_units && !*abort_flag) {
+      if (lane == 0 && i + NS < my_units && !*abort_flag) {  // the stage's bytes are consumed
         issue(unit + NS * gridDim.x, s);
         ++issued;
       }
+      // unit i's partials sit in buffer i % 2NS; the next unit to use that buffer
+      // is i + 2NS, whose bytes are only requested after unit i + NS is stashed,
+      // i.e. after this epilogue
+      if (lane < RL * RPT) {
+        const int jl = unit / upp;
+        gateup_epilogue<RPT, WARP_RED>(red0 + (i % (2 * NS)) * red_floats, RL, C, s_gs[jl][0],
+                                       s_gs[jl][1], s_j[jl], unit - jl * upp, xup, hbuf, I, lane);
+      }
+      __syncwarp();
     }
     if (lane == 0 && *abort_flag)  // let the copies in flight land (bounded)
       for (int m = issued - NS > 0 ? issued - NS : 0; m < issued; ++m)
@@ -532,7 +546,7 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
       *abort_flag = 1;  // flagged; the remaining units are computed on whatever is staged
     float a[V];
     gateup_partials<RPT>(base + (size_t)s * stage_bytes, H, RL, g, c, xh, a);
-    stash_partials<V, WARP_RED>(a, red0 + s * red_floats, g, c, C, lane);
+    stash_partials<V, WARP_RED>(a, red0 + (i % (2 * NS)) * red_floats, g, c, C, lane);
     named_arrive(1 + s, NC + 32);
   }
 }
@@ -653,12 +667,16 @@ gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restric
     } else {
       write_through(st, sg, nseg);
     }
-    if (tid == 0) s_next[i & 1] = taken < NL ? taken : -1;
+    if (tid == 0) {  // before the barrier: with one stage the next iteration reads it before any barrier
+      const int nv = taken < NL ? taken : -1;
+      s_next[i & 1] = nv;
+      s_unit[stage] = nv;
+    }
     __syncthreads();
     if (r < upp && tid < RL * RPT)
-      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan, pick_of(jl), r, xup, hbuf, I, tid);
+      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan->gs[pick_of(jl)][0],
+                                     plan->gs[pick_of(jl)][1], pick_of(jl), r, xup, hbuf, I, tid);
     const int nxt = s_next[i & 1];
-    if (tid == 0) s_unit[stage] = nxt;
     if (nxt >= 0) fill(nxt, stage);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -806,12 +824,12 @@ GateUpShape gateup_shape(int H, int stages) {
   const int red_floats = s.warp_red ? s.RL * (s.C / 32) * V : s.NT * V;
   const int stage = 2 * R * H / 2 + 2 * R * H / 16;
   const int per_cta = kSmemPerSm / 2 - 1024;  // two CTAs per SM
-  // stages, their mbarriers and partial sums, the abort word
-  int ns = (per_cta - 16) / (stage + 8 + red_floats * 4);
+  // stages, their mbarriers, two sets of partial sums a stage, the abort word
+  int ns = (per_cta - 16) / (stage + 8 + 2 * red_floats * 4);
   if (ns > 6) ns = 6;  // <= kMaxStages, and named barriers 1 .. 6
   if (stages > 0 && stages < ns) ns = stages;
   s.NS = ns;
-  s.smem = ns * stage + 8 * ns + 8 + ns * red_floats * 4;
+  s.smem = ns * stage + 8 * ns + 8 + 2 * ns * red_floats * 4;
   return s;
 }
 
