@@ -516,8 +516,8 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     int issued = 0;
     if (lane == 0)
       for (; issued < NS && issued < my_units; ++issued) issue(blockIdx.x + issued * gridDim.x, issued);
+    int s = 0, rbuf = 0;  // stage and partial-sum buffer of unit i (no runtime division)
     for (int i = 0; i < my_units; ++i) {
-      const int s = i % NS;
       named_sync(1 + s, NC + 32);  // every compute thread has stashed unit i
       const int unit = blockIdx.x + i * gridDim.x;
       if (lane == 0 && i + NS < my_units && !*abort_flag) {  // the stage's bytes are consumed
@@ -529,10 +529,12 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
       // i.e. after this epilogue
       if (lane < RL * RPT) {
         const int jl = unit / upp;
-        gateup_epilogue<RPT, WARP_RED>(red0 + (i % (2 * NS)) * red_floats, RL, C, s_gs[jl][0],
+        gateup_epilogue<RPT, WARP_RED>(red0 + rbuf * red_floats, RL, C, s_gs[jl][0],
                                        s_gs[jl][1], s_j[jl], unit - jl * upp, xup, hbuf, I, lane);
       }
       __syncwarp();
+      if (++s == NS) s = 0;
+      if (++rbuf == 2 * NS) rbuf = 0;
     }
     if (lane == 0 && *abort_flag)  // let the copies in flight land (bounded)
       for (int m = issued - NS > 0 ? issued - NS : 0; m < issued; ++m)
@@ -540,14 +542,20 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
     return;
   }
   // ---- compute threads
+  int s = 0, rbuf = 0;
+  uint32_t phase = 0;  // parity of stage s's current fill
   for (int i = 0; i < my_units; ++i) {
-    const int s = i % NS;
-    if (!*abort_flag && !mbar_wait_bounded(&full[s], (uint32_t)((i / NS) & 1), flags))
+    if (!*abort_flag && !mbar_wait_bounded(&full[s], phase, flags))
       *abort_flag = 1;  // flagged; the remaining units are computed on whatever is staged
     float a[V];
     gateup_partials<RPT>(base + (size_t)s * stage_bytes, H, RL, g, c, xh, a);
-    stash_partials<V, WARP_RED>(a, red0 + (i % (2 * NS)) * red_floats, g, c, C, lane);
+    stash_partials<V, WARP_RED>(a, red0 + rbuf * red_floats, g, c, C, lane);
     named_arrive(1 + s, NC + 32);
+    if (++s == NS) {
+      s = 0;
+      phase ^= 1u;
+    }
+    if (++rbuf == 2 * NS) rbuf = 0;
   }
 }
 
@@ -769,10 +777,10 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
         hv[m][e] = c < C ? hs[e * C + c] : 0.f;
       }
   }
-  int n = 0;
+  int n = 0, s = 0;
+  uint32_t phase = 0;  // parity of stage s's current fill
   for (; n < my_items; ++n) {
-    const int s = n % NSW;
-    const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((n / NSW) & 1), flags);
+    const bool ok = mbar_wait_bounded(&bars[s], phase, flags);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;  // flagged; this warp's rows stay unwritten
     const uint8_t* st = ring + (size_t)s * item_b;
     const int r0 = row0(n);
@@ -789,6 +797,10 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
     }
     __syncwarp();  // every lane is done with the stage
     if (lane == 0 && n + NSW < my_items) issue(n + NSW, s);
+    if (++s == NSW) {
+      s = 0;
+      phase ^= 1u;
+    }
   }
   if (n < my_items && lane == 0)  // after a timeout: let the copies in flight land (bounded)
     for (int m = n; m < n + NSW && m < my_items; ++m)

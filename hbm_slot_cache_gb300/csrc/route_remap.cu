@@ -455,12 +455,228 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   }
 }
 
+// One row, one warp: the same decisions as route_remap_kernel's one-row path,
+// without a CTA barrier.  Every global load is issued before any is used; the
+// top-k takes k rounds of a warp max (the rounds of route_row) and reads each
+// selected logit back from its key; hits, misses (ascending id) and victims
+// (k rounds at most of a warp min over the unused slots' (stamp, slot) keys)
+// come from ballots and shuffles; the bookkeeping is spread over lanes.
+template <int KPL>  // keys per lane >= ceil(max(E, S) / 32)
+__global__ void __launch_bounds__(32, 1)
+route_one_kernel(const float* __restrict__ logits, int E, int k, int S, long long Bw, long long Bs,
+                 LayerDev L, Plan* __restrict__ plan) {
+  __shared__ int32_t s_map[MOE_MAX_EXPERTS];
+  __shared__ int32_t s_owner[MOE_MAX_EXPERTS];
+  __shared__ unsigned long long s_skey[MOE_MAX_EXPERTS];  // (stamp, slot); ~0: used this step
+  __shared__ int32_t s_ids[MOE_MAX_TOPK];
+  __shared__ float s_wts[MOE_MAX_TOPK];
+  __shared__ int32_t s_miss_e[MOE_MAX_TOPK], s_victim[MOE_MAX_TOPK];
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int lane = threadIdx.x;
+  const unsigned full = 0xFFFFFFFFu;
+  uint32_t* const fl = &L.stats->flags;
+  if (lane < MOE_MAX_TOPK) {  // in range even where a failed plan check skips a write
+    s_ids[lane] = 0;
+    s_miss_e[lane] = 0;
+    s_victim[lane] = 0;
+  }
+  __syncwarp();
+
+  // ---- every global load in flight at once
+  float lg[KPL];
+  int32_t mp[KPL], ow[KPL];
+  uint32_t sp[KPL];
+#pragma unroll
+  for (int q = 0; q < KPL; ++q) {
+    const int e = lane + 32 * q;
+    lg[q] = e < E ? logits[e] : 0.f;
+    mp[q] = e < E ? L.map[e] : -1;
+    ow[q] = e < S ? L.owner[e] : -1;
+    sp[q] = e < S ? L.stamp[e] : 0u;
+  }
+  const uint32_t clk = *L.clock;
+  const uint32_t head = L.trace_cap ? *L.trace_head : 0u;
+#pragma unroll
+  for (int q = 0; q < KPL; ++q) {
+    const int e = lane + 32 * q;
+    if (e < E) s_map[e] = mp[q];
+    if (e < S) {
+      s_owner[e] = ow[q];
+      s_skey[e] = ((unsigned long long)sp[q] << 32) | (unsigned)e;
+    }
+  }
+
+  // ---- router: (logit desc, id asc), k rounds of a warp max
+  unsigned long long key[KPL];
+  bool bad = false;
+#pragma unroll
+  for (int q = 0; q < KPL; ++q) {
+    const int e = lane + 32 * q;
+    key[q] = 0ull;
+    if (e < E) {
+      bad |= !isfinite(lg[q]);
+      key[q] = route_key(lg[q], e);
+    }
+  }
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int q = 0; q < KPL; ++q) best = umax64(best, key[q]);
+  float lsel = 0.f;  // lane j < k: the j-th selected logit
+  for (int j = 0; j < k; ++j) {
+    unsigned long long w = best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w = umax64(w, __shfl_xor_sync(full, w, o));
+    const int e = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
+    if ((e & 31) == lane) {  // the owning lane drops the winner and rescans
+      best = 0ull;
+#pragma unroll
+      for (int q = 0; q < KPL; ++q) {
+        if (lane + 32 * q == e) key[q] = 0ull;
+        best = umax64(best, key[q]);
+      }
+    }
+    if (lane == 0 && plan_ok(e >= 0 && e < E, fl)) s_ids[j] = e;
+    if (lane == j) lsel = key_logit(w);
+  }
+  route_weights(lsel, k, lane, s_wts);
+  const bool any_bad = __any_sync(full, bad) != 0;
+  __syncwarp();
+
+  // the picks' global scales, in flight while the remap decisions are taken
+  const int e_me = lane < k ? s_ids[lane] : 0;
+  float gs0 = 0.f, gs1 = 0.f, gs2 = 0.f;
+  if (lane < k && plan_ok(e_me >= 0 && e_me < E, fl)) {
+    gs0 = L.gscale[3 * e_me + 0];
+    gs1 = L.gscale[3 * e_me + 1];
+    gs2 = L.gscale[3 * e_me + 2];
+  }
+
+  // ---- hits (slot marked used) and misses in ascending expert id
+  const int v_me = lane < k ? s_map[e_me] : -1;
+  const bool hit = lane < k && v_me >= 0 && plan_ok(v_me < S, fl);
+  const bool miss = lane < k && v_me < 0;
+  const uint32_t hitmask = __ballot_sync(full, hit), missmask = __ballot_sync(full, miss);
+  if (hit) s_skey[v_me] = ~0ull;
+  const int n_hits = __popc(hitmask), n_miss = __popc(missmask);
+  int mrank = 0;
+  for (int q = 0; q < k; ++q) {
+    const int eq = __shfl_sync(full, e_me, q);
+    mrank += ((missmask >> q) & 1u) && eq < e_me;
+  }
+  if (miss) s_miss_e[mrank] = e_me;
+  __syncwarp();
+
+  // ---- victims: the n_miss smallest (stamp, slot) among slots unused this step
+  const uint32_t t = clk + 1u;
+  for (int r = 0; r < n_miss; ++r) {
+    unsigned long long m = ~0ull;
+#pragma unroll
+    for (int q = 0; q < KPL; ++q) {
+      const int v = lane + 32 * q;
+      if (v < S) m = umin64(m, s_skey[v]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = umin64(m, __shfl_xor_sync(full, m, o));
+    const int v = (int)(m & 0xFFFFFFFFull);
+    if (lane == 0 && plan_ok(m != ~0ull && v < S, fl)) {
+      s_victim[r] = v;
+      s_skey[v] = ~0ull;
+    }
+    __syncwarp();
+  }
+
+  // ---- fill: evict the previous owner, then map the missing expert
+  int ev = -1;
+  if (lane < n_miss) {
+    const int e = s_miss_e[lane], v = s_victim[lane];
+    ev = s_owner[v];
+    if (ev >= 0) L.map[ev] = -1;
+    L.map[e] = v;
+    L.owner[v] = e;
+    L.stamp[v] = t;
+    s_map[e] = v;
+    plan->miss_e[lane] = e;
+    plan->miss_v[lane] = v;
+  }
+  const int n_evict = __popc(__ballot_sync(full, lane < n_miss && ev >= 0));
+  if (hit) L.stamp[v_me] = t;
+  __syncwarp();
+
+  // ---- per pick: the slot it reads, the trace, the order (hits, then misses)
+  moe_step_record_t* rec = L.trace_cap ? L.trace + (head % L.trace_cap) : nullptr;
+  if (lane < k) {
+    const int v = s_map[e_me];
+    plan->ids[lane] = e_me;
+    plan->wts[lane] = s_wts[lane];
+    plan->wptr[lane] = L.slot_w + (long long)v * Bw;
+    plan->sptr[lane] = L.slot_s + (long long)v * Bs;
+    plan->hwptr[lane] = L.host_w + (long long)e_me * Bw;
+    plan->hsptr[lane] = L.host_s + (long long)e_me * Bs;
+    plan->gs[lane][0] = gs0;
+    plan->gs[lane][1] = gs1;
+    plan->gs[lane][2] = gs2;
+    const uint32_t below = (1u << lane) - 1u;
+    plan->order[hit ? __popc(hitmask & below) : n_hits + __popc(missmask & below)] = lane;
+    if (rec) {
+      rec->ids[lane] = e_me;
+      rec->weights[lane] = s_wts[lane];
+      rec->slot[lane] = v;
+      rec->hit[lane] = hit ? 1 : 0;
+    }
+  }
+  if (rec && lane < n_miss) {
+    rec->miss_expert[lane] = s_miss_e[lane];
+    rec->miss_slot[lane] = s_victim[lane];
+    rec->miss_evicted[lane] = ev;
+  }
+  DevStats* st = L.stats;
+  if (lane == 0) {
+    plan->rows = 1;
+    plan->npicks = k;
+    plan->n_union = k;
+    plan->n_miss = n_miss;
+    plan->bypass = 0;
+    plan->n_hit = n_hits;
+    *L.clock = t;
+  } else if (lane == 1) {
+    atomicAdd(&st->steps, 1ull);
+  } else if (lane == 2) {
+    atomicAdd(&st->picks, (unsigned long long)k);
+  } else if (lane == 3) {
+    atomicAdd(&st->hits, (unsigned long long)n_hits);
+  } else if (lane == 4) {
+    atomicAdd(&st->misses, (unsigned long long)n_miss);
+  } else if (lane == 5) {
+    atomicAdd(&st->evictions, (unsigned long long)n_evict);
+  } else if (lane == 6) {
+    atomicAdd(&st->bytes_copied, (unsigned long long)n_miss * (unsigned long long)(Bw + Bs));
+  } else if (lane == 7 && any_bad) {
+    atomicOr(&st->flags, MOE_FLAG_NONFINITE_LOGIT);
+  } else if (lane == 8 && rec) {
+    rec->clock = t;
+    rec->rows = 1;
+    rec->n_union = k;
+    rec->n_miss = n_miss;
+    rec->bypass = 0;
+    *L.trace_head = head + 1u;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_remap(cudaStream_t st, const float* logits, int rows, int E, int k,
                                int S, long long Bw, long long Bs, const LayerDev& L, Plan* plan,
                                int all_resident, GroupPlan* gp) {
   const int kpl = (E + 31) / 32;
+  if (rows == 1 && !gp && k <= 32 && S <= E) {  // one row: the one-warp kernel
+#define RO(N)                                                                                   \
+    if (kpl <= N) {                                                                            \
+      route_one_kernel<N><<<1, 32, 0, st>>>(logits, E, k, S, Bw, Bs, L, plan);                 \
+      return cudaGetLastError();                                                               \
+    }
+    RO(1) RO(2) RO(4) RO(8) RO(16) RO(32)
+#undef RO
+  }
 #define RR(N)                                                                                   \
   if (kpl <= N) {                                                                              \
     static bool once = false;                                                                  \

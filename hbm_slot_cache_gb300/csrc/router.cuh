@@ -21,6 +21,9 @@ __device__ __forceinline__ uint32_t rank_key(float f) {
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
   return a > b ? a : b;
 }
+__device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) {
+  return a < b ? a : b;
+}
 
 // Softmax over the k selected logits; all 32 lanes call it, lane j < k holding
 // the j-th selected logit, and lane j writes wts[j].
@@ -33,6 +36,13 @@ __device__ __forceinline__ void route_weights(float lsel, int k, int lane, float
   float sum = 0.f;
   for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ej, j);
   if (lane < k) wts[lane] = ej / sum;
+}
+
+// The logit a ranking key was made from (rank_key inverted): -0 comes back as
+// +0 and NaN as a NaN, which route_weights treats exactly like the originals.
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+  const uint32_t kk = (uint32_t)(key >> 32);
+  return __uint_as_float((kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk);
 }
 
 // Ranking key of logit f for expert e: larger key = earlier rank; never 0.
