@@ -715,7 +715,8 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
   __shared__ int s_nlast;
   __shared__ int s_lastb[MOE_MAX_DIM / kDownUnitRows];
   constexpr int UR = kDownUnitRows, IR = kDownItemRows;
-  pdl_wait();  // h and the slots may come from the kernel before this one
+  // The plan was written by route/remap, which completed before the kernel
+  // this one may overlap (programmatic launch) started: it is read at once.
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   int pbeg = 0, pcnt = plan->npicks;
   if (subset == kPicksHit) pcnt = plan->n_hit;
@@ -754,13 +755,14 @@ gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
     bulk_g2s(dst, wsrc + (size_t)r0 * (I / 2), IR * (I / 2), &bars[s]);
     bulk_g2s(dst + IR * (I / 2), ssrc + (size_t)r0 * (I / 16), IR * (I / 16), &bars[s]);
   };
+  const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
+  pdl_wait();  // h and the slot bytes may come from the kernel before this one
   if (lane == 0) {
     for (int s = 0; s < NSW; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     for (int s = 0; s < NSW && s < my_items; ++s) issue(s, s);
   }
   {
-    const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
     for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
       hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
   }
