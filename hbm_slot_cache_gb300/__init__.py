@@ -103,6 +103,24 @@ class MoeCache:
         moe_cache_step(self.h, layer, rows, _dev_ptr(logits, torch.float32, "logits"),
                        _dev_ptr(x, torch.bfloat16, "x"), _dev_ptr(out, torch.float32, "out"), st)
 
+    def step_host(self, layer: int, logits, x, out, stream=None) -> None:
+        """The same step with host buffers (moe_cache_step_host): logits fp32 [rows, E],
+        x bf16 [rows, H], out fp32 [rows, H], CPU tensors (pinned for asynchronous
+        copies).  Enqueued on `stream`; the buffers must live until the stream
+        passes the step."""
+        import torch
+        rows = logits.shape[0]
+        if x.shape != (rows, self.hidden) or out.shape != (rows, self.hidden) or \
+                logits.shape != (rows, self.experts):
+            raise ValueError("shape mismatch")
+        for t, dt, nm in ((logits, torch.float32, "logits"), (x, torch.bfloat16, "x"),
+                          (out, torch.float32, "out")):
+            if t.device.type != "cpu" or t.dtype != dt or not t.is_contiguous():
+                raise ValueError(f"{nm}: expected a contiguous CPU {dt} tensor")
+        st = (stream or torch.cuda.current_stream()).cuda_stream
+        _lib.moe_cache_step_host(self.h, layer, rows, logits.data_ptr(), x.data_ptr(),
+                                 out.data_ptr(), st)
+
     def stats(self, layer: int = -1) -> dict:
         return moe_cache_stats(self.h, layer)
 

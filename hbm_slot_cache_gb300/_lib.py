@@ -29,7 +29,8 @@ MOE_MAX_PICKS = MOE_MAX_CACHED_ROWS * MOE_MAX_TOPK
 MOE_MAX_DIM = 8192
 MOE_COPY_SM = 0
 
-EXPORTS = ("moe_cache_create", "moe_cache_step", "moe_cache_stats", "moe_cache_slot_map",
+EXPORTS = ("moe_cache_create", "moe_cache_step", "moe_cache_step_host", "moe_cache_stats",
+           "moe_cache_slot_map",
            "moe_cache_slot_bytes", "moe_cache_trace", "moe_cache_reset", "moe_cache_destroy",
            "moe_cache_strerror", "moe_expert_bytes", "moe_host_alloc", "moe_host_free",
            "moe_probe_host_link", "moe_cache_set_timing_events", "moe_expert_pass_noalloc",
@@ -97,6 +98,7 @@ def lib() -> ctypes.CDLL:
         P, I, U64P = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)
         L.moe_cache_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, I, P, P]
         L.moe_cache_step.argtypes = [P, I, I, P, P, P, P]
+        L.moe_cache_step_host.argtypes = [P, I, I, P, P, P, P]
         L.moe_cache_stats.argtypes = [P, I, ctypes.POINTER(Stats)]
         L.moe_cache_slot_map.argtypes = [P, I, P]
         L.moe_cache_layer_slots.argtypes = [P, I, ctypes.POINTER(I)]
@@ -168,6 +170,12 @@ def moe_cache_create(layers: int, experts: int, slots: int, hidden: int, inter: 
 def moe_cache_step(h: int, layer: int, rows: int, router_logits: int, x: int, out: int,
                    stream: int = 0) -> None:
     _check(lib().moe_cache_step(h, layer, rows, router_logits, x, out, stream), "moe_cache_step")
+
+
+def moe_cache_step_host(h: int, layer: int, rows: int, router_logits: int, x: int, out: int,
+                        stream: int = 0) -> None:
+    _check(lib().moe_cache_step_host(h, layer, rows, router_logits, x, out, stream),
+           "moe_cache_step_host")
 
 
 def moe_cache_stats(h: int, layer: int = -1) -> dict:

@@ -466,56 +466,61 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
   volatile int* abort_flag = reinterpret_cast<int*>(full + NS);
   float* red0 = reinterpret_cast<float*>(full + NS + 1);
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-    *abort_flag = 0;
-  }
-  uint32_t xh[16];
-  const float xup = load_x_f16(x, c < C ? c : 0, s_xmax, xh);  // x is the step's input
-  pdl_wait();  // the plan comes from the kernel before this one
-
-  // the picks this launch covers
-  int pbeg = 0, pcnt = plan->npicks;
-  if (subset == kPicksHit) pcnt = plan->n_hit;
-  if (subset == kPicksMiss) {
-    pbeg = plan->n_hit;
-    pcnt = plan->npicks - plan->n_hit;
-  }
-  const int upp = I / R;  // units per pick
-  const int nunits = pcnt * upp;
-  const int my_units = units_of_block(nunits);
+  __shared__ int s_pcnt;
   // the launch's picks, once: no global round trip on the refill path
   __shared__ int s_j[MOE_MAX_TOPK];
   __shared__ const uint8_t* s_w[MOE_MAX_TOPK];
   __shared__ const uint8_t* s_s[MOE_MAX_TOPK];
   __shared__ float s_gs[MOE_MAX_TOPK][2];
-  if (tid < pcnt && tid < MOE_MAX_TOPK) {
-    const int j = subset == kPicksAll ? tid : plan->order[pbeg + tid];
-    s_j[tid] = j;
-    s_w[tid] = plan->wptr[j];
-    s_s[tid] = plan->sptr[j];
-    s_gs[tid][0] = plan->gs[j][0];
-    s_gs[tid][1] = plan->gs[j][1];
+  const int upp = I / R;  // units per pick
+
+  auto issue = [&](int unit, int stage) {  // control warp, lane 0
+    const int jl = unit / upp, rb = unit - jl * upp;
+    const uint8_t* w = s_w[jl];
+    const uint8_t* sc = s_s[jl];
+    const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
+    uint8_t* dst = base + (size_t)stage * stage_bytes;
+    mbar_arrive_expect_tx(&full[stage], (uint32_t)stage_bytes);
+    bulk_g2s(dst, w + og * (H / 2), cb, &full[stage]);
+    bulk_g2s(dst + cb, w + ou * (H / 2), cb, &full[stage]);
+    bulk_g2s(dst + 2 * cb, sc + og * (H / 16), sb, &full[stage]);
+    bulk_g2s(dst + 2 * cb + sb, sc + ou * (H / 16), sb, &full[stage]);
+  };
+  int issued = 0;
+  if (tid >= NC) {  // control warp: the plan and the first fills, while x loads below
+    pdl_wait();     // the plan comes from the kernel before this one
+    int pbeg = 0, pcnt = plan->npicks;
+    if (subset == kPicksHit) pcnt = plan->n_hit;
+    if (subset == kPicksMiss) {
+      pbeg = plan->n_hit;
+      pcnt = plan->npicks - plan->n_hit;
+    }
+    if (lane < pcnt && lane < MOE_MAX_TOPK) {
+      const int j = subset == kPicksAll ? lane : plan->order[pbeg + lane];
+      s_j[lane] = j;
+      s_w[lane] = plan->wptr[j];
+      s_s[lane] = plan->sptr[j];
+      s_gs[lane][0] = plan->gs[j][0];
+      s_gs[lane][1] = plan->gs[j][1];
+    }
+    if (lane == 0) {
+      s_pcnt = pcnt;
+      for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+      fence_mbar_init();
+      *abort_flag = 0;
+    }
+    __syncwarp();
+    const int my = units_of_block(pcnt * upp);
+    if (lane == 0)
+      for (; issued < NS && issued < my; ++issued) issue(blockIdx.x + issued * gridDim.x, issued);
   }
-  __syncthreads();
+  uint32_t xh[16];
+  const float xup = load_x_f16(x, c < C ? c : 0, s_xmax, xh);  // x: the step's input (one barrier)
+  const int pcnt = s_pcnt;
+  const int nunits = pcnt * upp;
+  const int my_units = units_of_block(nunits);
 
   if (tid >= NC) {  // ---- control warp
-    auto issue = [&](int unit, int stage) {  // lane 0
-      const int jl = unit / upp, rb = unit - jl * upp;
-      const uint8_t* w = s_w[jl];
-      const uint8_t* sc = s_s[jl];
-      const size_t og = (size_t)rb * R, ou = (size_t)I + (size_t)rb * R;
-      uint8_t* dst = base + (size_t)stage * stage_bytes;
-      mbar_arrive_expect_tx(&full[stage], (uint32_t)stage_bytes);
-      bulk_g2s(dst, w + og * (H / 2), cb, &full[stage]);
-      bulk_g2s(dst + cb, w + ou * (H / 2), cb, &full[stage]);
-      bulk_g2s(dst + 2 * cb, sc + og * (H / 16), sb, &full[stage]);
-      bulk_g2s(dst + 2 * cb + sb, sc + ou * (H / 16), sb, &full[stage]);
-    };
-    int issued = 0;
-    if (lane == 0)
-      for (; issued < NS && issued < my_units; ++issued) issue(blockIdx.x + issued * gridDim.x, issued);
     int s = 0, rbuf = 0;  // stage and partial-sum buffer of unit i (no runtime division)
     for (int i = 0; i < my_units; ++i) {
       named_sync(1 + s, NC + 32);  // every compute thread has stashed unit i

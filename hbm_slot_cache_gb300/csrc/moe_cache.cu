@@ -8,6 +8,7 @@
 #include <cstring>
 #include <new>
 #include <algorithm>
+#include <array>
 #include <vector>
 
 #include "internal.cuh"
@@ -59,6 +60,15 @@ struct moe_cache {
   // optional per-kernel timing events (caller-owned)
   cudaEvent_t ev[MOE_TIMING_EVENTS] = {};
   bool timing = false;
+  // moe_cache_step_host: device staging for max_rows rows, one-row step graphs per layer
+  float* st_logits = nullptr;   // [max_rows][E]
+  uint16_t* st_x = nullptr;     // [max_rows][H]
+  float* st_out = nullptr;      // [max_rows][H]
+  cudaStream_t cap = nullptr;   // capture stream
+  std::vector<cudaGraphExec_t> graph;  // [L], null until captured
+  std::vector<cudaGraph_t> graph_src;  // [L] the captured graphs (their nodes address the copies)
+  std::vector<std::array<cudaGraphNode_t, 3>> graph_cp;  // [L] logits, x, out copy nodes
+  std::vector<char> graph_warm;        // [L]: one eager one-row step done
 };
 
 namespace {
@@ -96,6 +106,20 @@ void free_all(moe_cache* h) {
   if (h->side) cudaStreamDestroy(h->side);
   h->fork = h->join = nullptr;
   h->side = nullptr;
+  for (cudaGraphExec_t g : h->graph)
+    if (g) cudaGraphExecDestroy(g);
+  h->graph.clear();
+  for (cudaGraph_t g : h->graph_src)
+    if (g) cudaGraphDestroy(g);
+  h->graph_src.clear();
+  if (h->cap) cudaStreamDestroy(h->cap);
+  h->cap = nullptr;
+  cudaFree(h->st_logits);
+  cudaFree(h->st_x);
+  cudaFree(h->st_out);
+  h->st_logits = nullptr;
+  h->st_x = nullptr;
+  h->st_out = nullptr;
 }
 
 // Group plan, quantised-activation buffers and bypass ids for steps of up to
@@ -325,6 +349,17 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
            cudaSuccess &&
        cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming) == cudaSuccess;
+  // host-buffer steps: staging for max_rows rows and a capture stream
+  ok = ok && dalloc(&h->st_logits, (size_t)o.max_rows * experts) == cudaSuccess &&
+       dalloc(&h->st_x, (size_t)o.max_rows * hidden) == cudaSuccess &&
+       dalloc(&h->st_out, (size_t)o.max_rows * hidden) == cudaSuccess &&
+       cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking) == cudaSuccess;
+  if (ok) {
+    h->graph.assign(layers, nullptr);
+    h->graph_src.assign(layers, nullptr);
+    h->graph_cp.assign(layers, {nullptr, nullptr, nullptr});
+    h->graph_warm.assign(layers, 0);
+  }
   if (!ok) {
     cudaGetLastError();
     free_all(h);
@@ -557,6 +592,110 @@ int moe_cache_trace(const moe_cache_t* h, int layer, moe_step_record_t* recs, in
   }
   *n_recs = (int)n;
   return cuda_err(e);
+}
+
+namespace {
+
+bool is_pinned(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+// The step's copies and kernels on stream s: logits and x host -> staging, the
+// step over the staging buffers, out staging -> host.
+int step_host_enqueue(moe_cache* h, int layer, int rows, const float* lg, const uint16_t* x,
+                      float* out, cudaStream_t s) {
+  const size_t nl = (size_t)rows * h->E, nx = (size_t)rows * h->H;
+  cudaError_t e = cudaMemcpyAsync(h->st_logits, lg, nl * sizeof(float), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h->st_x, x, nx * sizeof(uint16_t), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int rc = moe_cache_step(h, layer, rows, h->st_logits, h->st_x, h->st_out, s);
+  if (rc != MOE_OK) return rc;
+  return cuda_err(cudaMemcpyAsync(out, h->st_out, nx * sizeof(float), cudaMemcpyDeviceToHost, s));
+}
+
+// Capture the layer's one-row step with its copies; find the three copy nodes.
+int capture_step_graph(moe_cache* h, int layer, const float* lg, const uint16_t* x, float* out) {
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int rc = step_host_enqueue(h, layer, 1, lg, x, out, h->cap);
+  e = cudaStreamEndCapture(h->cap, &g);
+  if (rc != MOE_OK || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return rc != MOE_OK ? rc : MOE_ERR_CUDA;
+  }
+  size_t n = 0;
+  e = cudaGraphGetNodes(g, nullptr, &n);
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (e == cudaSuccess) e = cudaGraphGetNodes(g, nodes.data(), &n);
+  std::array<cudaGraphNode_t, 3> cp = {nullptr, nullptr, nullptr};
+  for (size_t i = 0; i < n && e == cudaSuccess; ++i) {
+    cudaGraphNodeType t;
+    if ((e = cudaGraphNodeGetType(nodes[i], &t)) != cudaSuccess || t != cudaGraphNodeTypeMemcpy)
+      continue;
+    cudaMemcpy3DParms mp{};
+    if ((e = cudaGraphMemcpyNodeGetParams(nodes[i], &mp)) != cudaSuccess) break;
+    if (mp.dstPtr.ptr == h->st_logits) cp[0] = nodes[i];
+    else if (mp.dstPtr.ptr == h->st_x) cp[1] = nodes[i];
+    else if (mp.srcPtr.ptr == h->st_out) cp[2] = nodes[i];
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (e == cudaSuccess && cp[0] && cp[1] && cp[2]) e = cudaGraphInstantiate(&ex, g, 0);
+  if (e != cudaSuccess || !ex) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  h->graph[layer] = ex;
+  h->graph_src[layer] = g;
+  h->graph_cp[layer] = cp;
+  return MOE_OK;
+}
+
+}  // namespace
+
+int moe_cache_step_host(moe_cache_t* h, int layer, int rows, const float* router_logits,
+                        const uint16_t* x, float* out, void* stream) {
+  if (!h || layer < 0 || layer >= h->L || rows < 1 || rows > h->opts.max_rows || !router_logits ||
+      !x || !out)
+    return MOE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // One-row steps with page-locked buffers replay a graph of the copies and the
+  // step: the layer's first such step runs eagerly (its launches set every
+  // kernel's attributes), the second captures the graph on the handle's own
+  // stream, later ones point its copy nodes at the call's buffers and launch it.
+  if (rows == 1 && !h->timing && h->graph_warm[layer] && is_pinned(router_logits) &&
+      is_pinned(x) && is_pinned(out)) {
+    if (!h->graph[layer]) {
+      const int rc = capture_step_graph(h, layer, router_logits, x, out);
+      if (rc != MOE_OK) return rc;
+    } else {
+      const auto& cp = h->graph_cp[layer];
+      cudaGraphExec_t ex = h->graph[layer];
+      cudaError_t e = cudaGraphExecMemcpyNodeSetParams1D(
+          ex, cp[0], h->st_logits, router_logits, (size_t)h->E * sizeof(float),
+          cudaMemcpyHostToDevice);
+      if (e == cudaSuccess)
+        e = cudaGraphExecMemcpyNodeSetParams1D(ex, cp[1], h->st_x, x,
+                                               (size_t)h->H * sizeof(uint16_t),
+                                               cudaMemcpyHostToDevice);
+      if (e == cudaSuccess)
+        e = cudaGraphExecMemcpyNodeSetParams1D(ex, cp[2], out, h->st_out,
+                                               (size_t)h->H * sizeof(float),
+                                               cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return cuda_err(cudaGraphLaunch(h->graph[layer], st));
+  }
+  if (rows == 1 && !h->timing) h->graph_warm[layer] = 1;
+  return step_host_enqueue(h, layer, rows, router_logits, x, out, st);
 }
 
 int moe_cache_reset(moe_cache_t* h) {

@@ -167,6 +167,21 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
 int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logits,
                    const uint16_t* x, float* out, void* stream);
 
+/* The same layer-step with host buffers: router_logits (fp32 [rows][experts])
+ * and x (bf16 bits [rows][hidden]) are copied host -> device into the handle's
+ * staging, the step runs, and out (fp32 [rows][hidden]) is copied device ->
+ * host, all enqueued on `stream` in that order.  Returns without waiting: the
+ * host buffers must stay valid and unchanged until the stream has passed the
+ * step (page-locked buffers make the copies asynchronous; pageable ones work,
+ * synchronously).  rows <= max_rows.  One-row steps replay a CUDA graph of the
+ * step over the staging buffers, captured for each layer on its second
+ * one-row call (never with timing events set, which take the eager path); the
+ * handle's addresses never change, so a graph stays valid until
+ * moe_cache_destroy.  Steps on one handle must be ordered on one stream, as for
+ * moe_cache_step.  Errors: as moe_cache_step; MOE_ERR_ARG for rows > max_rows. */
+int moe_cache_step_host(moe_cache_t* h, int layer, int rows, const float* router_logits,
+                        const uint16_t* x, float* out, void* stream);
+
 /* Counters of one layer (layer >= 0) or summed over all layers (layer == -1;
  * error_flags OR-ed).  Waits for all device work (device synchronize). */
 int moe_cache_stats(const moe_cache_t* h, int layer, moe_cache_stats_t* out);
