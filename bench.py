@@ -429,6 +429,26 @@ def run_ours(args) -> None:
         dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
     e2e_value = world * Ke / (float(e2e_ms.item()) * 1e-3)
 
+    # cold: the first steps from an empty ring (the same routing stream), one
+    # graph, after the steady-state measurement
+    n_cold = min(300, prewarm + W + K)
+    cache.reset()
+    g_cold = capture(0, n_cold)
+    cache.reset()  # capture does not execute; start from empty
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        c0.record(stream)
+        g_cold.replay()
+        c1.record(stream)
+    stream.synchronize()
+    sc = cache.stats(0)
+    cold = {"value": n_cold / (c0.elapsed_time(c1) * 1e-3), "unit": UNIT, "steps": n_cold,
+            "misses_per_step": sc["misses"] / n_cold,
+            "note": "steps 0..n from an empty ring, one CUDA graph (the value above is steady "
+                    "state after a 64-step pre-warm)"}
+    del g_cold
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_layer_steps(cfg, banks, seconds=12.0, max_steps=8)
@@ -456,7 +476,7 @@ def run_ours(args) -> None:
                                   "note": "mean over the traced steps of max(hit bytes / HBM "
                                           "peak, miss bytes / link peak)"},
                               "hit_rate": hits / picks if picks else None},
-            "roofline": roofline, "kernels": kern, "timing_split": timing_split,
+            "roofline": roofline, "kernels": kern, "timing_split": timing_split, "cold": cold,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": E * 4 + H * 2,
                     "d2h_bytes_per_step": H * 4, "steps": Ke},
