@@ -4,47 +4,42 @@
 // expert kernel reads the same bytes as in the all-HBM case, only the index
 // changes; "A correction first": 0.041 ms for the all-HBM layer under graphs.)
 //
-// Both kernels are HBM-bound GEMVs (~3.6 flop per weight byte) whose limit on
-// CUDA cores is the instruction issue rate of FP4 decode, so the inner loops
-// are built around the cheapest exact decode: the hardware E2M1x2 -> f16x2
-// conversion, then products into fp32 accumulators.
+// Both passes are GEMVs (~3.6 flop per weight byte) whose limit on CUDA cores
+// is the instruction issue rate of FP4 decode, so the inner loops are built
+// around the cheapest exact decode: the hardware E2M1x2 -> f16x2 conversion,
+// then products into fp32 accumulators.
 //
-// gate/up + SwiGLU: persistent grid.  A unit is R row pairs of one pick (gate
-// rows r.., up rows I+r..), contiguous in the expert's bytes; its code and
-// scale rows are staged into shared memory NS units ahead.  A thread owns a
-// 16-element block of every row it touches and keeps the matching 16
-// activations in registers as f16 (the row is prescaled by a power of two so
-// no activation overflows f16; bf16 -> f16 is then exact apart from f16
-// subnormals), so each product is one mixed-precision fma.rn.f32.f16.  Row
-// sums: reduce-scatter butterfly of shuffles, then a fixed-order sum across
-// warps.  The epilogue writes h = silu(gate) * up in fp32.
+// gate/up + SwiGLU (resident picks): persistent grid, warp-specialised.  A
+// unit is kGateUpRows row pairs of one pick (gate rows r.., up rows I+r..);
+// its four segments (gate codes, up codes, gate scales, up scales) arrive by
+// 1-D TMA bulk copies on the stage's mbarrier.  A compute thread owns 32
+// columns of every row it touches and keeps the matching activations in
+// registers as f16 (the row prescaled by a power of two so none overflows;
+// bf16 -> f16 is then exact apart from f16 subnormals), so each product is
+// one mixed-precision fma.rn.f32.f16.  Row sums: a reduce-scatter butterfly of
+// shuffles, then a fixed-order sum across warps.  Compute warps signal a
+// per-stage named barrier without waiting; a control warp refills the stage
+// and writes h = silu(gate) * up in fp32.
 //
-// down: persistent grid.  A thread owns one (pick j, 32-element block of I)
-// pair and keeps gscale_j * w_j * h_j for it in registers for the whole
-// kernel; a unit is a few output rows of the launch's picks, reduced per pick
-// (shuffles within the pick's lanes, then its warps) into the weighted output
-// y'_j.  The last CTA of the step's down launches to finish adds
+// down (resident or missed picks): one CTA per SM serves one pick; each warp
+// owns a ring of 2-row stages (TMA bulk copies) and reduces each W2 row with
+// w2_row_warp_g against gscale_j * w_j * h_j held in registers, writing the
+// weighted output y'_j.  At exit a CTA counts its 32-row output blocks; the CTA
+// that completes a block's count over all the step's picks adds that block of
 // out = sum_j y'_j in rank order.
 //
-// Both GEMVs run on a subset of the step's picks (the resident ones, the
-// missed ones, or all) and stage slot bytes from HBM with 1-D TMA bulk copies
-// (cp.async.bulk) on an mbarrier.
-//
-// read-through: the missed picks take one launch that reads each missed
-// expert once over the host link and uses it on the way in.  Every thread
-// stages 16-byte pieces from host memory with cp.async, an mbarrier counts
-// the threads' completions, and after use each stage is written through to
-// the pick's victim slot.  Phase A is the gate/up kernel above on the W13
-// rows; each finished unit is counted per pick.  Phase B takes the pick's W2
-// rows (prefetched from the launch's start, so the link never idles): once
-// the pick's count shows all its h is written, a warp per row computes y'_j,
-// with the per-thread blocks and reduction tree of the down kernel.
+// read-through (missed picks): one launch reads each missed expert once over
+// the host link.  Its work list (units taken one at a time from a step
+// counter) holds each missed pick's gate/up units, computed on arrival with
+// the functions the resident gate/up uses, then the pick's W2 bytes as copy
+// units; every unit is written through to the pick's victim slot.  Every
+// thread stages 16-byte pieces from host memory with cp.async and an mbarrier
+// counts the threads' completions.  The missed picks' down pass is the down
+// kernel, launched after it.
 //
 // A pick's computation and reduction order do not depend on the subset, the
 // source or the kernel it runs in, so a cached step and an all-resident step
-// give the same bits.  Every launch that writes y'_j counts its CTAs in a
-// step counter; the CTA that completes the count adds out = sum_j y'_j in
-// rank order and resets the counters.
+// give the same bits.
 #include "internal.cuh"
 
 namespace moe {
