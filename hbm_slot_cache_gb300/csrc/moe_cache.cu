@@ -414,8 +414,9 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     // resident picks' gate/up and down run on the caller's stream, so the hit
     // experts' HBM reads overlap the host-link transfer.  Each pick's weighted
     // output y'_j is computed the same way whichever path it takes, and the
-    // last CTA of the step's two down launches adds them in rank order, so the
-    // result does not depend on the hit/miss split.
+    // CTA that completes an output block's count over the step's picks (from
+    // either down launch) adds that block in rank order, so the result does
+    // not depend on the hit/miss split.
     if (e == cudaSuccess)
       e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S_of[layer], h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, nullptr);
