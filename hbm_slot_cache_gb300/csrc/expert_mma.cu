@@ -57,7 +57,7 @@ struct MmaArgs {
   QuantBuf act; // gate/up: by token row; down: by pick
   float* out;   // gate/up: h [P][I]; down: y [P][H]
   uint32_t* flags;
-  int g0, g1;   // the launch's groups [g0, g1)
+  int g0, g1;   // the launch's groups [g0, g1) (kHitGroups: the step's hit-group count)
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
@@ -108,8 +108,11 @@ grouped_mma_kernel(MmaArgs a) {
   const GroupPlan* gp = a.gp;
   // this launch's jobs: those of groups [g0, g1)
   const int ng = gp->n_groups;
-  const int jbeg = a.g0 < ng ? gp->g_job[a.g0] : gp->n_jobs;
-  const int jend = gp->g_job[a.g1 < ng ? a.g1 : ng];
+  const int nh = min(max(gp->n_hit_groups, 0), ng);
+  const int g0 = a.g0 == kHitGroups ? nh : max(a.g0, 0);
+  const int g1 = a.g1 == kHitGroups ? nh : a.g1;
+  const int jbeg = g0 < ng ? gp->g_job[g0] : gp->n_jobs;
+  const int jend = gp->g_job[g1 < ng ? g1 : ng];
   if (jbeg + (int)blockIdx.x >= jend) return;  // uniform: before any TMEM or barrier use
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.y;

@@ -64,8 +64,13 @@ struct Plan {
 // largest step (P = max_rows * top_k picks).
 constexpr int kLevels = 6;       // residual NVFP4 levels of the activations
 constexpr int kRowsPerJob = 5;   // members per MMA N-tile (5 * 6 = 30 of 32 columns)
+// Groups list the experts resident at step start (hits) first, then the rest,
+// each part in ascending expert id, so a step can run the hit groups while the
+// misses copy.  kHitGroups as a launch's g0 or g1 stands for n_hit_groups.
+constexpr int kHitGroups = -1;
 struct GroupPlan {
   int32_t n_groups, n_jobs, rows, npicks;
+  int32_t n_hit_groups;    // groups [0, n_hit_groups) need no copy this step
   int32_t* g_expert;       // [G]
   int32_t* g_start;        // [G] first member
   int32_t* g_count;        // [G]

@@ -3,6 +3,7 @@
 // (fixed addresses; "GLM 5.3 Testing: HBM Expert Allocation", "What the slot
 // cache is": fixed addresses and shapes keep the step CUDA-graph safe), and a
 // step only enqueues kernels.
+#include <climits>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -460,14 +461,21 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   }
   // several rows: experts grouped, each read once for all its rows (tensor cores)
   const int npicks = rows * h->k;
-  if (rows <= h->opts.bypass_rows) {
+  const bool cached_rows = rows <= h->opts.bypass_rows;
+  if (cached_rows) {
+    // The misses copy host -> slot on the second stream (a grid that keeps the
+    // host link busy without taking the SMs) while the caller's stream runs
+    // the hit groups below; the miss groups wait for the copy.
     if (e == cudaSuccess)
       e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S_of[layer], h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, h->gp);
     if (e == cudaSuccess) e = mark(1, st);
+    if (e == cudaSuccess) e = cudaEventRecord(h->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork, 0);
     if (e == cudaSuccess && !h->opts.all_resident)
-      e = launch_miss_copy(st, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
-                           2 * h->num_sms);
+      e = launch_miss_copy(h->side, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
+                           std::max(8, h->num_sms / 2));
+    if (e == cudaSuccess) e = cudaEventRecord(h->join, h->side);
   } else {
     // prefill bypass: experts read from host memory, cache untouched
     if (e == cudaSuccess)
@@ -506,6 +514,26 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     }
     if (e == cudaSuccess) e = mark(3, st);
     if (e == cudaSuccess) e = mark(5, st);
+    if (e == cudaSuccess) e = mark(4, st);
+    if (e == cudaSuccess) e = mark(6, st);
+  } else if (cached_rows) {
+    // hit groups [0, n_hit) now, miss groups [n_hit, n) once their bytes are in
+    // the slots: gate/up, the members' h in residual NVFP4, down, each pass
+    const int gr[3] = {0, kHitGroups, INT_MAX};
+    for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
+      if (pass == 1) e = cudaStreamWaitEvent(st, h->join, 0);
+      if (e == cudaSuccess)
+        e = launch_grouped_mma(st, h->gp, npicks, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf,
+                               flags, gr[pass], gr[pass + 1]);
+      if (e == cudaSuccess)
+        e = launch_quantize_members(st, h->gemv.hbuf, h->I, h->gp, gr[pass], gr[pass + 1],
+                                    h->hq, h->num_sms);
+      if (e == cudaSuccess)
+        e = launch_grouped_mma(st, h->gp, npicks, false, h->H, h->I, h->k, h->hq, h->gemv.ypart,
+                               flags, gr[pass], gr[pass + 1]);
+      if (e == cudaSuccess && pass == 0) e = mark(3, st);
+      if (e == cudaSuccess && pass == 0) e = mark(5, st);
+    }
     if (e == cudaSuccess) e = mark(4, st);
     if (e == cudaSuccess) e = mark(6, st);
   } else {

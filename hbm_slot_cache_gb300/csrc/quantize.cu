@@ -126,13 +126,17 @@ quantize_rows_kernel(const void* __restrict__ src, int K, QuantBuf q) {
 }
 
 // The rows named by the members of groups [g0, g1) (members are stored group
-// after group, so they are one contiguous range).
+// after group, so they are one contiguous range; kHitGroups: the hit-group count).
 __global__ void __launch_bounds__(1024)
 quantize_members_kernel(const float* __restrict__ src, int K, const GroupPlan* __restrict__ gp,
                         int g0, int g1, QuantBuf q) {
   __shared__ float red[32];
   const int ng = gp->n_groups;
-  if (g0 >= ng) return;
+  const int nh = min(max(gp->n_hit_groups, 0), ng);
+  if (g0 == kHitGroups) g0 = nh;
+  if (g1 == kHitGroups) g1 = nh;
+  if (g0 < 0) g0 = 0;
+  if (g0 >= ng || g1 <= g0) return;
   const int mbeg = gp->g_start[g0];
   const int mend = g1 < ng ? gp->g_start[g1] : gp->npicks;
   for (int i = mbeg + blockIdx.x; i < mend; i += gridDim.x) {

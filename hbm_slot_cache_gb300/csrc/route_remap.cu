@@ -41,13 +41,17 @@ constexpr int kThreads = 512;
 constexpr int kWords = MOE_MAX_EXPERTS / 32;
 
 // Multi-row steps: group the picks by expert for the grouped tensor-core pass.
-// Groups are the union's experts in ascending id (group = rank in the union),
-// members are pick indices in ascending order, jobs are tiles of kRowsPerJob
-// members.  Called by every thread of the CTA.
-__device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
+// Groups are the union's experts resident at step start (hits) in ascending
+// id, then the others (misses) in ascending id, so the hit groups can run
+// while the misses copy; members are pick indices in ascending order, jobs
+// are tiles of kRowsPerJob members.  s_hpre / s_mpre: hits / misses of the
+// union before each 32-expert word; n_hitu: hits in the union.  Called by
+// every thread of the CTA.
+__device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union, int n_hitu,
                             const int32_t* s_ids, const float* s_wts,
                             const uint8_t* const* s_wp, const uint8_t* const* s_sp,
-                            const uint32_t* s_union, const int32_t* s_upre, int32_t* s_pgroup,
+                            const uint32_t* s_union, const uint32_t* s_missmask,
+                            const int32_t* s_hpre, const int32_t* s_mpre, int32_t* s_pgroup,
                             int32_t* s_gcount, int32_t* s_gstart, int32_t* s_jstart,
                             const float* gscale, int E, uint32_t* fl) {
   const int tid = threadIdx.x;
@@ -56,7 +60,10 @@ __device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
   for (int p = tid; p < npicks; p += kThreads) {
     const int e = s_ids[p];
     if (!plan_ok(e >= 0 && e < E, fl)) continue;
-    const int g = s_upre[e >> 5] + __popc(s_union[e >> 5] & ((1u << (e & 31)) - 1u));
+    const uint32_t below = (1u << (e & 31)) - 1u, mw = s_missmask[e >> 5];
+    const int g = ((mw >> (e & 31)) & 1u)
+                      ? n_hitu + s_mpre[e >> 5] + __popc(mw & below)
+                      : s_hpre[e >> 5] + __popc(s_union[e >> 5] & ~mw & below);
     if (!plan_ok(g >= 0 && g < n_union, fl)) continue;
     s_pgroup[p] = g;
     atomicAdd(&s_gcount[g], 1);
@@ -72,6 +79,7 @@ __device__ void emit_groups(GroupPlan* gp, int rows, int npicks, int n_union,
       j += (s_gcount[g] + kRowsPerJob - 1) / kRowsPerJob;
     }
     gp->n_groups = n_union;
+    gp->n_hit_groups = n_hitu;
     gp->n_jobs = j;
     gp->rows = rows;
     gp->npicks = npicks;
@@ -122,6 +130,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   __shared__ uint32_t s_union[kWords];
   __shared__ uint32_t s_missmask[kWords];
   __shared__ int32_t s_upre[kWords];                   // union ranks before each word
+  __shared__ int32_t s_hpre[kWords], s_mpre[kWords];   // hits / misses of the union before it
   __shared__ const uint8_t* s_wp[MOE_MAX_PICKS];       // bytes each pick reads
   __shared__ const uint8_t* s_sp[MOE_MAX_PICKS];
   __shared__ int32_t s_pgroup[MOE_MAX_PICKS], s_gcount[MOE_MAX_PICKS];
@@ -276,6 +285,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
       }
     }
     s_upre[lane] = uincl - nu;
+    s_mpre[lane] = incl - nm;
+    s_hpre[lane] = (uincl - nu) - (incl - nm);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tot_u += __shfl_xor_sync(0xFFFFFFFFu, tot_u, o);
     int i = incl - nm;
@@ -318,7 +329,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
     }
     __syncthreads();
     if (gp)
-      emit_groups(gp, rows, npicks, n_union, s_ids, s_wts, s_wp, s_sp, s_union, s_upre, s_pgroup,
+      emit_groups(gp, rows, npicks, n_union, n_union - n_miss, s_ids, s_wts, s_wp, s_sp, s_union,
+                  s_missmask, s_hpre, s_mpre, s_pgroup,
                   s_gcount, s_gstart, s_jstart, L.gscale, E, fl);
     if (tid == 0) {
       plan->rows = rows;
@@ -416,7 +428,8 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
   }
   __syncthreads();
   if (gp)
-    emit_groups(gp, rows, npicks, n_union, s_ids, s_wts, s_wp, s_sp, s_union, s_upre, s_pgroup,
+    emit_groups(gp, rows, npicks, n_union, n_union - n_miss, s_ids, s_wts, s_wp, s_sp, s_union,
+                  s_missmask, s_hpre, s_mpre, s_pgroup,
                 s_gcount, s_gstart, s_jstart, L.gscale, E, fl);
   if (rows == 1 && warp == 0) {  // hits first, then misses, each in rank order (npicks <= 32)
     const bool in = lane < npicks;

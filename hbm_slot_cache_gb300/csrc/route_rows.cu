@@ -103,6 +103,7 @@ group_rows_kernel(const int32_t* __restrict__ ids, int rows, int E, int k, long 
   if (tid == 0) {
     gp->g_job[n_groups] = n_jobs;
     gp->n_groups = n_groups;
+    gp->n_hit_groups = n_groups;  // a bypass copies nothing
     gp->n_jobs = n_jobs;
     gp->rows = rows;
     gp->npicks = npicks;
