@@ -264,13 +264,18 @@ constexpr int kWorkCtr = 1;    // read-through units taken
 constexpr int kBlockCtr = 2;   // + b: picks done for output block b
 constexpr int kMaxStages = 8;  // gate/up stages at most
 
+// The plan, h and the partial outputs y' are written by a grid that may still
+// be running when a kernel here reads them (a programmatic launch reads them
+// after its dependency wait; the per-block combine reads other CTAs' y'), so
+// they carry no __restrict__: with it the compiler may read them through the
+// non-coherent path or move a load ahead of the wait.
+
 // Every thread of a down CTA, once all its units' rows are written: count
 // each unit (this CTA's pick, output blocks b0, b0 + db, ...) for its block;
 // for every block whose count this CTA completes over the step's npicks
 // picks, one warp adds out = sum_j y'_j over the block's rows in rank order
 // and resets the count.  s_lastb: room for nunits ints.
-__device__ __forceinline__ void count_blocks(const Plan* __restrict__ plan,
-                                             const float* __restrict__ ypart,
+__device__ __forceinline__ void count_blocks(const Plan* plan, const float* ypart,
                                              float* __restrict__ out, int H, uint32_t* ctr,
                                              int b0, int db, int nunits, int* s_lastb,
                                              int* s_nlast) {
@@ -443,7 +448,7 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 // warp ever waits for another.
 template <int RPT, bool WARP_RED>
 __global__ void __launch_bounds__(kGateUpThreads + 32, 2)
-gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
+gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
                    float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
                    int subset) {
   constexpr int V = 2 * RPT;
@@ -572,7 +577,7 @@ gemv_gateup_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x
 // from L2) with the same row routine, hence the same bits.
 template <int RPT, bool WARP_RED>
 __global__ void __launch_bounds__(kGateUpThreads, 2)
-gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restrict__ x,
+gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
                         float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
                         uint32_t* ctr) {
   constexpr int V = 2 * RPT;
@@ -708,9 +713,8 @@ gemv_readthrough_kernel(const Plan* __restrict__ plan, const uint16_t* __restric
 // per-block combine.
 template <int MB>  // h blocks a lane keeps in registers (0: read them from shared memory)
 __global__ void __launch_bounds__(kDownThreads, 1)
-gemv_down_kernel(const Plan* __restrict__ plan, const float* __restrict__ hbuf,
-                 float* __restrict__ ypart, int H, int I, int NSW, uint32_t* flags, int subset,
-                 float* __restrict__ out, uint32_t* __restrict__ ctr) {
+gemv_down_kernel(const Plan* plan, const float* hbuf, float* ypart, int H, int I, int NSW,
+                 uint32_t* flags, int subset, float* __restrict__ out, uint32_t* ctr) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_nlast;
   __shared__ int s_lastb[MOE_MAX_DIM / kDownUnitRows];
