@@ -125,10 +125,6 @@ __device__ __forceinline__ float w2_block(uint4 cw, uint32_t s2, Get v) {
   return __fmaf_rn(d0, sc.x, __fmul_rn(d1, sc.y));
 }
 
-__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
-  return e4m3x2_to_float2(byte & 0xFFu).x;
-}
-
 // Reduce-scatter V values across the 32 lanes: afterwards lane l holds the
 // warp sum of value (l >> (5 - log2 V)) & (V - 1).
 template <int V>
