@@ -176,7 +176,7 @@ def run_reference(args) -> None:
         return
     import oracle
     cfg = workload.CONFIGS["glm"]
-    banks = Banks(cfg)
+    banks = Banks(cfg, pinned=False)  # the oracle reads the bytes on the CPU only
     rt = workload.Routing(cfg)
     sim = oracle.LRUSim(cfg.experts, cfg.slots, check_list=False)
     # size the per-step sample so warmup + steps take about a minute

@@ -30,18 +30,34 @@ def assert_within_tolerance(got, ref, what=""):
     return m
 
 
-class Banks:
-    """Pinned host banks for `distinct` layers of a config (layers beyond that alias
-    bank l % distinct; routing stays independent per layer)."""
+class PlainBank:
+    """Ordinary host memory with HostBank's interface (.array, .close()), for
+    users that only read the bytes on the CPU."""
 
-    def __init__(self, cfg: workload.Config, distinct: int = 1):
-        from hbm_slot_cache_gb300 import HostBank
+    def __init__(self, nbytes: int):
+        self.array = np.empty(int(nbytes), np.uint8)
+
+    def close(self) -> None:
+        self.array = None
+
+
+class Banks:
+    """Host banks for `distinct` layers of a config (layers beyond that alias
+    bank l % distinct; routing stays independent per layer): pinned, mapped
+    memory the library can read, or (pinned=False) ordinary memory for the
+    oracle alone."""
+
+    def __init__(self, cfg: workload.Config, distinct: int = 1, pinned: bool = True):
+        if pinned:
+            from hbm_slot_cache_gb300 import HostBank as Bank
+        else:
+            Bank = PlainBank
         self.cfg = cfg
         self.Bw, self.Bs = workload.storage_bytes(cfg.hidden, cfg.inter)
         self.w, self.s, self.g = [], [], []
         for l in range(distinct):
-            w = HostBank(cfg.experts * self.Bw)
-            s = HostBank(cfg.experts * self.Bs)
+            w = Bank(cfg.experts * self.Bw)
+            s = Bank(cfg.experts * self.Bs)
             workload.fill_bank(w.array, s.array, cfg.experts, cfg.hidden, cfg.inter, cfg.seed, l)
             self.w.append(w)
             self.s.append(s)
