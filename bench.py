@@ -46,6 +46,19 @@ def _peaks():
     return 6800.0, "fallback (6.8 TB/s)"
 
 
+def job_rate(ms_local: float, units_local: int, world: int, device) -> tuple[float, float]:
+    """Whole-job rate of `world` replicas that each processed `units_local` units:
+    the job's time is the slowest rank's (max over ranks, an all-reduce when
+    world > 1).  Returns (units per second over all ranks, that time in ms)."""
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    return world * units_local / (ms * 1e-3), ms
+
+
 def _src_sha() -> str:
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "hbm_slot_cache_gb300", "csrc")
@@ -300,11 +313,7 @@ def run_ours(args) -> None:
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms_total = start.elapsed_time(end)
-    t_max = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms_total_max = float(t_max.item())
+    value, ms_total_max = job_rate(start.elapsed_time(end), K, world, "cuda")
     s1 = cache.stats(0)
     misses = s1["misses"] - s0["misses"]
     hits = s1["hits"] - s0["hits"]
@@ -350,7 +359,6 @@ def run_ours(args) -> None:
 
     Bexp = banks.Bw + banks.Bs
     ms_step = ms_total_max / K
-    value = world * K / (ms_total_max * 1e-3)
     miss_per_step = misses / K
     hbm_bytes = k * Bexp                       # expert bytes the kernels read per step
     link_bytes = miss_per_step * Bexp           # miss bytes over the host link per step
@@ -426,10 +434,7 @@ def run_ours(args) -> None:
             cache.step_host(0, lg_t, x_t, out_t, stream)
         e1.record(stream)
     stream.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = world * Ke / (float(e2e_ms.item()) * 1e-3)
+    e2e_value, _ = job_rate(e0.elapsed_time(e1), Ke, world, "cuda")
 
     # cold: the first steps from an empty ring (the same routing stream), one
     # graph, after the steady-state measurement
