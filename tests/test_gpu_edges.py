@@ -12,7 +12,9 @@
 
 Each runs from an empty ring against the oracle (trace bit for bit, outputs
 within max |d|/max|ref| <= 2e-2 and mean |d| <= 1e-3), and the wide case
-also cached against all-resident, bit for bit.
+also cached against all-resident, bit for bit.  The multi-row cached path at
+its row-count ends: 2 rows, and 16 (the most a cached step takes) on a ring
+large enough that no step bypasses.
 """
 import dataclasses
 
@@ -21,7 +23,8 @@ import pytest
 import torch
 
 import workload
-from harness import Banks, make_cache
+from harness import (Banks, assert_within_tolerance, check_record_against_sim, make_cache,
+                     record_ids)
 from test_gpu_decode import _check_trace_and_outputs, _run_outputs
 
 pytestmark = pytest.mark.gpu
@@ -84,3 +87,40 @@ def test_wide_inter_cached_equals_all_resident_bitwise(lib):
     banks.close()
     for t, (x, y) in enumerate(zip(outs_a, outs_b)):
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32)), f"step {t}"
+
+
+@pytest.mark.parametrize("rows,slots", [(2, 4), (16, 16)])
+def test_multirow_row_count_edges(lib, orc, rows, slots):
+    cfg = dataclasses.replace(TINY, name=f"rows{rows}", slots=slots, rows=rows, steps=24,
+                              seed=9)
+    banks = Banks(cfg)
+    cache = make_cache(cfg, banks, trace_capacity=cfg.steps)
+    rt = workload.Routing(cfg)
+    xs = workload.activations(cfg.seed, 0, cfg.steps, rows, cfg.hidden)
+    sim = orc.LRUSim(cfg.experts, cfg.slots)
+    w, s, g = banks.layer_arrays(0)
+    lg_d = torch.empty((rows, cfg.experts), dtype=torch.float32, device="cuda")
+    x_d = torch.empty((rows, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    out_d = torch.empty((rows, cfg.hidden), dtype=torch.float32, device="cuda")
+    ids_ref, worst = [], {}
+    for t in range(cfg.steps):
+        lg = rt.step(rows)
+        lg_d.copy_(torch.from_numpy(np.ascontiguousarray(lg)))
+        x_d.copy_(torch.from_numpy(np.ascontiguousarray(xs[t]).view(np.int16)).view(torch.bfloat16))
+        cache.step(0, lg_d, x_d, out_d)
+        ref, ids, _, _ = orc.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
+                                      lg, xs[t])
+        m = assert_within_tolerance(out_d.cpu().numpy(), ref, f"rows {rows} step {t}")
+        worst = {k: max(worst.get(k, 0.0), v) for k, v in m.items()}
+        ids_ref.append(ids)
+    print(f"rows {rows} worst", worst)
+    for t, rec in enumerate(cache.trace(0)):
+        assert np.array_equal(record_ids(rec, rows, cfg.top_k), ids_ref[t]), f"ids step {t}"
+        sr = sim.step(ids_ref[t].ravel())
+        assert not sr["bypass"]  # the union always fits the ring: the cached path ran
+        check_record_against_sim(rec, sr, rows, cfg.top_k)
+    st = cache.stats(0)
+    assert st["misses"] == sim.stats["misses"] > 0 and st["hits"] == sim.stats["hits"]
+    assert st["bypass_calls"] == 0 and st["error_flags"] == 0
+    cache.close()
+    banks.close()
