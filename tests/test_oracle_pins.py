@@ -281,6 +281,31 @@ def test_moe_rows_special_cases(orc):
     assert np.allclose(o1, o2, rtol=1e-12, atol=1e-12) and np.allclose(o1[0], y0, rtol=1e-12, atol=1e-12)
 
 
+def test_moe_rows_rank_weights_pair_with_their_experts(orc):
+    """Two constant experts whose outputs differ only in their down codes
+    (-1.0 and 2.0), routed with logits (ln 3, 0): weights 3/4 and 1/4 by the
+    router's closed form, so the layer is (3/4 d_first + 1/4 d_second) times
+    the shared FFN value, in both routing orders."""
+    H, I, E = 64, 32, 2
+    wa, sa = _const_expert(H, I, 2, 3, 0xA)   # gate 1.0, up 1.5, down -1.0
+    wb, sb = _const_expert(H, I, 2, 3, 0x4)   # gate 1.0, up 1.5, down 2.0
+    w, s = np.concatenate([wa, wb]), np.concatenate([sa, sb])
+    gs = np.tile(np.array([[0.5, 0.25, 2.0]], np.float32), (E, 1))
+    x = workload.to_bf16_bits(np.linspace(-0.4, 0.9, H, dtype=np.float32)[None, :])
+    S = sum(orc.bf16(int(b)) for b in x[0])
+    g, u = 1.0 * 0.5 * S, 1.5 * 0.25 * S
+    ffn = 2.0 * I * (g / (1 + math.exp(-g)) * u)   # y_e = d_e * ffn for each output
+    for lg, first, d in (([math.log(3.0), 0.0], 0, (-1.0, 2.0)),
+                         ([0.0, math.log(3.0)], 1, (2.0, -1.0))):
+        out, ids, wts, _ = orc.moe_rows(w, s, gs, E, H, I, 2, np.array([lg], np.float32), x)
+        assert ids[0, 0] == first
+        assert np.allclose(wts[0], [0.75, 0.25], rtol=1e-6)
+        # the logit ln 3 is rounded to fp32, so the weights are 3/4 only to ~1e-7
+        expect = (wts[0, 0] * d[0] + wts[0, 1] * d[1]) * ffn
+        assert np.allclose(out[0], expect, rtol=1e-12, atol=1e-12)
+        assert np.allclose(out[0], (0.75 * d[0] + 0.25 * d[1]) * ffn, rtol=1e-6)
+
+
 # ---------------------------------------------------------------- LRU trace
 
 def test_lru_hand_computed_trace(orc):
