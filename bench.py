@@ -428,12 +428,17 @@ def run_ours(args) -> None:
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # the step's buffers exist before its call, as a caller's would
     bufs = [(lg_h[t], x_h[t], out_h[t]) for t in range(Ke)]
+    se0 = cache.stats(0)
     with torch.cuda.stream(stream):
         e0.record(stream)
+        h0 = time.perf_counter()
         for lg_t, x_t, out_t in bufs:
             cache.step_host(0, lg_t, x_t, out_t, stream)
+        h1 = time.perf_counter()
         e1.record(stream)
     stream.synchronize()
+    e2e_host_us = 1e6 * (h1 - h0) / Ke  # host time a call spends enqueueing (copies + step)
+    e2e_miss = (cache.stats(0)["misses"] - se0["misses"]) / Ke
     e2e_value, _ = job_rate(e0.elapsed_time(e1), Ke, world, "cuda")
 
     # cold: the first steps from an empty ring (the same routing stream), one
@@ -485,7 +490,9 @@ def run_ours(args) -> None:
                               "hit_rate": hits / picks if picks else None},
             "roofline": roofline, "kernels": kern, "timing_split": timing_split, "cold": cold,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": E * 4 + H * 2,
+            "e2e": {"value": e2e_value, "unit": UNIT, "host_us_per_call": e2e_host_us,
+                    "misses_per_step": e2e_miss,
+                    "h2d_bytes_per_step": E * 4 + H * 2,
                     "d2h_bytes_per_step": H * 4, "steps": Ke},
             "gpu_launches": K * 5, "clocks": clocks,
         }
