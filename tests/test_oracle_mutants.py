@@ -54,7 +54,14 @@ MUTANTS = {
                           "  for (int e = E - 1; e >= 0; --e) {\n    if (!inU[e] || map[e] >= 0) continue;\n"
                           "    int best = -1;", False),
     "bypass_at_S": ("if (nU > S) {", "if (nU >= S) {", True),
-    "hits_not_restamped": ("      used[v] = 1;\n      stamp[v] = t;", "      used[v] = 1;", False),
+    "gate_gscale_of_up": ("orc_nvfp4_matvec(w_e, s_e, (double)gs3[0], I, H, x, g);",
+                          "orc_nvfp4_matvec(w_e, s_e, (double)gs3[1], I, H, x, g);", False),
+    "softmax_over_all_E": ("for (int j = 0; j < k; ++j) w[j] /= sum;",
+                           "{ double se = 0.0; for (int e2 = 0; e2 < E; ++e2) se += "
+                           "isnan(logits[e2]) ? 0.0 : exp((double)logits[e2] - lmax); "
+                           "for (int j = 0; j < k; ++j) w[j] /= se; (void)sum; }", False),
+    "max_not_subtracted": ("w[j] = (l == lmax) ? 1.0 : exp(l - lmax);", "w[j] = exp(l);", False),
+    "hits_not_restamped":("      used[v] = 1;\n      stamp[v] = t;", "      used[v] = 1;", False),
     "nan_ranks_first": ("    if (na && nb) return a < b;\n    return nb;",
                         "    if (na && nb) return a < b;\n    return na;", False),
     "list_victim_recent_end": ("    for (int pos = 0; pos < S; ++pos) {\n      if (!used[order[pos]]) {",
