@@ -4,17 +4,24 @@ One step = one layer-step of the whole hot path (route + remap/LRU, miss copy
 over the host link, NVFP4 gate/up + SwiGLU, down + combine) on one row, GLM
 shape (hidden 6144, inter 2048, 256 experts, top-8, 128 slots), seeded
 synthetic routing (Zipf(1.1) popularity, ~0.27 step-to-step overlap) and
-weights.  The cache is warmed to steady state first; each timed step routes a
-fresh row, so misses are real and counted.
+weights.  The cache is warmed to steady state first (300 eager steps); every
+timed step then routes a row no earlier step has seen, so misses are real and
+counted, whatever K is.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+                  [--workload glm|flash|sweep|multirow|prefill]
 
-Our arm: inputs resident in HBM, the K steps captured as CUDA graphs and
-replayed; per-kernel times come from event-record nodes in the last graph of
-the timed region.  N > 1 (torchrun): independent replicas, one per GPU
-("replicas only": the layer has no exchange step), value = all ranks' steps /
-max time.  The reference arm (--impl reference) times the CPU oracle as it
-stands on a bounded sample of the same workload.
+Our arm: the per-step inputs are resident in HBM; a CUDA graph of a few steps
+is captured once, and its first node (moe_feed_inputs, a device step cursor)
+copies the next step's logits and x into the fixed buffers the step reads, so
+every replay runs on fresh inputs.  The plain graph (programmatic launches on)
+is timed in 5 runs of K steps each; the value is the median run.  Per-kernel
+times come from an event-instrumented graph on further fresh steps after the
+timed runs, and the end-to-end leg (moe_cache_step_host with pinned host
+buffers) runs on steps after those.  N > 1 (torchrun): independent replicas,
+one per GPU ("replicas only": the layer has no exchange step), value = all
+ranks' steps / max time.  The reference arm (--impl reference) times the CPU
+oracle as it stands on the same workload.
 """
 from __future__ import annotations
 
@@ -182,6 +189,11 @@ def oracle_sampled_step(cfg, banks, sim, rt, x, frac: float) -> float:
 
 
 def run_reference(args) -> None:
+    """The CPU oracle as it stands, single-threaded, on the glm workload.  Every
+    step is the oracle's full layer-step (route, LRU, the k experts' NVFP4 FFN in
+    double, combine) when warm-up + steps fit in about three minutes at ~2.7 s a
+    step; otherwise each step runs the FFN on a fraction of every matrix's rows
+    and its time is scaled to a full step (the line then says "extrapolated")."""
     import workload
     from harness import Banks
     rank = int(os.environ.get("RANK", "0"))
@@ -192,25 +204,44 @@ def run_reference(args) -> None:
     banks = Banks(cfg, pinned=False)  # the oracle reads the bytes on the CPU only
     rt = workload.Routing(cfg)
     sim = oracle.LRUSim(cfg.experts, cfg.slots, check_list=False)
-    # size the per-step sample so warmup + steps take about a minute
-    budget_s = 60.0
-    full_step_s = 7.0
-    frac = min(1.0, max(1.0 / 2048, budget_s / (full_step_s * (args.steps + args.warmup))))
-    xs = workload.activations(cfg.seed, 0, 1, 1, cfg.hidden)
-    for _ in range(args.warmup):
-        oracle_sampled_step(cfg, banks, sim, rt, xs[0], frac)
-    t = [oracle_sampled_step(cfg, banks, sim, rt, xs[0], frac) for _ in range(args.steps)]
+    n = args.steps + args.warmup
+    full = n * 2.7 <= 180.0
+    xs = workload.activations(cfg.seed, 0, n, 1, cfg.hidden)
+    w, s, g = banks.layer_arrays(0)
+
+    def full_step(i):
+        t0 = time.perf_counter()
+        lg = rt.step()
+        _, ids, _, _ = oracle.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
+                                       lg, xs[i])
+        sim.step(ids)
+        return time.perf_counter() - t0
+
+    frac = 1.0
+    if full:
+        for i in range(args.warmup):
+            full_step(i)
+        t = [full_step(args.warmup + i) for i in range(args.steps)]
+        sample = "every step in full: route, LRU, 8 experts x 3 NVFP4 matvecs in double, combine"
+    else:
+        frac = min(1.0, max(1.0 / 2048, 60.0 / (7.0 * n)))
+        for i in range(args.warmup):
+            oracle_sampled_step(cfg, banks, sim, rt, xs[i], frac)
+        t = [oracle_sampled_step(cfg, banks, sim, rt, xs[args.warmup + i], frac)
+             for i in range(args.steps)]
+        sample = (f"per step: route + LRU in full, expert FFN on {frac:.5f} of each matrix's "
+                  "rows, time scaled to a full layer-step")
     sec = float(np.sum(t))
     value = args.steps / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
+            "data": "synthetic", "extrapolated": not full,
             "config": {"workload": "glm-layer M=1 S=128 (hidden 6144, inter 2048, 256 experts, top-8)",
                        "global_batch": 1, "parallelism": "cpu oracle, 1 thread"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"per step: route + LRU in full, expert FFN on {frac:.5f} "
-                                       "of each matrix's rows, time scaled to a full layer-step"},
+                             "sample": sample, "extrapolated": not full,
+                             "fraction_of_rows_computed": frac},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     banks.close()
@@ -218,7 +249,55 @@ def run_reference(args) -> None:
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args) -> None:
+RUNS = 5  # timed runs of K rounds each, over distinct fresh rounds; the median is reported
+
+
+class Feeder:
+    """Seeded per-round inputs held in device memory, the fixed buffers a captured
+    round reads, and the device step cursor (moe_feed_inputs) that copies the next
+    round's inputs into those buffers as the round's first node, so one graph
+    replays over rounds it has never seen."""
+
+    def __init__(self, lgs: np.ndarray, xs: np.ndarray):
+        import torch
+        # lgs: fp32 [T, L, E]; xs: bf16 bits [T, L, H]
+        self.T = lgs.shape[0]
+        self.lg_tr = torch.from_numpy(np.ascontiguousarray(lgs, np.float32)).cuda()
+        self.x_tr = torch.from_numpy(np.ascontiguousarray(xs).view(np.int16)).cuda()
+        self.lg = torch.empty_like(self.lg_tr[0])
+        self.x = torch.empty_like(self.x_tr[0]).view(torch.bfloat16)
+        self.cursor = torch.zeros(2, dtype=torch.int32, device="cuda")
+
+    def feed(self, stream) -> None:
+        from hbm_slot_cache_gb300 import _lib
+        _lib.moe_feed_inputs(self.lg_tr.data_ptr(), self.x_tr.data_ptr(),
+                             self.lg.numel() * 4, self.x.numel() * 2, self.T,
+                             self.lg.data_ptr(), self.x.data_ptr(), self.cursor.data_ptr(),
+                             stream.cuda_stream)
+
+    def position(self) -> int:
+        return int(self.cursor[0].item())
+
+    def seek(self, t: int) -> None:
+        import torch
+        torch.cuda.synchronize()
+        self.cursor.zero_()
+        self.cursor[0] = t
+        torch.cuda.synchronize()
+
+
+def decode_bench(cfg, *, layers: int, slots: int, K: int, W: int, prewarm: int,
+                 ev_rounds: int, e2e_rounds: int, cold_rounds: int, world: int, rank: int,
+                 banks=None, seed_layers_from: int = 0) -> dict:
+    """One-row decode rounds (each round steps `layers` layers once) of config `cfg`
+    with `slots` slots a layer.  Every timed round consumes fresh inputs.
+
+    Sequence: `prewarm` eager rounds from an empty ring (steady state), W warm-up
+    rounds through the graphs, RUNS timed runs of K rounds (the plain graph with
+    programmatic launches; the value is the median run), then, on further fresh
+    rounds, an event-instrumented graph for per-kernel times, the end-to-end leg
+    through moe_cache_step_host with pinned host buffers, and a cold start (the
+    first rounds again from an empty ring).  Returns the measurements."""
     import torch
     import torch.distributed as dist
 
@@ -226,153 +305,228 @@ def run_ours(args) -> None:
     from harness import Banks, make_cache
     import hbm_slot_cache_gb300 as hsc
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    hsc.build()
-
-    cfg = workload.CONFIGS["glm"]
-    E, H, k = cfg.experts, cfg.hidden, cfg.top_k
-    banks = Banks(cfg)
-    cache = make_cache(cfg, banks, layers=1, trace_capacity=200)
-    prewarm = 64
-    W, K = args.warmup, args.steps
-    G = min(K, 200)  # steps in the final (event-instrumented) graph
-    total = prewarm + W + K
-    rt = workload.Routing(cfg)
-    lgs = np.stack([rt.step() for _ in range(total)])                 # [T, 1, E]
-    xs = workload.activations(cfg.seed, 0, total, 1, H)               # [T, 1, H] bf16 bits
-    lg_d = torch.from_numpy(lgs).cuda()
-    x_d = torch.from_numpy(xs.view(np.int16)).cuda().view(torch.bfloat16)
-    out_d = torch.empty((1, H), dtype=torch.float32, device="cuda")
+    E, H, I, k, L = cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, layers
+    own_banks = banks is None
+    if own_banks:
+        banks = Banks(cfg)
+    cache = make_cache(cfg, banks, layers=L, slots=slots, trace_capacity=max(ev_rounds, 8))
+    B = max(1, min(10, W - 1))            # rounds in the multi-round graph
+    T_dev = prewarm + W + RUNS * K + ev_rounds
+    T = T_dev + e2e_rounds
+    rts = [workload.Routing(cfg, layer=seed_layers_from + l) for l in range(L)]
+    lgs = np.empty((T, L, E), np.float32)
+    for t in range(T):
+        for l in range(L):
+            lgs[t, l] = rts[l].step(1)[0]
+    xs = np.stack([workload.activations(cfg.seed, seed_layers_from + l, T, 1, H)[:, 0]
+                   for l in range(L)], axis=1)                      # [T, L, H] bf16 bits
+    fd = Feeder(lgs[:T_dev], xs[:T_dev])
+    out = torch.empty((L, 1, H), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
+    evs = None
 
-    def steps_on(t0, t1):
-        for t in range(t0, t1):
-            cache.step(0, lg_d[t], x_d[t], out_d)
+    def one_round(with_events=False, r=0):
+        fd.feed(stream)
+        for l in range(L):
+            if with_events:
+                hsc.moe_cache_set_timing_events(cache.h, [e.cuda_event for e in evs[r * L + l]])
+            cache.step(l, fd.lg[l:l + 1], fd.x[l:l + 1], out[l], stream)
+        if with_events:
+            hsc.moe_cache_set_timing_events(cache.h, None)
 
-    with torch.cuda.stream(stream):
-        steps_on(0, prewarm)                      # fill the ring to steady state (eager)
-    stream.synchronize()
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(G)]
-    for row in evs:
-        for e in row:
-            e.record(stream)                      # materialise the event handles
-    stream.synchronize()
-
-    def capture(t0, t1, with_events=False):
+    def capture(n, with_events=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for t in range(t0, t1):
-                if with_events:
-                    hsc.moe_cache_set_timing_events(cache.h, [e.cuda_event for e in evs[t - t0]])
-                cache.step(0, lg_d[t], x_d[t], out_d)
-            hsc.moe_cache_set_timing_events(cache.h, None)
+            for r in range(n):
+                one_round(with_events, r)
         return g
 
-    t_w = prewarm + W
-    g_warm = capture(prewarm, t_w)
-    g_main = capture(t_w, t_w + K - G) if K > G else None
-    g_ev = capture(t_w + K - G, t_w + K, with_events=True)
+    def replay(g1, gB, n):
+        for _ in range(n // B):
+            gB.replay()
+        for _ in range(n % B):
+            g1.replay()
 
-    # Warm-up: the W-step graph, then one untimed pass of each timed graph (a
-    # graph's first launch uploads it; the timed replays are the second).
     with torch.cuda.stream(stream):
-        g_warm.replay()
-        if g_main is not None:
-            g_main.replay()
-        g_ev.replay()
+        for _ in range(prewarm):           # eager: fills the rings to steady state
+            one_round()
     stream.synchronize()
-    s0 = cache.stats(0)
+    g1, gB = capture(1), capture(B)
+    with torch.cuda.stream(stream):       # warm-up: uploads both graphs (W = B + (W - B))
+        gB.replay()
+        for _ in range(W - B):
+            g1.replay()
+    stream.synchronize()
+    assert fd.position() == prewarm + W, fd.position()
 
     uuid = None
     try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
     except Exception:
         pass
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    s0 = cache.stats(-1)
     sampler = ClockSampler(uuid)
     time.sleep(0.15)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    mid = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        if g_main is not None:
-            g_main.replay()
-        mid.record(stream)
-        g_ev.replay()
-        end.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    run_ms = []
+    for _ in range(RUNS):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            replay(g1, gB, K)
+            b.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        run_ms.append(a.elapsed_time(b))
     clocks = sampler.stop()
-    value, ms_total_max = job_rate(start.elapsed_time(end), K, world, "cuda")
-    s1 = cache.stats(0)
-    misses = s1["misses"] - s0["misses"]
-    hits = s1["hits"] - s0["hits"]
-    picks = s1["picks"] - s0["picks"]
+    s1 = cache.stats(-1)
     assert s1["error_flags"] == 0, s1
+    rates = [job_rate(ms, K * L, world, "cuda") for ms in run_ms]   # (units/s, max ms)
+    order = np.argsort([r[1] for r in rates])
+    med = rates[order[len(order) // 2]]
+    ls = RUNS * K * L
+    misses = (s1["misses"] - s0["misses"]) / ls
+    hits, picks = s1["hits"] - s0["hits"], s1["picks"] - s0["picks"]
 
-    # per-kernel times over the instrumented graph (last G steps of the timed
-    # region); per-step hit/miss counts from the cache's trace ring
-    recs = cache.trace(0)[-G:]
-    n_miss = np.array([r.n_miss for r in recs], np.float64)
-    n_hit = k - n_miss
+    # per-kernel times: an event-instrumented graph over fresh rounds (events
+    # between kernels break programmatic launch, so this graph is slower)
+    nev = ev_rounds * L
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(hsc._lib.MOE_TIMING_EVENTS)]
+           for _ in range(nev)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
+    g_ev = capture(ev_rounds, with_events=True)
+    with torch.cuda.stream(stream):
+        g_ev.replay()
+    stream.synchronize()
     ev_ms = np.array([[row[0].elapsed_time(row[i]) for i in range(8)] for row in evs])
-    t_route = ev_ms[:, 1]
-    t_rt = ev_ms[:, 3] - ev_ms[:, 2]        # missed picks: read-through pass (link + gate/up)
-    t_dn_miss = ev_ms[:, 4] - ev_ms[:, 3]   # missed picks: down from their slots
-    t_gu_hit = ev_ms[:, 5] - ev_ms[:, 1]    # resident picks: gate/up from HBM slots
-    t_dn_hit = ev_ms[:, 6] - ev_ms[:, 5]    # resident picks: down (+ combine if last)
-    gap_ms = sum(evs[t][7].elapsed_time(evs[t + 1][0]) for t in range(G - 1)) / max(G - 1, 1)
-    timing_split = {"ms_per_step_plain_graph": start.elapsed_time(mid) / (K - G) if K > G else None,
-                    "ms_per_step_event_graph": mid.elapsed_time(end) / G,
-                    "ms_between_steps": gap_ms,
-                    "ms_miss_path": float(np.mean(ev_ms[:, 4] - ev_ms[:, 1])),
-                    "ms_hit_path": float(np.mean(ev_ms[:, 6] - ev_ms[:, 1])),
-                    "ms_route": float(np.mean(t_route)),
-                    "ms_step_with_miss": float(np.mean(ev_ms[n_miss > 0, 7])) if (n_miss > 0).any() else None,
-                    "ms_step_no_miss": float(np.mean(ev_ms[n_miss == 0, 7])) if (n_miss == 0).any() else None,
-                    "frac_steps_with_miss": float(np.mean(n_miss > 0)),
-                    "no_miss_breakdown_ms": _breakdown(ev_ms[n_miss == 0]),
-                    "with_miss_breakdown_ms": _breakdown(ev_ms[n_miss > 0])}
+    recs = []
+    for l in range(L):
+        recs.append(cache.trace(l)[-ev_rounds:])
+    n_miss = np.array([recs[l][r].n_miss for r in range(ev_rounds) for l in range(L)], np.float64)
+    del g_ev
 
-    # host-link bandwidth probed in the same session
+    # end to end through the public API on further fresh rounds: moe_cache_step_host
+    # with pinned host buffers (H2D of logits and x, the step, D2H of out), every
+    # layer-step inside the timed region
+    e2e = None
+    if e2e_rounds > 0:
+        lg_h = torch.from_numpy(lgs[T_dev:].copy()).pin_memory()
+        x_h = torch.from_numpy(xs[T_dev:].view(np.int16).copy()).pin_memory().view(torch.bfloat16)
+        out_h = torch.empty((e2e_rounds, L, 1, H), dtype=torch.float32).pin_memory()
+        bufs = [(l, lg_h[t, l:l + 1], x_h[t, l:l + 1], out_h[t, l])
+                for t in range(e2e_rounds) for l in range(L)]
+        with torch.cuda.stream(stream):   # untimed: each layer's eager step, then its capture
+            for l, lg_t, x_t, o_t in bufs[:2 * L]:
+                cache.step_host(l, lg_t, x_t, o_t, stream)
+        stream.synchronize()
+        bufs = bufs[2 * L:]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        se0 = cache.stats(-1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            h0 = time.perf_counter()
+            for l, lg_t, x_t, o_t in bufs:
+                cache.step_host(l, lg_t, x_t, o_t, stream)
+            h1 = time.perf_counter()
+            e1.record(stream)
+        stream.synchronize()
+        n = len(bufs)
+        e2e_value, _ = job_rate(e0.elapsed_time(e1), n, world, "cuda")
+        e2e = {"value": e2e_value, "unit": UNIT, "host_us_per_call": 1e6 * (h1 - h0) / n,
+               "misses_per_step": (cache.stats(-1)["misses"] - se0["misses"]) / n,
+               "h2d_bytes_per_step": E * 4 + H * 2, "d2h_bytes_per_step": H * 4, "steps": n,
+               "note": "fresh rounds after the device-resident ones; pinned host buffers"}
+
+    # cold: the first rounds again from an empty ring, through the same graphs
+    cold = None
+    if cold_rounds > 0:
+        cache.reset()
+        fd.seek(0)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            c0.record(stream)
+            replay(g1, gB, cold_rounds)
+            c1.record(stream)
+        stream.synchronize()
+        sc = cache.stats(-1)
+        cold = {"value": cold_rounds * L / (c0.elapsed_time(c1) * 1e-3), "unit": UNIT,
+                "rounds": cold_rounds, "misses_per_step": sc["misses"] / (cold_rounds * L),
+                "note": "rounds 0..n from an empty ring, the same graphs (the value is steady "
+                        f"state after a {prewarm}-round pre-warm)"}
+    del g1, gB
+    cache.close()
+    if own_banks:
+        banks.close()
+    return {"run_ms": run_ms, "value": med[0], "ms_total": med[1], "misses_per_step": misses,
+            "hit_rate": hits / picks if picks else None, "clocks": clocks, "ev_ms": ev_ms,
+            "ev_n_miss": n_miss, "e2e": e2e, "cold": cold, "K": K, "L": L, "B": B,
+            "Bexp": banks.Bw + banks.Bs}
+
+
+def link_probe() -> tuple[float, float]:
+    """Host-link bandwidth in the same session: SM 16-byte loads and cudaMemcpyAsync,
+    1 GiB pinned -> HBM, best of 5 each."""
+    import torch
     from hbm_slot_cache_gb300 import HostBank, moe_probe_host_link
     nb = 1 << 30
     hb = HostBank(nb)
     hb.array[::4096] = 1
     dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
-    link_sm = moe_probe_host_link(hb.ptr, dst.data_ptr(), nb, 0, 5)
-    link_ce = moe_probe_host_link(hb.ptr, dst.data_ptr(), nb, 1, 5)
-    del dst
-    hb.close()
-    link_peak = max(link_sm, link_ce)
-    hbm_peak, hbm_src = _peaks()
+    try:
+        return (moe_probe_host_link(hb.ptr, dst.data_ptr(), nb, 0, 5),
+                moe_probe_host_link(hb.ptr, dst.data_ptr(), nb, 1, 5))
+    finally:
+        del dst
+        hb.close()
 
-    Bexp = banks.Bw + banks.Bs
-    ms_step = ms_total_max / K
-    miss_per_step = misses / K
-    hbm_bytes = k * Bexp                       # expert bytes the kernels read per step
-    link_bytes = miss_per_step * Bexp           # miss bytes over the host link per step
-    t_roof_s = hbm_bytes / (hbm_peak * 1e9) + link_bytes / (link_peak * 1e9)
-    path_frac = t_roof_s / (ms_step * 1e-3)
-    # with the miss path overlapped and read through, a step is bound by the
-    # larger of its hit bytes over HBM and its miss bytes over the host link
-    t_max_s = float(np.mean(np.maximum(n_hit * Bexp / (hbm_peak * 1e9),
-                                       n_miss * Bexp / (link_peak * 1e9))))
 
-    # kernel rooflines: algorithmic bytes of the launch / its measured time,
-    # summed over the instrumented steps
-    gu_pick = 2 * cfg.inter * (H // 2 + H // 16)   # gate/up bytes of one pick
-    dn_pick = H * (cfg.inter // 2 + cfg.inter // 16)
+def roofline_terms(cfg, res: dict, hbm_peak: float, link_peak: float) -> dict:
+    """Serial path roofline of the timed rounds (k experts' bytes over HBM + the
+    counted miss bytes over the host link, per layer-step) and the overlapped
+    bound over the instrumented layer-steps."""
+    k, Bexp = cfg.top_k, res["Bexp"]
+    ms_step = res["ms_total"] / (res["K"] * res["L"])
+    hbm_bytes = k * Bexp
+    link_bytes = res["misses_per_step"] * Bexp
+    t_roof = hbm_bytes / (hbm_peak * 1e9) + link_bytes / (link_peak * 1e9)
+    nm = res["ev_n_miss"]
+    t_max = float(np.mean(np.maximum((k - nm) * Bexp / (hbm_peak * 1e9),
+                                     nm * Bexp / (link_peak * 1e9))))
+    return {"frac": t_roof / (ms_step * 1e-3), "t_roofline_us": t_roof * 1e6,
+            "t_measured_us": ms_step * 1e3, "hbm_bytes_per_step": hbm_bytes,
+            "link_bytes_per_step": link_bytes, "hbm_peak_gbs": hbm_peak,
+            "link_peak_gbs": link_peak, "misses_per_step": res["misses_per_step"],
+            "hit_rate": res["hit_rate"],
+            "overlapped_bound": {"t_us": t_max * 1e6, "frac": t_max / (ms_step * 1e-3),
+                                 "note": "mean over the instrumented steps of max(hit bytes / "
+                                         "HBM peak, miss bytes / link peak)"}}
+
+
+def kernel_table(cfg, res: dict, hbm_peak: float, link_peak: float) -> tuple[dict, dict]:
+    """Per-kernel rooflines from the event-instrumented layer-steps: algorithmic
+    bytes of each launch over its event-timed duration."""
+    H, I, k, Bexp = cfg.hidden, cfg.inter, cfg.top_k, res["Bexp"]
+    ev, n_miss = res["ev_ms"], res["ev_n_miss"]
+    n_hit = k - n_miss
+    G = len(ev)
+    t_route = ev[:, 1]
+    t_rt = ev[:, 3] - ev[:, 2]
+    t_dn_miss = ev[:, 4] - ev[:, 3]
+    t_gu_hit = ev[:, 5] - ev[:, 1]
+    t_dn_hit = ev[:, 6] - ev[:, 5]
+    gu_pick = 2 * I * (H // 2 + H // 16)
+    dn_pick = H * (I // 2 + I // 16)
+
     def entry(bytes_total, ms_total, peak, bound, launches):
         ach = bytes_total / (ms_total * 1e-3) / 1e9 if ms_total > 0 else None
         return {"bound": bound, "achieved": ach, "peak": peak, "unit": "GB/s",
@@ -403,71 +557,67 @@ def run_ours(args) -> None:
         "; whole missed experts over the host link, gate/up computed on the way in, "
         "written to their slots")
     kern["gemv_down[missed picks]"]["note"] += "; W2 rows read back from the slots just written"
+    split = {"ms_per_step_event_graph": float(ev[:, 7].mean()),
+             "ms_miss_path": float(np.mean(ev[:, 4] - ev[:, 1])),
+             "ms_hit_path": float(np.mean(ev[:, 6] - ev[:, 1])),
+             "ms_route": float(np.mean(t_route)),
+             "ms_step_with_miss": float(np.mean(ev[hm, 7])) if hm.any() else None,
+             "ms_step_no_miss": float(np.mean(ev[~hm, 7])) if (~hm).any() else None,
+             "frac_steps_with_miss": float(np.mean(hm)),
+             "no_miss_breakdown_ms": _breakdown(ev[~hm]),
+             "with_miss_breakdown_ms": _breakdown(ev[hm]),
+             "instrumented_steps": G}
+    return kern, split
 
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import workload
+    import hbm_slot_cache_gb300 as hsc
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hsc.build()
+    cfg = workload.CONFIGS["glm"]
+    K, W = args.steps, args.warmup
+    res = decode_bench(cfg, layers=1, slots=cfg.slots, K=K, W=W, prewarm=300, ev_rounds=200,
+                       e2e_rounds=min(K, 1000) + 2, cold_rounds=300, world=world, rank=rank)
+    # sanity: the timed rounds must exercise the miss path at S = 128
+    if not 0.3 <= res["misses_per_step"] <= 4.0:
+        raise SystemExit(f"timed rounds saw {res['misses_per_step']:.3f} misses per layer-step at "
+                         f"S={cfg.slots}: outside the workload's band, measurement invalid")
+    link_sm, link_ce = link_probe()
+    link_peak = max(link_sm, link_ce)
+    hbm_peak, hbm_src = _peaks()
+    path = roofline_terms(cfg, res, hbm_peak, link_peak)
+    path.update(hbm_peak_source=hbm_src, link_probe_sm_gbs=link_sm, link_probe_memcpy_gbs=link_ce)
+    kern, split = kernel_table(cfg, res, hbm_peak, link_peak)
+    split["ms_per_step_plain_graph_runs"] = [m / K for m in res["run_ms"]]
+    nm = max(int((res["ev_n_miss"] > 0).sum()), 1)
+    G = len(res["ev_ms"])
     share = {n: v["ms_per_launch"] * (nm if "missed" in n else G) for n, v in kern.items()}
     dom = max(share, key=share.get)
     roofline = dict(kern[dom])
     roofline["kernel"] = dom
     roofline["peak_source"] = (hbm_src if roofline.get("bound") == "hbm"
                                else "moe_probe_host_link, same session (best of SM copy / cudaMemcpyAsync)")
-
-    # end to end through the public API: moe_cache_step_host with pinned host
-    # buffers (H2D of the step's logits and x, the step, D2H of its output,
-    # every step inside the timed region)
-    Ke = min(K, 1000)
-    lg_h = torch.from_numpy(lgs[prewarm:prewarm + Ke].copy()).pin_memory()
-    x_h = torch.from_numpy(xs[prewarm:prewarm + Ke].view(np.int16).copy()).pin_memory().view(torch.bfloat16)
-    out_h = torch.empty((Ke, 1, H), dtype=torch.float32).pin_memory()
-    with torch.cuda.stream(stream):  # untimed: the layer's eager step, then its graph capture
-        for t in range(2):
-            cache.step_host(0, lg_h[t], x_h[t], out_h[t], stream)
-    stream.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # the step's buffers exist before its call, as a caller's would
-    bufs = [(lg_h[t], x_h[t], out_h[t]) for t in range(Ke)]
-    se0 = cache.stats(0)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        h0 = time.perf_counter()
-        for lg_t, x_t, out_t in bufs:
-            cache.step_host(0, lg_t, x_t, out_t, stream)
-        h1 = time.perf_counter()
-        e1.record(stream)
-    stream.synchronize()
-    e2e_host_us = 1e6 * (h1 - h0) / Ke  # host time a call spends enqueueing (copies + step)
-    e2e_miss = (cache.stats(0)["misses"] - se0["misses"]) / Ke
-    e2e_value, _ = job_rate(e0.elapsed_time(e1), Ke, world, "cuda")
-
-    # cold: the first steps from an empty ring (the same routing stream), one
-    # graph, after the steady-state measurement
-    n_cold = min(300, prewarm + W + K)
-    cache.reset()
-    g_cold = capture(0, n_cold)
-    cache.reset()  # capture does not execute; start from empty
-    torch.cuda.synchronize()
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        c0.record(stream)
-        g_cold.replay()
-        c1.record(stream)
-    stream.synchronize()
-    sc = cache.stats(0)
-    cold = {"value": n_cold / (c0.elapsed_time(c1) * 1e-3), "unit": UNIT, "steps": n_cold,
-            "misses_per_step": sc["misses"] / n_cold,
-            "note": "steps 0..n from an empty ring, one CUDA graph (the value above is steady "
-                    "state after a 64-step pre-warm)"}
-    del g_cold
-
+    banks_cpu = None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_layer_steps(cfg, banks, seconds=12.0, max_steps=8)
-
+        from harness import Banks
+        banks_cpu = Banks(cfg, pinned=False)
+        cpu = oracle_layer_steps(cfg, banks_cpu, seconds=12.0, max_steps=8)
+        banks_cpu.close()
     if rank == 0:
+        ms_step = res["ms_total"] / K
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "nvfp4 weights, fp32 accumulate", "data": "synthetic",
             "config": {"workload": "glm-layer M=1 S=128: hidden 6144, inter 2048, 256 experts, "
@@ -475,32 +625,93 @@ def run_ours(args) -> None:
                        "global_batch": world, "seq_len": 1,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2: 170 MB of expert bytes per step > 126 MB L2; "
-                             "2.7 GB slot ring", "graph": "CUDA graphs, eager prewarm of 64 steps"},
-            "tok_s_equivalent": value / GLM_MOE_LAYERS,
-            "path_roofline": {"frac": path_frac, "t_roofline_us": t_roof_s * 1e6,
-                              "t_measured_us": ms_step * 1e3, "hbm_bytes_per_step": hbm_bytes,
-                              "link_bytes_per_step": link_bytes, "hbm_peak_gbs": hbm_peak,
-                              "hbm_peak_source": hbm_src, "link_peak_gbs": link_peak,
-                              "link_probe_sm_gbs": link_sm, "link_probe_memcpy_gbs": link_ce,
-                              "misses_per_step": miss_per_step,
-                              "overlapped_bound": {
-                                  "t_us": t_max_s * 1e6, "frac": t_max_s / (ms_step * 1e-3),
-                                  "note": "mean over the traced steps of max(hit bytes / HBM "
-                                          "peak, miss bytes / link peak)"},
-                              "hit_rate": hits / picks if picks else None},
-            "roofline": roofline, "kernels": kern, "timing_split": timing_split, "cold": cold,
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "host_us_per_call": e2e_host_us,
-                    "misses_per_step": e2e_miss,
-                    "h2d_bytes_per_step": E * 4 + H * 2,
-                    "d2h_bytes_per_step": H * 4, "steps": Ke},
-            "gpu_launches": K * 5, "clocks": clocks,
+                             "2.7 GB slot ring",
+                       "graph": f"one CUDA graph of {res['B']} rounds (and a one-round graph) "
+                                "replayed; its first node feeds each round fresh inputs from a "
+                                "device trace (moe_feed_inputs); programmatic launches on",
+                       "timing": f"{RUNS} runs of K fresh steps each after a 300-step pre-warm; "
+                                 "value = median run"},
+            "tok_s_equivalent": res["value"] / GLM_MOE_LAYERS,
+            "path_roofline": path, "roofline": roofline, "kernels": kern, "timing_split": split,
+            "cold": res["cold"], "cpu_baseline": cpu, "e2e": res["e2e"],
+            "gpu_launches": K * 6, "launches_per_step": "feeder + route/remap + read-through + "
+                                                        "missed down + gate/up + resident down",
+            "clocks": res["clocks"],
         }
         print(json.dumps(line), flush=True)
-    cache.close()
-    banks.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_flash_or_sweep(args) -> None:
+    """The Flash-shaped 16-layer stack, or the GLM slot sweep over S: their own
+    JSON line (not the headline)."""
+    import torch
+
+    import workload
+    import hbm_slot_cache_gb300 as hsc
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    hsc.build()
+    hbm_peak, hbm_src = _peaks()
+    link_sm, link_ce = link_probe()
+    link_peak = max(link_sm, link_ce)
+    W = args.warmup
+    if args.workload == "flash":
+        cfg = workload.CONFIGS["flash"]
+        L = args.layers or cfg.layers
+        K = args.steps
+        res = decode_bench(cfg, layers=L, slots=cfg.slots, K=K, W=W, prewarm=64, ev_rounds=16,
+                           e2e_rounds=0, cold_rounds=0, world=1, rank=0)
+        path = roofline_terms(cfg, res, hbm_peak, link_peak)
+        kern, split = kernel_table(cfg, res, hbm_peak, link_peak)
+        ls = K * L
+        line = {"metric": "Flash-shape MoE decode layer-steps/s (M=1, 16 layers, S=54)",
+                "value": res["value"], "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W,
+                "ms_per_round": res["ms_total"] / K, "higher_is_better": True,
+                "dtype": "nvfp4 weights, fp32 accumulate", "data": "synthetic",
+                "config": {"workload": f"flash stack: {L} layers, hidden 4096, inter 2048, 288 "
+                                       "experts, top-8, S=54 per layer, Zipf(1.05) routing "
+                                       "independent per layer, one host bank aliased by every "
+                                       "layer",
+                           "graph": "one CUDA graph per round of all layers, fed fresh inputs",
+                           "timing": f"{RUNS} runs of K rounds, median"},
+                "tok_s_equivalent": res["value"] / 42, "layer_steps": ls,
+                "path_roofline": path, "kernels": kern, "timing_split": split,
+                "clocks": res["clocks"]}
+    else:
+        from harness import Banks
+        cfg = workload.CONFIGS["prefill"]
+        L = args.layers or cfg.layers
+        K = args.steps
+        per_s = []
+        clocks = []
+        banks = Banks(cfg)
+        for S in workload.SWEEP_SLOTS:
+            res = decode_bench(cfg, layers=L, slots=S, K=K, W=W, prewarm=300, ev_rounds=8,
+                               e2e_rounds=0, cold_rounds=300, world=1, rank=0, banks=banks)
+            path = roofline_terms(cfg, res, hbm_peak, link_peak)
+            per_s.append({"S": S, "layer_steps_per_s": res["value"],
+                          "ms_per_layer_step": res["ms_total"] / (K * L),
+                          "hit_rate": res["hit_rate"], "misses_per_step": res["misses_per_step"],
+                          "path_roofline_frac": path["frac"],
+                          "overlapped_bound_frac": path["overlapped_bound"]["frac"],
+                          "cold": res["cold"]})
+            clocks.append(res["clocks"])
+        line = {"metric": "GLM-shape MoE decode layer-steps/s and hit rate per slot count "
+                          "(M=1, 8 layers)",
+                "value": per_s[[p["S"] for p in per_s].index(128)]["layer_steps_per_s"],
+                "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W, "higher_is_better": True,
+                "dtype": "nvfp4 weights, fp32 accumulate", "data": "synthetic",
+                "config": {"workload": f"slot sweep: {L} layers, GLM shape, Zipf(1.1) routing "
+                                       "independent per layer, S in "
+                                       f"{list(workload.SWEEP_SLOTS)}; value = S=128",
+                           "timing": f"300-round pre-warm, then {RUNS} runs of K fresh rounds, "
+                                     "median; cold = 300 rounds from empty"},
+                "per_slots": per_s, "link_peak_gbs": link_peak, "hbm_peak_gbs": hbm_peak,
+                "clocks": clocks}
+        banks.close()
+    print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------- multi-row / prefill rounds
@@ -644,15 +855,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="glm", choices=["glm", "multirow", "prefill"],
-                    help="glm: the one-row decode step (the headline line); multirow / "
-                         "prefill: M=16 rounds or M=512 bypass, their own line")
-    ap.add_argument("--layers", type=int, default=0, help="multirow/prefill: layers (0: config)")
+    ap.add_argument("--workload", default="glm",
+                    choices=["glm", "flash", "sweep", "multirow", "prefill"],
+                    help="glm: the one-row decode step (the headline line); flash: the "
+                         "16-layer Flash stack; sweep: GLM decode per slot count; multirow / "
+                         "prefill: M=16 rounds or M=512 bypass; each its own line")
+    ap.add_argument("--layers", type=int, default=0, help="non-glm workloads: layers (0: config)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in ("flash", "sweep"):
+        run_flash_or_sweep(args)
     elif args.workload != "glm":
         run_rows(args)
     else:

@@ -35,7 +35,7 @@ EXPORTS = ("moe_cache_create", "moe_cache_step", "moe_cache_step_host", "moe_cac
            "moe_cache_strerror", "moe_expert_bytes", "moe_host_alloc", "moe_host_free",
            "moe_probe_host_link", "moe_cache_set_timing_events", "moe_expert_pass_noalloc",
            "moe_policy_lru", "moe_policy_static", "moe_policy_hybrid", "moe_policy_lru_curve",
-           "moe_policy_size_layers", "moe_cache_layer_slots")
+           "moe_policy_size_layers", "moe_cache_layer_slots", "moe_feed_inputs")
 
 
 class MoeError(RuntimeError):
@@ -115,6 +115,7 @@ def lib() -> ctypes.CDLL:
                                           ctypes.POINTER(ctypes.c_double)]
         L.moe_cache_set_timing_events.argtypes = [P, P]
         L.moe_expert_pass_noalloc.argtypes = [I, I, I, P, P, P, P, P, P, P]
+        L.moe_feed_inputs.argtypes = [P, P, ctypes.c_size_t, ctypes.c_size_t, I, P, P, P, P]
         PR = ctypes.POINTER(PolicyResult)
         L.moe_policy_lru.argtypes = [P, I, I, I, I, PR]
         L.moe_policy_static.argtypes = [P, I, I, I, I, PR]
@@ -250,6 +251,15 @@ def moe_expert_pass_noalloc(k: int, hidden: int, inter: int, expert_w, expert_s,
                                          ctypes.cast(sa, ctypes.c_void_p), g.ctypes.data,
                                          w.ctypes.data, x, out, stream),
            "moe_expert_pass_noalloc")
+
+
+def moe_feed_inputs(logits_trace: int, x_trace: int, logits_bytes: int, x_bytes: int,
+                    steps: int, logits_dst: int, x_dst: int, cursor: int,
+                    stream: int = 0) -> None:
+    """Copy entry cursor[0] mod steps of the device traces into the fixed buffers and
+    advance the device cursor (see the header)."""
+    _check(lib().moe_feed_inputs(logits_trace, x_trace, logits_bytes, x_bytes, steps, logits_dst,
+                                 x_dst, cursor, stream), "moe_feed_inputs")
 
 
 def moe_host_alloc(nbytes: int) -> int:

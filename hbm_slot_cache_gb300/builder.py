@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 SO = os.path.join(PKG, "libmoe_slot_cache.so")
 SOURCES = ["route_remap.cu", "route_rows.cu", "miss_copy.cu", "expert_gemv.cu", "expert_mma.cu",
-           "quantize.cu", "moe_cache.cu", "noalloc.cu", "policy.cu"]
+           "quantize.cu", "moe_cache.cu", "noalloc.cu", "policy.cu",
+           "feed.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

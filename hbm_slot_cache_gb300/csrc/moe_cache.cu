@@ -177,6 +177,27 @@ int device_view(const void* p, const uint8_t** out) {
   return MOE_OK;
 }
 
+// True when every byte of the n-byte scale bank is a finite, non-negative E4M3
+// code: sign bit clear and not the NaN code 0x7F.  The tensor-core path reads
+// block scales as unsigned E4M3, so a sign bit would be read as a different
+// value there than on the CUDA-core path; the check keeps both paths defined
+// alike.  Word-wise (eight bytes at a time), then the tail.
+bool scales_valid(const uint8_t* p, size_t n) {
+  const uint64_t hi = 0x8080808080808080ull, lo = 0x0101010101010101ull;
+  size_t i = 0;
+  if (((uintptr_t)p & 7) == 0) {
+    for (; i + 8 <= n; i += 8) {
+      uint64_t v;
+      std::memcpy(&v, p + i, 8);
+      const uint64_t t = v ^ (0x7Full * lo);  // a zero byte where v has 0x7F
+      if ((v & hi) || ((t - lo) & ~t & hi)) return false;
+    }
+  }
+  for (; i < n; ++i)
+    if ((p[i] & 0x80) || p[i] == 0x7F) return false;
+  return true;
+}
+
 int init_state(moe_cache* h) {
   const size_t LE = (size_t)h->L * h->E, LS = h->slot_off[h->L];
   std::vector<int32_t> map(LE, -1), owner(LS, -1);
@@ -302,6 +323,12 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
       return rc;
     }
     std::memcpy(gs.data() + (size_t)l * experts * 3, hl.gscale, sizeof(float) * experts * 3);
+    bool seen = false;  // layers may share one bank: check each bank once
+    for (int m = 0; m < l && !seen; ++m) seen = host_backing[m].s == hl.s;
+    if (!seen && !scales_valid(static_cast<const uint8_t*>(hl.s), (size_t)experts * h->Bs)) {
+      delete h;
+      return MOE_ERR_ARG;
+    }
   }
   const size_t LS = h->slot_off[layers], LE = (size_t)layers * experts;
   size_t max_picks = (size_t)o.max_rows * top_k;

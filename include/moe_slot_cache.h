@@ -74,6 +74,12 @@ typedef struct moe_cache moe_cache_t; /* opaque, library-owned */
  *     consecutive elements of a row, same row order: [rows][K/16].
  *   gscale[3*e .. 3*e+2]: fp32 global scales (gate, up, down).
  * The weight of row r, element i is e2m1(code) * e4m3(scale) * gscale.
+ * Block scales are non-negative: every scale byte must be a finite E4M3 code
+ * with the sign bit clear (0x00 .. 0x7E; the tensor-core path reads them as
+ * unsigned E4M3).  moe_cache_create reads the scale banks once and returns
+ * MOE_ERR_ARG if a byte has the sign bit set or is the NaN code 0x7F; the
+ * contents must therefore be in place at create and must not change while
+ * the handle lives.
  * w and s must be pinned, mapped host memory (e.g. from moe_host_alloc or
  * cudaHostAlloc with cudaHostAllocMapped), 16-byte aligned, of at least
  * experts*Bw and experts*Bs bytes.  gscale is ordinary host memory, read once
@@ -249,6 +255,31 @@ int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int m
  * NULL stops recording.  The library does not own the events. */
 #define MOE_TIMING_EVENTS 8
 int moe_cache_set_timing_events(moe_cache_t* h, void* const* events);
+
+/* Step-input feeder (a device step cursor).  A decode round is captured once
+ * as a CUDA graph over fixed input buffers ("GLM 5.3 Testing: HBM Expert
+ * Allocation", "What the slot cache is": fixed addresses and shapes make a
+ * round replayable as a graph).  Put this call first in the captured round and
+ * one graph replays over fresh inputs: each call copies entry
+ * t = cursor[0] mod steps of two device-resident input traces into the fixed
+ * buffers the round's steps read, then adds one to cursor[0].
+ *   logits_trace: device, steps entries of logits_bytes each (e.g. fp32
+ *     [layers][rows][experts] per round);
+ *   x_trace: device, steps entries of x_bytes each (e.g. bf16 bits
+ *     [layers][rows][hidden]); NULL with x_bytes == 0 copies logits only
+ *     (and the reverse);
+ *   logits_dst, x_dst: device buffers of one entry each, the addresses the
+ *     captured steps read;
+ *   cursor: device uint32 [2], caller-owned, zero before the first call;
+ *     cursor[0] counts the entries fed (set it to restart the trace at an
+ *     entry), cursor[1] is the launch's own count and must stay zero between
+ *     calls.
+ * Byte counts multiples of 16; every pointer 16-byte aligned (cursor 4-byte).
+ * Enqueues one kernel on `stream` (capturable); calls on one cursor must be
+ * ordered on the device.  Errors: MOE_ERR_ARG, MOE_ERR_CUDA. */
+int moe_feed_inputs(const void* logits_trace, const void* x_trace, size_t logits_bytes,
+                    size_t x_bytes, int steps, void* logits_dst, void* x_dst, uint32_t* cursor,
+                    void* stream);
 
 /* --------------------------------------------------- offline slot policy */
 

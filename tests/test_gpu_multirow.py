@@ -47,13 +47,16 @@ def _oracle_rows(orc, banks, cfg, lg, xb, rows):
     return out
 
 
-def test_tiny_multirow_trace_outputs_and_device_bypass(lib, orc):
-    cfg = workload.CONFIGS["tiny"]
+@pytest.mark.parametrize("name,wide_x", [("tiny", False), ("tiny_wide", False),
+                                         ("tiny_wide", True)])
+def test_tiny_multirow_trace_outputs_and_device_bypass(lib, orc, name, wide_x):
+    cfg = workload.CONFIGS[name]
     M, steps = 4, 40
     banks = Banks(cfg)
     cache = make_cache(cfg, banks, trace_capacity=steps)
     rt = workload.Routing(cfg)
-    xs = workload.activations(cfg.seed, 0, steps, M, cfg.hidden)
+    act = workload.activations_wide if wide_x else workload.activations
+    xs = act(cfg.seed, 0, steps, M, cfg.hidden)
     sim = orc.LRUSim(cfg.experts, cfg.slots)
     lg_d, x_d, out_d = _dev(cfg, M)
     ids_ref, worst = [], {}
@@ -64,10 +67,10 @@ def test_tiny_multirow_trace_outputs_and_device_bypass(lib, orc):
         w, s, g = banks.layer_arrays(0)
         ref, ids, _, _ = orc.moe_rows(w, s, g, cfg.experts, cfg.hidden, cfg.inter, cfg.top_k,
                                       lg, xs[t])
-        m = assert_within_tolerance(out_d.cpu().numpy(), ref, f"step {t}")
+        m = assert_within_tolerance(out_d.cpu().numpy(), ref, f"step {t}", scale_free=wide_x)
         worst = {k: max(worst.get(k, 0.0), v) for k, v in m.items()}
         ids_ref.append(ids)
-    print("tiny multirow worst", worst)
+    print(name, "multirow worst", "(wide x)" if wide_x else "", worst)
     recs = cache.trace(0)
     n_bypass = 0
     for t, rec in enumerate(recs):
@@ -79,6 +82,27 @@ def test_tiny_multirow_trace_outputs_and_device_bypass(lib, orc):
     assert st["misses"] == sim.stats["misses"] and st["hits"] == sim.stats["hits"]
     assert st["bypass_calls"] == sim.stats["bypass"]
     assert 0 < n_bypass < steps      # both the cached and the union > S path ran
+    cache.close()
+    banks.close()
+
+
+def test_glm_multirow_wide_x(lib, orc):
+    """GLM shape, one 16-row round of x with a wide dynamic range (elements up to
+    6e4 and below 1e-5): sampled rows within the scale-free tolerance."""
+    cfg = workload.CONFIGS["multirow"]
+    M = cfg.rows
+    banks = Banks(cfg)
+    cache = make_cache(cfg, banks, layers=1)
+    lg = workload.Routing(cfg).step()
+    xb = workload.activations_wide(cfg.seed, 0, 1, M, cfg.hidden)[0]
+    lg_d, x_d, out_d = _dev(cfg, M)
+    _put(lg_d, x_d, lg, xb)
+    cache.step(0, lg_d, x_d, out_d)
+    rows = [0, 7, 15]
+    ref = _oracle_rows(orc, banks, cfg, lg, xb, rows)
+    print("glm multirow wide x", assert_within_tolerance(out_d.cpu().numpy()[rows], ref,
+                                                          scale_free=True))
+    assert cache.stats(0)["error_flags"] == 0
     cache.close()
     banks.close()
 
@@ -129,9 +153,9 @@ def test_glm_multirow_rounds(lib, orc):
     banks.close()
 
 
-@pytest.mark.parametrize("rows", [17, 64])
-def test_tiny_prefill_bypass(lib, orc, rows):
-    cfg = workload.CONFIGS["tiny"]
+@pytest.mark.parametrize("name,rows", [("tiny", 17), ("tiny", 64), ("tiny_wide", 64)])
+def test_tiny_prefill_bypass(lib, orc, name, rows):
+    cfg = workload.CONFIGS[name]
     banks = Banks(cfg)
     cache = make_cache(cfg, banks)
     # warm the ring with a few decode steps, then bypass
@@ -179,11 +203,12 @@ def test_glm_prefill_bypass_sampled_rows(lib, orc):
     banks.close()
 
 
-def test_tiny_prefill_staged_equals_zero_copy(lib, orc):
+@pytest.mark.parametrize("name", ["tiny", "tiny_wide"])
+def test_tiny_prefill_staged_equals_zero_copy(lib, orc, name):
     """Staged prefill (experts copied into HBM a chunk at a time, two chunks held)
     gives the same bits as reading host memory directly, for chunk sizes that
     cover the union in one chunk, in several, and with a ragged last chunk."""
-    cfg = workload.CONFIGS["tiny"]
+    cfg = workload.CONFIGS[name]
     rows = 64
     banks = Banks(cfg)
     lg = workload.prefill_logits(cfg, 0, rows)
@@ -240,7 +265,7 @@ def test_glm_prefill_staged_graph_and_zero_copy(lib, orc):
     banks.close()
 
 
-@pytest.mark.parametrize("name", ["tiny", "multirow"])
+@pytest.mark.parametrize("name", ["tiny", "tiny_wide", "multirow"])
 def test_batch_invariant_rows(lib, orc, name):
     """Batch-invariant mode: every row of a round (M = 16, cached) is bit-identical
     to the same row stepped alone through another cached handle.  Both handles'
@@ -256,7 +281,7 @@ def test_batch_invariant_rows(lib, orc, name):
     single = make_cache(cfg, banks, layers=1, batch_invariant=True)
     lgM, xM, oM = _dev(cfg, M)
     lg1, x1, o1 = _dev(cfg, 1)
-    rows = range(M) if name == "tiny" else (0, 5, 15)
+    rows = range(M) if name.startswith("tiny") else (0, 5, 15)
     for t in range(steps):
         _put(lgM, xM, lgs[t], xs[t])
         rounds.step(0, lgM, xM, oM)

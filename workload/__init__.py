@@ -23,7 +23,7 @@ import math
 import numpy as np
 
 # purposes for independent random streams
-_P_WEIGHTS, _P_X, _P_ROUTE, _P_PERM, _P_DRAFT = 1, 2, 3, 4, 5
+_P_WEIGHTS, _P_X, _P_ROUTE, _P_PERM, _P_DRAFT, _P_GSCALE, _P_XWIDE = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclasses.dataclass(frozen=True)
@@ -44,11 +44,20 @@ class Config:
     streams: int = 1                   # multi-row rounds: streams x (1 + drafts)
     drafts: int = 0
     draft_shared: int = 0              # ids a draft row keeps from its stream's row 0
+    # scales: "literal" = block scales from the 16 E4M3 codes 0x30..0x3F and every
+    # global scale 1/64 (the tiny configuration as stated); "wide" = block scales
+    # over every finite positive E4M3 code 0x01..0x7E (subnormals included) and a
+    # distinct seeded global scale per (expert, matrix)
+    scales: str = "wide"
 
 
 CONFIGS = {
     # 1 layer, H256/I128, 16 experts, top-2, S=4, 64 steps, N(0,1) + Zipf(1.1) bias
-    "tiny": Config("tiny", 1, 256, 128, 16, 2, 4, 1, 64, 1.1, 0.0, 0, literal_normal_bias=True),
+    "tiny": Config("tiny", 1, 256, 128, 16, 2, 4, 1, 64, 1.1, 0.0, 0, literal_normal_bias=True,
+                   scales="literal"),
+    # the same layer with wide block scales and per-(expert, matrix) global scales
+    "tiny_wide": Config("tiny_wide", 1, 256, 128, 16, 2, 4, 1, 64, 1.1, 0.0, 5,
+                        literal_normal_bias=True),
     # GLM-5.3-shaped layer: H6144/I2048, 256 experts, top-8, S=128, M=1, 300 churn steps
     "glm": Config("glm", 1, 6144, 2048, 256, 8, 128, 1, 300, 1.1, 0.1, 1),
     # Flash-shaped stack: 16 layers, H4096/I2048, 288 experts top-8, S=54, 512 steps
@@ -74,23 +83,43 @@ def rng_for(seed: int, *stream: int) -> np.random.Generator:
 
 
 def fill_bank(w: np.ndarray, s: np.ndarray, experts: int, hidden: int, inter: int,
-              seed: int, layer: int = 0) -> None:
+              seed: int, layer: int = 0, scales: str = "literal") -> None:
     """Fill one layer's expert bank in place.
 
-    Codes: uniform over all 16 nibbles (uniform random bytes).  Scales: uniform
-    over the 16 E4M3 codes 0x30..0x3F (values 0.5 .. 1.875)."""
+    Codes: uniform over all 16 nibbles (uniform random bytes).  Scales
+    ("literal"): uniform over the 16 E4M3 codes 0x30..0x3F (values 0.5 ..
+    1.875); ("wide"): uniform over the 126 finite positive E4M3 codes
+    0x01..0x7E (2^-9 .. 448, subnormals included)."""
     bw, bs = storage_bytes(hidden, inter)
     assert w.size >= experts * bw and s.size >= experts * bs
+    assert scales in ("literal", "wide")
     for e in range(experts):
         r = rng_for(seed, _P_WEIGHTS, layer, e)
         w[e * bw:(e + 1) * bw] = np.frombuffer(r.bytes(bw), np.uint8)
         sb = np.frombuffer(r.bytes(bs), np.uint8)
-        s[e * bs:(e + 1) * bs] = 0x30 | (sb & 0x0F)
+        if scales == "literal":
+            s[e * bs:(e + 1) * bs] = 0x30 | (sb & 0x0F)
+        else:
+            # 0x01 + (16-bit draw mod 126): the bias of the modulus is below 2e-3
+            u = np.frombuffer(r.bytes(2 * bs), np.uint16)
+            s[e * bs:(e + 1) * bs] = (1 + u % 126).astype(np.uint8)
 
 
-def global_scales(experts: int) -> np.ndarray:
-    """fp32 (gate, up, down) global scales per expert: all 1/64."""
-    return np.full((experts, 3), 1.0 / 64.0, np.float32)
+def global_scales(experts: int, scales: str = "literal", seed: int = 0,
+                  layer: int = 0) -> np.ndarray:
+    """fp32 (gate, up, down) global scales per expert.  "literal": all 1/64.
+    "wide": 2^(j - 13) * (1 + u) per (expert, matrix), j uniform in {-1, 0, 1}
+    and u uniform in [0, 1), so the three matrices of an expert, and the
+    experts, all differ; 2^-13 * 1.5 offsets the wide block scales' larger
+    magnitude (RMS ~100 against ~1.16 for the literal codes), keeping the
+    layer's outputs near the literal configuration's scale."""
+    if scales == "literal":
+        return np.full((experts, 3), 1.0 / 64.0, np.float32)
+    assert scales == "wide"
+    r = rng_for(seed, _P_GSCALE, layer)
+    j = r.integers(-1, 2, size=(experts, 3))
+    u = r.random((experts, 3))
+    return (np.ldexp(1.0 + u, j - 13)).astype(np.float32)
 
 
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -104,6 +133,23 @@ def activations(seed: int, layer: int, steps: int, rows: int, hidden: int) -> np
     """bf16 bits [steps, rows, hidden] of N(0,1), fresh every step."""
     r = rng_for(seed, _P_X, layer)
     return to_bf16_bits(r.standard_normal((steps, rows, hidden), dtype=np.float32))
+
+
+def activations_wide(seed: int, layer: int, steps: int, rows: int, hidden: int) -> np.ndarray:
+    """bf16 bits [steps, rows, hidden]: N(0,1) with, in every row, 4 elements of
+    magnitude U(1e3, 4e3), 2 of magnitude U(3.3e4, 6e4) (above the f16 range's
+    half, so a kernel that holds x in f16 must rescale the row) and 4 of
+    magnitude U(1e-6, 1e-5) (below f16's normal range), random signs and
+    positions."""
+    r = rng_for(seed, _P_XWIDE, layer)
+    a = r.standard_normal((steps, rows, hidden), dtype=np.float32)
+    for t in range(steps):
+        for m in range(rows):
+            pos = r.choice(hidden, size=10, replace=False)
+            mag = np.concatenate([r.uniform(1e3, 4e3, 4), r.uniform(3.3e4, 6e4, 2),
+                                  r.uniform(1e-6, 1e-5, 4)])
+            a[t, m, pos] = (mag * r.choice([-1.0, 1.0], size=10)).astype(np.float32)
+    return to_bf16_bits(a)
 
 
 class Routing:
