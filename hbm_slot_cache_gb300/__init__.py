@@ -140,6 +140,11 @@ class MoeCache:
     def reset(self) -> None:
         moe_cache_reset(self.h)
 
+    def set_wait_timeout(self, microseconds: int) -> None:
+        """Failure-detection hook: bound the one-row expert kernels' copy waits
+        (0: the default limit).  See moe_cache_set_wait_timeout."""
+        _lib.moe_cache_set_wait_timeout(self.h, microseconds)
+
     def close(self) -> None:
         if getattr(self, "h", None):
             moe_cache_destroy(self.h)

@@ -35,7 +35,8 @@ EXPORTS = ("moe_cache_create", "moe_cache_step", "moe_cache_step_host", "moe_cac
            "moe_cache_strerror", "moe_expert_bytes", "moe_host_alloc", "moe_host_free",
            "moe_probe_host_link", "moe_cache_set_timing_events", "moe_expert_pass_noalloc",
            "moe_policy_lru", "moe_policy_static", "moe_policy_hybrid", "moe_policy_lru_curve",
-           "moe_policy_size_layers", "moe_cache_layer_slots", "moe_feed_inputs")
+           "moe_policy_size_layers", "moe_cache_layer_slots", "moe_feed_inputs",
+           "moe_cache_set_wait_timeout")
 
 
 class MoeError(RuntimeError):
@@ -106,6 +107,7 @@ def lib() -> ctypes.CDLL:
         L.moe_cache_trace.argtypes = [P, I, P, I, ctypes.POINTER(ctypes.c_int)]
         L.moe_cache_reset.argtypes = [P]
         L.moe_cache_destroy.argtypes = [P]
+        L.moe_cache_set_wait_timeout.argtypes = [P, I]
         L.moe_cache_strerror.argtypes = [I]
         L.moe_cache_strerror.restype = ctypes.c_char_p
         L.moe_expert_bytes.argtypes = [I, I, U64P, U64P]
@@ -114,7 +116,7 @@ def lib() -> ctypes.CDLL:
         L.moe_probe_host_link.argtypes = [P, P, ctypes.c_size_t, I, I,
                                           ctypes.POINTER(ctypes.c_double)]
         L.moe_cache_set_timing_events.argtypes = [P, P]
-        L.moe_expert_pass_noalloc.argtypes = [I, I, I, P, P, P, P, P, P, P]
+        L.moe_expert_pass_noalloc.argtypes = [I, I, I, P, P, P, P, P, P, P, P]
         L.moe_feed_inputs.argtypes = [P, P, ctypes.c_size_t, ctypes.c_size_t, I, P, P, P, P]
         PR = ctypes.POINTER(PolicyResult)
         L.moe_policy_lru.argtypes = [P, I, I, I, I, PR]
@@ -219,6 +221,10 @@ def moe_cache_reset(h: int) -> None:
     _check(lib().moe_cache_reset(h), "moe_cache_reset")
 
 
+def moe_cache_set_wait_timeout(h: int, microseconds: int) -> None:
+    _check(lib().moe_cache_set_wait_timeout(h, microseconds), "moe_cache_set_wait_timeout")
+
+
 def moe_cache_destroy(h: int) -> None:
     _check(lib().moe_cache_destroy(h), "moe_cache_destroy")
 
@@ -239,17 +245,19 @@ def moe_cache_set_timing_events(h: int, events) -> None:
 
 
 def moe_expert_pass_noalloc(k: int, hidden: int, inter: int, expert_w, expert_s, gscale,
-                            weights, x: int, out: int, stream: int = 0) -> None:
+                            weights, x: int, out: int, stream: int = 0,
+                            flags_out: int = 0) -> None:
     """One-row expert pass without any device allocation (see the header).
 
-    expert_w / expert_s: k device addresses; gscale float32 [k, 3]; weights float32 [k]."""
+    expert_w / expert_s: k device addresses; gscale float32 [k, 3]; weights float32 [k];
+    flags_out: device address of a uint32 that receives the call's error flags (0: none)."""
     wa = (ctypes.c_void_p * k)(*[int(p) for p in expert_w])
     sa = (ctypes.c_void_p * k)(*[int(p) for p in expert_s])
     g = np.ascontiguousarray(gscale, np.float32).reshape(k, 3)
     w = np.ascontiguousarray(weights, np.float32).reshape(k)
     _check(lib().moe_expert_pass_noalloc(k, hidden, inter, ctypes.cast(wa, ctypes.c_void_p),
                                          ctypes.cast(sa, ctypes.c_void_p), g.ctypes.data,
-                                         w.ctypes.data, x, out, stream),
+                                         w.ctypes.data, x, out, flags_out or None, stream),
            "moe_expert_pass_noalloc")
 
 

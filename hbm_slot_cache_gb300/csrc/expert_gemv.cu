@@ -17,9 +17,9 @@
 // registers as f16 (the row prescaled by a power of two so none overflows;
 // bf16 -> f16 is then exact apart from f16 subnormals), so each product is
 // one mixed-precision fma.rn.f32.f16.  Row sums: a reduce-scatter butterfly of
-// shuffles, then a fixed-order sum across warps.  Compute warps signal a
-// per-stage named barrier without waiting; a control warp refills the stage
-// and writes h = silu(gate) * up in fp32.
+// shuffles, then a fixed-order sum across warps.  Compute warps count
+// themselves in on a per-stage mbarrier without waiting; a control warp
+// refills the stage and writes h = silu(gate) * up in fp32.
 //
 // down (resident or missed picks): one CTA per SM serves one pick; each warp
 // owns a ring of 2-row stages (TMA bulk copies) and reduces each W2 row with
@@ -189,19 +189,6 @@ __device__ __forceinline__ Stages carve(uint8_t* smem, int NS, int stage_bytes) 
   s.abort_flag = reinterpret_cast<int*>(s.full + NS);
   s.red = reinterpret_cast<float*>(s.full + NS + 1);
   return s;
-}
-
-// After a timed-out wait: wait (bounded) for the fills still in flight into
-// this CTA's shared memory, so none lands after the CTA is done with it.
-template <bool FROM_HOST>
-__device__ void drain_fills(const Stages& S, int i, int NS, int my_units, uint32_t* flags) {
-  if constexpr (FROM_HOST) {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-  } else {
-    if (threadIdx.x != 0) return;
-    for (int ii = i; ii < i + NS && ii < my_units; ++ii)
-      if (!mbar_wait_bounded(&S.full[ii % NS], (uint32_t)((ii / NS) & 1), flags)) return;
-  }
 }
 
 __device__ __forceinline__ int units_of_block(int nunits) {
@@ -428,25 +415,24 @@ __device__ __forceinline__ void gateup_epilogue(const float* red, int RL, int C,
   hbuf[(size_t)j * I + rb * kGateUpRows + gg + q * RL] = gate / (1.0f + expf(-gate)) * up;
 }
 
-__device__ __forceinline__ void named_arrive(int id, int n) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // Resident picks: slot bytes from HBM, units assigned round-robin over the
 // persistent grid.  Warp-specialised: the C * RL compute threads wait only for
-// their unit's bytes (an mbarrier per stage), stash their partial sums and
-// signal the stage's named barrier without waiting; one control warp (the
-// CTA's last) waits on that barrier, forms h for the unit's rows and refills
-// the stage with the unit's four segments by 1-D TMA bulk copies.  No compute
-// warp ever waits for another.
+// their unit's bytes (the stage's "full" mbarrier), stash their partial sums
+// and count their warp in on the stage's "stashed" mbarrier without waiting;
+// one control warp (the CTA's last) waits on "stashed", refills the stage with
+// a later unit's four segments by 1-D TMA bulk copies and forms h for the
+// unit's rows.  No compute warp ever waits for another.  Every wait is
+// bounded: a compute warp whose wait runs out sets the CTA's abort word and
+// stops; the control warp, waiting on a stage no stopped warp will stash,
+// sees the word, stops issuing, waits (bounded) for its copies in flight and
+// returns.  A compute warp can never run more than the stage ring ahead of the
+// control warp, since each of its units waits for a fill the control warp
+// issues only after the stage's previous unit was stashed.
 template <int RPT, bool WARP_RED>
 __global__ void __launch_bounds__(kGateUpThreads + 32, 2)
 gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
                    float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
-                   int subset) {
+                   int subset, PickBounds bounds) {
   constexpr int V = 2 * RPT;
   constexpr int R = kGateUpRows;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -460,8 +446,9 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   const int red_floats = WARP_RED ? RL * (C / 32) * V : NC * V;  // per stage
   uint8_t* base = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
-  volatile int* abort_flag = reinterpret_cast<int*>(full + NS);
-  float* red0 = reinterpret_cast<float*>(full + NS + 1);
+  uint64_t* stashed = full + NS;
+  volatile int* abort_flag = reinterpret_cast<int*>(full + 2 * NS);
+  float* red0 = reinterpret_cast<float*>(full + 2 * NS + 1);
   __shared__ int s_pcnt;
   // the launch's picks, once: no global round trip on the refill path
   __shared__ int s_j[MOE_MAX_TOPK];
@@ -485,14 +472,19 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   int issued = 0;
   if (tid >= NC) {  // control warp: the plan and the first fills, while x loads below
     pdl_wait();     // the plan comes from the kernel before this one
-    int pbeg = 0, pcnt = plan->npicks;
-    if (subset == kPicksHit) pcnt = plan->n_hit;
-    if (subset == kPicksMiss) {
-      pbeg = plan->n_hit;
-      pcnt = plan->npicks - plan->n_hit;
+    // the subset's picks, checked before they address memory: a bad plan skips
+    // the whole launch (MOE_FLAG_BAD_PLAN)
+    int pbeg = 0, pcnt = 0;
+    bool ok = subset_range(plan, subset, pbeg, pcnt);
+    const int npicks = ok ? plan->npicks : 0;
+    int j = 0;
+    if (lane < pcnt) {
+      j = subset == kPicksAll ? lane : plan->order[pbeg + lane];
+      ok = ok && pick_ok(plan, j, npicks, bounds, false);
     }
-    if (lane < pcnt && lane < MOE_MAX_TOPK) {
-      const int j = subset == kPicksAll ? lane : plan->order[pbeg + lane];
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (!plan_ok(ok || lane != 0, flags) || !ok) pcnt = 0;
+    if (lane < pcnt) {
       s_j[lane] = j;
       s_w[lane] = plan->wptr[j];
       s_s[lane] = plan->sptr[j];
@@ -501,7 +493,10 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     }
     if (lane == 0) {
       s_pcnt = pcnt;
-      for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&stashed[s], (uint32_t)(NC / 32));  // one arrival per compute warp
+      }
       fence_mbar_init();
       *abort_flag = 0;
     }
@@ -518,10 +513,17 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
 
   if (tid >= NC) {  // ---- control warp
     int s = 0, rbuf = 0;  // stage and partial-sum buffer of unit i (no runtime division)
+    uint32_t sphase = 0;  // parity of stage s's current "stashed" phase
+    bool stopped = false;
     for (int i = 0; i < my_units; ++i) {
-      named_sync(1 + s, NC + 32);  // every compute thread has stashed unit i
+      // every compute warp has stashed unit i, unless one stopped
+      const bool got = mbar_wait_or_abort(&stashed[s], sphase, abort_flag, flags);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        stopped = true;
+        break;
+      }
       const int unit = blockIdx.x + i * gridDim.x;
-      if (lane == 0 && i + NS < my_units && !*abort_flag) {  // the stage's bytes are consumed
+      if (lane == 0 && i + NS < my_units) {  // the stage's bytes are consumed
         issue(unit + NS * gridDim.x, s);
         ++issued;
       }
@@ -534,24 +536,34 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
                                        s_gs[jl][1], s_j[jl], unit - jl * upp, xup, hbuf, I, lane);
       }
       __syncwarp();
-      if (++s == NS) s = 0;
+      if (++s == NS) {
+        s = 0;
+        sphase ^= 1u;
+      }
       if (++rbuf == 2 * NS) rbuf = 0;
     }
-    if (lane == 0 && *abort_flag)  // let the copies in flight land (bounded)
+    // after a stop: the last fill issued on each stage is the only one that may
+    // still be in flight; let each land (bounded) before the CTA's memory goes
+    if (stopped && lane == 0)
       for (int m = issued - NS > 0 ? issued - NS : 0; m < issued; ++m)
         if (!mbar_wait_bounded(&full[m % NS], (uint32_t)((m / NS) & 1), flags)) break;
     return;
   }
-  // ---- compute threads
+  // ---- compute threads (whole warps)
   int s = 0, rbuf = 0;
   uint32_t phase = 0;  // parity of stage s's current fill
+  const uint64_t wait_ns = plan_wait_ns(plan);
   for (int i = 0; i < my_units; ++i) {
-    if (!*abort_flag && !mbar_wait_bounded(&full[s], phase, flags))
-      *abort_flag = 1;  // flagged; the remaining units are computed on whatever is staged
+    const bool ok = mbar_wait_bounded(&full[s], phase, flags, wait_ns);
+    if (__any_sync(0xFFFFFFFFu, !ok || *abort_flag)) {  // flagged: this warp stops
+      if (lane == 0) *abort_flag = 1;
+      break;
+    }
     float a[V];
     gateup_partials<RPT>(base + (size_t)s * stage_bytes, H, RL, g, c, xh, a);
     stash_partials<V, WARP_RED>(a, red0 + rbuf * red_floats, g, c, C, lane);
-    named_arrive(1 + s, NC + 32);
+    __syncwarp();  // the warp's partials are written before its arrival releases them
+    if (lane == 0) mbar_arrive(&stashed[s]);
     if (++s == NS) {
       s = 0;
       phase ^= 1u;
@@ -575,13 +587,15 @@ template <int RPT, bool WARP_RED>
 __global__ void __launch_bounds__(kGateUpThreads, 2)
 gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
                         float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
-                        uint32_t* ctr) {
+                        uint32_t* ctr, PickBounds bounds) {
   constexpr int V = 2 * RPT;
   constexpr int R = kGateUpRows;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_xmax[kGateUpThreads / 32];
   __shared__ int s_unit[kMaxStages];  // link unit staged in each stage, -1: none
   __shared__ int s_next[2];           // by iteration parity: read after the writer moved on
+  __shared__ int s_pick[MOE_MAX_TOPK];  // the missed picks, checked
+  __shared__ int s_pcnt;
   const int C = H / 32;
   const int tid = threadIdx.x, lane = tid & 31;
   const int g = tid / C, c = tid - g * C;
@@ -589,13 +603,31 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   const int SB = 2 * cb + 2 * sb;  // stage bytes
   Stages S = carve(smem, NS, SB);
 
-  const int pbeg = plan->n_hit, pcnt = plan->npicks - plan->n_hit;
-  auto pick_of = [&](int jl) { return plan->order[pbeg + jl]; };
+  // The missed picks, each checked (index, slot and host pointers) before it
+  // addresses memory: a bad plan skips the whole launch (MOE_FLAG_BAD_PLAN).
+  if (tid < 32) {
+    int pbeg = 0, pcnt = 0;
+    bool ok = subset_range(plan, kPicksMiss, pbeg, pcnt);
+    const int npicks = ok ? plan->npicks : 0;
+    int j = 0;
+    if (tid < pcnt) {
+      j = plan->order[pbeg + tid];
+      ok = ok && pick_ok(plan, j, npicks, bounds, true);
+    }
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (!plan_ok(ok || tid != 0, flags) || !ok) pcnt = 0;
+    if (tid < pcnt) s_pick[tid] = j;
+    if (tid == 0) s_pcnt = pcnt;
+  }
+  __syncthreads();
+  const int pcnt = s_pcnt;
+  auto pick_of = [&](int jl) { return s_pick[jl]; };
   const int upp = I / R;                                   // gate/up units per pick
   const size_t w2c = (size_t)H * (I / 2), w2s = (size_t)H * (I / 16);
   const int ncc = (int)((w2c + SB - 1) / SB), ncs = (int)((w2s + SB - 1) / SB);
   const int upk = upp + ncc + ncs;                         // link units per pick
   const int NL = pcnt * upk;
+  const uint64_t wait_ns = plan_wait_ns(plan);
 
   // link unit u: its byte segments in host memory and in the pick's slot
   auto segs = [&](int u, int& nseg) {
@@ -655,15 +687,20 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   uint32_t xh[16];
   const float xup = load_x_f16(x, c, s_xmax, xh);
 
+  int i_abort = -1;  // the iteration a timed-out wait stopped the loop at (uniform)
   for (int i = 0;; ++i) {
     const int stage = i % NS;
     const int unit = s_unit[stage];
     if (unit < 0) break;  // units are taken in order: none left for this CTA
     // the unit that refills this stage: taken now, used at the end
     const int taken = tid == 0 ? (int)atomicAdd(&ctr[kWorkCtr], 1u) : 0;
-    if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags)) *S.abort_flag = 1;
+    if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags, wait_ns))
+      *S.abort_flag = 1;
     __syncthreads();
-    if (*S.abort_flag) break;  // flagged; the copies in flight are drained below
+    if (*S.abort_flag) {  // flagged; the copies in flight are drained below
+      i_abort = i;
+      break;
+    }
     const int jl = unit / upk, r = unit - jl * upk;
     const uint8_t* st = S.base + (size_t)stage * SB;
     int nseg = 0;
@@ -689,6 +726,19 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     if (nxt >= 0) fill(nxt, stage);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
+  if (i_abort >= 0) {
+    // Every thread's copies have landed; each fill's completion also arrives
+    // on its stage's mbarrier, so wait (default limit) until the pending fills'
+    // phases are complete: no arrival may reach this CTA's shared memory after
+    // it exits.  Iteration it consumes phase it / NS of stage it % NS.
+    if (tid == 0)
+      for (int d = 0; d < NS; ++d) {
+        const int it = i_abort + d, st = it % NS;
+        if (s_unit[st] >= 0 && !mbar_wait_bounded(&S.full[st], (uint32_t)((it / NS) & 1), flags))
+          break;
+      }
+    __syncthreads();
+  }
   // the last CTA out (no unit is taken after it) resets the launch's counters
   if (tid == 0 && atomicAdd(&ctr[kRtDoneCtr], 1u) == gridDim.x - 1) {
     ctr[kWorkCtr] = 0u;
@@ -710,7 +760,8 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
 template <int MB>  // h blocks a lane keeps in registers (0: read them from shared memory)
 __global__ void __launch_bounds__(kDownThreads, 1)
 gemv_down_kernel(const Plan* plan, const float* hbuf, float* ypart, int H, int I, int NSW,
-                 uint32_t* flags, int subset, float* __restrict__ out, uint32_t* ctr) {
+                 uint32_t* flags, int subset, float* __restrict__ out, uint32_t* ctr,
+                 PickBounds bounds) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_nlast;
   __shared__ int s_lastb[MOE_MAX_DIM / kDownUnitRows];
@@ -718,11 +769,11 @@ gemv_down_kernel(const Plan* plan, const float* hbuf, float* ypart, int H, int I
   // The plan was written by route/remap, which completed before the kernel
   // this one may overlap (programmatic launch) started: it is read at once.
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  int pbeg = 0, pcnt = plan->npicks;
-  if (subset == kPicksHit) pcnt = plan->n_hit;
-  if (subset == kPicksMiss) {
-    pbeg = plan->n_hit;
-    pcnt = plan->npicks - plan->n_hit;
+  int pbeg = 0, pcnt = 0;
+  const bool range_ok = subset_range(plan, subset, pbeg, pcnt);
+  if (!range_ok) {  // uniform: nothing is addressed through a bad plan
+    if (tid == 0) plan_ok(false, flags);
+    return;
   }
   // this CTA's pick and its share of the pick's units
   const int jl = pcnt > 0 ? (int)blockIdx.x % pcnt : 0;
@@ -732,6 +783,10 @@ gemv_down_kernel(const Plan* plan, const float* hbuf, float* ypart, int H, int I
   const int my_units = (pcnt > 0 && q < units) ? (units - 1 - q) / nq + 1 : 0;
   if (my_units == 0) return;  // uniform
   const int j = subset == kPicksAll ? jl : plan->order[pbeg + jl];
+  if (!pick_ok(plan, j, plan->npicks, bounds, false)) {  // uniform
+    if (tid == 0) plan_ok(false, flags);
+    return;
+  }
   const uint8_t* wsrc = plan->wptr[j] + (size_t)I * H;     // W2 codes
   const uint8_t* ssrc = plan->sptr[j] + (size_t)I * H / 8; // W2 scales
 
@@ -781,8 +836,9 @@ gemv_down_kernel(const Plan* plan, const float* hbuf, float* ypart, int H, int I
   }
   int n = 0, s = 0;
   uint32_t phase = 0;  // parity of stage s's current fill
+  const uint64_t wait_ns = plan_wait_ns(plan);
   for (; n < my_items; ++n) {
-    const bool ok = mbar_wait_bounded(&bars[s], phase, flags);
+    const bool ok = mbar_wait_bounded(&bars[s], phase, flags, wait_ns);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;  // flagged; this warp's rows stay unwritten
     const uint8_t* st = ring + (size_t)s * item_b;
     const int r0 = row0(n);
@@ -838,19 +894,19 @@ GateUpShape gateup_shape(int H, int stages) {
   const int red_floats = s.warp_red ? s.RL * (s.C / 32) * V : s.NT * V;
   const int stage = 2 * R * H / 2 + 2 * R * H / 16;
   const int per_cta = kSmemPerSm / 2 - 1024;  // two CTAs per SM
-  // stages, their mbarriers, two sets of partial sums a stage, the abort word
-  int ns = (per_cta - 16) / (stage + 8 + 2 * red_floats * 4);
-  if (ns > 6) ns = 6;  // <= kMaxStages, and named barriers 1 .. 6
+  // stages, their two mbarriers, two sets of partial sums a stage, the abort word
+  int ns = (per_cta - 16) / (stage + 16 + 2 * red_floats * 4);
+  if (ns > 6) ns = 6;  // <= kMaxStages
   if (stages > 0 && stages < ns) ns = stages;
   s.NS = ns;
-  s.smem = ns * stage + 8 * ns + 8 + 2 * ns * red_floats * 4;
+  s.smem = ns * stage + 16 * ns + 8 + 2 * ns * red_floats * 4;
   return s;
 }
 
 template <int RPT, bool WR>
 cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
                        const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
-                       int subset, bool pdl) {
+                       int subset, bool pdl, const PickBounds& b) {
   auto kern = gemv_gateup_kernel<RPT, WR>;
   static int smem_set = 0;  // raise the opt-in limit once per size (not a stream operation)
   if (s.smem > smem_set) {
@@ -861,15 +917,15 @@ cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Pl
   }
   if (pdl)
     return launch_pdl(kern, dim3(grid), dim3(s.NT + 32), s.smem, st, plan, x, hbuf, H, I, s.RL,
-                      s.NS, flags, subset);
-  kern<<<grid, s.NT + 32, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset);
+                      s.NS, flags, subset, b);
+  kern<<<grid, s.NT + 32, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, subset, b);
   return cudaGetLastError();
 }
 
 template <int RPT, bool WR>
 cudaError_t run_readthrough(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
                             const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
-                            uint32_t* ctr) {
+                            uint32_t* ctr, const PickBounds& b) {
   auto kern = gemv_readthrough_kernel<RPT, WR>;
   static int smem_set = 0;
   if (s.smem > smem_set) {
@@ -878,7 +934,7 @@ cudaError_t run_readthrough(cudaStream_t st, int grid, const GateUpShape& s, con
     if (e != cudaSuccess) return e;
     smem_set = s.smem;
   }
-  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, ctr);
+  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, ctr, b);
   return cudaGetLastError();
 }
 
@@ -910,7 +966,7 @@ DownShape down_shape(int I, int stages) {
 template <int MB>
 cudaError_t run_down(cudaStream_t st, int grid, const DownShape& d, const Plan* plan,
                      const GemvWorkspace& ws, int H, int I, uint32_t* flags, int subset,
-                     float* out, uint32_t* ctr, bool pdl) {
+                     float* out, uint32_t* ctr, bool pdl, const PickBounds& b) {
   auto kern = gemv_down_kernel<MB>;
   static int smem_set = 0;
   if (d.smem > smem_set) {
@@ -921,9 +977,9 @@ cudaError_t run_down(cudaStream_t st, int grid, const DownShape& d, const Plan* 
   }
   if (pdl)
     return launch_pdl(kern, dim3(grid), dim3(kDownThreads), d.smem, st, plan, ws.hbuf, ws.ypart,
-                      H, I, d.NS, flags, subset, out, ctr);
+                      H, I, d.NS, flags, subset, out, ctr, b);
   kern<<<grid, kDownThreads, d.smem, st>>>(plan, ws.hbuf, ws.ypart, H, I, d.NS, flags, subset,
-                                           out, ctr);
+                                           out, ctr, b);
   return cudaGetLastError();
 }
 
@@ -955,7 +1011,8 @@ cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t
   const GateUpShape s = gateup_shape(H, how.stages);
   if (s.NS < 1 || s.NT > kGateUpThreads || how.from_host) return cudaErrorInvalidConfiguration;
   const int grid = gateup_grid(I, k, num_sms, how);
-  GATEUP_DISPATCH(run_gateup, st, grid, s, plan, x, ws.hbuf, H, I, flags, how.subset, how.pdl)
+  GATEUP_DISPATCH(run_gateup, st, grid, s, plan, x, ws.hbuf, H, I, flags, how.subset, how.pdl,
+                  how.bounds)
 }
 
 int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how) {
@@ -969,7 +1026,7 @@ cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uin
   if (s.NS < 1 || s.NT > kGateUpThreads || !how.from_host || how.subset != kPicksMiss)
     return cudaErrorInvalidConfiguration;
   const int grid = gemv_readthrough_grid(I, k, num_sms, how);
-  GATEUP_DISPATCH(run_readthrough, st, grid, s, plan, x, ws.hbuf, H, I, flags, ctr)
+  GATEUP_DISPATCH(run_readthrough, st, grid, s, plan, x, ws.hbuf, H, I, flags, ctr, how.bounds)
 }
 #undef GATEUP_DISPATCH
 
@@ -987,9 +1044,11 @@ cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, in
   if (d.NS < 1 || how.from_host) return cudaErrorInvalidConfiguration;  // slot bytes only
   const int grid = gemv_down_grid(H, num_sms, how);
   const int C = I / 32;  // h blocks per W2 row: in registers up to two per lane
-  if (C <= 32) return run_down<1>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl);
-  if (C == 64) return run_down<2>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl);
-  return run_down<0>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl);
+  if (C <= 32)
+    return run_down<1>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl, how.bounds);
+  if (C == 64)
+    return run_down<2>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl, how.bounds);
+  return run_down<0>(st, grid, d, plan, ws, H, I, flags, how.subset, out, ctr, how.pdl, how.bounds);
 }
 
 }  // namespace moe

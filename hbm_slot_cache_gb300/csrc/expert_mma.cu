@@ -100,7 +100,7 @@ template <int P>  // 16-byte pieces per row per chunk (8: 256 elements, 4: 128)
 __global__ void __launch_bounds__(kThreads)
 grouped_mma_kernel(MmaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t s_bar[2];  // MMA commits of even / odd chunks
+  __shared__ __align__(8) uint64_t s_bar[3];  // MMA commits of even / odd chunks; [2]: drain
   __shared__ uint32_t s_tmem;
   __shared__ int s_pick[kRowsPerJob], s_brow[kRowsPerJob];
   __shared__ float s_gl[kRowsPerJob][kLevels];
@@ -133,6 +133,7 @@ grouped_mma_kernel(MmaArgs a) {
   if (tid == 0) {
     mbar_init(&s_bar[0], 1);
     mbar_init(&s_bar[1], 1);
+    mbar_init(&s_bar[2], 1);
     fence_mbar_init();
     s_fail = 0;
   }
@@ -360,6 +361,22 @@ grouped_mma_kernel(MmaArgs a) {
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if (s_fail) {
+    // A wait gave up, so MMAs this CTA committed may still be running: before
+    // the TMEM is released, one more commit (it arrives once every earlier
+    // tcgen05 operation of the issuing thread, thread 0, is complete) is waited
+    // for under the default limit.
+    if (tid == 0) {
+      asm volatile(
+          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+              smem_addr(&s_bar[2]))
+          : "memory");
+      mbar_wait_bounded(&s_bar[2], 0u, a.flags);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+  }
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols));

@@ -43,7 +43,11 @@ struct LayerDev {
 struct Plan {
   int32_t rows, npicks, n_union, n_miss, bypass;
   int32_t n_hit;   // picks resident at step start (one-row steps)
-  int32_t pad[2];
+  uint32_t wait_us;  // not written by the steps (moe_cache_set_wait_timeout sets it): the
+                     // one-row expert kernels' waits for their stages give up after this
+                     // many microseconds (0: the default limit); waits that drain copies
+                     // in flight keep the default
+  int32_t pad;
   int32_t order[MOE_MAX_PICKS];  // picks, hits first, each part in rank order
   int32_t ids[MOE_MAX_PICKS];
   float wts[MOE_MAX_PICKS];
@@ -141,6 +145,20 @@ struct GemvWorkspace {
 // Pick subsets of a one-row step: the picks resident at step start, the
 // missed picks, or all picks.
 enum PickSubset { kPicksHit = 0, kPicksMiss = 1, kPicksAll = 2 };
+// Where a one-row step's expert pointers may point: expert i of the layer's
+// host bank is host_w + i*Bw (and host_s + i*Bs), i < host_n; slot v of its
+// ring is slot_w + v*Bw, v < slot_n.  The kernels check every pointer the plan
+// hands them against these before they address memory (MOE_FLAG_BAD_PLAN and
+// no access on a failure).  A null slot_w / host_w leaves that range
+// unchecked (the no-allocation pass, whose experts are the caller's).
+struct PickBounds {
+  const uint8_t* slot_w = nullptr;
+  const uint8_t* slot_s = nullptr;
+  const uint8_t* host_w = nullptr;
+  const uint8_t* host_s = nullptr;
+  unsigned long long slot_n = 0, host_n = 0;
+  long long Bw = 0, Bs = 0;
+};
 struct GemvLaunch {
   int subset;      // PickSubset
   bool from_host;  // read-through launch only: the picks come from host memory
@@ -148,6 +166,7 @@ struct GemvLaunch {
   int stages;      // units in flight per CTA (0: as many as fit)
   bool pdl = false;  // gate/up and down launches: programmatic dependent launch
                      // on the previous kernel of their stream (see pdl_wait)
+  PickBounds bounds{};
 };
 // Counters of a one-row step (zero between steps; each user resets its own):
 //   [0] read-through CTAs that have finished, [1] read-through units taken,
@@ -250,27 +269,59 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Plain arrival (count one) on an mbarrier, release at CTA scope.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
 
-// Waits on an mbarrier phase for at most ~2 s; on timeout sets
-// MOE_FLAG_WAIT_TIMEOUT in *flags and returns false (never traps).
+// Waits on an mbarrier phase for at most limit_ns (default ~2 s); on timeout
+// sets MOE_FLAG_WAIT_TIMEOUT in *flags and returns false (never traps).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t* flags) {
+                                                  uint32_t* flags,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) {
+      atomicOr(flags, MOE_FLAG_WAIT_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Waits on an mbarrier phase until it completes (true), the CTA's abort word
+// is set, or the default limit runs out (MOE_FLAG_WAIT_TIMEOUT); false in both
+// of the latter cases.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   const volatile int* abort_word,
+                                                   uint32_t* flags) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_word) return false;
     if (global_ns() - t0 > kWaitLimitNs) {
       atomicOr(flags, MOE_FLAG_WAIT_TIMEOUT);
       return false;
     }
     __nanosleep(64);
   }
+}
+
+// A plan's wait limit in nanoseconds (Plan::wait_us; 0: the default).
+__device__ __forceinline__ uint64_t plan_wait_ns(const Plan* plan) {
+  const uint32_t us = plan->wait_us;
+  return us ? (uint64_t)us * 1000ull : kWaitLimitNs;
 }
 
 // Index check on plan data one kernel hands to the next: false (and the sticky
@@ -334,6 +385,44 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
       __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
   __half2 h = *reinterpret_cast<__half2*>(&r);
   return __half22float2(h);
+}
+
+// Expert pointer check: p == base + i * stride for some i < n (base null:
+// unchecked).
+__device__ __forceinline__ bool expert_ptr_ok(const uint8_t* p, const uint8_t* base,
+                                              unsigned long long n, long long stride) {
+  if (!base) return p != nullptr;
+  if (p < base || stride <= 0) return false;
+  const unsigned long long off = (unsigned long long)(p - base);
+  return off % (unsigned long long)stride == 0 && off / (unsigned long long)stride < n;
+}
+
+// One pick's plan entries for a one-row kernel: j indexes the step's picks,
+// its slot pointers lie in the ring and (host) its backing pointers in the bank.
+__device__ __forceinline__ bool pick_ok(const Plan* plan, int j, int npicks,
+                                        const PickBounds& b, bool host) {
+  if (j < 0 || j >= npicks || j >= MOE_MAX_TOPK) return false;
+  if (!expert_ptr_ok(plan->wptr[j], b.slot_w, b.slot_n, b.Bw) ||
+      !expert_ptr_ok(plan->sptr[j], b.slot_s, b.slot_n, b.Bs))
+    return false;
+  return !host || (expert_ptr_ok(plan->hwptr[j], b.host_w, b.host_n, b.Bw) &&
+                   expert_ptr_ok(plan->hsptr[j], b.host_s, b.host_n, b.Bs));
+}
+
+// The subset's pick range of a one-row plan, checked: 0 <= n_hit <= npicks <=
+// MOE_MAX_TOPK.  False (and no picks) when the plan fails the check.
+__device__ __forceinline__ bool subset_range(const Plan* plan, int subset, int& pbeg, int& pcnt) {
+  const int npicks = plan->npicks, n_hit = plan->n_hit;
+  pbeg = 0;
+  pcnt = 0;
+  if (npicks < 0 || npicks > MOE_MAX_TOPK || n_hit < 0 || n_hit > npicks) return false;
+  pcnt = npicks;
+  if (subset == kPicksHit) pcnt = n_hit;
+  if (subset == kPicksMiss) {
+    pbeg = n_hit;
+    pcnt = npicks - n_hit;
+  }
+  return true;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits) {

@@ -17,7 +17,6 @@
 using namespace moe;
 
 namespace {
-constexpr int kDefaultMaxRows = 512;  // largest prefill chunk a handle takes by default
 constexpr int kDefaultPrefillChunk = 32;  // experts staged per prefill chunk (two chunks held)
 }
 
@@ -258,15 +257,18 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
   moe_cache_opts_t o{};
   o.copy_backend = MOE_COPY_SM;
   o.bypass_rows = MOE_MAX_CACHED_ROWS;
-  o.max_rows = kDefaultMaxRows;
+  o.max_rows = 0;
   if (opts) {
     o = *opts;
     if (o.bypass_rows <= 0) o.bypass_rows = MOE_MAX_CACHED_ROWS;
-    if (o.max_rows <= 0) o.max_rows = kDefaultMaxRows;
     if (o.prefill_chunk == 0) o.prefill_chunk = kDefaultPrefillChunk;
   } else {
     o.prefill_chunk = kDefaultPrefillChunk;
   }
+  // Every cached step (up to bypass_rows rows) must fit the multi-row workspace,
+  // so max_rows is at least bypass_rows; the default (0) is exactly that: a
+  // decode-only handle with no bypass workspace and no prefill staging.
+  if (o.max_rows < o.bypass_rows) o.max_rows = o.bypass_rows;
   if (o.prefill_chunk < -1 || o.batch_invariant < 0 || o.batch_invariant > 1) return MOE_ERR_ARG;
   if (o.batch_invariant && !mma_supported(hidden, inter)) return MOE_ERR_UNSUPPORTED;
   if (layers < 1 || experts < 1 || top_k < 1 || hidden < 1 || inter < 1 || !host_backing)
@@ -395,6 +397,7 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
     return MOE_ERR_OOM;
   }
   e = cudaMemcpy(h->gscale, gs.data(), gs.size() * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(h->plan, 0, sizeof(Plan));  // wait_us 0: default limit
   if (e == cudaSuccess && o.all_resident) {
     for (int l = 0; l < layers && e == cudaSuccess; ++l) {
       e = cudaMemcpy(h->slot_w + h->slot_off[l] * h->Bw, host_backing[l].w,
@@ -454,16 +457,26 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     // missed picks: a small grid keeps the host link saturated without taking
     // many SMs from the resident picks
     const int rt_grid = h->num_sms / 2 > 8 ? h->num_sms / 2 : 8;
-    const GemvLaunch miss{kPicksMiss, true, rt_grid, 2};
+    // the ring and bank every pointer of the plan must lie in (checked on the device)
+    PickBounds pb;
+    pb.slot_w = L.slot_w;
+    pb.slot_s = L.slot_s;
+    pb.slot_n = (unsigned long long)h->S_of[layer];
+    pb.host_w = L.host_w;
+    pb.host_s = L.host_s;
+    pb.host_n = (unsigned long long)h->E;
+    pb.Bw = h->Bw;
+    pb.Bs = h->Bs;
+    const GemvLaunch miss{kPicksMiss, true, rt_grid, 2, false, pb};
     // their down pass starts as the read-through launch drains (not across a timing event)
-    const GemvLaunch miss_dn{kPicksMiss, false, 0, 4, !h->timing};
+    const GemvLaunch miss_dn{kPicksMiss, false, 0, 4, !h->timing, pb};
     // resident picks: slot bytes from HBM
     // Gate/up is launched normally, after route/remap, so the second stream's
     // higher priority places the read-through CTAs first (two gate/up CTAs
     // fill an SM's registers); the down pass starts as gate/up drains
     // (programmatic launch, not across timing events).
-    const GemvLaunch hit_gu{kPicksHit, false, 0, 3, false},
-        hit_dn{kPicksHit, false, 0, 4, !h->timing};
+    const GemvLaunch hit_gu{kPicksHit, false, 0, 3, false, pb},
+        hit_dn{kPicksHit, false, 0, 4, !h->timing, pb};
     if (e == cudaSuccess) e = mark(2, h->side);
     if (e == cudaSuccess)
       e = launch_gemv_readthrough(h->side, h->plan, x, h->H, h->I, h->k, h->gemv, flags,
@@ -759,6 +772,14 @@ int moe_cache_reset(moe_cache_t* h) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return init_state(h);
+}
+
+int moe_cache_set_wait_timeout(moe_cache_t* h, int microseconds) {
+  if (!h || microseconds < 0) return MOE_ERR_ARG;
+  const uint32_t us = (uint32_t)microseconds;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&h->plan->wait_us, &us, sizeof us, cudaMemcpyHostToDevice);
+  return cuda_err(e);
 }
 
 int moe_cache_destroy(moe_cache_t* h) {

@@ -15,8 +15,12 @@
 // current, resolves its device address with cudaGetSymbolAddress (so make that
 // first call before any stream capture), and kernels get that address.
 // All calls share the one array and it keeps the last call's contents: the
-// tile tickets are cleared on every call, and two calls whose work overlaps on
-// the GPU (different streams without ordering) race on it.
+// tile tickets and the error-flags word are cleared on every call, and two
+// calls whose work overlaps on the GPU (different streams without ordering)
+// race on it.  A call's device-side error flags (a bounded wait that gave up,
+// a plan check that failed) reach the caller through an optional device word.
+// The array's address is looked up once per device for the life of the
+// process: the pass must not be used on a device after cudaDeviceReset.
 #include <mutex>
 
 #include "internal.cuh"
@@ -53,8 +57,10 @@ struct PlanArgs {
   int k;
 };
 
-// Writes the one-row plan into the scratch array and clears the tile tickets.
-__global__ void noalloc_plan_kernel(PlanArgs a, Plan* plan, uint32_t* tile_cnt, int ntiles) {
+// Writes the one-row plan into the scratch array and clears the tile tickets
+// and the error flags.
+__global__ void noalloc_plan_kernel(PlanArgs a, Plan* plan, uint32_t* tile_cnt, int ntiles,
+                                    uint32_t* flags) {
   const int t = threadIdx.x;
   if (t < a.k) {
     plan->ids[t] = t;
@@ -72,8 +78,16 @@ __global__ void noalloc_plan_kernel(PlanArgs a, Plan* plan, uint32_t* tile_cnt, 
     plan->n_union = a.k;
     plan->n_miss = 0;
     plan->bypass = 0;
+    plan->n_hit = 0;
+    plan->wait_us = 0;  // the default wait limit
+    *flags = 0u;
   }
   for (int i = t; i < ntiles; i += blockDim.x) tile_cnt[i] = 0;
+}
+
+// The call's error flags to the caller's word (after the expert kernels).
+__global__ void noalloc_flags_kernel(const uint32_t* flags, uint32_t* flags_out) {
+  *flags_out = *reinterpret_cast<const volatile uint32_t*>(flags);
 }
 
 // Once per device, with that device current: resolve the array's address.
@@ -106,9 +120,9 @@ using namespace moe;
 extern "C" int moe_expert_pass_noalloc(int k, int hidden, int inter, const void* const* expert_w,
                                        const void* const* expert_s, const float* gscale,
                                        const float* weights, const uint16_t* x, float* out,
-                                       void* stream) {
+                                       uint32_t* flags_out, void* stream) {
   if (k < 1 || hidden < 1 || inter < 1 || !expert_w || !expert_s || !gscale || !weights || !x ||
-      !out || ((uintptr_t)x & 15) || ((uintptr_t)out & 15))
+      !out || ((uintptr_t)x & 15) || ((uintptr_t)out & 15) || ((uintptr_t)flags_out & 3))
     return MOE_ERR_ARG;
   if (k > kMaxK || hidden > kMaxDim || inter > kMaxDim || hidden % 128 || inter % 128 ||
       !gemv_supported(hidden, inter, k))
@@ -143,12 +157,16 @@ extern "C" int moe_expert_pass_noalloc(int k, int hidden, int inter, const void*
     a.wts[j] = weights[j];
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  noalloc_plan_kernel<<<1, 64, 0, st>>>(a, plan, ws.tile_cnt, (int)kTileWords);
+  noalloc_plan_kernel<<<1, 64, 0, st>>>(a, plan, ws.tile_cnt, (int)kTileWords, flags);
   cudaError_t e = cudaGetLastError();
-  const GemvLaunch all{kPicksAll, false, 0, 0};
+  const GemvLaunch all{kPicksAll, false, 0, 0};  // the caller's experts: pointers unchecked
   if (e == cudaSuccess)
     e = launch_gemv_gateup(st, plan, x, hidden, inter, k, ws, flags, d->num_sms, all);
   if (e == cudaSuccess)
     e = launch_gemv_down(st, plan, hidden, inter, k, ws, flags, d->num_sms, all, out, ws.tile_cnt);
+  if (e == cudaSuccess && flags_out) {
+    noalloc_flags_kernel<<<1, 1, 0, st>>>(flags, flags_out);
+    e = cudaGetLastError();
+  }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -96,7 +96,11 @@ typedef struct {
   int all_resident;   /* 1: every expert lives in HBM (S = experts, loaded at create);
                          same kernels, used to check that caching changes no output bit */
   int trace_capacity; /* per-layer ring of moe_step_record_t for cached steps (0 = off) */
-  int max_rows;       /* largest rows of any step (sizes the bypass workspace); default 512 */
+  int max_rows;       /* largest rows of any step (sizes the multi-row and bypass
+                         workspaces); raised to bypass_rows if smaller.  Default (0):
+                         bypass_rows, a decode-only handle: steps with more rows return
+                         MOE_ERR_UNSUPPORTED and no prefill staging is allocated.  Set it
+                         to the largest prefill chunk to take bypass steps */
   int prefill_chunk;  /* bypass steps: experts staged into HBM per chunk, two chunks held at
                          once (a 2 * prefill_chunk expert staging area, allocated at create
                          when max_rows > bypass_rows); 0: default 32; -1: no staging, the
@@ -211,6 +215,18 @@ int moe_cache_trace(const moe_cache_t* h, int layer, moe_step_record_t* recs, in
 /* Empty every ring, zero counters, flags and traces (all_resident: reload
  * identity map).  Device synchronize. */
 int moe_cache_reset(moe_cache_t* h);
+
+/* Failure-detection hook (for tests of the timeout path; production code
+ * leaves the default).  Every device wait in the library is bounded; this sets
+ * the limit of the one-row expert kernels' waits for their own weight copies
+ * to `microseconds` (0: the default, about 2 s) for the steps enqueued after
+ * the call.  A wait that runs out sets MOE_FLAG_WAIT_TIMEOUT, and the kernel
+ * finishes the step on whatever bytes arrived (output undefined; a missed
+ * expert's slot may be left incomplete, so moe_cache_reset before relying on
+ * the cache again).  Copies still in flight are always drained under the
+ * default limit before a kernel exits.  Synchronous (device synchronize).
+ * Errors: MOE_ERR_ARG (microseconds < 0), MOE_ERR_CUDA. */
+int moe_cache_set_wait_timeout(moe_cache_t* h, int microseconds);
 
 /* Free everything the handle owns (not the host backing).  NULL is a no-op. */
 int moe_cache_destroy(moe_cache_t* h);
@@ -344,18 +360,26 @@ int moe_policy_size_layers(const uint64_t* host_experts, int layers, int max_slo
  *     moe_host_layer_t, 16-byte aligned;
  *   gscale: host [k][3]; weights: host [k] (router weights, rank order);
  *   x: device bf16 [hidden]; out: device fp32 [hidden] (written); both
- *     16-byte aligned.
+ *     16-byte aligned;
+ *   flags_out: device uint32, 4-byte aligned, or NULL: receives the call's
+ *     MOE_FLAG_* bits once its kernels are done (0: clean; MOE_FLAG_WAIT_TIMEOUT:
+ *     a wait for the call's own weight copies gave up, MOE_FLAG_BAD_PLAN: a
+ *     plan check failed; either leaves out undefined).
  * Allocates nothing: its scratch (about 1.1 MB: plan, h, per-expert partial
  * outputs, tile tickets) is one file-scope device array, fixed in size for
  * k <= MOE_MAX_TOPK and hidden, inter <= MOE_MAX_DIM, held by every GPU that
  * loads the library until the process exits; larger sizes return
  * MOE_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
- * address (make it before any stream capture).  All calls share the array:
- * calls whose work overlaps on the GPU race and must be ordered by the caller.
+ * address (make it before any stream capture) and keeps it for the life of
+ * the process: do not use the pass on a device after cudaDeviceReset.  All
+ * calls share the array and it keeps the last call's contents (each call
+ * clears what must start at zero): calls whose work overlaps on the GPU race
+ * and must be ordered by the caller.
  * Errors: MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
 int moe_expert_pass_noalloc(int k, int hidden, int inter, const void* const* expert_w,
                             const void* const* expert_s, const float* gscale,
-                            const float* weights, const uint16_t* x, float* out, void* stream);
+                            const float* weights, const uint16_t* x, float* out,
+                            uint32_t* flags_out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -114,7 +114,7 @@ def test_glm_prefill_512_rows(lib, orc):
     cfg = workload.CONFIGS["prefill"]
     rows = cfg.rows
     banks = Banks(cfg)
-    cache = make_cache(cfg, banks, layers=1)
+    cache = make_cache(cfg, banks, layers=1, max_rows=rows)
     lg = workload.prefill_logits(cfg, 0, rows)
     xb = workload.activations(cfg.seed, 2, 1, rows, cfg.hidden)[0]
     lg_d, x_d, out_d = _dev(cfg, rows)
@@ -154,8 +154,13 @@ def test_host_side_errors(lib):
         with pytest.raises(L.MoeError) as e:
             make_cache(cfg, banks, slots=S)
         assert e.value.code == L.MOE_ERR_ARG
-    cache = make_cache(cfg, banks, max_rows=32)
+    dflt = make_cache(cfg, banks)   # default: a decode-only handle (no bypass rows)
     lg_d, x_d, out_d = _dev(cfg, 33)
+    with pytest.raises(L.MoeError) as e:
+        L.moe_cache_step(dflt.h, 0, 17, lg_d.data_ptr(), x_d.data_ptr(), out_d.data_ptr(), 0)
+    assert e.value.code == L.MOE_ERR_UNSUPPORTED
+    dflt.close()
+    cache = make_cache(cfg, banks, max_rows=32)
     with pytest.raises(L.MoeError) as e:   # more rows than the handle was sized for
         L.moe_cache_step(cache.h, 0, 33, lg_d.data_ptr(), x_d.data_ptr(), out_d.data_ptr(), 0)
     assert e.value.code == L.MOE_ERR_UNSUPPORTED

@@ -157,7 +157,7 @@ def test_glm_multirow_rounds(lib, orc):
 def test_tiny_prefill_bypass(lib, orc, name, rows):
     cfg = workload.CONFIGS[name]
     banks = Banks(cfg)
-    cache = make_cache(cfg, banks)
+    cache = make_cache(cfg, banks, max_rows=rows)
     # warm the ring with a few decode steps, then bypass
     lg1, x1, o1 = _dev(cfg, 1)
     rt = workload.Routing(cfg)
@@ -187,7 +187,7 @@ def test_glm_prefill_bypass_sampled_rows(lib, orc):
     cfg = workload.CONFIGS["prefill"]
     rows = 64
     banks = Banks(cfg)
-    cache = make_cache(cfg, banks, layers=1)
+    cache = make_cache(cfg, banks, layers=1, max_rows=rows)
     lg = workload.prefill_logits(cfg, 0, rows)
     xb = workload.activations(cfg.seed, 0, 1, rows, cfg.hidden)[0]
     lg_d, x_d, out_d = _dev(cfg, rows)
@@ -217,7 +217,7 @@ def test_tiny_prefill_staged_equals_zero_copy(lib, orc, name):
     _put(lg_d, x_d, lg, xb)
     outs = {}
     for chunk in (-1, 0, 4, 3, 1):
-        cache = make_cache(cfg, banks, prefill_chunk=chunk)
+        cache = make_cache(cfg, banks, prefill_chunk=chunk, max_rows=rows)
         for _ in range(2):   # twice: the staging halves are reused across steps
             cache.step(0, lg_d, x_d, out_d)
         outs[chunk] = out_d.cpu().numpy().copy()
@@ -242,11 +242,11 @@ def test_glm_prefill_staged_graph_and_zero_copy(lib, orc):
     xb = workload.activations(cfg.seed, 4, 1, rows, cfg.hidden)[0]
     lg_d, x_d, out_d = _dev(cfg, rows)
     _put(lg_d, x_d, lg, xb)
-    zc = make_cache(cfg, banks, layers=1, prefill_chunk=-1)
+    zc = make_cache(cfg, banks, layers=1, prefill_chunk=-1, max_rows=rows)
     zc.step(0, lg_d, x_d, out_d)
     ref_bits = out_d.cpu().numpy().copy()
     zc.close()
-    cache = make_cache(cfg, banks, layers=1)
+    cache = make_cache(cfg, banks, layers=1, max_rows=rows)
     cache.step(0, lg_d, x_d, out_d)
     eager = out_d.cpu().numpy().copy()
     assert np.array_equal(eager.view(np.uint32), ref_bits.view(np.uint32))

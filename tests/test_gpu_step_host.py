@@ -63,12 +63,15 @@ def test_step_host_equals_device_step(lib, name, layers, steps):
 
 
 def test_step_host_rejects_too_many_rows(lib):
+    """max_rows below the cached-row limit is raised to it (every cached step
+    fits the workspaces); more rows than that are refused."""
     cfg = workload.CONFIGS["tiny"]
     banks = Banks(cfg, distinct=1)
     cache = make_cache(cfg, banks, layers=1, max_rows=2)
-    lg = torch.zeros((3, cfg.experts), dtype=torch.float32).pin_memory()
-    x = torch.zeros((3, cfg.hidden), dtype=torch.bfloat16).pin_memory()
-    out = torch.zeros((3, cfg.hidden), dtype=torch.float32).pin_memory()
+    rows = lib._lib.MOE_MAX_CACHED_ROWS + 1
+    lg = torch.zeros((rows, cfg.experts), dtype=torch.float32).pin_memory()
+    x = torch.zeros((rows, cfg.hidden), dtype=torch.bfloat16).pin_memory()
+    out = torch.zeros((rows, cfg.hidden), dtype=torch.float32).pin_memory()
     with pytest.raises(lib.MoeError):
         cache.step_host(0, lg, x, out)
     cache.close()
