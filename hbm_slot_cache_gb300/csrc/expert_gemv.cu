@@ -244,7 +244,8 @@ __device__ __forceinline__ void write_through(const uint8_t* stage, const Segs<N
 // Step counters (see kStepCounterWords).
 constexpr int kRtDoneCtr = 0;  // read-through CTAs finished
 constexpr int kWorkCtr = 1;    // read-through units taken
-constexpr int kBlockCtr = 2;   // + b: picks done for output block b
+constexpr int kBlockCtr = 2;   // + b: (pick, row) pairs finished for output block b
+constexpr int kHCtr = 2 + MOE_MAX_DIM / kOutBlockRows;  // + jl: missed pick jl's gate/up units done
 constexpr int kMaxStages = 8;  // gate/up stages at most
 
 // The plan, h and the partial outputs y' are written by a grid that may still
@@ -253,27 +254,26 @@ constexpr int kMaxStages = 8;  // gate/up stages at most
 // they carry no __restrict__: with it the compiler may read them through the
 // non-coherent path or move a load ahead of the wait.
 
-// Every thread of a down CTA, once all its units' rows are written: count
-// each unit (this CTA's pick, output blocks b0, b0 + db, ...) for its block;
-// for every block whose count this CTA completes over the step's npicks
-// picks, one warp adds out = sum_j y'_j over the block's rows in rank order
-// and resets the count.  s_lastb: room for nunits ints.
-__device__ __forceinline__ void count_blocks(const Plan* plan, const float* ypart,
-                                             float* __restrict__ out, int H, uint32_t* ctr,
-                                             int b0, int db, int nunits, int* s_lastb,
-                                             int* s_nlast) {
-  const int npicks = plan->npicks;
+// Output blocks are combined by whoever finishes them.  Each block of
+// kOutBlockRows output rows has a counter of finished (pick, row) pairs; a
+// kernel that has written y'_j for some rows of a block adds their number, and
+// the CTA whose addition brings the count to npicks * kOutBlockRows adds that
+// block's out = sum_j y'_j in rank order and resets the count.  The one-row
+// down pass finishes whole blocks of a pick; the read-through pass finishes
+// the rows of its W2 units, which may straddle blocks.
+
+// True when adding `rows` finished rows to block b completed it.
+__device__ __forceinline__ bool add_block_rows(uint32_t* ctr, int b, uint32_t rows, int npicks) {
+  const uint32_t total = (uint32_t)npicks * kOutBlockRows;
+  return atomicAdd(&ctr[kBlockCtr + b], rows) + rows == total;
+}
+
+// Every thread of the CTA: the nl blocks listed in s_lastb were completed by
+// this CTA; one warp per block (a lane per row) adds out for it.
+__device__ __forceinline__ void combine_blocks(int npicks, const float* ypart,
+                                               float* __restrict__ out, int H, uint32_t* ctr,
+                                               const int* s_lastb, int nl) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  __threadfence();
-  if (threadIdx.x == 0) *s_nlast = 0;
-  __syncthreads();
-  for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
-    const int b = b0 + u * db;
-    if (atomicAdd(&ctr[kBlockCtr + b], 1u) == (uint32_t)(npicks - 1))
-      s_lastb[atomicAdd(s_nlast, 1)] = b;
-  }
-  __syncthreads();
-  const int nl = *s_nlast;
   if (nl == 0) return;
   __threadfence();
   for (int t = warp; t < nl; t += nwarps) {  // a lane per row of the block
@@ -290,6 +290,26 @@ __device__ __forceinline__ void count_blocks(const Plan* plan, const float* ypar
     out[row] = acc;
     if (lane == 0) ctr[kBlockCtr + b] = 0u;
   }
+}
+
+// Every thread of a down CTA, once all its units' rows are written: count
+// each unit (this CTA's pick, output blocks b0, b0 + db, ...) as a whole block
+// of one pick, then combine the blocks this CTA completed.  s_lastb: room for
+// nunits ints.
+__device__ __forceinline__ void count_blocks(const Plan* plan, const float* ypart,
+                                             float* __restrict__ out, int H, uint32_t* ctr,
+                                             int b0, int db, int nunits, int* s_lastb,
+                                             int* s_nlast) {
+  const int npicks = plan->npicks;
+  __threadfence();
+  if (threadIdx.x == 0) *s_nlast = 0;
+  __syncthreads();
+  for (int u = threadIdx.x; u < nunits; u += blockDim.x) {
+    const int b = b0 + u * db;
+    if (add_block_rows(ctr, b, kOutBlockRows, npicks)) s_lastb[atomicAdd(s_nlast, 1)] = b;
+  }
+  __syncthreads();
+  combine_blocks(npicks, ypart, out, H, ctr, s_lastb, *s_nlast);
 }
 
 // One W2 row, one warp: y = sum over the row's 32-element blocks c, each the
@@ -574,20 +594,43 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
 
 // ---------------------------------------------------------- read-through
 
-// The missed picks' host-link pass, one launch.  Its work list holds, for
-// each missed pick in rank order, the pick's gate/up units (computed on
-// arrival with the functions above, then written through to the victim slot)
-// followed by its W2 bytes in stage-sized copy units (written through only).
+// A read-through stage holds a gate/up unit (kGateUpRows row pairs of W13)
+// or at least two whole W2 rows, whichever is larger.
+__host__ __device__ inline int rt_stage_bytes(int H, int I) {
+  const int gu = 2 * kGateUpRows * (H / 2) + 2 * kGateUpRows * (H / 16);
+  const int w2 = 2 * (I / 2 + I / 16);
+  return gu > w2 ? gu : w2;
+}
+
+// W2 rows in one read-through unit: the most whole rows (codes and scales)
+// that fit a stage, an even number so the scale segment stays 16-byte sized.
+__host__ __device__ inline int w2_unit_rows(int H, int I) {
+  int r = rt_stage_bytes(H, I) / (I / 2 + I / 16);
+  r &= ~1;
+  return r < H ? r : H;
+}
+
+// The missed picks' host-link pass, one launch.  Its work list holds the
+// gate/up units of every missed pick (rank order), then the W2 units of every
+// missed pick: each missed expert's bytes are read once over the host link
+// and written through to its victim slot.  A gate/up unit is computed on
+// arrival with the functions above and counts itself for its pick once its h
+// rows are written.  A W2 unit (whole rows, codes and scales) is reduced on
+// arrival too, against gscale * w * h of its pick, once every gate/up unit of
+// that pick has counted itself (a bounded wait; those units were all taken
+// before any W2 unit, by CTAs that finish them without waiting on anything,
+// so the wait always ends); its y' rows then count for their output blocks.
 // Units are taken one at a time from a step counter, so CTAs that get more of
-// the link take more, and the link streams without waiting for any h.  The
-// missed picks' down pass is the resident down kernel, launched after this
-// one on the same stream: it reads W2 from the slot (just written, so mostly
-// from L2) with the same row routine, hence the same bits.
+// the link take more.  The rows are reduced with the row routine of the down
+// pass (h staged in shared memory instead of registers), so a missed pick's
+// y' has the same bits as if it were resident.
+// (Half the SMs, one CTA each; 96 registers a thread leave room on the SM for
+// one CTA of the resident picks' gate/up beside it at the GLM shape.)
 template <int RPT, bool WARP_RED>
-__global__ void __launch_bounds__(kGateUpThreads, 2)
+__global__ void __maxnreg__(96)
 gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
-                        float* __restrict__ hbuf, int H, int I, int RL, int NS, uint32_t* flags,
-                        uint32_t* ctr, PickBounds bounds) {
+                        float* hbuf, float* ypart, float* __restrict__ out, int H, int I,
+                        int RL, int NS, uint32_t* flags, uint32_t* ctr, PickBounds bounds) {
   constexpr int V = 2 * RPT;
   constexpr int R = kGateUpRows;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -596,12 +639,19 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   __shared__ int s_next[2];           // by iteration parity: read after the writer moved on
   __shared__ int s_pick[MOE_MAX_TOPK];  // the missed picks, checked
   __shared__ int s_pcnt;
+  __shared__ int s_hpick;   // missed pick whose f * h sits in hs (-1: none)
+  __shared__ int s_hwait;   // the wait for a pick's h ended (1) or gave up (0)
+  __shared__ int s_lastb[MOE_MAX_DIM / kOutBlockRows];
+  __shared__ int s_nlast;
   const int C = H / 32;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int g = tid / C, c = tid - g * C;
   const int cb = R * H / 2, sb = R * H / 16;
-  const int SB = 2 * cb + 2 * sb;  // stage bytes
+  const int SB = rt_stage_bytes(H, I);  // stage bytes
   Stages S = carve(smem, NS, SB);
+  const int red_floats = WARP_RED ? RL * (C / 32) * V : (int)blockDim.x * V;
+  float* hs = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(S.red + red_floats) + 15) & ~(uintptr_t)15);  // [I], transposed
 
   // The missed picks, each checked (index, slot and host pointers) before it
   // addresses memory: a bad plan skips the whole launch (MOE_FLAG_BAD_PLAN).
@@ -617,28 +667,32 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     ok = __all_sync(0xFFFFFFFFu, ok);
     if (!plan_ok(ok || tid != 0, flags) || !ok) pcnt = 0;
     if (tid < pcnt) s_pick[tid] = j;
-    if (tid == 0) s_pcnt = pcnt;
+    if (tid == 0) {
+      s_pcnt = pcnt;
+      s_hpick = -1;
+    }
   }
   __syncthreads();
   const int pcnt = s_pcnt;
+  const int npicks = plan->npicks;
   auto pick_of = [&](int jl) { return s_pick[jl]; };
-  const int upp = I / R;                                   // gate/up units per pick
-  const size_t w2c = (size_t)H * (I / 2), w2s = (size_t)H * (I / 16);
-  const int ncc = (int)((w2c + SB - 1) / SB), ncs = (int)((w2s + SB - 1) / SB);
-  const int upk = upp + ncc + ncs;                         // link units per pick
-  const int NL = pcnt * upk;
+  const int upp = I / R;                   // gate/up units per pick
+  const int R2 = w2_unit_rows(H, I);       // W2 rows per unit
+  const int n2 = (H + R2 - 1) / R2;        // W2 units per pick
+  const int NG = pcnt * upp;               // the gate/up units come first
+  const int NL = NG + pcnt * n2;
   const uint64_t wait_ns = plan_wait_ns(plan);
 
   // link unit u: its byte segments in host memory and in the pick's slot
   auto segs = [&](int u, int& nseg) {
-    const int jl = u / upk, r = u - jl * upk;
-    const int j = pick_of(jl);
-    const uint8_t* hw = plan->hwptr[j];
-    const uint8_t* hsc = plan->hsptr[j];
-    uint8_t* dw = const_cast<uint8_t*>(plan->wptr[j]);
-    uint8_t* ds = const_cast<uint8_t*>(plan->sptr[j]);
     Segs<4> sg;
-    if (r < upp) {
+    if (u < NG) {
+      const int jl = u / upp, r = u - jl * upp;
+      const int j = pick_of(jl);
+      const uint8_t* hw = plan->hwptr[j];
+      const uint8_t* hsc = plan->hsptr[j];
+      uint8_t* dw = const_cast<uint8_t*>(plan->wptr[j]);
+      uint8_t* ds = const_cast<uint8_t*>(plan->sptr[j]);
       const size_t og = (size_t)r * R, ou = (size_t)I + (size_t)r * R;
       sg.src[0] = hw + og * (H / 2);
       sg.src[1] = hw + ou * (H / 2);
@@ -651,20 +705,19 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
       sg.n[0] = sg.n[1] = cb;
       sg.n[2] = sg.n[3] = sb;
       nseg = 4;
-    } else if (r < upp + ncc) {  // W2 codes follow the 2I W13 code rows
-      const size_t k0 = (size_t)(r - upp) * SB;
-      const size_t off = (size_t)I * H + k0;
-      sg.src[0] = hw + off;
-      sg.dst[0] = dw + off;
-      sg.n[0] = (int)(w2c - k0 < (size_t)SB ? w2c - k0 : (size_t)SB);
-      nseg = 1;
-    } else {  // W2 scales follow the 2I W13 scale rows
-      const size_t k0 = (size_t)(r - upp - ncc) * SB;
-      const size_t off = (size_t)I * H / 8 + k0;
-      sg.src[0] = hsc + off;
-      sg.dst[0] = ds + off;
-      sg.n[0] = (int)(w2s - k0 < (size_t)SB ? w2s - k0 : (size_t)SB);
-      nseg = 1;
+    } else {  // W2 rows r0 .. r0 + nr - 1: codes after the 2I W13 code rows, scales likewise
+      const int v = u - NG, jl = v / n2, r0 = (v - jl * n2) * R2;
+      const int nr = H - r0 < R2 ? H - r0 : R2;
+      const int j = pick_of(jl);
+      const size_t oc = (size_t)I * H + (size_t)r0 * (I / 2);
+      const size_t os = (size_t)I * H / 8 + (size_t)r0 * (I / 16);
+      sg.src[0] = plan->hwptr[j] + oc;
+      sg.src[1] = plan->hsptr[j] + os;
+      sg.dst[0] = const_cast<uint8_t*>(plan->wptr[j]) + oc;
+      sg.dst[1] = const_cast<uint8_t*>(plan->sptr[j]) + os;
+      sg.n[0] = nr * (I / 2);
+      sg.n[1] = nr * (I / 16);
+      nseg = 2;
     }
     return sg;
   };
@@ -701,17 +754,58 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
       i_abort = i;
       break;
     }
-    const int jl = unit / upk, r = unit - jl * upk;
     const uint8_t* st = S.base + (size_t)stage * SB;
     int nseg = 0;
     const Segs<4> sg = segs(unit, nseg);
-    if (r < upp) {  // uniform over the CTA
+    const bool gu = unit < NG;  // uniform over the CTA
+    int jl = 0, r = 0;
+    if (gu) {
+      jl = unit / upp;
+      r = unit - jl * upp;
       float a[V];
       gateup_partials<RPT>(st, H, RL, g, c, xh, a);
       write_through(st, sg, nseg);
       stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
     } else {
+      const int v = unit - NG;
+      jl = v / n2;
+      const int r0 = (v - jl * n2) * R2, nr = H - r0 < R2 ? H - r0 : R2;
       write_through(st, sg, nseg);
+      if (s_hpick != jl) {  // uniform: this pick's h into shared memory, once it is complete
+        if (tid == 0)
+          s_hwait = count_wait_bounded(&ctr[kHCtr + jl], (uint32_t)upp, flags, wait_ns) ? 1 : 0;
+        __syncthreads();
+        if (!s_hwait) {
+          if (tid == 0) *S.abort_flag = 1;
+          i_abort = i;
+          break;  // uniform; the copies in flight are drained below
+        }
+        const int j = pick_of(jl);
+        const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
+        for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
+          hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
+        if (tid == 0) s_hpick = jl;
+        __syncthreads();
+      }
+      const int j = pick_of(jl);
+      for (int rr = warp; rr < nr; rr += nwarps) {  // a warp per row, as in the down pass
+        const float y = w2_row_warp(st + rr * (I / 2), st + nr * (I / 2) + rr * (I / 16), hs, I,
+                                    lane);
+        if (lane == 0) ypart[(size_t)j * H + r0 + rr] = y;
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {  // count the rows for their output blocks; combine what completes
+        int nl = 0;
+        for (int b = r0 / kOutBlockRows; b * kOutBlockRows < r0 + nr; ++b) {
+          const int lo = b * kOutBlockRows > r0 ? b * kOutBlockRows : r0;
+          const int hi = (b + 1) * kOutBlockRows < r0 + nr ? (b + 1) * kOutBlockRows : r0 + nr;
+          if (add_block_rows(ctr, b, (uint32_t)(hi - lo), npicks)) s_lastb[nl++] = b;
+        }
+        s_nlast = nl;
+      }
+      __syncthreads();
+      combine_blocks(npicks, ypart, out, H, ctr, s_lastb, s_nlast);
     }
     if (tid == 0) {  // before the barrier: with one stage the next iteration reads it before any barrier
       const int nv = taken < NL ? taken : -1;
@@ -719,9 +813,18 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
       s_unit[stage] = nv;
     }
     __syncthreads();
-    if (r < upp && tid < RL * RPT)
-      gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan->gs[pick_of(jl)][0],
-                                     plan->gs[pick_of(jl)][1], pick_of(jl), r, xup, hbuf, I, tid);
+    if (gu) {  // h rows of the unit, then the unit counts for its pick
+      if (tid < RL * RPT) {
+        gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan->gs[pick_of(jl)][0],
+                                       plan->gs[pick_of(jl)][1], pick_of(jl), r, xup, hbuf, I, tid);
+        __threadfence();
+      }
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        atomicAdd(&ctr[kHCtr + jl], 1u);
+      }
+    }
     const int nxt = s_next[i & 1];
     if (nxt >= 0) fill(nxt, stage);
   }
@@ -731,10 +834,11 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     // on its stage's mbarrier, so wait (default limit) until the pending fills'
     // phases are complete: no arrival may reach this CTA's shared memory after
     // it exits.  Iteration it consumes phase it / NS of stage it % NS.
+    __syncthreads();
     if (tid == 0)
       for (int d = 0; d < NS; ++d) {
-        const int it = i_abort + d, st = it % NS;
-        if (s_unit[st] >= 0 && !mbar_wait_bounded(&S.full[st], (uint32_t)((it / NS) & 1), flags))
+        const int it = i_abort + d, stg = it % NS;
+        if (s_unit[stg] >= 0 && !mbar_wait_bounded(&S.full[stg], (uint32_t)((it / NS) & 1), flags))
           break;
       }
     __syncthreads();
@@ -742,6 +846,7 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   // the last CTA out (no unit is taken after it) resets the launch's counters
   if (tid == 0 && atomicAdd(&ctr[kRtDoneCtr], 1u) == gridDim.x - 1) {
     ctr[kWorkCtr] = 0u;
+    for (int q = 0; q < MOE_MAX_TOPK; ++q) ctr[kHCtr + q] = 0u;
     ctr[kRtDoneCtr] = 0u;
   }
 }
@@ -924,17 +1029,22 @@ cudaError_t run_gateup(cudaStream_t st, int grid, const GateUpShape& s, const Pl
 
 template <int RPT, bool WR>
 cudaError_t run_readthrough(cudaStream_t st, int grid, const GateUpShape& s, const Plan* plan,
-                            const uint16_t* x, float* hbuf, int H, int I, uint32_t* flags,
-                            uint32_t* ctr, const PickBounds& b) {
+                            const uint16_t* x, const GemvWorkspace& ws, float* out, int H, int I,
+                            uint32_t* flags, uint32_t* ctr, const PickBounds& b) {
   auto kern = gemv_readthrough_kernel<RPT, WR>;
+  // stages, their mbarriers, the abort word, one set of partial sums, and the
+  // W2 units' f * h (transposed, 16-byte aligned)
+  const int V = 2 * s.RPT;
+  const int red_floats = s.warp_red ? s.RL * (s.C / 32) * V : s.NT * V;
+  const int smem = s.NS * rt_stage_bytes(H, I) + 8 * s.NS + 8 + red_floats * 4 + 16 + I * 4;
   static int smem_set = 0;
-  if (s.smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = prefer_max_shared(kern);
     if (e != cudaSuccess) return e;
-    smem_set = s.smem;
+    smem_set = smem;
   }
-  kern<<<grid, s.NT, s.smem, st>>>(plan, x, hbuf, H, I, s.RL, s.NS, flags, ctr, b);
+  kern<<<grid, s.NT, smem, st>>>(plan, x, ws.hbuf, ws.ypart, out, H, I, s.RL, s.NS, flags, ctr, b);
   return cudaGetLastError();
 }
 
@@ -1021,12 +1131,12 @@ int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how) {
 
 cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uint16_t* x, int H,
                                     int I, int k, const GemvWorkspace& ws, uint32_t* flags,
-                                    int num_sms, const GemvLaunch& how, uint32_t* ctr) {
+                                    int num_sms, const GemvLaunch& how, float* out, uint32_t* ctr) {
   const GateUpShape s = gateup_shape(H, how.stages);
   if (s.NS < 1 || s.NT > kGateUpThreads || !how.from_host || how.subset != kPicksMiss)
     return cudaErrorInvalidConfiguration;
   const int grid = gemv_readthrough_grid(I, k, num_sms, how);
-  GATEUP_DISPATCH(run_readthrough, st, grid, s, plan, x, ws.hbuf, H, I, flags, ctr, how.bounds)
+  GATEUP_DISPATCH(run_readthrough, st, grid, s, plan, x, ws, out, H, I, flags, ctr, how.bounds)
 }
 #undef GATEUP_DISPATCH
 

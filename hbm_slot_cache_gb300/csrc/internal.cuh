@@ -170,20 +170,23 @@ struct GemvLaunch {
 };
 // Counters of a one-row step (zero between steps; each user resets its own):
 //   [0] read-through CTAs that have finished, [1] read-through units taken,
-//   [2 + b] picks whose y'_j rows of output block b (kOutBlockRows rows) are written.
+//   [2 + b] (pick, row) pairs whose y'_j row of output block b (kOutBlockRows
+//   rows) is written, [2 + H / kOutBlockRows max + jl] gate/up units of missed
+//   pick jl whose h rows are written (read-through).
 constexpr int kOutBlockRows = 32;
-constexpr int kStepCounterWords = 2 + MOE_MAX_DIM / kOutBlockRows;
+constexpr int kStepCounterWords = 2 + MOE_MAX_DIM / kOutBlockRows + MOE_MAX_TOPK;
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
                                int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
                                const GemvLaunch& how);
 // The missed picks' host-link pass (subset kPicksMiss, from_host): each
-// missed expert read once from host memory and written through to its slot,
-// gate/up + SwiGLU computed on its W13 rows on the way in -> ws.hbuf.  Takes
-// its work from ctr[1]; its last CTA resets ctr[0..1].  Their down pass is
-// launch_gemv_down with subset kPicksMiss, after this launch on its stream.
+// missed expert read once from host memory and written through to its slot;
+// gate/up + SwiGLU computed on its W13 rows on the way in -> ws.hbuf, then
+// its W2 rows reduced on the way in -> ws.ypart, counted for their output
+// blocks (combined into out by whichever launch completes a block).  Takes
+// its work from ctr[1]; its last CTA resets ctr[0..1] and the h counters.
 cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uint16_t* x, int H,
                                     int I, int k, const GemvWorkspace& ws, uint32_t* flags,
-                                    int num_sms, const GemvLaunch& how, uint32_t* ctr);
+                                    int num_sms, const GemvLaunch& how, float* out, uint32_t* ctr);
 int gemv_readthrough_grid(int I, int k, int num_sms, const GemvLaunch& how);
 // y'_j = gscale_j * w_j * (W2_j h_j) for the subset's picks -> ws.ypart [k][H], a unit
 // being kOutBlockRows rows of one pick.  Each finished unit is counted in ctr[2 + b] for
@@ -335,16 +338,18 @@ __device__ __forceinline__ bool plan_ok(bool cond, uint32_t* flags) {
   return cond;
 }
 
-// Waits (acquire, at most ~2 s) until the global counter *ctr reaches target;
-// on timeout sets MOE_FLAG_WAIT_TIMEOUT in *flags and returns false.
+// Waits (acquire, at most limit_ns, default ~2 s) until the global counter
+// *ctr reaches target; on timeout sets MOE_FLAG_WAIT_TIMEOUT in *flags and
+// returns false.
 __device__ __forceinline__ bool count_wait_bounded(const uint32_t* ctr, uint32_t target,
-                                                   uint32_t* flags) {
+                                                   uint32_t* flags,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = global_ns();
   while (true) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
     if (v >= target) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(flags, MOE_FLAG_WAIT_TIMEOUT);
       return false;
     }

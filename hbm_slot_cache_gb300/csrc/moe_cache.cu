@@ -440,14 +440,14 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
   if (one_row) {
     // One row.  After route/remap the missed picks take a second stream: one
     // read-through launch reads each missed expert once over the host link,
-    // computes its gate/up on the way in and writes it through to the victim
-    // slot; then their down pass reads W2 back from the slot.  Meanwhile the
-    // resident picks' gate/up and down run on the caller's stream, so the hit
-    // experts' HBM reads overlap the host-link transfer.  Each pick's weighted
-    // output y'_j is computed the same way whichever path it takes, and the
-    // CTA that completes an output block's count over the step's picks (from
-    // either down launch) adds that block in rank order, so the result does
-    // not depend on the hit/miss split.
+    // writes it through to the victim slot and computes its gate/up and then
+    // its down rows on the way in.  Meanwhile the resident picks' gate/up and
+    // down run on the caller's stream, so the hit experts' HBM reads overlap
+    // the host-link transfer.  Each pick's weighted output y'_j is computed
+    // with the same arithmetic whichever path it takes, and the CTA that
+    // completes an output block's count over the step's picks (from either
+    // launch) adds that block in rank order, so the result does not depend on
+    // the hit/miss split.
     if (e == cudaSuccess)
       e = launch_route_remap(st, router_logits, rows, h->E, h->k, h->S_of[layer], h->Bw, h->Bs, L, h->plan,
                              h->opts.all_resident, nullptr);
@@ -468,8 +468,6 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     pb.Bw = h->Bw;
     pb.Bs = h->Bs;
     const GemvLaunch miss{kPicksMiss, true, rt_grid, 2, false, pb};
-    // their down pass starts as the read-through launch drains (not across a timing event)
-    const GemvLaunch miss_dn{kPicksMiss, false, 0, 4, !h->timing, pb};
     // resident picks: slot bytes from HBM
     // Gate/up is launched normally, after route/remap, so the second stream's
     // higher priority places the read-through CTAs first (two gate/up CTAs
@@ -480,11 +478,8 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     if (e == cudaSuccess) e = mark(2, h->side);
     if (e == cudaSuccess)
       e = launch_gemv_readthrough(h->side, h->plan, x, h->H, h->I, h->k, h->gemv, flags,
-                                  h->num_sms, miss, h->gemv.tile_cnt);
+                                  h->num_sms, miss, out, h->gemv.tile_cnt);
     if (e == cudaSuccess) e = mark(3, h->side);
-    if (e == cudaSuccess)
-      e = launch_gemv_down(h->side, h->plan, h->H, h->I, h->k, h->gemv, flags, h->num_sms,
-                           miss_dn, out, h->gemv.tile_cnt);
     if (e == cudaSuccess) e = mark(4, h->side);
     if (e == cudaSuccess) e = cudaEventRecord(h->join, h->side);
     if (e == cudaSuccess)

@@ -193,10 +193,19 @@ int moe_cache_step_host(moe_cache_t* h, int layer, int rows, const float* router
                         const uint16_t* x, float* out, void* stream);
 
 /* Counters of one layer (layer >= 0) or summed over all layers (layer == -1;
- * error_flags OR-ed).  Waits for all device work (device synchronize). */
+ * error_flags OR-ed).  The counts follow how the pages account for the cache
+ * ("GB300 GLM 5.3 Testing": the September 14 correction counts misses per
+ * layer-step; the September 7 E0/E1/E5 window history takes the hit rate over
+ * the routed picks of an engine step, rows * top_k): hit rate = hits / picks,
+ * misses are unique experts fetched per layer-step.  Waits for all device work
+ * (device synchronize). */
 int moe_cache_stats(const moe_cache_t* h, int layer, moe_cache_stats_t* out);
 
-/* expert_of_slot: host int32 [layer's ring size]; -1 = empty.  Device synchronize. */
+/* The ring's owner table ("GLM 5.3 Testing: HBM Expert Allocation", "What the
+ * slot cache is": the router asks by expert id and the cache answers with a
+ * slot; this is the reverse view, which expert each slot holds).
+ * expert_of_slot: host int32 [layer's ring size]; -1 = empty.  Device
+ * synchronize. */
 int moe_cache_slot_map(const moe_cache_t* h, int layer, int32_t* expert_of_slot);
 
 /* *slots = the ring size of `layer`. */
@@ -213,7 +222,10 @@ int moe_cache_trace(const moe_cache_t* h, int layer, moe_step_record_t* recs, in
                     int* n_recs);
 
 /* Empty every ring, zero counters, flags and traces (all_resident: reload
- * identity map).  Device synchronize. */
+ * identity map): the state at create.  The cache state is a function of the
+ * routing history alone (exact LRU with stamps, "What the slot cache is"), so
+ * reset + replaying a routing history reproduces any earlier state; the pages
+ * have no further checkpoint for it.  Device synchronize. */
 int moe_cache_reset(moe_cache_t* h);
 
 /* Failure-detection hook (for tests of the timeout path; production code
@@ -228,9 +240,12 @@ int moe_cache_reset(moe_cache_t* h);
  * Errors: MOE_ERR_ARG (microseconds < 0), MOE_ERR_CUDA. */
 int moe_cache_set_wait_timeout(moe_cache_t* h, int microseconds);
 
-/* Free everything the handle owns (not the host backing).  NULL is a no-op. */
+/* Free everything the handle owns (not the host backing).  NULL is a no-op.
+ * Handle lifetime is the library's own; the pages have no counterpart. */
 int moe_cache_destroy(moe_cache_t* h);
 
+/* A static string naming a MOE_OK / MOE_ERR_* code (the library's own; the
+ * pages have no counterpart). */
 const char* moe_cache_strerror(int code);
 
 /* Byte sizes of one expert's codes (Bw) and scales (Bs) for (hidden, inter). */
@@ -261,8 +276,8 @@ int moe_probe_host_link(const void* host_src, void* dev_dst, size_t bytes, int m
  * event-record nodes):
  *   0 before route/remap, 1 after it (caller's stream);
  *   one-row steps, the library's second stream: 2 before the missed picks'
- *     read-through pass (host -> slot with gate/up on the way in), 3 after
- *     it, 4 after the missed picks' down pass;
+ *     read-through pass (host -> slot with gate/up and down on the way in),
+ *     3 and 4 after it;
  *   multi-row steps, the caller's stream: 2 after the miss copy, 3 after the
  *     grouped gate/up, 4 after the grouped down;
  *   5 after the resident picks' gate/up, 6 after their down (one-row steps;
