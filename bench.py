@@ -92,7 +92,7 @@ def _breakdown(ev):
     if len(ev) == 0:
         return None
     m = ev.mean(axis=0)
-    return {"route": m[1], "read_through": m[3] - m[2], "missed_down": m[4] - m[3],
+    return {"route": m[1], "read_through": m[3] - m[2],
             "resident_gateup": m[5] - m[1],
             "resident_down": m[6] - m[5], "join_to_end": m[7] - max(m[6], m[4]), "step": m[7]}
 
@@ -521,7 +521,6 @@ def kernel_table(cfg, res: dict, hbm_peak: float, link_peak: float) -> tuple[dic
     G = len(ev)
     t_route = ev[:, 1]
     t_rt = ev[:, 3] - ev[:, 2]
-    t_dn_miss = ev[:, 4] - ev[:, 3]
     t_gu_hit = ev[:, 5] - ev[:, 1]
     t_dn_hit = ev[:, 6] - ev[:, 5]
     gu_pick = 2 * I * (H // 2 + H // 16)
@@ -542,21 +541,18 @@ def kernel_table(cfg, res: dict, hbm_peak: float, link_peak: float) -> tuple[dic
                                            hbm_peak, "hbm", G),
         "gemv_readthrough[missed picks]": entry(float((n_miss * Bexp).sum()),
                                                 float(t_rt[hm].sum()), link_peak, "host-link", nm),
-        "gemv_down[missed picks]": entry(float((n_miss * dn_pick).sum()), float(t_dn_miss[hm].sum()),
-                                         hbm_peak, "hbm", nm),
         "route_remap": {"ms_per_launch": float(t_route.mean())},
     }
     for n in kern:
         if "resident" in n:
             kern[n]["traffic"] = _traffic(n.split("[")[0], float(n_hit.mean()))
         elif "missed" in n:
-            kern[n]["traffic"] = _traffic(n.split("[")[0] + ("_missed" if "down" in n else ""),
+            kern[n]["traffic"] = _traffic(n.split("[")[0],
                                           float(n_miss[hm].mean()) if hm.any() else 0.0)
             kern[n]["note"] = "steps with at least one miss"
     kern["gemv_readthrough[missed picks]"]["note"] += (
-        "; whole missed experts over the host link, gate/up computed on the way in, "
-        "written to their slots")
-    kern["gemv_down[missed picks]"]["note"] += "; W2 rows read back from the slots just written"
+        "; whole missed experts over the host link, written to their slots, gate/up and "
+        "down computed on the way in; traffic = its DRAM bytes (the slot write-through)")
     split = {"ms_per_step_event_graph": float(ev[:, 7].mean()),
              "ms_miss_path": float(np.mean(ev[:, 4] - ev[:, 1])),
              "ms_hit_path": float(np.mean(ev[:, 6] - ev[:, 1])),
@@ -634,8 +630,8 @@ def run_ours(args) -> None:
             "tok_s_equivalent": res["value"] / GLM_MOE_LAYERS,
             "path_roofline": path, "roofline": roofline, "kernels": kern, "timing_split": split,
             "cold": res["cold"], "cpu_baseline": cpu, "e2e": res["e2e"],
-            "gpu_launches": K * 6, "launches_per_step": "feeder + route/remap + read-through + "
-                                                        "missed down + gate/up + resident down",
+            "gpu_launches": K * 5, "launches_per_step": "feeder + route/remap + read-through + "
+                                                        "gate/up + resident down",
             "clocks": res["clocks"],
         }
         print(json.dumps(line), flush=True)
