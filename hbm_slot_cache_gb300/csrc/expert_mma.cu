@@ -30,6 +30,11 @@
 // warp writes its own lane quadrant, and each step's word is written to four
 // adjacent columns, so the MMA finds the scales whichever of those columns its
 // quadrant reads.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "internal.cuh"
 
 namespace moe {
@@ -58,6 +63,13 @@ struct MmaArgs {
   float* out;   // gate/up: h [P][I]; down: y [P][H]
   uint32_t* flags;
   int g0, g1;   // the launch's groups [g0, g1) (kHitGroups: the step's hit-group count)
+  // cp.async kernel only: a launch whose first group's expert lies in this
+  // region (base, experts, bytes per expert; null: none) is left to the TMA
+  // kernel launched beside it.  A step's groups are all in one place: the
+  // slots, the staging halves, or host memory (a bypass).
+  const uint8_t* skip_w;
+  unsigned long long skip_n;
+  long long skip_Bw;
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
@@ -96,6 +108,23 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&w)[4]
       : "memory");
 }
 
+// Epilogue arithmetic shared by both grouped kernels, so a member gets the same
+// bits from either: the levels of one accumulator row (columns
+// s * kLevels + l) summed in level order with their level scales, and
+// h = silu(gate) * up with the expert's global scales applied first.
+__device__ __forceinline__ float level_sum(const float (&gl)[kLevels], const uint32_t* v) {
+  float acc = 0.f;
+#pragma unroll
+  for (int l = 0; l < kLevels; ++l) acc = fmaf(gl[l], __uint_as_float(v[l]), acc);
+  return acc;
+}
+
+__device__ __forceinline__ float swiglu_h(float gs_gate, float vg, float gs_up, float vu) {
+  const float gate = gs_gate * vg;
+  const float up = gs_up * vu;
+  return gate / (1.0f + expf(-gate)) * up;
+}
+
 template <int P>  // 16-byte pieces per row per chunk (8: 256 elements, 4: 128)
 __global__ void __launch_bounds__(kThreads)
 grouped_mma_kernel(MmaArgs a) {
@@ -114,6 +143,7 @@ grouped_mma_kernel(MmaArgs a) {
   const int jbeg = g0 < ng ? gp->g_job[g0] : gp->n_jobs;
   const int jend = gp->g_job[g1 < ng ? g1 : ng];
   if (jbeg + (int)blockIdx.x >= jend) return;  // uniform: before any TMEM or barrier use
+  if (a.skip_w && expert_ptr_ok(gp->g_wptr[g0], a.skip_w, a.skip_n, a.skip_Bw)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.y;
   const int K = a.K, H = a.H, I = a.I;
@@ -330,12 +360,7 @@ grouped_mma_kernel(MmaArgs a) {
     const int row = 32 * warp + lane;  // tile row
     float val[kRowsPerJob];
 #pragma unroll
-    for (int s = 0; s < kRowsPerJob; ++s) {
-      float acc = 0.f;
-#pragma unroll
-      for (int l = 0; l < kLevels; ++l) acc = fmaf(s_gl[s][l], __uint_as_float(v[s * kLevels + l]), acc);
-      val[s] = acc;
-    }
+    for (int s = 0; s < kRowsPerJob; ++s) val[s] = level_sum(s_gl[s], v + s * kLevels);
     const float* gsc = gp->g_gs + 3 * g;
     if (a.gate_up) {
       float* s_up = reinterpret_cast<float*>(smem);  // stages are idle now
@@ -344,11 +369,9 @@ grouped_mma_kernel(MmaArgs a) {
         for (int s = 0; s < kRowsPerJob; ++s) s_up[(row - 64) * kRowsPerJob + s] = val[s];
       __syncthreads();
       if (row < 64) {
-        for (int s = 0; s < nmem; ++s) {
-          const float gate = gsc[0] * val[s];
-          const float up = gsc[1] * s_up[row * kRowsPerJob + s];
-          a.out[(size_t)s_pick[s] * I + 64 * mt + row] = gate / (1.0f + expf(-gate)) * up;
-        }
+        for (int s = 0; s < nmem; ++s)
+          a.out[(size_t)s_pick[s] * I + 64 * mt + row] =
+              swiglu_h(gsc[0], val[s], gsc[1], s_up[row * kRowsPerJob + s]);
       }
     } else {
       for (int s = 0; s < nmem; ++s)
@@ -382,6 +405,399 @@ grouped_mma_kernel(MmaArgs a) {
                  "r"(kTmemCols));
 }
 
+// ------------------------------------------------- TMA-staged grouped kernel
+//
+// The same jobs and arithmetic, the weight operand moved by the tensor memory
+// accelerator.  Slot (or staging) bytes are viewed as 2-D row arrays (the
+// TmaSource views), and each chunk's weight tile is two 128-row x 128-byte
+// boxes (256 elements of K) in the 128-byte swizzle the MMA reads directly,
+// plus the boxes of their scale words.  A work item is (job, tile): gate/up
+// tiles pair 128 gate rows with the matching 128 up rows (one MMA each, so a
+// TMEM lane holds both of its row's accumulators), down tiles are 256 W2
+// rows.  One persistent CTA per SM takes items round robin.  Warp 4 keeps
+// kTStages chunks in flight (TMA for the weight codes and scales, 16-byte
+// cp.async for the members' activation levels and their scales) and runs on
+// into the CTA's next item, so the HBM stream does not stop at an item
+// boundary.  Warps 0-3 own the TMEM lane quadrants: per chunk they move the
+// scale words to TMEM and count in on an mbarrier, thread 0 issues the
+// chunk's MMAs and commits them to the stage's "empty" mbarrier; after an
+// item's last chunk they read the accumulators and write h or y.  Every wait
+// is bounded: one that runs out sets the CTA's abort word and everyone stops;
+// copies and MMAs in flight are drained (bounded) before the TMEM is freed.
+
+constexpr int kTThreads = 160;
+constexpr int kTRows = 128;                     // rows of one MMA (M); two per item
+constexpr int kTABytes = kTRows * 128;          // one weight box: 128 rows x 256 elements
+constexpr int kTSfaBytes = kTRows * 16;         // its rows' scale words for the chunk
+constexpr int kTOffSfa = 2 * kTABytes;
+constexpr int kTOffB = kTOffSfa + 2 * kTSfaBytes;
+constexpr int kTOffSfb = kTOffB + kBBytes;
+constexpr int kTStageBytes = 41 * 1024;         // kTOffSfb + kSfbBytes, rounded up to 1 KB
+constexpr int kTStages = 4;
+constexpr int kTSmemBytes = kTStages * kTStageBytes + 1024;  // + room to align to 1 KB
+constexpr int kTTmemCols = 256;
+constexpr int kTColSF = 64;  // scale slot s (chunk parity): 64 + 64 s; SFA halves +0, +16; SFB +32
+static_assert(kTOffSfb + kSfbBytes <= kTStageBytes, "stage layout");
+static_assert(kTStageBytes % 1024 == 0, "weight boxes must stay 1 KB aligned");
+
+struct MmaTmaArgs {
+  TmaMap map_w;  // codes view of the launch's matrix block
+  TmaMap map_s;  // its scales view
+  MmaArgs m;
+  const uint8_t* base_w;
+  const uint8_t* base_s;
+  long long Bw, Bs;
+  unsigned long long n;  // experts in the region
+  int rps;               // view rows per expert: 3I (K = H) or 3H (K = I)
+  int row0;              // first view row of the block within an expert: 0 (W13), 2H (W2)
+};
+
+// K-major operand in the 128-byte swizzle: 8-row groups 1 KB apart; a 64-element
+// K step inside the 128-byte row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;              // leading byte offset: unused for this layout
+  d |= (uint64_t)(1024u >> 4) << 32;   // 8-row groups: 1 KB
+  d |= (uint64_t)1 << 46;              // sm_100-family descriptor version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const TmaMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// The mbarrier receives one arrival once this thread's earlier cp.async
+// copies have landed (counted in its expected arrivals).
+__device__ __forceinline__ void cp_async_bar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+// One work item's plan entries, checked before they address memory (a bad
+// entry sets MOE_FLAG_BAD_PLAN and the item is skipped by every warp alike:
+// the plan does not change during the launch).
+struct TItem {
+  int g, gstart, m0, nmem, mt;
+  int vw, vs;  // the group's expert in the region: codes, scales
+};
+
+__device__ __forceinline__ bool t_item(const MmaTmaArgs& a, int jbeg, int m_tiles, int it,
+                                       TItem& t) {
+  const GroupPlan* gp = a.m.gp;
+  uint32_t* fl = a.m.flags;
+  const int jo = it / m_tiles;
+  const int job = jbeg + jo;
+  t.mt = it - jo * m_tiles;
+  if (!plan_ok(job >= 0 && job < gp->n_jobs, fl)) return false;
+  const int jv = gp->jobs[job];
+  t.g = jv >> 8;
+  const int tile = jv & 255;
+  if (!plan_ok(t.g >= 0 && t.g < gp->n_groups, fl)) return false;
+  t.gstart = gp->g_start[t.g];
+  const int gcount = gp->g_count[t.g];
+  if (!plan_ok(t.gstart >= 0 && gcount >= 1 && t.gstart + gcount <= gp->npicks, fl)) return false;
+  t.m0 = tile * kRowsPerJob;
+  if (!plan_ok(t.m0 < gcount, fl)) return false;
+  t.nmem = min(kRowsPerJob, gcount - t.m0);
+  const uint8_t* w = gp->g_wptr[t.g];
+  const uint8_t* s = gp->g_sptr[t.g];
+  if (!plan_ok(expert_ptr_ok(w, a.base_w, a.n, a.Bw) && expert_ptr_ok(s, a.base_s, a.n, a.Bs), fl))
+    return false;
+  t.vw = (int)((w - a.base_w) / a.Bw);
+  t.vs = (int)((s - a.base_s) / a.Bs);
+  return true;
+}
+
+// Member s of the item's tile: its pick index, and the activation row its
+// levels start at (gate/up: the token row, down: the pick).
+__device__ __forceinline__ void t_member(const MmaTmaArgs& a, const TItem& t, int s, int& pick,
+                                         int& brow) {
+  pick = -1;
+  brow = 0;
+  if (s < t.nmem) {
+    int p = a.m.gp->members[t.gstart + t.m0 + s];
+    if (!plan_ok(p >= 0 && p < a.m.gp->npicks, a.m.flags)) p = 0;
+    pick = p;
+    brow = a.m.gate_up ? p / a.m.k : p;
+  }
+}
+
+__global__ void __launch_bounds__(kTThreads, 1)
+grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t s_full[kTStages], s_empty[kTStages], s_sfready, s_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const MmaArgs& m = a.m;
+  const GroupPlan* gp = m.gp;
+  const int ng = gp->n_groups;
+  const int nh = min(max(gp->n_hit_groups, 0), ng);
+  const int g0 = m.g0 == kHitGroups ? nh : max(m.g0, 0);
+  const int g1 = m.g1 == kHitGroups ? nh : m.g1;
+  const int jbeg = g0 < ng ? gp->g_job[g0] : gp->n_jobs;
+  const int jend = gp->g_job[g1 < ng ? g1 : ng];
+  const int m_tiles = m.gate_up ? m.I / kTRows : m.H / (2 * kTRows);
+  const int n_items = max(jend - jbeg, 0) * m_tiles;
+  const int mine =
+      (int)blockIdx.x < n_items ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (mine == 0) return;  // uniform: before any TMEM or barrier use
+  // experts outside the region (a bypass step's host memory): the cp.async kernel's
+  if (!expert_ptr_ok(gp->g_wptr[g0], a.base_w, a.n, a.Bw)) return;
+  const int nchunks = m.K / 256;
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_word = &s_abort;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&s_tmem)),
+                 "r"(kTTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(&s_full[s], 33);  // the expect_tx arrival + one per loader lane (its cp.async)
+      mbar_init(&s_empty[s], 1);  // the chunk's MMA commit
+    }
+    mbar_init(&s_sfready, 128);
+    mbar_init(&s_drain, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ loads
+    int g = 0;  // chunks issued
+    bool run = true;
+    for (int i = 0; i < mine && run; ++i) {
+      TItem t;
+      if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+      // this lane's activation pieces: rows n = lane / 8 + 4 q, piece lane % 8;
+      // its scale row: n = lane.  Rows past the tile's members are zero-filled.
+      const uint8_t* b_src[8];
+      uint32_t b_n[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int n = (lane >> 3) + 4 * q;
+        const int s = n / kLevels, l = n - s * kLevels;
+        int pick, brow;
+        t_member(a, t, s < kRowsPerJob ? s : kRowsPerJob, pick, brow);
+        const bool ok = n < kRowsPerJob * kLevels && pick >= 0;
+        b_n[q] = ok ? 16u : 0u;
+        b_src[q] = ok ? m.act.codes + ((size_t)brow * kLevels + l) * (m.K / 2) + (lane & 7) * 16
+                      : m.act.codes;
+      }
+      const uint8_t* sfb_src;
+      uint32_t sfb_n;
+      {
+        const int s = lane / kLevels, l = lane - s * kLevels;
+        int pick, brow;
+        t_member(a, t, s < kRowsPerJob ? s : kRowsPerJob, pick, brow);
+        const bool ok = lane < kRowsPerJob * kLevels && pick >= 0;
+        sfb_n = ok ? 16u : 0u;
+        sfb_src = ok ? m.act.scales + ((size_t)brow * kLevels + l) * (m.K / 16) : m.act.scales;
+      }
+      int yw[2], ys[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int off = m.gate_up ? h * m.I + t.mt * kTRows : (2 * t.mt + h) * kTRows;
+        yw[h] = t.vw * a.rps + a.row0 + off;
+        ys[h] = t.vs * a.rps + a.row0 + off;
+      }
+      for (int c = 0; c < nchunks; ++c, ++g) {
+        const int st = g % kTStages;
+        if (g >= kTStages &&
+            !mbar_wait_or_abort(&s_empty[st], (uint32_t)((g / kTStages - 1) & 1), abort_word,
+                                m.flags)) {
+          *abort_word = 1;
+          run = false;
+          break;
+        }
+        uint8_t* sg = smem + st * kTStageBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&s_full[st], 2 * kTABytes + 2 * kTSfaBytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d(sg + h * kTABytes, &a.map_w, c * 128, yw[h], &s_full[st]);
+            tma_load_2d(sg + kTOffSfa + h * kTSfaBytes, &a.map_s, c * 16, ys[h], &s_full[st]);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int n = (lane >> 3) + 4 * q;
+          cp_async16(sg + kTOffB + (n >> 3) * 1024 + (lane & 7) * 128 + (n & 7) * 16,
+                     b_n[q] ? b_src[q] + (size_t)c * 128 : b_src[q], b_n[q]);
+        }
+        cp_async16(sg + kTOffSfb + 16 * lane, sfb_n ? sfb_src + (size_t)c * 16 : sfb_src, sfb_n);
+        cp_async_bar_arrive(&s_full[st]);
+      }
+    }
+    // the last chunks issued have landed before the CTA may exit
+    for (int d = g > kTStages ? g - kTStages : 0; d < g; ++d)
+      mbar_wait_bounded(&s_full[d % kTStages], (uint32_t)((d / kTStages) & 1), m.flags);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    // ------------------------------------------ scales, MMAs, epilogue
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    int g = 0;  // chunks consumed
+    bool run = true;
+    for (int i = 0; i < mine && run; ++i) {
+      TItem t;
+      if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+      int pick[kRowsPerJob];
+      float gl[kRowsPerJob][kLevels];
+#pragma unroll
+      for (int s = 0; s < kRowsPerJob; ++s) {
+        int brow;
+        t_member(a, t, s, pick[s], brow);
+#pragma unroll
+        for (int l = 0; l < kLevels; ++l)
+          gl[s][l] = pick[s] >= 0 ? m.act.gl[(size_t)brow * kLevels + l] : 0.f;
+      }
+      for (int c = 0; c < nchunks; ++c, ++g) {
+        const int st = g % kTStages, sf = g & 1;
+        // the chunk's bytes, and the scale slot free (chunk g - 2's MMAs done)
+        if (!mbar_wait_or_abort(&s_full[st], (uint32_t)((g / kTStages) & 1), abort_word,
+                                m.flags) ||
+            (g >= 2 && !mbar_wait_or_abort(&s_empty[(g - 2) % kTStages],
+                                           (uint32_t)(((g - 2) / kTStages) & 1), abort_word,
+                                           m.flags))) {
+          *abort_word = 1;
+          run = false;
+          break;
+        }
+        const uint8_t* sg = smem + st * kTStageBytes;
+        uint32_t w0[4], w1[4], wb[4];
+        {
+          const uint4 x0 = *reinterpret_cast<const uint4*>(sg + kTOffSfa + 16 * tid);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(sg + kTOffSfa + kTSfaBytes + 16 * tid);
+          const uint4 xb = *reinterpret_cast<const uint4*>(sg + kTOffSfb + 16 * lane);
+          w0[0] = x0.x; w0[1] = x0.y; w0[2] = x0.z; w0[3] = x0.w;
+          w1[0] = x1.x; w1[1] = x1.y; w1[2] = x1.z; w1[3] = x1.w;
+          wb[0] = xb.x; wb[1] = xb.y; wb[2] = xb.z; wb[3] = xb.w;
+        }
+        const uint32_t sft = kTColSF + 64 * sf;
+        __syncwarp();  // tcgen05.st is .sync.aligned: the warp reconverges after the waits
+        tmem_st16(tmem + lane_base + sft, w0);
+        tmem_st16(tmem + lane_base + sft + 16, w1);
+        tmem_st16(tmem + lane_base + sft + 32, wb);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(&s_sfready);
+        if (!mbar_wait_or_abort(&s_sfready, (uint32_t)(g & 1), abort_word, m.flags)) {
+          *abort_word = 1;
+          run = false;
+          break;
+        }
+        if (tid == 0) {
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const uint32_t sA = smem_addr(sg), sB = sA + kTOffB;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t db = umma_desc(sB + 256 * ks);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t da = umma_desc_sw128(sA + h * kTABytes + 32 * ks);
+              const uint32_t sfa_t = tmem + sft + 16 * h + 4 * ks;
+              const uint32_t sfb_t = tmem + sft + 32 + 4 * ks;
+              const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                  "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                      tmem + 32 * h),
+                  "l"(da), "l"(db), "r"(umma_idesc()), "r"(sfa_t), "r"(sfb_t), "r"(acc)
+                  : "memory");
+            }
+          }
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                  smem_addr(&s_empty[st]))
+              : "memory");
+        }
+      }
+      if (!run) break;
+      // the item's accumulators, once its last chunk's MMAs are done
+      const int gl_last = g - 1;
+      if (!mbar_wait_or_abort(&s_empty[gl_last % kTStages], (uint32_t)((gl_last / kTStages) & 1),
+                              abort_word, m.flags)) {
+        *abort_word = 1;
+        run = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      uint32_t v0[32], v1[32];
+      __syncwarp();
+      tmem_ld32(tmem + lane_base, v0);
+      tmem_ld32(tmem + lane_base + 32, v1);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      const float* gsc = gp->g_gs + 3 * t.g;
+      if (m.gate_up) {
+        const int row = t.mt * kTRows + tid;  // gate row = index into h
+#pragma unroll
+        for (int s = 0; s < kRowsPerJob; ++s)
+          if (pick[s] >= 0)
+            m.out[(size_t)pick[s] * m.I + row] =
+                swiglu_h(gsc[0], level_sum(gl[s], v0 + s * kLevels), gsc[1],
+                         level_sum(gl[s], v1 + s * kLevels));
+      } else {
+        const int row = 2 * t.mt * kTRows + tid;
+#pragma unroll
+        for (int s = 0; s < kRowsPerJob; ++s)
+          if (pick[s] >= 0) {
+            m.out[(size_t)pick[s] * m.H + row] = gsc[2] * level_sum(gl[s], v0 + s * kLevels);
+            m.out[(size_t)pick[s] * m.H + row + kTRows] =
+                gsc[2] * level_sum(gl[s], v1 + s * kLevels);
+          }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (*abort_word) {  // uniform after the barrier
+    // MMAs thread 0 committed may still run: one more commit (it arrives once
+    // all earlier tcgen05 operations of thread 0 are complete) is waited for
+    // under the default limit before the TMEM is released.
+    if (tid == 0) {
+      asm volatile(
+          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+              smem_addr(&s_drain))
+          : "memory");
+      mbar_wait_bounded(&s_drain, 0u, m.flags);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+  }
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTTmemCols));
+}
+
 // out[m][o] = sum_j w[m*k + j] * y[m*k + j][o], j in rank order.
 __global__ void combine_kernel(const GroupPlan* __restrict__ gp, const float* __restrict__ y,
                                float* __restrict__ out, int H, int k) {
@@ -394,6 +810,19 @@ __global__ void combine_kernel(const GroupPlan* __restrict__ gp, const float* __
     acc = fmaf(gp->wts[p], y[(size_t)p * H + o], acc);
   }
   out[(size_t)m * H + o] = acc;
+}
+
+cudaError_t run_mma_tma(cudaStream_t st, const MmaTmaArgs& a, int grid) {
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_mma_tma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmemBytes);
+    if (e == cudaSuccess) e = prefer_max_shared(grouped_mma_tma_kernel);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  grouped_mma_tma_kernel<<<grid, kTThreads, kTSmemBytes, st>>>(a);
+  return cudaGetLastError();
 }
 
 template <int P>
@@ -412,6 +841,57 @@ cudaError_t run_mma(cudaStream_t st, const MmaArgs& a, int grid_x, int m_tiles) 
 
 }  // namespace
 
+bool make_tma_source(const uint8_t* w, const uint8_t* s, unsigned long long n, int H, int I,
+                     long long Bw, long long Bs, int num_sms, TmaSource* out) {
+  *out = TmaSource{};
+  if (!w || !s || n == 0 || H % 256 != 0 || I % 256 != 0 || num_sms <= 0) return false;
+  if (Bw != 3LL * H * I / 2 || Bs != 3LL * H * I / 16) return false;
+  const unsigned long long rows13 = n * 3ull * (unsigned long long)I;
+  const unsigned long long rows2 = n * 3ull * (unsigned long long)H;
+  if (rows2 >= (1ull << 31) || rows13 >= (1ull << 31)) return false;  // TMA row coordinates
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  auto make = [&](TmaMap* dst, const uint8_t* base, unsigned long long row_bytes,
+                  unsigned long long rows, unsigned box_x, bool swizzle) {
+    CUtensorMap tm;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_x, (cuuint32_t)kTRows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    static_assert(sizeof(CUtensorMap) == sizeof(TmaMap), "tensor map size");
+    if (r != CUDA_SUCCESS) return false;
+    std::memcpy(dst->b, &tm, sizeof tm);
+    return true;
+  };
+  const bool ok = make(&out->w13, w, H / 2, rows13, 128, true) &&
+                  make(&out->w2, w, I / 2, rows2, 128, true) &&
+                  make(&out->s13, s, H / 16, rows13, 16, false) &&
+                  make(&out->s2, s, I / 16, rows2, 16, false);
+  if (!ok) {
+    *out = TmaSource{};
+    return false;
+  }
+  out->base_w = w;
+  out->base_s = s;
+  out->n = n;
+  out->grid = num_sms;
+  out->ok = true;
+  return true;
+}
+
 bool mma_supported(int H, int I) {
   auto ok = [](int K) { return K % 64 == 0 && (K <= 256 ? (K == 128 || K == 256) : K % 256 == 0); };
   return ok(H) && ok(I) && I % 64 == 0 && H % 128 == 0;
@@ -419,7 +899,8 @@ bool mma_supported(int H, int I) {
 
 cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int grid_x, bool gate_up,
                                int H, int I, int k, const QuantBuf& act, float* out,
-                               uint32_t* flags, int g0, int g1) {
+                               uint32_t* flags, int g0, int g1, const TmaSource* tma,
+                               bool maybe_host) {
   if (grid_x <= 0) return cudaSuccess;
   MmaArgs a;
   a.gp = gp;
@@ -433,6 +914,27 @@ cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int grid_x,
   a.flags = flags;
   a.g0 = g0;
   a.g1 = g1;
+  a.skip_w = nullptr;
+  a.skip_n = 0;
+  a.skip_Bw = 0;
+  if (tma && tma->ok) {
+    MmaTmaArgs t;
+    t.map_w = gate_up ? tma->w13 : tma->w2;
+    t.map_s = gate_up ? tma->s13 : tma->s2;
+    t.m = a;
+    t.base_w = tma->base_w;
+    t.base_s = tma->base_s;
+    t.Bw = 3LL * H * I / 2;
+    t.Bs = 3LL * H * I / 16;
+    t.n = tma->n;
+    t.rps = gate_up ? 3 * I : 3 * H;
+    t.row0 = gate_up ? 0 : 2 * H;
+    cudaError_t e = run_mma_tma(st, t, tma->grid);
+    if (e != cudaSuccess || !maybe_host) return e;
+    a.skip_w = tma->base_w;
+    a.skip_n = tma->n;
+    a.skip_Bw = t.Bw;
+  }
   const int m_tiles = gate_up ? I / 64 : H / kTileM;
   if (a.K >= 256) return run_mma<8>(st, a, grid_x, m_tiles);
   return run_mma<4>(st, a, grid_x, m_tiles);

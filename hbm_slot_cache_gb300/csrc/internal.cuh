@@ -109,13 +109,40 @@ cudaError_t launch_route_rows(cudaStream_t st, const float* logits, int rows, in
 // activations (bf16 or fp32 rows of K) -> residual NVFP4 levels.
 cudaError_t launch_quantize_rows(cudaStream_t st, const void* src, bool bf16_in, int rows, int K,
                                  const QuantBuf& q);
+// Tensor maps (the 128 opaque bytes cuTensorMapEncodeTiled writes) over a
+// device region of n experts, codes [n][Bw] and scales [n][Bs], each viewed
+// as 2-D row arrays for the grouped MMA's weight tiles: w13 (rows of H/2
+// bytes; expert v's W13 = rows [3I v, 3I v + 2I)), w2 (rows of I/2 bytes;
+// its W2 = rows [3H v + 2H, 3H (v + 1))), and the matching scale views s13
+// (rows of H/16 bytes) and s2 (rows of I/16 bytes).  ok is false when the
+// shape has no such views (H or I not a multiple of 256) or encoding failed;
+// the grouped MMA then stages its operands with cp.async.
+struct alignas(64) TmaMap {
+  unsigned char b[128];
+};
+struct TmaSource {
+  TmaMap w13, w2, s13, s2;
+  const uint8_t* base_w = nullptr;
+  const uint8_t* base_s = nullptr;
+  unsigned long long n = 0;
+  int grid = 0;  // persistent CTAs (one per SM)
+  bool ok = false;
+};
+bool make_tma_source(const uint8_t* w, const uint8_t* s, unsigned long long n, int H, int I,
+                     long long Bw, long long Bs, int num_sms, TmaSource* out);
+
 // grouped tcgen05 expert matmuls: gate/up + SwiGLU -> h [P][I], or down -> y [P][H].
-// Jobs of groups [g0, g1) (all groups: g0 = 0, g1 = INT_MAX); grid_x CTAs per weight tile
-// loop over them.
+// Jobs of groups [g0, g1) (all groups: g0 = 0, g1 = INT_MAX).  With tma (ok)
+// the weight tiles of experts in its region come by TMA and a persistent grid
+// takes the (job, tile) items; experts elsewhere (host memory) are staged with
+// cp.async by grid_x CTAs per weight tile, launched too when tma is null or
+// maybe_host says the step may read host memory (a device-side bypass).  Both
+// kernels give the same bits.
 bool mma_supported(int H, int I);
 cudaError_t launch_grouped_mma(cudaStream_t st, const GroupPlan* gp, int grid_x, bool gate_up,
                                int H, int I, int k, const QuantBuf& act, float* out,
-                               uint32_t* flags, int g0 = 0, int g1 = 0x7FFFFFFF);
+                               uint32_t* flags, int g0 = 0, int g1 = 0x7FFFFFFF,
+                               const TmaSource* tma = nullptr, bool maybe_host = false);
 // residual-NVFP4 quantisation of the rows of src named by the members of groups [g0, g1)
 cudaError_t launch_quantize_members(cudaStream_t st, const float* src, int K, const GroupPlan* gp,
                                     int g0, int g1, const QuantBuf& q, int grid);

@@ -57,6 +57,8 @@ struct moe_cache {
   uint8_t* stage_w = nullptr;  // [2 * chunk][Bw]
   uint8_t* stage_s = nullptr;  // [2 * chunk][Bs]
   std::vector<cudaEvent_t> ev_staged, ev_used;  // [nchunks]
+  // tensor maps of the slot arrays and of the staging halves (grouped MMA weight tiles)
+  TmaSource tma_slots, tma_stage;
   // optional per-kernel timing events (caller-owned)
   cudaEvent_t ev[MOE_TIMING_EVENTS] = {};
   bool timing = false;
@@ -369,6 +371,15 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
       if (b) h->ev_used.push_back(b);
     }
   }
+  // Multi-row steps read slot (and staged) weights as TMA tiles where the
+  // shape allows; otherwise (and for host-memory experts) with cp.async.
+  if (ok) {
+    make_tma_source(h->slot_w, h->slot_s, LS, hidden, inter, h->Bw, h->Bs, h->num_sms,
+                    &h->tma_slots);
+    if (h->stage_w)
+      make_tma_source(h->stage_w, h->stage_s, 2ull * h->chunk, hidden, inter, h->Bw, h->Bs,
+                      h->num_sms, &h->tma_stage);
+  }
   // The second stream carries the missed picks' read-through pass, the step's
   // critical path: highest priority, so its CTAs are placed before the
   // resident picks' persistent grids fill the SMs.
@@ -539,12 +550,12 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
       if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->ev_staged[q], 0);
       if (e == cudaSuccess)
         e = launch_grouped_mma(st, h->gp, gx_gu, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf,
-                               flags, g0, g1);
+                               flags, g0, g1, &h->tma_stage);
       if (e == cudaSuccess)
         e = launch_quantize_members(st, h->gemv.hbuf, h->I, h->gp, g0, g1, h->hq, h->num_sms);
       if (e == cudaSuccess)
         e = launch_grouped_mma(st, h->gp, gx_dn, false, h->H, h->I, h->k, h->hq, h->gemv.ypart,
-                               flags, g0, g1);
+                               flags, g0, g1, &h->tma_stage);
       if (e == cudaSuccess) e = cudaEventRecord(h->ev_used[q], st);
     }
     if (e == cudaSuccess) e = mark(3, st);
@@ -553,19 +564,22 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     if (e == cudaSuccess) e = mark(6, st);
   } else if (cached_rows) {
     // hit groups [0, n_hit) now, miss groups [n_hit, n) once their bytes are in
-    // the slots: gate/up, the members' h in residual NVFP4, down, each pass
+    // the slots: gate/up, the members' h in residual NVFP4, down, each pass.
+    // A union larger than the ring (possible only when npicks > S) bypasses on
+    // the device and reads host memory.
     const int gr[3] = {0, kHitGroups, INT_MAX};
+    const bool may_bypass = npicks > h->S_of[layer];
     for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
       if (pass == 1) e = cudaStreamWaitEvent(st, h->join, 0);
       if (e == cudaSuccess)
         e = launch_grouped_mma(st, h->gp, npicks, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf,
-                               flags, gr[pass], gr[pass + 1]);
+                               flags, gr[pass], gr[pass + 1], &h->tma_slots, may_bypass);
       if (e == cudaSuccess)
         e = launch_quantize_members(st, h->gemv.hbuf, h->I, h->gp, gr[pass], gr[pass + 1],
                                     h->hq, h->num_sms);
       if (e == cudaSuccess)
         e = launch_grouped_mma(st, h->gp, npicks, false, h->H, h->I, h->k, h->hq, h->gemv.ypart,
-                               flags, gr[pass], gr[pass + 1]);
+                               flags, gr[pass], gr[pass + 1], &h->tma_slots, may_bypass);
       if (e == cudaSuccess && pass == 0) e = mark(3, st);
       if (e == cudaSuccess && pass == 0) e = mark(5, st);
     }

@@ -48,7 +48,8 @@ def _oracle_rows(orc, banks, cfg, lg, xb, rows):
 
 
 @pytest.mark.parametrize("name,wide_x", [("tiny", False), ("tiny_wide", False),
-                                         ("tiny_wide", True)])
+                                         ("tiny_wide", True), ("small", False),
+                                         ("small", True)])
 def test_tiny_multirow_trace_outputs_and_device_bypass(lib, orc, name, wide_x):
     cfg = workload.CONFIGS[name]
     M, steps = 4, 40
@@ -203,11 +204,13 @@ def test_glm_prefill_bypass_sampled_rows(lib, orc):
     banks.close()
 
 
-@pytest.mark.parametrize("name", ["tiny", "tiny_wide"])
+@pytest.mark.parametrize("name", ["tiny", "tiny_wide", "small"])
 def test_tiny_prefill_staged_equals_zero_copy(lib, orc, name):
     """Staged prefill (experts copied into HBM a chunk at a time, two chunks held)
     gives the same bits as reading host memory directly, for chunk sizes that
-    cover the union in one chunk, in several, and with a ragged last chunk."""
+    cover the union in one chunk, in several, and with a ragged last chunk.
+    At the small shape the staged chunks run the TMA-tiled kernel and the
+    zero-copy path the cp.async one."""
     cfg = workload.CONFIGS[name]
     rows = 64
     banks = Banks(cfg)
@@ -265,7 +268,7 @@ def test_glm_prefill_staged_graph_and_zero_copy(lib, orc):
     banks.close()
 
 
-@pytest.mark.parametrize("name", ["tiny", "tiny_wide", "multirow"])
+@pytest.mark.parametrize("name", ["tiny", "tiny_wide", "small", "multirow"])
 def test_batch_invariant_rows(lib, orc, name):
     """Batch-invariant mode: every row of a round (M = 16, cached) is bit-identical
     to the same row stepped alone through another cached handle.  Both handles'
@@ -281,7 +284,7 @@ def test_batch_invariant_rows(lib, orc, name):
     single = make_cache(cfg, banks, layers=1, batch_invariant=True)
     lgM, xM, oM = _dev(cfg, M)
     lg1, x1, o1 = _dev(cfg, 1)
-    rows = range(M) if name.startswith("tiny") else (0, 5, 15)
+    rows = range(M) if name in ("tiny", "tiny_wide", "small") else (0, 5, 15)
     for t in range(steps):
         _put(lgM, xM, lgs[t], xs[t])
         rounds.step(0, lgM, xM, oM)

@@ -58,6 +58,10 @@ CONFIGS = {
     # the same layer with wide block scales and per-(expert, matrix) global scales
     "tiny_wide": Config("tiny_wide", 1, 256, 128, 16, 2, 4, 1, 64, 1.1, 0.0, 5,
                         literal_normal_bias=True),
+    # a small layer whose dimensions are multiples of 256 (the grouped MMA's TMA
+    # tiles): H512/I256, 16 experts, top-4, S=8, wide scales
+    "small": Config("small", 1, 512, 256, 16, 4, 8, 1, 64, 1.1, 0.0, 9,
+                    literal_normal_bias=True),
     # GLM-5.3-shaped layer: H6144/I2048, 256 experts, top-8, S=128, M=1, 300 churn steps
     "glm": Config("glm", 1, 6144, 2048, 256, 8, 128, 1, 300, 1.1, 0.1, 1),
     # Flash-shaped stack: 16 layers, H4096/I2048, 288 experts top-8, S=54, 512 steps
