@@ -414,18 +414,26 @@ grouped_mma_kernel(MmaArgs a) {
 // plus the boxes of their scale words.  A work item is (job, tile): gate/up
 // tiles pair 128 gate rows with the matching 128 up rows (one MMA each, so a
 // TMEM lane holds both of its row's accumulators), down tiles are 256 W2
-// rows.  One persistent CTA per SM takes items round robin.  Warp 4 keeps
-// kTStages chunks in flight (TMA for the weight codes and scales, 16-byte
-// cp.async for the members' activation levels and their scales) and runs on
-// into the CTA's next item, so the HBM stream does not stop at an item
-// boundary.  Warps 0-3 own the TMEM lane quadrants: per chunk they move the
-// scale words to TMEM and count in on an mbarrier, thread 0 issues the
-// chunk's MMAs and commits them to the stage's "empty" mbarrier; after an
-// item's last chunk they read the accumulators and write h or y.  Every wait
-// is bounded: one that runs out sets the CTA's abort word and everyone stops;
-// copies and MMAs in flight are drained (bounded) before the TMEM is freed.
+// rows.  One persistent CTA per SM takes items round robin, in four roles:
+//   warp 4 (loads): keeps kTStages chunks in flight (TMA for the weight codes
+//     and scales, 16-byte cp.async for the members' activation levels and
+//     their scales) and runs on into the CTA's next item, so the HBM stream
+//     does not stop at an item boundary;
+//   warps 0-3 (scales, one TMEM lane quadrant each): move each chunk's scale
+//     words into one of kTSfSlots TMEM slots and count in on the slot's
+//     mbarrier;
+//   warp 5, one thread (MMA): issues each chunk's MMAs into the item's
+//     accumulator buffer (two, by item parity) once its scales are in, and
+//     commits them to the stage's "empty" mbarrier (which also frees the
+//     scale slot); after an item's last chunk it commits to the buffer's
+//     "full" mbarrier;
+//   warps 6-9 (epilogue, one lane quadrant each): read an item's accumulators,
+//     release the buffer, write h or y while the next item's MMAs run.
+// Every wait is bounded: one that runs out sets the CTA's abort word and
+// everyone stops; copies and MMAs in flight are drained (bounded) before the
+// TMEM is freed.
 
-constexpr int kTThreads = 160;
+constexpr int kTThreads = 320;
 constexpr int kTRows = 128;                     // rows of one MMA (M); two per item
 constexpr int kTABytes = kTRows * 128;          // one weight box: 128 rows x 256 elements
 constexpr int kTSfaBytes = kTRows * 16;         // its rows' scale words for the chunk
@@ -433,12 +441,19 @@ constexpr int kTOffSfa = 2 * kTABytes;
 constexpr int kTOffB = kTOffSfa + 2 * kTSfaBytes;
 constexpr int kTOffSfb = kTOffB + kBBytes;
 constexpr int kTStageBytes = 41 * 1024;         // kTOffSfb + kSfbBytes, rounded up to 1 KB
-constexpr int kTStages = 4;
+constexpr int kTStages = 5;
 constexpr int kTSmemBytes = kTStages * kTStageBytes + 1024;  // + room to align to 1 KB
-constexpr int kTTmemCols = 256;
-constexpr int kTColSF = 64;  // scale slot s (chunk parity): 64 + 64 s; SFA halves +0, +16; SFB +32
+constexpr int kTSfSlots = 4;                    // < kTStages (see the scale warps' wait)
+constexpr int kTTmemCols = 512;
+// TMEM columns: accumulator buffer b at 64 b (half h at + 32 h); scale slot q
+// at 128 + 48 q: SFA of half 0 at +0, half 1 at +16, SFB at +32, each K step's
+// word written to four adjacent columns (the step's scale columns are 4-column
+// aligned, as the MMA requires).
+constexpr int kTColSF = 128;
 static_assert(kTOffSfb + kSfbBytes <= kTStageBytes, "stage layout");
 static_assert(kTStageBytes % 1024 == 0, "weight boxes must stay 1 KB aligned");
+static_assert(kTSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kTColSF + 48 * kTSfSlots <= kTTmemCols && kTSfSlots < kTStages, "TMEM columns");
 
 struct MmaTmaArgs {
   TmaMap map_w;  // codes view of the launch's matrix block
@@ -544,7 +559,8 @@ __device__ __forceinline__ void t_member(const MmaTmaArgs& a, const TItem& t, in
 __global__ void __launch_bounds__(kTThreads, 1)
 grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t s_full[kTStages], s_empty[kTStages], s_sfready, s_drain;
+  __shared__ __align__(8) uint64_t s_full[kTStages], s_empty[kTStages], s_sfready[kTSfSlots],
+      s_accf[2], s_acce[2], s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const MmaArgs& m = a.m;
@@ -578,7 +594,11 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
       mbar_init(&s_full[s], 33);  // the expect_tx arrival + one per loader lane (its cp.async)
       mbar_init(&s_empty[s], 1);  // the chunk's MMA commit
     }
-    mbar_init(&s_sfready, 128);
+    for (int q = 0; q < kTSfSlots; ++q) mbar_init(&s_sfready[q], 128);  // every scale thread
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_accf[b], 1);    // an item's last MMA commit
+      mbar_init(&s_acce[b], 128);  // every epilogue thread has read the buffer
+    }
     mbar_init(&s_drain, 1);
     fence_mbar_init();
     s_abort = 0;
@@ -659,32 +679,26 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
     for (int d = g > kTStages ? g - kTStages : 0; d < g; ++d)
       mbar_wait_bounded(&s_full[d % kTStages], (uint32_t)((d / kTStages) & 1), m.flags);
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else {
-    // ------------------------------------------ scales, MMAs, epilogue
+  } else if (warp < 4) {
+    // ----------------------------------------------------------- scales
+    // Chunk g's scales go to slot g % kTSfSlots once chunk g - kTSfSlots's
+    // MMAs (the slot's last reader) are done.  That wait also keeps a thread
+    // from arriving twice on a slot's mbarrier before the MMA thread saw the
+    // first phase complete.
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    int g = 0;  // chunks consumed
+    int g = 0;
     bool run = true;
     for (int i = 0; i < mine && run; ++i) {
       TItem t;
       if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
-      int pick[kRowsPerJob];
-      float gl[kRowsPerJob][kLevels];
-#pragma unroll
-      for (int s = 0; s < kRowsPerJob; ++s) {
-        int brow;
-        t_member(a, t, s, pick[s], brow);
-#pragma unroll
-        for (int l = 0; l < kLevels; ++l)
-          gl[s][l] = pick[s] >= 0 ? m.act.gl[(size_t)brow * kLevels + l] : 0.f;
-      }
       for (int c = 0; c < nchunks; ++c, ++g) {
-        const int st = g % kTStages, sf = g & 1;
-        // the chunk's bytes, and the scale slot free (chunk g - 2's MMAs done)
+        const int st = g % kTStages, q = g % kTSfSlots;
+        const int gp_ = g - kTSfSlots;
         if (!mbar_wait_or_abort(&s_full[st], (uint32_t)((g / kTStages) & 1), abort_word,
                                 m.flags) ||
-            (g >= 2 && !mbar_wait_or_abort(&s_empty[(g - 2) % kTStages],
-                                           (uint32_t)(((g - 2) / kTStages) & 1), abort_word,
-                                           m.flags))) {
+            (gp_ >= 0 && !mbar_wait_or_abort(&s_empty[gp_ % kTStages],
+                                             (uint32_t)((gp_ / kTStages) & 1), abort_word,
+                                             m.flags))) {
           *abort_word = 1;
           run = false;
           break;
@@ -699,37 +713,58 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
           w1[0] = x1.x; w1[1] = x1.y; w1[2] = x1.z; w1[3] = x1.w;
           wb[0] = xb.x; wb[1] = xb.y; wb[2] = xb.z; wb[3] = xb.w;
         }
-        const uint32_t sft = kTColSF + 64 * sf;
+        const uint32_t sft = kTColSF + 48 * q;
         __syncwarp();  // tcgen05.st is .sync.aligned: the warp reconverges after the waits
         tmem_st16(tmem + lane_base + sft, w0);
         tmem_st16(tmem + lane_base + sft + 16, w1);
         tmem_st16(tmem + lane_base + sft + 32, wb);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        mbar_arrive(&s_sfready);
-        if (!mbar_wait_or_abort(&s_sfready, (uint32_t)(g & 1), abort_word, m.flags)) {
+        mbar_arrive(&s_sfready[q]);
+      }
+    }
+  } else if (warp == 5) {
+    // -------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      int g = 0, ni = 0;  // chunks consumed, items done
+      bool run = true;
+      for (int i = 0; i < mine && run; ++i) {
+        TItem t;
+        if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+        const int b = ni & 1;
+        // the buffer's previous item (ni - 2) has been read by the epilogue
+        if (ni >= 2 && !mbar_wait_or_abort(&s_acce[b], (uint32_t)(((ni >> 1) - 1) & 1),
+                                           abort_word, m.flags)) {
           *abort_word = 1;
-          run = false;
           break;
         }
-        if (tid == 0) {
+        for (int c = 0; c < nchunks; ++c, ++g) {
+          const int st = g % kTStages, q = g % kTSfSlots;
+          // the chunk's scales are in TMEM (so its bytes have landed too)
+          if (!mbar_wait_or_abort(&s_sfready[q], (uint32_t)((g / kTSfSlots) & 1), abort_word,
+                                  m.flags)) {
+            *abort_word = 1;
+            run = false;
+            break;
+          }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          const uint32_t sA = smem_addr(sg), sB = sA + kTOffB;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // cp.async bytes -> MMA
+          const uint32_t sA = smem_addr(smem + st * kTStageBytes);
+          const uint32_t sB = sA + kTOffB;
+          const uint32_t sft = tmem + kTColSF + 48 * q;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t db = umma_desc(sB + 256 * ks);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const uint64_t da = umma_desc_sw128(sA + h * kTABytes + 32 * ks);
-              const uint32_t sfa_t = tmem + sft + 16 * h + 4 * ks;
-              const uint32_t sfb_t = tmem + sft + 32 + 4 * ks;
               const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
                   "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                      tmem + 32 * h),
-                  "l"(da), "l"(db), "r"(umma_idesc()), "r"(sfa_t), "r"(sfb_t), "r"(acc)
+                      tmem + 64 * b + 32 * h),
+                  "l"(da), "l"(db), "r"(umma_idesc()), "r"(sft + 16 * h + 4 * ks),
+                  "r"(sft + 32 + 4 * ks), "r"(acc)
                   : "memory");
             }
           }
@@ -738,40 +773,64 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
                   smem_addr(&s_empty[st]))
               : "memory");
         }
+        if (!run) break;
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                smem_addr(&s_accf[b]))
+            : "memory");
+        ++ni;
       }
-      if (!run) break;
-      // the item's accumulators, once its last chunk's MMAs are done
-      const int gl_last = g - 1;
-      if (!mbar_wait_or_abort(&s_empty[gl_last % kTStages], (uint32_t)((gl_last / kTStages) & 1),
-                              abort_word, m.flags)) {
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int qd = warp & 3;  // warps 6, 7, 8, 9: lane quadrants 2, 3, 0, 1
+    const int r = 32 * qd + lane;
+    const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+    int ni = 0;
+    for (int i = 0; i < mine; ++i) {
+      TItem t;
+      if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+      int pick[kRowsPerJob];
+      float gl[kRowsPerJob][kLevels];
+#pragma unroll
+      for (int s = 0; s < kRowsPerJob; ++s) {
+        int brow;
+        t_member(a, t, s, pick[s], brow);
+#pragma unroll
+        for (int l = 0; l < kLevels; ++l)
+          gl[s][l] = pick[s] >= 0 ? m.act.gl[(size_t)brow * kLevels + l] : 0.f;
+      }
+      const float* gsc = gp->g_gs + 3 * t.g;
+      const float gs0 = gsc[0], gs1 = gsc[1], gs2 = gsc[2];
+      const int b = ni & 1;
+      if (!mbar_wait_or_abort(&s_accf[b], (uint32_t)((ni >> 1) & 1), abort_word, m.flags)) {
         *abort_word = 1;
-        run = false;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       uint32_t v0[32], v1[32];
-      __syncwarp();
-      tmem_ld32(tmem + lane_base, v0);
-      tmem_ld32(tmem + lane_base + 32, v1);
+      __syncwarp();  // tcgen05.ld is .sync.aligned
+      tmem_ld32(tmem + lane_base + 64 * b, v0);
+      tmem_ld32(tmem + lane_base + 64 * b + 32, v1);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      const float* gsc = gp->g_gs + 3 * t.g;
+      mbar_arrive(&s_acce[b]);
+      ++ni;
       if (m.gate_up) {
-        const int row = t.mt * kTRows + tid;  // gate row = index into h
+        const int row = t.mt * kTRows + r;  // gate row = index into h
 #pragma unroll
         for (int s = 0; s < kRowsPerJob; ++s)
           if (pick[s] >= 0)
             m.out[(size_t)pick[s] * m.I + row] =
-                swiglu_h(gsc[0], level_sum(gl[s], v0 + s * kLevels), gsc[1],
+                swiglu_h(gs0, level_sum(gl[s], v0 + s * kLevels), gs1,
                          level_sum(gl[s], v1 + s * kLevels));
       } else {
-        const int row = 2 * t.mt * kTRows + tid;
+        const int row = 2 * t.mt * kTRows + r;
 #pragma unroll
         for (int s = 0; s < kRowsPerJob; ++s)
           if (pick[s] >= 0) {
-            m.out[(size_t)pick[s] * m.H + row] = gsc[2] * level_sum(gl[s], v0 + s * kLevels);
-            m.out[(size_t)pick[s] * m.H + row + kTRows] =
-                gsc[2] * level_sum(gl[s], v1 + s * kLevels);
+            m.out[(size_t)pick[s] * m.H + row] = gs2 * level_sum(gl[s], v0 + s * kLevels);
+            m.out[(size_t)pick[s] * m.H + row + kTRows] = gs2 * level_sum(gl[s], v1 + s * kLevels);
           }
       }
     }
@@ -779,10 +838,10 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (*abort_word) {  // uniform after the barrier
-    // MMAs thread 0 committed may still run: one more commit (it arrives once
-    // all earlier tcgen05 operations of thread 0 are complete) is waited for
-    // under the default limit before the TMEM is released.
-    if (tid == 0) {
+    // MMAs the MMA thread issued may still run: one more commit from it (it
+    // arrives once all its earlier tcgen05 operations are complete) is waited
+    // for under the default limit before the TMEM is released.
+    if (tid == 5 * 32) {
       asm volatile(
           "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
               smem_addr(&s_drain))
