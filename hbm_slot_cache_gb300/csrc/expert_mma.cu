@@ -414,7 +414,10 @@ grouped_mma_kernel(MmaArgs a) {
 // plus the boxes of their scale words.  A work item is (job, tile): gate/up
 // tiles pair 128 gate rows with the matching 128 up rows (one MMA each, so a
 // TMEM lane holds both of its row's accumulators), down tiles are 256 W2
-// rows.  One persistent CTA per SM takes items round robin, in four roles:
+// rows.  One persistent CTA per SM takes items round robin, in five roles:
+//   warp 10 (plan): reads each item's plan entries (checked) into a ring of
+//     kTRing records in shared memory, ahead of the others, so no role waits
+//     on a chain of global loads at an item boundary;
 //   warp 4 (loads): keeps kTStages chunks in flight (TMA for the weight codes
 //     and scales, 16-byte cp.async for the members' activation levels and
 //     their scales) and runs on into the CTA's next item, so the HBM stream
@@ -428,12 +431,16 @@ grouped_mma_kernel(MmaArgs a) {
 //     scale slot); after an item's last chunk it commits to the buffer's
 //     "full" mbarrier;
 //   warps 6-9 (epilogue, one lane quadrant each): read an item's accumulators,
-//     release the buffer, write h or y while the next item's MMAs run.
+//     release the buffer and the item's record, write h or y while the next
+//     item's MMAs run.
+// An item whose plan entries fail their checks (MOE_FLAG_BAD_PLAN) has no
+// chunks; it still passes through the MMA thread and the epilogue so every
+// role counts the same items.
 // Every wait is bounded: one that runs out sets the CTA's abort word and
 // everyone stops; copies and MMAs in flight are drained (bounded) before the
 // TMEM is freed.
 
-constexpr int kTThreads = 320;
+constexpr int kTThreads = 352;
 constexpr int kTRows = 128;                     // rows of one MMA (M); two per item
 constexpr int kTABytes = kTRows * 128;          // one weight box: 128 rows x 256 elements
 constexpr int kTSfaBytes = kTRows * 16;         // its rows' scale words for the chunk
@@ -444,6 +451,7 @@ constexpr int kTStageBytes = 41 * 1024;         // kTOffSfb + kSfbBytes, rounded
 constexpr int kTStages = 5;
 constexpr int kTSmemBytes = kTStages * kTStageBytes + 1024;  // + room to align to 1 KB
 constexpr int kTSfSlots = 4;                    // < kTStages (see the scale warps' wait)
+constexpr int kTRing = 4;                       // item records decoded ahead
 constexpr int kTTmemCols = 512;
 // TMEM columns: accumulator buffer b at 64 b (half h at + 32 h); scale slot q
 // at 128 + 48 q: SFA of half 0 at +0, half 1 at +16, SFB at +32, each K step's
@@ -556,11 +564,21 @@ __device__ __forceinline__ void t_member(const MmaTmaArgs& a, const TItem& t, in
   }
 }
 
+// One work item as the plan warp decoded it.
+struct TRec {
+  int good, mt, vw, vs;
+  int pick[kRowsPerJob];  // -1: no member
+  int brow[kRowsPerJob];  // the member's activation row
+  float gl[kRowsPerJob][kLevels];
+  float gs[3];
+};
+
 __global__ void __launch_bounds__(kTThreads, 1)
 grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t s_full[kTStages], s_empty[kTStages], s_sfready[kTSfSlots],
-      s_accf[2], s_acce[2], s_drain;
+      s_accf[2], s_acce[2], s_rfull[kTRing], s_rfree[kTRing], s_drain;
+  __shared__ TRec s_rec[kTRing];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const MmaArgs& m = a.m;
@@ -599,6 +617,10 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
       mbar_init(&s_accf[b], 1);    // an item's last MMA commit
       mbar_init(&s_acce[b], 128);  // every epilogue thread has read the buffer
     }
+    for (int q = 0; q < kTRing; ++q) {
+      mbar_init(&s_rfull[q], 1);    // the plan warp wrote the record
+      mbar_init(&s_rfree[q], 128);  // every epilogue thread is done with it (the last reader)
+    }
     mbar_init(&s_drain, 1);
     fence_mbar_init();
     s_abort = 0;
@@ -608,13 +630,56 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
 
-  if (warp == 4) {
+  if (warp == 10) {
+    // ------------------------------------------------------------- plan
+    for (int i = 0; i < mine; ++i) {
+      const int slot = i % kTRing;
+      if (i >= kTRing && !mbar_wait_or_abort(&s_rfree[slot], (uint32_t)((i / kTRing - 1) & 1),
+                                             abort_word, m.flags)) {
+        *abort_word = 1;
+        break;
+      }
+      TItem t;
+      const bool good = t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t);
+      int pick = -1, brow = 0;
+      if (good && lane < kRowsPerJob) t_member(a, t, lane, pick, brow);
+      const int sm = lane / kLevels < kRowsPerJob ? lane / kLevels : 0;
+      const int pick_s = __shfl_sync(0xFFFFFFFFu, pick, sm);
+      const int brow_s = __shfl_sync(0xFFFFFFFFu, brow, sm);
+      TRec& r = s_rec[slot];
+      if (lane < kRowsPerJob * kLevels)
+        r.gl[lane / kLevels][lane % kLevels] =
+            (good && pick_s >= 0) ? m.act.gl[(size_t)brow_s * kLevels + lane % kLevels] : 0.f;
+      if (lane < kRowsPerJob) {
+        r.pick[lane] = pick;
+        r.brow[lane] = brow;
+      }
+      if (lane < 3) r.gs[lane] = good ? gp->g_gs[3 * t.g + lane] : 0.f;
+      if (lane == 0) {
+        r.good = good ? 1 : 0;
+        r.mt = good ? t.mt : 0;
+        r.vw = good ? t.vw : 0;
+        r.vs = good ? t.vs : 0;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        mbar_arrive(&s_rfull[slot]);
+      }
+    }
+  } else if (warp == 4) {
     // ------------------------------------------------------------ loads
     int g = 0;  // chunks issued
     bool run = true;
     for (int i = 0; i < mine && run; ++i) {
-      TItem t;
-      if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+      const int slot = i % kTRing;
+      if (!mbar_wait_or_abort(&s_rfull[slot], (uint32_t)((i / kTRing) & 1), abort_word,
+                              m.flags)) {
+        *abort_word = 1;
+        break;
+      }
+      const TRec& r = s_rec[slot];
+      if (!r.good) continue;
       // this lane's activation pieces: rows n = lane / 8 + 4 q, piece lane % 8;
       // its scale row: n = lane.  Rows past the tile's members are zero-filled.
       const uint8_t* b_src[8];
@@ -623,9 +688,8 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
       for (int q = 0; q < 8; ++q) {
         const int n = (lane >> 3) + 4 * q;
         const int s = n / kLevels, l = n - s * kLevels;
-        int pick, brow;
-        t_member(a, t, s < kRowsPerJob ? s : kRowsPerJob, pick, brow);
-        const bool ok = n < kRowsPerJob * kLevels && pick >= 0;
+        const bool ok = s < kRowsPerJob && r.pick[s < kRowsPerJob ? s : 0] >= 0;
+        const int brow = ok ? r.brow[s] : 0;
         b_n[q] = ok ? 16u : 0u;
         b_src[q] = ok ? m.act.codes + ((size_t)brow * kLevels + l) * (m.K / 2) + (lane & 7) * 16
                       : m.act.codes;
@@ -634,18 +698,17 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
       uint32_t sfb_n;
       {
         const int s = lane / kLevels, l = lane - s * kLevels;
-        int pick, brow;
-        t_member(a, t, s < kRowsPerJob ? s : kRowsPerJob, pick, brow);
-        const bool ok = lane < kRowsPerJob * kLevels && pick >= 0;
+        const bool ok = s < kRowsPerJob && r.pick[s < kRowsPerJob ? s : 0] >= 0;
+        const int brow = ok ? r.brow[s] : 0;
         sfb_n = ok ? 16u : 0u;
         sfb_src = ok ? m.act.scales + ((size_t)brow * kLevels + l) * (m.K / 16) : m.act.scales;
       }
       int yw[2], ys[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int off = m.gate_up ? h * m.I + t.mt * kTRows : (2 * t.mt + h) * kTRows;
-        yw[h] = t.vw * a.rps + a.row0 + off;
-        ys[h] = t.vs * a.rps + a.row0 + off;
+        const int off = m.gate_up ? h * m.I + r.mt * kTRows : (2 * r.mt + h) * kTRows;
+        yw[h] = r.vw * a.rps + a.row0 + off;
+        ys[h] = r.vs * a.rps + a.row0 + off;
       }
       for (int c = 0; c < nchunks; ++c, ++g) {
         const int st = g % kTStages;
@@ -689,8 +752,12 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
     int g = 0;
     bool run = true;
     for (int i = 0; i < mine && run; ++i) {
-      TItem t;
-      if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+      if (!mbar_wait_or_abort(&s_rfull[i % kTRing], (uint32_t)((i / kTRing) & 1), abort_word,
+                              m.flags)) {
+        *abort_word = 1;
+        break;
+      }
+      if (!s_rec[i % kTRing].good) continue;
       for (int c = 0; c < nchunks; ++c, ++g) {
         const int st = g % kTStages, q = g % kTSfSlots;
         const int gp_ = g - kTSfSlots;
@@ -729,8 +796,12 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
       int g = 0, ni = 0;  // chunks consumed, items done
       bool run = true;
       for (int i = 0; i < mine && run; ++i) {
-        TItem t;
-        if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+        if (!mbar_wait_or_abort(&s_rfull[i % kTRing], (uint32_t)((i / kTRing) & 1), abort_word,
+                                m.flags)) {
+          *abort_word = 1;
+          break;
+        }
+        const bool good = s_rec[i % kTRing].good != 0;
         const int b = ni & 1;
         // the buffer's previous item (ni - 2) has been read by the epilogue
         if (ni >= 2 && !mbar_wait_or_abort(&s_acce[b], (uint32_t)(((ni >> 1) - 1) & 1),
@@ -738,7 +809,7 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
           *abort_word = 1;
           break;
         }
-        for (int c = 0; c < nchunks; ++c, ++g) {
+        for (int c = 0; good && c < nchunks; ++c, ++g) {
           const int st = g % kTStages, q = g % kTSfSlots;
           // the chunk's scales are in TMEM (so its bytes have landed too)
           if (!mbar_wait_or_abort(&s_sfready[q], (uint32_t)((g / kTSfSlots) & 1), abort_word,
@@ -788,36 +859,44 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
     const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
     int ni = 0;
     for (int i = 0; i < mine; ++i) {
-      TItem t;
-      if (!t_item(a, jbeg, m_tiles, (int)blockIdx.x + i * (int)gridDim.x, t)) continue;
+      const int slot = i % kTRing;
+      if (!mbar_wait_or_abort(&s_rfull[slot], (uint32_t)((i / kTRing) & 1), abort_word,
+                              m.flags)) {
+        *abort_word = 1;
+        break;
+      }
+      const TRec& rec = s_rec[slot];
+      const bool good = rec.good != 0;
+      const int mt = rec.mt;
       int pick[kRowsPerJob];
       float gl[kRowsPerJob][kLevels];
 #pragma unroll
       for (int s = 0; s < kRowsPerJob; ++s) {
-        int brow;
-        t_member(a, t, s, pick[s], brow);
+        pick[s] = rec.pick[s];
 #pragma unroll
-        for (int l = 0; l < kLevels; ++l)
-          gl[s][l] = pick[s] >= 0 ? m.act.gl[(size_t)brow * kLevels + l] : 0.f;
+        for (int l = 0; l < kLevels; ++l) gl[s][l] = rec.gl[s][l];
       }
-      const float* gsc = gp->g_gs + 3 * t.g;
-      const float gs0 = gsc[0], gs1 = gsc[1], gs2 = gsc[2];
+      const float gs0 = rec.gs[0], gs1 = rec.gs[1], gs2 = rec.gs[2];
       const int b = ni & 1;
       if (!mbar_wait_or_abort(&s_accf[b], (uint32_t)((ni >> 1) & 1), abort_word, m.flags)) {
         *abort_word = 1;
         break;
       }
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       uint32_t v0[32], v1[32];
-      __syncwarp();  // tcgen05.ld is .sync.aligned
-      tmem_ld32(tmem + lane_base + 64 * b, v0);
-      tmem_ld32(tmem + lane_base + 64 * b + 32, v1);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      if (good) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        __syncwarp();  // tcgen05.ld is .sync.aligned
+        tmem_ld32(tmem + lane_base + 64 * b, v0);
+        tmem_ld32(tmem + lane_base + 64 * b + 32, v1);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      }
       mbar_arrive(&s_acce[b]);
+      mbar_arrive(&s_rfree[slot]);  // every other role is past this item's record
       ++ni;
+      if (!good) continue;
       if (m.gate_up) {
-        const int row = t.mt * kTRows + r;  // gate row = index into h
+        const int row = mt * kTRows + r;  // gate row = index into h
 #pragma unroll
         for (int s = 0; s < kRowsPerJob; ++s)
           if (pick[s] >= 0)
@@ -825,7 +904,7 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
                 swiglu_h(gs0, level_sum(gl[s], v0 + s * kLevels), gs1,
                          level_sum(gl[s], v1 + s * kLevels));
       } else {
-        const int row = 2 * t.mt * kTRows + r;
+        const int row = 2 * mt * kTRows + r;
 #pragma unroll
         for (int s = 0; s < kRowsPerJob; ++s)
           if (pick[s] >= 0) {
