@@ -553,6 +553,20 @@ def kernel_table(cfg, res: dict, hbm_peak: float, link_peak: float) -> tuple[dic
     kern["gemv_readthrough[missed picks]"]["note"] += (
         "; whole missed experts over the host link, written to their slots, gate/up and "
         "down computed on the way in; traffic = its DRAM bytes (the slot write-through)")
+    if hm.any():
+        # read-through time against the step's miss count: mean per count, and a
+        # least-squares line t = fixed + n * per_miss (the per-miss slope is the
+        # marginal link rate, the intercept the launch's fixed part)
+        by = {int(n): round(float(t_rt[n_miss == n].mean()) * 1e3, 1)
+              for n in np.unique(n_miss[hm])}
+        fit = None
+        if len(by) >= 2:
+            slope, icpt = np.polyfit(n_miss[hm].astype(float), t_rt[hm] * 1e-3, 1)
+            fit = {"fixed_us": round(float(icpt) * 1e6, 1),
+                   "per_miss_us": round(float(slope) * 1e6, 1),
+                   "marginal_link_gbs": round(Bexp / slope / 1e9, 1) if slope > 0 else None}
+        kern["gemv_readthrough[missed picks]"]["us_by_misses"] = by
+        kern["gemv_readthrough[missed picks]"]["fit"] = fit
     split = {"ms_per_step_event_graph": float(ev[:, 7].mean()),
              "ms_miss_path": float(np.mean(ev[:, 4] - ev[:, 1])),
              "ms_hit_path": float(np.mean(ev[:, 6] - ev[:, 1])),
