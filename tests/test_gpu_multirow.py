@@ -49,7 +49,8 @@ def _oracle_rows(orc, banks, cfg, lg, xb, rows):
 
 @pytest.mark.parametrize("name,wide_x", [("tiny", False), ("tiny_wide", False),
                                          ("tiny_wide", True), ("small", False),
-                                         ("small", True)])
+                                         ("small", True), ("small_wide_i", False),
+                                         ("small_wide_h", False)])
 def test_tiny_multirow_trace_outputs_and_device_bypass(lib, orc, name, wide_x):
     cfg = workload.CONFIGS[name]
     M, steps = 4, 40
@@ -204,7 +205,7 @@ def test_glm_prefill_bypass_sampled_rows(lib, orc):
     banks.close()
 
 
-@pytest.mark.parametrize("name", ["tiny", "tiny_wide", "small"])
+@pytest.mark.parametrize("name", ["tiny", "tiny_wide", "small", "small_wide_i", "small_wide_h"])
 def test_tiny_prefill_staged_equals_zero_copy(lib, orc, name):
     """Staged prefill (experts copied into HBM a chunk at a time, two chunks held)
     gives the same bits as reading host memory directly, for chunk sizes that

@@ -62,6 +62,12 @@ CONFIGS = {
     # tiles): H512/I256, 16 experts, top-4, S=8, wide scales
     "small": Config("small", 1, 512, 256, 16, 4, 8, 1, 64, 1.1, 0.0, 9,
                     literal_normal_bias=True),
+    # the same with one 256-element chunk of K for gate/up and a 4-chunk down pass
+    # (H256/I1024, top-2, S=4), and with the hidden size 1024 (H1024/I256, top-4, S=8)
+    "small_wide_i": Config("small_wide_i", 1, 256, 1024, 16, 2, 4, 1, 64, 1.1, 0.0, 10,
+                           literal_normal_bias=True),
+    "small_wide_h": Config("small_wide_h", 1, 1024, 256, 16, 4, 8, 1, 64, 1.1, 0.0, 11,
+                           literal_normal_bias=True),
     # GLM-5.3-shaped layer: H6144/I2048, 256 experts, top-8, S=128, M=1, 300 churn steps
     "glm": Config("glm", 1, 6144, 2048, 256, 8, 128, 1, 300, 1.1, 0.1, 1),
     # Flash-shaped stack: 16 layers, H4096/I2048, 288 experts top-8, S=54, 512 steps
