@@ -490,29 +490,21 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     bulk_g2s(dst + 2 * cb + sb, sc + ou * (H / 16), sb, &full[stage]);
   };
   int issued = 0;
-  if (tid >= NC) {  // control warp: the plan and the first fills, while x loads below
+  if (tid >= NC) {  // control warp: the plan, while x loads below
     pdl_wait();     // the plan comes from the kernel before this one
-    // the subset's picks, checked before they address memory: a bad plan skips
-    // the whole launch (MOE_FLAG_BAD_PLAN)
-    int pbeg = 0, pcnt = 0;
-    bool ok = subset_range(plan, subset, pbeg, pcnt);
-    const int npicks = ok ? plan->npicks : 0;
-    int j = 0;
-    if (lane < pcnt) {
-      j = subset == kPicksAll ? lane : plan->order[pbeg + lane];
-      ok = ok && pick_ok(plan, j, npicks, bounds, false);
-    }
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    if (!plan_ok(ok || lane != 0, flags) || !ok) pcnt = 0;
-    if (lane < pcnt) {
-      s_j[lane] = j;
-      s_w[lane] = plan->wptr[j];
-      s_s[lane] = plan->sptr[j];
-      s_gs[lane][0] = plan->gs[j][0];
-      s_gs[lane][1] = plan->gs[j][1];
+    // the subset's picks in one round of loads, checked before they address
+    // memory: a bad plan skips the whole launch (MOE_FLAG_BAD_PLAN)
+    const WarpPicks p = warp_picks(plan, subset, bounds, false, lane);
+    plan_ok(p.ok || lane != 0, flags);
+    if (lane < p.pcnt) {
+      s_j[lane] = p.j;
+      s_w[lane] = p.w;
+      s_s[lane] = p.s;
+      s_gs[lane][0] = p.gs0;
+      s_gs[lane][1] = p.gs1;
     }
     if (lane == 0) {
-      s_pcnt = pcnt;
+      s_pcnt = p.pcnt;
       for (int s = 0; s < NS; ++s) {
         mbar_init(&full[s], 1);
         mbar_init(&stashed[s], (uint32_t)(NC / 32));  // one arrival per compute warp
@@ -521,17 +513,20 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
       *abort_flag = 0;
     }
     __syncwarp();
-    const int my = units_of_block(pcnt * upp);
-    if (lane == 0)
-      for (; issued < NS && issued < my; ++issued) issue(blockIdx.x + issued * gridDim.x, issued);
   }
+  // x: the step's input (one barrier, which also publishes the picks and the
+  // mbarriers).  The first fills are issued after it, so the compute warps
+  // never wait at the barrier for the copy issue.
   uint32_t xh[16];
-  const float xup = load_x_f16(x, c < C ? c : 0, s_xmax, xh);  // x: the step's input (one barrier)
+  const float xup = load_x_f16(x, c < C ? c : 0, s_xmax, xh);
   const int pcnt = s_pcnt;
   const int nunits = pcnt * upp;
   const int my_units = units_of_block(nunits);
 
   if (tid >= NC) {  // ---- control warp
+    if (lane == 0)
+      for (; issued < NS && issued < my_units; ++issued)
+        issue(blockIdx.x + issued * gridDim.x, issued);
     int s = 0, rbuf = 0;  // stage and partial-sum buffer of unit i (no runtime division)
     uint32_t sphase = 0;  // parity of stage s's current "stashed" phase
     bool stopped = false;
@@ -638,6 +633,13 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   __shared__ int s_unit[kMaxStages];  // link unit staged in each stage, -1: none
   __shared__ int s_next[2];           // by iteration parity: read after the writer moved on
   __shared__ int s_pick[MOE_MAX_TOPK];  // the missed picks, checked
+  // their host and slot pointers and scales, read once: no plan round trip on
+  // the fill path
+  __shared__ const uint8_t* s_hw[MOE_MAX_TOPK];
+  __shared__ const uint8_t* s_hsc[MOE_MAX_TOPK];
+  __shared__ const uint8_t* s_dw[MOE_MAX_TOPK];
+  __shared__ const uint8_t* s_ds[MOE_MAX_TOPK];
+  __shared__ float s_pg[MOE_MAX_TOPK][3];  // gate, up global scales; down scale x router weight
   __shared__ int s_pcnt;
   __shared__ int s_hpick;   // missed pick whose f * h sits in hs (-1: none)
   __shared__ int s_hwait;   // the wait for a pick's h ended (1) or gave up (0)
@@ -656,19 +658,20 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   // The missed picks, each checked (index, slot and host pointers) before it
   // addresses memory: a bad plan skips the whole launch (MOE_FLAG_BAD_PLAN).
   if (tid < 32) {
-    int pbeg = 0, pcnt = 0;
-    bool ok = subset_range(plan, kPicksMiss, pbeg, pcnt);
-    const int npicks = ok ? plan->npicks : 0;
-    int j = 0;
-    if (tid < pcnt) {
-      j = plan->order[pbeg + tid];
-      ok = ok && pick_ok(plan, j, npicks, bounds, true);
+    const WarpPicks p = warp_picks(plan, kPicksMiss, bounds, true, tid);
+    plan_ok(p.ok || tid != 0, flags);
+    if (tid < p.pcnt) {
+      s_pick[tid] = p.j;
+      s_hw[tid] = p.hw;
+      s_hsc[tid] = p.hs;
+      s_dw[tid] = p.w;
+      s_ds[tid] = p.s;
+      s_pg[tid][0] = p.gs0;
+      s_pg[tid][1] = p.gs1;
+      s_pg[tid][2] = __fmul_rn(p.gs2, p.wt);
     }
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    if (!plan_ok(ok || tid != 0, flags) || !ok) pcnt = 0;
-    if (tid < pcnt) s_pick[tid] = j;
     if (tid == 0) {
-      s_pcnt = pcnt;
+      s_pcnt = p.pcnt;
       s_hpick = -1;
     }
   }
@@ -688,11 +691,10 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     Segs<4> sg;
     if (u < NG) {
       const int jl = u / upp, r = u - jl * upp;
-      const int j = pick_of(jl);
-      const uint8_t* hw = plan->hwptr[j];
-      const uint8_t* hsc = plan->hsptr[j];
-      uint8_t* dw = const_cast<uint8_t*>(plan->wptr[j]);
-      uint8_t* ds = const_cast<uint8_t*>(plan->sptr[j]);
+      const uint8_t* hw = s_hw[jl];
+      const uint8_t* hsc = s_hsc[jl];
+      uint8_t* dw = const_cast<uint8_t*>(s_dw[jl]);
+      uint8_t* ds = const_cast<uint8_t*>(s_ds[jl]);
       const size_t og = (size_t)r * R, ou = (size_t)I + (size_t)r * R;
       sg.src[0] = hw + og * (H / 2);
       sg.src[1] = hw + ou * (H / 2);
@@ -708,13 +710,12 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     } else {  // W2 rows r0 .. r0 + nr - 1: codes after the 2I W13 code rows, scales likewise
       const int v = u - NG, jl = v / n2, r0 = (v - jl * n2) * R2;
       const int nr = H - r0 < R2 ? H - r0 : R2;
-      const int j = pick_of(jl);
       const size_t oc = (size_t)I * H + (size_t)r0 * (I / 2);
       const size_t os = (size_t)I * H / 8 + (size_t)r0 * (I / 16);
-      sg.src[0] = plan->hwptr[j] + oc;
-      sg.src[1] = plan->hsptr[j] + os;
-      sg.dst[0] = const_cast<uint8_t*>(plan->wptr[j]) + oc;
-      sg.dst[1] = const_cast<uint8_t*>(plan->sptr[j]) + os;
+      sg.src[0] = s_hw[jl] + oc;
+      sg.src[1] = s_hsc[jl] + os;
+      sg.dst[0] = const_cast<uint8_t*>(s_dw[jl]) + oc;
+      sg.dst[1] = const_cast<uint8_t*>(s_ds[jl]) + os;
       sg.n[0] = nr * (I / 2);
       sg.n[1] = nr * (I / 16);
       nseg = 2;
@@ -781,7 +782,7 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
           break;  // uniform; the copies in flight are drained below
         }
         const int j = pick_of(jl);
-        const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
+        const float f = s_pg[jl][2];
         for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
           hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
         if (tid == 0) s_hpick = jl;
@@ -815,8 +816,8 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     __syncthreads();
     if (gu) {  // h rows of the unit, then the unit counts for its pick
       if (tid < RL * RPT) {
-        gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, plan->gs[pick_of(jl)][0],
-                                       plan->gs[pick_of(jl)][1], pick_of(jl), r, xup, hbuf, I, tid);
+        gateup_epilogue<RPT, WARP_RED>(S.red, RL, C, s_pg[jl][0], s_pg[jl][1], pick_of(jl), r,
+                                       xup, hbuf, I, tid);
         __threadfence();
       }
       __syncthreads();

@@ -431,20 +431,27 @@ __device__ __forceinline__ bool expert_ptr_ok(const uint8_t* p, const uint8_t* b
 
 // One pick's plan entries for a one-row kernel: j indexes the step's picks,
 // its slot pointers lie in the ring and (host) its backing pointers in the bank.
+__device__ __forceinline__ bool pick_ok_v(int j, int npicks, const uint8_t* w, const uint8_t* s,
+                                          const uint8_t* hw, const uint8_t* hs,
+                                          const PickBounds& b, bool host) {
+  if (j < 0 || j >= npicks || j >= MOE_MAX_TOPK) return false;
+  if (!expert_ptr_ok(w, b.slot_w, b.slot_n, b.Bw) || !expert_ptr_ok(s, b.slot_s, b.slot_n, b.Bs))
+    return false;
+  return !host || (expert_ptr_ok(hw, b.host_w, b.host_n, b.Bw) &&
+                   expert_ptr_ok(hs, b.host_s, b.host_n, b.Bs));
+}
+
 __device__ __forceinline__ bool pick_ok(const Plan* plan, int j, int npicks,
                                         const PickBounds& b, bool host) {
   if (j < 0 || j >= npicks || j >= MOE_MAX_TOPK) return false;
-  if (!expert_ptr_ok(plan->wptr[j], b.slot_w, b.slot_n, b.Bw) ||
-      !expert_ptr_ok(plan->sptr[j], b.slot_s, b.slot_n, b.Bs))
-    return false;
-  return !host || (expert_ptr_ok(plan->hwptr[j], b.host_w, b.host_n, b.Bw) &&
-                   expert_ptr_ok(plan->hsptr[j], b.host_s, b.host_n, b.Bs));
+  return pick_ok_v(j, npicks, plan->wptr[j], plan->sptr[j], host ? plan->hwptr[j] : nullptr,
+                   host ? plan->hsptr[j] : nullptr, b, host);
 }
 
 // The subset's pick range of a one-row plan, checked: 0 <= n_hit <= npicks <=
 // MOE_MAX_TOPK.  False (and no picks) when the plan fails the check.
-__device__ __forceinline__ bool subset_range(const Plan* plan, int subset, int& pbeg, int& pcnt) {
-  const int npicks = plan->npicks, n_hit = plan->n_hit;
+__device__ __forceinline__ bool subset_range_v(int npicks, int n_hit, int subset, int& pbeg,
+                                               int& pcnt) {
   pbeg = 0;
   pcnt = 0;
   if (npicks < 0 || npicks > MOE_MAX_TOPK || n_hit < 0 || n_hit > npicks) return false;
@@ -455,6 +462,60 @@ __device__ __forceinline__ bool subset_range(const Plan* plan, int subset, int& 
     pcnt = npicks - n_hit;
   }
   return true;
+}
+
+__device__ __forceinline__ bool subset_range(const Plan* plan, int subset, int& pbeg, int& pcnt) {
+  return subset_range_v(plan->npicks, plan->n_hit, subset, pbeg, pcnt);
+}
+
+// A one-row kernel's picks of `subset`, read by one warp in a single round of
+// independent loads (every lane < MOE_MAX_TOPK loads entry `lane` of each plan
+// array; the subset's picks are then gathered by shuffles) and checked.  Lane l
+// < pcnt returns pick j and its entries; ok is warp-uniform and false (pcnt 0)
+// when any check fails.  host: the backing pointers are loaded and checked too.
+struct WarpPicks {
+  int pcnt, npicks, j;
+  bool ok;
+  const uint8_t *w, *s, *hw, *hs;
+  float gs0, gs1, gs2, wt;
+};
+__device__ __forceinline__ WarpPicks warp_picks(const Plan* plan, int subset,
+                                                const PickBounds& b, bool host, int lane) {
+  WarpPicks p;
+  const int np_raw = plan->npicks, nh_raw = plan->n_hit;
+  const bool in = lane < MOE_MAX_TOPK;
+  const int ol = in ? plan->order[lane] : 0;
+  const uint8_t* wl = in ? plan->wptr[lane] : nullptr;
+  const uint8_t* sl = in ? plan->sptr[lane] : nullptr;
+  const uint8_t* hwl = (in && host) ? plan->hwptr[lane] : nullptr;
+  const uint8_t* hsl = (in && host) ? plan->hsptr[lane] : nullptr;
+  const float g0 = in ? plan->gs[lane][0] : 0.f, g1 = in ? plan->gs[lane][1] : 0.f;
+  const float g2 = in ? plan->gs[lane][2] : 0.f, wt = in ? plan->wts[lane] : 0.f;
+  int pbeg = 0, pcnt = 0;
+  bool ok = subset_range_v(np_raw, nh_raw, subset, pbeg, pcnt);
+  p.npicks = ok ? np_raw : 0;
+  const int oi = pbeg + lane;
+  const int oj = __shfl_sync(0xFFFFFFFFu, ol, oi < MOE_MAX_TOPK ? oi : 0);
+  int j = 0;
+  if (lane < pcnt) j = subset == kPicksAll ? lane : oj;
+  const int src = (j >= 0 && j < MOE_MAX_TOPK) ? j : 0;
+  p.w = reinterpret_cast<const uint8_t*>(
+      __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(wl), src));
+  p.s = reinterpret_cast<const uint8_t*>(
+      __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(sl), src));
+  p.hw = reinterpret_cast<const uint8_t*>(
+      __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(hwl), src));
+  p.hs = reinterpret_cast<const uint8_t*>(
+      __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(hsl), src));
+  p.gs0 = __shfl_sync(0xFFFFFFFFu, g0, src);
+  p.gs1 = __shfl_sync(0xFFFFFFFFu, g1, src);
+  p.gs2 = __shfl_sync(0xFFFFFFFFu, g2, src);
+  p.wt = __shfl_sync(0xFFFFFFFFu, wt, src);
+  if (lane < pcnt) ok = ok && pick_ok_v(j, p.npicks, p.w, p.s, p.hw, p.hs, b, host);
+  p.ok = __all_sync(0xFFFFFFFFu, ok);
+  p.pcnt = p.ok ? pcnt : 0;
+  p.j = j;
+  return p;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits) {
