@@ -249,7 +249,21 @@ def run_reference(args) -> None:
 
 # ---------------------------------------------------------------- our arm
 
-RUNS = 5  # timed runs of K rounds each, over distinct fresh rounds; the median is reported
+# Timed runs of K rounds each, over distinct fresh rounds; the median run is
+# reported.  At least 5 runs, and enough that the runs cover ~RUN_LAYER_STEPS
+# layer-steps together (at most 50 runs), so a short K still samples the
+# workload's miss mix instead of a handful of steps.
+RUNS_MIN, RUNS_MAX, RUN_LAYER_STEPS = 5, 50, 1500
+
+
+def n_runs(K: int, L: int = 1) -> int:
+    return max(RUNS_MIN, min(RUNS_MAX, -(-RUN_LAYER_STEPS // max(K * L, 1))))
+# Untimed fresh rounds replayed right before the timed runs, about this long: after
+# even a fraction of a second idle (graph capture, the clock sampler's start) the
+# first ~100 ms of steps ran up to 2-3x slower (the host link and memory come back
+# from idle), so the timed runs start on a busy GPU.
+PRERUN_S = 0.25
+PRERUN_EST_ROUND_S = 1.7e-4  # per layer-step, to size the pre-run's slice of the trace
 
 
 class Feeder:
@@ -293,7 +307,7 @@ def decode_bench(cfg, *, layers: int, slots: int, K: int, W: int, prewarm: int,
     with `slots` slots a layer.  Every timed round consumes fresh inputs.
 
     Sequence: `prewarm` eager rounds from an empty ring (steady state), W warm-up
-    rounds through the graphs, RUNS timed runs of K rounds (the plain graph with
+    rounds through the graphs, n_runs(K) timed runs of K rounds (the plain graph with
     programmatic launches; the value is the median run), then, on further fresh
     rounds, an event-instrumented graph for per-kernel times, the end-to-end leg
     through moe_cache_step_host with pinned host buffers, and a cold start (the
@@ -311,7 +325,9 @@ def decode_bench(cfg, *, layers: int, slots: int, K: int, W: int, prewarm: int,
         banks = Banks(cfg)
     cache = make_cache(cfg, banks, layers=L, slots=slots, trace_capacity=max(ev_rounds, 8))
     B = max(1, min(10, W - 1))            # rounds in the multi-round graph
-    T_dev = prewarm + W + RUNS * K + ev_rounds
+    prerun = max(2 * B, min(2000, int(PRERUN_S / (PRERUN_EST_ROUND_S * L))))
+    RUNS = n_runs(K, L)
+    T_dev = prewarm + W + prerun + RUNS * K + ev_rounds
     T = T_dev + e2e_rounds
     rts = [workload.Routing(cfg, layer=seed_layers_from + l) for l in range(L)]
     lgs = np.empty((T, L, E), np.float32)
@@ -364,9 +380,10 @@ def decode_bench(cfg, *, layers: int, slots: int, K: int, W: int, prewarm: int,
         uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
     except Exception:
         pass
-    s0 = cache.stats(-1)
     sampler = ClockSampler(uuid)
-    time.sleep(0.15)
+    with torch.cuda.stream(stream):       # pre-run: fresh rounds, untimed, no idle gap after
+        replay(g1, gB, prerun)
+    s0 = cache.stats(-1)                  # (synchronizes)
     run_ms = []
     for _ in range(RUNS):
         if world > 1:
@@ -470,6 +487,7 @@ def decode_bench(cfg, *, layers: int, slots: int, K: int, W: int, prewarm: int,
     return {"run_ms": run_ms, "value": med[0], "ms_total": med[1], "misses_per_step": misses,
             "hit_rate": hits / picks if picks else None, "clocks": clocks, "ev_ms": ev_ms,
             "ev_n_miss": n_miss, "e2e": e2e, "cold": cold, "K": K, "L": L, "B": B,
+            "prerun": prerun, "runs": RUNS,
             "Bexp": banks.Bw + banks.Bs}
 
 
@@ -597,7 +615,7 @@ def run_ours(args) -> None:
     cfg = workload.CONFIGS["glm"]
     K, W = args.steps, args.warmup
     res = decode_bench(cfg, layers=1, slots=cfg.slots, K=K, W=W, prewarm=300, ev_rounds=200,
-                       e2e_rounds=min(K, 1000) + 2, cold_rounds=300, world=world, rank=rank)
+                       e2e_rounds=max(min(K, 1000), 300) + 2, cold_rounds=300, world=world, rank=rank)
     # sanity: the timed rounds must exercise the miss path at S = 128
     if not 0.3 <= res["misses_per_step"] <= 4.0:
         raise SystemExit(f"timed rounds saw {res['misses_per_step']:.3f} misses per layer-step at "
@@ -639,7 +657,8 @@ def run_ours(args) -> None:
                        "graph": f"one CUDA graph of {res['B']} rounds (and a one-round graph) "
                                 "replayed; its first node feeds each round fresh inputs from a "
                                 "device trace (moe_feed_inputs); programmatic launches on",
-                       "timing": f"{RUNS} runs of K fresh steps each after a 300-step pre-warm; "
+                       "timing": f"{res['runs']} runs of K fresh steps each after a 300-step pre-warm "
+                                 f"and an untimed pre-run of {res['prerun']} fresh steps; "
                                  "value = median run"},
             "tok_s_equivalent": res["value"] / GLM_MOE_LAYERS,
             "path_roofline": path, "roofline": roofline, "kernels": kern, "timing_split": split,
@@ -685,7 +704,8 @@ def run_flash_or_sweep(args) -> None:
                                        "independent per layer, one host bank aliased by every "
                                        "layer",
                            "graph": "one CUDA graph per round of all layers, fed fresh inputs",
-                           "timing": f"{RUNS} runs of K rounds, median"},
+                           "timing": f"{res['runs']} runs of K fresh rounds after an untimed pre-run "
+                                     f"of {res['prerun']} fresh rounds, median"},
                 "tok_s_equivalent": res["value"] / 42, "layer_steps": ls,
                 "path_roofline": path, "kernels": kern, "timing_split": split,
                 "clocks": res["clocks"]}
@@ -716,7 +736,8 @@ def run_flash_or_sweep(args) -> None:
                 "config": {"workload": f"slot sweep: {L} layers, GLM shape, Zipf(1.1) routing "
                                        "independent per layer, S in "
                                        f"{list(workload.SWEEP_SLOTS)}; value = S=128",
-                           "timing": f"300-round pre-warm, then {RUNS} runs of K fresh rounds, "
+                           "timing": f"300-round pre-warm and an untimed pre-run of ~{PRERUN_S} s "
+                                     f"of fresh rounds, then {n_runs(K, L)} runs of K fresh rounds, "
                                      "median; cold = 300 rounds from empty"},
                 "per_slots": per_s, "link_peak_gbs": link_peak, "hbm_peak_gbs": hbm_peak,
                 "clocks": clocks}
