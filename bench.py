@@ -763,47 +763,50 @@ def run_rows(args) -> None:
     E, H, I, k, M = cfg.experts, cfg.hidden, cfg.inter, cfg.top_k, cfg.rows
     L = args.layers or cfg.layers
     W, K = args.warmup, args.steps
-    if K * L > 4096:
-        raise SystemExit("--workload multirow/prefill: steps x layers must be <= 4096 (one graph)")
-    T = W + K
-    banks = Banks(cfg)
     prefill = args.workload == "prefill"
+    # untimed fresh rounds right before the timed ones (see PRERUN_S)
+    pre = max(2, int(PRERUN_S / (L * (26e-3 if prefill else 1.3e-3))) + 1)
+    T = W + pre + K
+    banks = Banks(cfg)
     cache = make_cache(cfg, banks, layers=L, trace_capacity=0 if prefill else T,
                        max_rows=max(M, 16))
     Bexp = banks.Bw + banks.Bs
-    # inputs: per (step, layer) logits; activations per step, shared by the layers
+    # inputs: per (round, layer) logits; activations per round, shared by the layers
     if prefill:
         lgs = np.stack([np.stack([workload.prefill_logits(cfg, l, M) for l in range(L)])] * T)
     else:
         rts = [workload.Routing(cfg, layer=l) for l in range(L)]
         lgs = np.stack([np.stack([rts[l].step() for l in range(L)]) for _ in range(T)])
     xs = workload.activations(cfg.seed, 0, T, M, H)
-    lg_d = torch.from_numpy(lgs.astype(np.float32)).cuda()               # [T, L, M, E]
-    x_d = torch.from_numpy(xs.view(np.int16)).cuda().view(torch.bfloat16)  # [T, M, H]
+    # every round reads fresh inputs: a one-round graph whose first node copies the
+    # next trace entry into the fixed buffers (moe_feed_inputs), replayed
+    fd = Feeder(lgs.astype(np.float32), xs)                  # lg [L, M, E], x [M, H]
     out_d = torch.empty((M, H), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
 
-    def run(t0, t1):
-        for t in range(t0, t1):
-            for l in range(L):
-                cache.step(l, lg_d[t, l], x_d[t], out_d)
+    def one_round():
+        fd.feed(stream)
+        for l in range(L):
+            cache.step(l, fd.lg[l], fd.x, out_d, stream)
 
     with torch.cuda.stream(stream):
-        run(0, W)                                  # eager warm-up (fills the rings)
+        for _ in range(W):                         # eager warm-up (fills the rings)
+            one_round()
     stream.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        run(W, T)
-    with torch.cuda.stream(stream):
-        g.replay()                                 # upload; the rings move on, steady state
-    stream.synchronize()
-    s0 = cache.stats(-1)
+        one_round()
     sampler = ClockSampler(None)
-    time.sleep(0.15)
+    with torch.cuda.stream(stream):
+        for _ in range(pre):                       # uploads the graph, then the pre-run
+            g.replay()
+    s0 = cache.stats(-1)                           # (synchronizes)
+    assert fd.position() == W + pre, fd.position()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        g.replay()
+        for _ in range(K):
+            g.replay()
         e1.record(stream)
     stream.synchronize()
     clocks = sampler.stop()
@@ -865,7 +868,10 @@ def run_rows(args) -> None:
             "data": "synthetic",
             "config": {"workload": f"{args.workload}: hidden {H}, inter {I}, {E} experts, top-{k}, "
                                    f"M={M} rows, {L} layers, S={cfg.slots}",
-                       "graph": "one CUDA graph over the timed steps"},
+                       "graph": "a one-round graph (all layers) replayed K times, its first node "
+                                "feeding each round fresh inputs from a device trace",
+                       "timing": f"{W} eager warm-up rounds, an untimed pre-run of {pre} fresh "
+                                 "rounds, then K fresh rounds timed"},
             "layer_steps_per_s": layer_steps / (ms * 1e-3),
             "experts_read_per_layer_step": union, "misses_per_layer_step": misses / layer_steps,
             "roofline": roof,
