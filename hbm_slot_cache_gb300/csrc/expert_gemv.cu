@@ -918,14 +918,14 @@ gemv_down_kernel(const Plan* plan, const float* hbuf, float* ypart, int H, int I
   };
   const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
   pdl_wait();  // h and the slot bytes may come from the kernel before this one
+  {  // h first: its loads do not queue behind the ring's copy issue
+    for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
+      hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
+  }
   if (lane == 0) {
     for (int s = 0; s < NSW; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     for (int s = 0; s < NSW && s < my_items; ++s) issue(s, s);
-  }
-  {
-    for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
-      hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
   }
   __syncthreads();
   // this lane's blocks of the pick's h, kept in registers for the whole kernel
