@@ -62,7 +62,7 @@ struct MmaArgs {
   QuantBuf act; // gate/up: by token row; down: by pick
   float* out;   // gate/up: h [P][I]; down: y [P][H]
   uint32_t* flags;
-  int g0, g1;   // the launch's groups [g0, g1) (kHitGroups: the step's hit-group count)
+  int g0, g1;   // the launch's groups [g0, g1) (bounds as resolve_group takes them)
   // cp.async kernel only: a launch whose first group's expert lies in this
   // region (base, experts, bytes per expert; null: none) is left to the TMA
   // kernel launched beside it.  A step's groups are all in one place: the
@@ -138,8 +138,8 @@ grouped_mma_kernel(MmaArgs a) {
   // this launch's jobs: those of groups [g0, g1)
   const int ng = gp->n_groups;
   const int nh = min(max(gp->n_hit_groups, 0), ng);
-  const int g0 = a.g0 == kHitGroups ? nh : max(a.g0, 0);
-  const int g1 = a.g1 == kHitGroups ? nh : a.g1;
+  const int g0 = resolve_group(a.g0, nh, ng);
+  const int g1 = resolve_group(a.g1, nh, ng);
   const int jbeg = g0 < ng ? gp->g_job[g0] : gp->n_jobs;
   const int jend = gp->g_job[g1 < ng ? g1 : ng];
   if (jbeg + (int)blockIdx.x >= jend) return;  // uniform: before any TMEM or barrier use
@@ -585,8 +585,8 @@ grouped_mma_tma_kernel(const __grid_constant__ MmaTmaArgs a) {
   const GroupPlan* gp = m.gp;
   const int ng = gp->n_groups;
   const int nh = min(max(gp->n_hit_groups, 0), ng);
-  const int g0 = m.g0 == kHitGroups ? nh : max(m.g0, 0);
-  const int g1 = m.g1 == kHitGroups ? nh : m.g1;
+  const int g0 = resolve_group(m.g0, nh, ng);
+  const int g1 = resolve_group(m.g1, nh, ng);
   const int jbeg = g0 < ng ? gp->g_job[g0] : gp->n_jobs;
   const int jend = gp->g_job[g1 < ng ? g1 : ng];
   const int m_tiles = m.gate_up ? m.I / kTRows : m.H / (2 * kTRows);

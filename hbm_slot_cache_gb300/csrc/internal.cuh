@@ -70,8 +70,14 @@ constexpr int kLevels = 6;       // residual NVFP4 levels of the activations
 constexpr int kRowsPerJob = 5;   // members per MMA N-tile (5 * 6 = 30 of 32 columns)
 // Groups list the experts resident at step start (hits) first, then the rest,
 // each part in ascending expert id, so a step can run the hit groups while the
-// misses copy.  kHitGroups as a launch's g0 or g1 stands for n_hit_groups.
+// misses copy.  kHitGroups as a launch's g0 or g1 stands for n_hit_groups;
+// miss_part(p, P) for the first miss group of part p of P: the miss groups
+// [n_hit_groups, n_groups) cut at n_hit_groups + (n_groups - n_hit_groups) * p / P
+// (p = P: n_groups).  Part p's groups are the misses of part p of the plan's
+// miss list (also ascending expert id), so a step can compute the misses of
+// one part while the next part copies.  P < 16.
 constexpr int kHitGroups = -1;
+__host__ __device__ constexpr int miss_part(int p, int P) { return -(64 + 16 * p + P); }
 struct GroupPlan {
   int32_t n_groups, n_jobs, rows, npicks;
   int32_t n_hit_groups;    // groups [0, n_hit_groups) need no copy this step
@@ -155,10 +161,11 @@ cudaError_t launch_stage_copy(cudaStream_t st, GroupPlan* gp, int q, int C, cons
 cudaError_t launch_combine(cudaStream_t st, const GroupPlan* gp, const float* y, float* out,
                            int rows, int H, int k);
 
-// miss copy host -> slot, SM kernel; reads the miss list from the plan.
+// miss copy host -> slot, SM kernel; reads the miss list from the plan and copies
+// part `part` of `parts` of it (misses n * part / parts .. n * (part + 1) / parts).
 cudaError_t launch_miss_copy(cudaStream_t st, const Plan* plan, const uint8_t* host_w,
                              const uint8_t* host_s, uint8_t* slot_w, uint8_t* slot_s,
-                             long long Bw, long long Bs, int grid);
+                             long long Bw, long long Bs, int grid, int part = 0, int parts = 1);
 cudaError_t launch_link_probe(cudaStream_t st, const void* src, void* dst, size_t bytes,
                               int grid);
 
@@ -446,6 +453,17 @@ __device__ __forceinline__ bool pick_ok(const Plan* plan, int j, int npicks,
   if (j < 0 || j >= npicks || j >= MOE_MAX_TOPK) return false;
   return pick_ok_v(j, npicks, plan->wptr[j], plan->sptr[j], host ? plan->hwptr[j] : nullptr,
                    host ? plan->hsptr[j] : nullptr, b, host);
+}
+
+// A launch's group bound g (a group index, kHitGroups or miss_part(p, P)) for a
+// step with nh hit groups of ng: a group index in [0, ng] (or above ng for "all").
+__device__ __forceinline__ int resolve_group(int g, int nh, int ng) {
+  if (g == kHitGroups) return nh;
+  if (g <= -64) {
+    const int v = -g - 64, p = v / 16, P = v % 16;
+    return P > 0 ? nh + (int)((long long)(ng - nh) * p / P) : ng;
+  }
+  return g < 0 ? 0 : g;
 }
 
 // The subset's pick range of a one-row plan, checked: 0 <= n_hit <= npicks <=

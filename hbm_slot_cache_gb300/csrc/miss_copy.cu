@@ -39,15 +39,17 @@ __device__ __forceinline__ void copy_chunk(const uint8_t* __restrict__ src,
 __global__ void __launch_bounds__(kThreads)
 miss_copy_kernel(const Plan* __restrict__ plan, const uint8_t* __restrict__ host_w,
                  const uint8_t* __restrict__ host_s, uint8_t* __restrict__ slot_w,
-                 uint8_t* __restrict__ slot_s, long long Bw, long long Bs) {
-  const int n = plan->n_miss;
+                 uint8_t* __restrict__ slot_s, long long Bw, long long Bs, int part, int parts) {
+  const int nall = plan->n_miss;
+  const int m0 = nall * part / parts, m1 = nall * (part + 1) / parts;
+  const int n = m1 - m0;
   if (n <= 0) return;
   const long long ncw = (Bw + kChunk - 1) / kChunk;
   const long long ncs = (Bs + kChunk - 1) / kChunk;
   const long long nc = ncw + ncs;
   for (long long c = blockIdx.x; c < (long long)n * nc; c += gridDim.x) {
-    const int i = (int)(c / nc);
-    const long long r = c - (long long)i * nc;
+    const int i = m0 + (int)(c / nc);
+    const long long r = c - (long long)(i - m0) * nc;
     const long long e = plan->miss_e[i], v = plan->miss_v[i];
     if (r < ncw)
       copy_chunk(host_w + e * Bw, slot_w + v * Bw, r * kChunk, Bw);
@@ -98,14 +100,16 @@ link_probe_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, lo
 
 cudaError_t launch_miss_copy(cudaStream_t st, const Plan* plan, const uint8_t* host_w,
                              const uint8_t* host_s, uint8_t* slot_w, uint8_t* slot_s,
-                             long long Bw, long long Bs, int grid) {
+                             long long Bw, long long Bs, int grid, int part, int parts) {
+  if (parts < 1 || part < 0 || part >= parts) return cudaErrorInvalidValue;
   static bool once = false;
   if (!once) {
     cudaError_t e = prefer_max_shared(miss_copy_kernel);
     if (e != cudaSuccess) return e;
     once = true;
   }
-  miss_copy_kernel<<<grid, kThreads, 0, st>>>(plan, host_w, host_s, slot_w, slot_s, Bw, Bs);
+  miss_copy_kernel<<<grid, kThreads, 0, st>>>(plan, host_w, host_s, slot_w, slot_s, Bw, Bs, part,
+                                               parts);
   return cudaGetLastError();
 }
 

@@ -18,6 +18,9 @@ using namespace moe;
 
 namespace {
 constexpr int kDefaultPrefillChunk = 32;  // experts staged per prefill chunk (two chunks held)
+// A cached multi-row step copies its misses in this many parts; the miss groups
+// of a part run as soon as that part has landed, while the next one copies.
+constexpr int kMissParts = 3;
 }
 
 struct moe_cache {
@@ -52,6 +55,7 @@ struct moe_cache {
   // one-row steps fork the miss path onto a second stream
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t part_done[kMissParts] = {};  // multi-row steps: a part of the misses landed
   // staged prefill: two halves of `chunk` expert slots, events per chunk
   int chunk = 0, nchunks = 0;
   uint8_t* stage_w = nullptr;  // [2 * chunk][Bw]
@@ -105,6 +109,10 @@ void free_all(moe_cache* h) {
   h->ev_used.clear();
   if (h->fork) cudaEventDestroy(h->fork);
   if (h->join) cudaEventDestroy(h->join);
+  for (cudaEvent_t& ev : h->part_done) {
+    if (ev) cudaEventDestroy(ev);
+    ev = nullptr;
+  }
   if (h->side) cudaStreamDestroy(h->side);
   h->fork = h->join = nullptr;
   h->side = nullptr;
@@ -390,6 +398,8 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
            cudaSuccess &&
        cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming) == cudaSuccess;
+  for (int q = 0; ok && q < kMissParts; ++q)
+    ok = cudaEventCreateWithFlags(&h->part_done[q], cudaEventDisableTiming) == cudaSuccess;
   // host-buffer steps: staging for max_rows rows and a capture stream
   ok = ok && dalloc(&h->st_logits, (size_t)o.max_rows * experts) == cudaSuccess &&
        dalloc(&h->st_x, (size_t)o.max_rows * hidden) == cudaSuccess &&
@@ -518,9 +528,12 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     if (e == cudaSuccess) e = mark(1, st);
     if (e == cudaSuccess) e = cudaEventRecord(h->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork, 0);
-    if (e == cudaSuccess && !h->opts.all_resident)
-      e = launch_miss_copy(h->side, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw, h->Bs,
-                           std::max(8, h->num_sms / 2));
+    for (int q = 0; q < kMissParts && e == cudaSuccess; ++q) {
+      if (!h->opts.all_resident)
+        e = launch_miss_copy(h->side, h->plan, L.host_w, L.host_s, L.slot_w, L.slot_s, h->Bw,
+                             h->Bs, std::max(8, h->num_sms / 2), q, kMissParts);
+      if (e == cudaSuccess) e = cudaEventRecord(h->part_done[q], h->side);
+    }
     if (e == cudaSuccess) e = cudaEventRecord(h->join, h->side);
   } else {
     // prefill bypass: experts read from host memory, cache untouched
@@ -563,14 +576,17 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
     if (e == cudaSuccess) e = mark(4, st);
     if (e == cudaSuccess) e = mark(6, st);
   } else if (cached_rows) {
-    // hit groups [0, n_hit) now, miss groups [n_hit, n) once their bytes are in
-    // the slots: gate/up, the members' h in residual NVFP4, down, each pass.
-    // A union larger than the ring (possible only when npicks > S) bypasses on
-    // the device and reads host memory.
-    const int gr[3] = {0, kHitGroups, INT_MAX};
+    // hit groups [0, n_hit) now, then each part of the miss groups once that
+    // part's bytes are in the slots (the next part copies meanwhile): gate/up,
+    // the members' h in residual NVFP4, down, each pass.  A union larger than
+    // the ring (possible only when npicks > S) bypasses on the device and
+    // reads host memory.
+    int gr[kMissParts + 2] = {0, kHitGroups};
+    for (int q = 1; q <= kMissParts; ++q) gr[q + 1] = miss_part(q, kMissParts);
+    gr[kMissParts + 1] = INT_MAX;
     const bool may_bypass = npicks > h->S_of[layer];
-    for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
-      if (pass == 1) e = cudaStreamWaitEvent(st, h->join, 0);
+    for (int pass = 0; pass <= kMissParts && e == cudaSuccess; ++pass) {
+      if (pass >= 1) e = cudaStreamWaitEvent(st, h->part_done[pass - 1], 0);
       if (e == cudaSuccess)
         e = launch_grouped_mma(st, h->gp, npicks, true, h->H, h->I, h->k, h->xq, h->gemv.hbuf,
                                flags, gr[pass], gr[pass + 1], &h->tma_slots, may_bypass);

@@ -126,16 +126,15 @@ quantize_rows_kernel(const void* __restrict__ src, int K, QuantBuf q) {
 }
 
 // The rows named by the members of groups [g0, g1) (members are stored group
-// after group, so they are one contiguous range; kHitGroups: the hit-group count).
+// after group, so they are one contiguous range; bounds as resolve_group takes them).
 __global__ void __launch_bounds__(1024)
 quantize_members_kernel(const float* __restrict__ src, int K, const GroupPlan* __restrict__ gp,
                         int g0, int g1, QuantBuf q) {
   __shared__ float red[32];
   const int ng = gp->n_groups;
   const int nh = min(max(gp->n_hit_groups, 0), ng);
-  if (g0 == kHitGroups) g0 = nh;
-  if (g1 == kHitGroups) g1 = nh;
-  if (g0 < 0) g0 = 0;
+  g0 = resolve_group(g0, nh, ng);
+  g1 = resolve_group(g1, nh, ng);
   if (g0 >= ng || g1 <= g0) return;
   const int mbeg = gp->g_start[g0];
   const int mend = g1 < ng ? gp->g_start[g1] : gp->npicks;
