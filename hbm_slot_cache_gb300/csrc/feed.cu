@@ -44,7 +44,91 @@ feed_inputs_kernel(const uint4* __restrict__ a_src, uint4* __restrict__ a_dst, l
   }
 }
 
+// Host <-> device moves of a step's inputs and output by kernels that read or
+// write page-locked host memory directly (its device-side address): every
+// load of a launch is in flight at once, so a step's inputs cost a kernel
+// launch and one host-link round trip instead of two copy-engine transfers,
+// and its output one posted store per word.  Words of 16 bytes where both ends
+// are 16-byte aligned, else 4 (logits, output) or 2 bytes (x).
+constexpr int kIoThreads = 512;
+
+__device__ __forceinline__ bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+__global__ void __launch_bounds__(kIoThreads)
+host_in_kernel(const float* lg_h, const uint16_t* x_h, float* lg_d, uint16_t* x_d, int nl,
+               int nx) {
+  const int stride = gridDim.x * blockDim.x, i0 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (al16(lg_h) && al16(lg_d) && (nl & 3) == 0) {
+    for (int i = i0; i < nl / 4; i += stride)
+      reinterpret_cast<uint4*>(lg_d)[i] = reinterpret_cast<const uint4*>(lg_h)[i];
+  } else {
+    for (int i = i0; i < nl; i += stride) lg_d[i] = lg_h[i];
+  }
+  if (al16(x_h) && al16(x_d) && (nx & 7) == 0) {
+    for (int i = i0; i < nx / 8; i += stride)
+      reinterpret_cast<uint4*>(x_d)[i] = reinterpret_cast<const uint4*>(x_h)[i];
+  } else {
+    for (int i = i0; i < nx; i += stride) x_d[i] = x_h[i];
+  }
+}
+
+__global__ void __launch_bounds__(kIoThreads)
+host_out_kernel(const float* out_d, float* out_h, int n) {
+  const int stride = gridDim.x * blockDim.x, i0 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (al16(out_h) && al16(out_d) && (n & 3) == 0) {
+    for (int i = i0; i < n / 4; i += stride)
+      reinterpret_cast<uint4*>(out_h)[i] = reinterpret_cast<const uint4*>(out_d)[i];
+  } else {
+    for (int i = i0; i < n; i += stride) out_h[i] = out_d[i];
+  }
+}
+
+int io_grid(int words) {
+  const int g = (words + 4 * kIoThreads - 1) / (4 * kIoThreads);  // ~4 words a thread
+  return g < 1 ? 1 : (g > 64 ? 64 : g);
+}
+
 }  // namespace
+
+cudaError_t launch_host_in(cudaStream_t st, const float* lg_h, const uint16_t* x_h, float* lg_d,
+                           uint16_t* x_d, int nl, int nx) {
+  host_in_kernel<<<io_grid(nx / 8 > nl / 4 ? nx / 8 : nl / 4), kIoThreads, 0, st>>>(
+      lg_h, x_h, lg_d, x_d, nl, nx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_host_out(cudaStream_t st, const float* out_d, float* out_h, int n) {
+  host_out_kernel<<<io_grid(n / 4), kIoThreads, 0, st>>>(out_d, out_h, n);
+  return cudaGetLastError();
+}
+
+bool is_host_in_node(const void* func) { return func == reinterpret_cast<const void*>(host_in_kernel); }
+bool is_host_out_node(const void* func) {
+  return func == reinterpret_cast<const void*>(host_out_kernel);
+}
+
+cudaError_t set_host_in_node(cudaGraphExec_t ex, cudaGraphNode_t node, const float* lg_h,
+                             const uint16_t* x_h, float* lg_d, uint16_t* x_d, int nl, int nx) {
+  void* args[] = {&lg_h, &x_h, &lg_d, &x_d, &nl, &nx};
+  cudaKernelNodeParams p{};
+  p.func = reinterpret_cast<void*>(host_in_kernel);
+  p.gridDim = dim3(io_grid(nx / 8 > nl / 4 ? nx / 8 : nl / 4));
+  p.blockDim = dim3(kIoThreads);
+  p.kernelParams = args;
+  return cudaGraphExecKernelNodeSetParams(ex, node, &p);
+}
+
+cudaError_t set_host_out_node(cudaGraphExec_t ex, cudaGraphNode_t node, const float* out_d,
+                              float* out_h, int n) {
+  void* args[] = {&out_d, &out_h, &n};
+  cudaKernelNodeParams p{};
+  p.func = reinterpret_cast<void*>(host_out_kernel);
+  p.gridDim = dim3(io_grid(n / 4));
+  p.blockDim = dim3(kIoThreads);
+  p.kernelParams = args;
+  return cudaGraphExecKernelNodeSetParams(ex, node, &p);
+}
+
 }  // namespace moe
 
 using namespace moe;

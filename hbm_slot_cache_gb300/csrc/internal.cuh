@@ -168,6 +168,18 @@ cudaError_t launch_miss_copy(cudaStream_t st, const Plan* plan, const uint8_t* h
                              long long Bw, long long Bs, int grid, int part = 0, int parts = 1);
 cudaError_t launch_link_probe(cudaStream_t st, const void* src, void* dst, size_t bytes,
                               int grid);
+// A step's host-buffer inputs and output moved by kernels over page-locked
+// host memory's device-side addresses (lg_h, x_h, out_h); the set_* calls
+// point a captured graph's nodes of those kernels at another call's buffers.
+cudaError_t launch_host_in(cudaStream_t st, const float* lg_h, const uint16_t* x_h, float* lg_d,
+                           uint16_t* x_d, int nl, int nx);
+cudaError_t launch_host_out(cudaStream_t st, const float* out_d, float* out_h, int n);
+bool is_host_in_node(const void* func);
+bool is_host_out_node(const void* func);
+cudaError_t set_host_in_node(cudaGraphExec_t ex, cudaGraphNode_t node, const float* lg_h,
+                             const uint16_t* x_h, float* lg_d, uint16_t* x_d, int nl, int nx);
+cudaError_t set_host_out_node(cudaGraphExec_t ex, cudaGraphNode_t node, const float* out_d,
+                              float* out_h, int n);
 
 // M = 1 expert path: gate/up + SwiGLU -> hbuf [k][I]; down + combine -> out [H].
 struct GemvWorkspace {

@@ -73,7 +73,7 @@ struct moe_cache {
   cudaStream_t cap = nullptr;   // capture stream
   std::vector<cudaGraphExec_t> graph;  // [L], null until captured
   std::vector<cudaGraph_t> graph_src;  // [L] the captured graphs (their nodes address the copies)
-  std::vector<std::array<cudaGraphNode_t, 3>> graph_cp;  // [L] logits, x, out copy nodes
+  std::vector<std::array<cudaGraphNode_t, 2>> graph_cp;  // [L] input and output move nodes
   std::vector<char> graph_warm;        // [L]: one eager one-row step done
 };
 
@@ -408,7 +408,7 @@ int moe_cache_create(moe_cache_t** out, int layers, int experts, int slots, int 
   if (ok) {
     h->graph.assign(layers, nullptr);
     h->graph_src.assign(layers, nullptr);
-    h->graph_cp.assign(layers, {nullptr, nullptr, nullptr});
+    h->graph_cp.assign(layers, {nullptr, nullptr});
     h->graph_warm.assign(layers, 0);
   }
   if (!ok) {
@@ -690,30 +690,44 @@ int moe_cache_trace(const moe_cache_t* h, int layer, moe_step_record_t* recs, in
 
 namespace {
 
-bool is_pinned(const void* p) {
+// The device-side address of page-locked host memory (null for pageable or
+// device memory).
+void* mapped(const void* p) {
   cudaPointerAttributes a{};
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return nullptr;
   }
-  return a.type == cudaMemoryTypeHost;
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
-// The step's copies and kernels on stream s: logits and x host -> staging, the
-// step over the staging buffers, out staging -> host.
+// The step's moves and kernels on stream s: logits and x host -> staging, the
+// step over the staging buffers, out staging -> host.  Page-locked buffers are
+// read and written by kernels through their device addresses; pageable ones
+// go through copies (synchronous for the host).
 int step_host_enqueue(moe_cache* h, int layer, int rows, const float* lg, const uint16_t* x,
                       float* out, cudaStream_t s) {
   const size_t nl = (size_t)rows * h->E, nx = (size_t)rows * h->H;
-  cudaError_t e = cudaMemcpyAsync(h->st_logits, lg, nl * sizeof(float), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
+  const void* dlg = mapped(lg);
+  const void* dx = mapped(x);
+  void* dout = mapped(out);
+  const bool direct = dlg && dx && dout;
+  cudaError_t e =
+      direct ? launch_host_in(s, static_cast<const float*>(dlg), static_cast<const uint16_t*>(dx),
+                              h->st_logits, h->st_x, (int)nl, (int)nx)
+             : cudaMemcpyAsync(h->st_logits, lg, nl * sizeof(float), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && !direct)
     e = cudaMemcpyAsync(h->st_x, x, nx * sizeof(uint16_t), cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int rc = moe_cache_step(h, layer, rows, h->st_logits, h->st_x, h->st_out, s);
   if (rc != MOE_OK) return rc;
-  return cuda_err(cudaMemcpyAsync(out, h->st_out, nx * sizeof(float), cudaMemcpyDeviceToHost, s));
+  return cuda_err(direct ? launch_host_out(s, h->st_out, static_cast<float*>(dout), (int)nx)
+                         : cudaMemcpyAsync(out, h->st_out, nx * sizeof(float),
+                                           cudaMemcpyDeviceToHost, s));
 }
 
-// Capture the layer's one-row step with its copies; find the three copy nodes.
+// Capture the layer's one-row step with its input and output moves (page-locked
+// buffers); find the nodes of the two move kernels.
 int capture_step_graph(moe_cache* h, int layer, const float* lg, const uint16_t* x, float* out) {
   cudaGraph_t g = nullptr;
   cudaError_t e = cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal);
@@ -729,19 +743,21 @@ int capture_step_graph(moe_cache* h, int layer, const float* lg, const uint16_t*
   e = cudaGraphGetNodes(g, nullptr, &n);
   std::vector<cudaGraphNode_t> nodes(n);
   if (e == cudaSuccess) e = cudaGraphGetNodes(g, nodes.data(), &n);
-  std::array<cudaGraphNode_t, 3> cp = {nullptr, nullptr, nullptr};
+  std::array<cudaGraphNode_t, 2> cp = {nullptr, nullptr};
   for (size_t i = 0; i < n && e == cudaSuccess; ++i) {
     cudaGraphNodeType t;
-    if ((e = cudaGraphNodeGetType(nodes[i], &t)) != cudaSuccess || t != cudaGraphNodeTypeMemcpy)
+    if ((e = cudaGraphNodeGetType(nodes[i], &t)) != cudaSuccess || t != cudaGraphNodeTypeKernel)
       continue;
-    cudaMemcpy3DParms mp{};
-    if ((e = cudaGraphMemcpyNodeGetParams(nodes[i], &mp)) != cudaSuccess) break;
-    if (mp.dstPtr.ptr == h->st_logits) cp[0] = nodes[i];
-    else if (mp.dstPtr.ptr == h->st_x) cp[1] = nodes[i];
-    else if (mp.srcPtr.ptr == h->st_out) cp[2] = nodes[i];
+    cudaKernelNodeParams kp{};
+    if (cudaGraphKernelNodeGetParams(nodes[i], &kp) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (is_host_in_node(kp.func)) cp[0] = nodes[i];
+    else if (is_host_out_node(kp.func)) cp[1] = nodes[i];
   }
   cudaGraphExec_t ex = nullptr;
-  if (e == cudaSuccess && cp[0] && cp[1] && cp[2]) e = cudaGraphInstantiate(&ex, g, 0);
+  if (e == cudaSuccess && cp[0] && cp[1]) e = cudaGraphInstantiate(&ex, g, 0);
   if (e != cudaSuccess || !ex) {
     cudaGraphDestroy(g);
     cudaGetLastError();
@@ -761,29 +777,25 @@ int moe_cache_step_host(moe_cache_t* h, int layer, int rows, const float* router
       !x || !out)
     return MOE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // One-row steps with page-locked buffers replay a graph of the copies and the
+  // One-row steps with page-locked buffers replay a graph of the moves and the
   // step: the layer's first such step runs eagerly (its launches set every
   // kernel's attributes), the second captures the graph on the handle's own
-  // stream, later ones point its copy nodes at the call's buffers and launch it.
-  if (rows == 1 && !h->timing && h->graph_warm[layer] && is_pinned(router_logits) &&
-      is_pinned(x) && is_pinned(out)) {
+  // stream, later ones point its move kernels at the call's buffers and launch it.
+  const void* dlg = rows == 1 ? mapped(router_logits) : nullptr;
+  const void* dx = rows == 1 ? mapped(x) : nullptr;
+  void* dout = rows == 1 ? mapped(out) : nullptr;
+  if (rows == 1 && !h->timing && h->graph_warm[layer] && dlg && dx && dout) {
     if (!h->graph[layer]) {
       const int rc = capture_step_graph(h, layer, router_logits, x, out);
       if (rc != MOE_OK) return rc;
     } else {
       const auto& cp = h->graph_cp[layer];
       cudaGraphExec_t ex = h->graph[layer];
-      cudaError_t e = cudaGraphExecMemcpyNodeSetParams1D(
-          ex, cp[0], h->st_logits, router_logits, (size_t)h->E * sizeof(float),
-          cudaMemcpyHostToDevice);
+      cudaError_t e = set_host_in_node(ex, cp[0], static_cast<const float*>(dlg),
+                                       static_cast<const uint16_t*>(dx), h->st_logits, h->st_x,
+                                       h->E, h->H);
       if (e == cudaSuccess)
-        e = cudaGraphExecMemcpyNodeSetParams1D(ex, cp[1], h->st_x, x,
-                                               (size_t)h->H * sizeof(uint16_t),
-                                               cudaMemcpyHostToDevice);
-      if (e == cudaSuccess)
-        e = cudaGraphExecMemcpyNodeSetParams1D(ex, cp[2], out, h->st_out,
-                                               (size_t)h->H * sizeof(float),
-                                               cudaMemcpyDeviceToHost);
+        e = set_host_out_node(ex, cp[1], h->st_out, static_cast<float*>(dout), h->H);
       if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return cuda_err(cudaGraphLaunch(h->graph[layer], st));

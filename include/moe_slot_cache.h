@@ -178,12 +178,13 @@ int moe_cache_step(moe_cache_t* h, int layer, int rows, const float* router_logi
                    const uint16_t* x, float* out, void* stream);
 
 /* The same layer-step with host buffers: router_logits (fp32 [rows][experts])
- * and x (bf16 bits [rows][hidden]) are copied host -> device into the handle's
- * staging, the step runs, and out (fp32 [rows][hidden]) is copied device ->
+ * and x (bf16 bits [rows][hidden]) are moved host -> device into the handle's
+ * staging, the step runs, and out (fp32 [rows][hidden]) is moved device ->
  * host, all enqueued on `stream` in that order.  Returns without waiting: the
  * host buffers must stay valid and unchanged until the stream has passed the
- * step (page-locked buffers make the copies asynchronous; pageable ones work,
- * synchronously).  rows <= max_rows.  One-row steps replay a CUDA graph of the
+ * step.  Page-locked buffers are read and written by two small kernels through
+ * their device addresses (asynchronous); pageable ones go through copies
+ * (synchronous for the host).  rows <= max_rows.  One-row steps replay a CUDA graph of the
  * step over the staging buffers, captured for each layer on its second
  * one-row call (never with timing events set, which take the eager path); the
  * handle's addresses never change, so a graph stays valid until

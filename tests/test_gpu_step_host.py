@@ -3,8 +3,9 @@
 A twin cache stepped through moe_cache_step on device buffers is the
 reference: every step's output must be bit-identical and the layer counters
 equal, over several layers (each one-row layer replays its own captured
-graph from its second step), a mid-run multi-row round (eager path) and the
-tiny and GLM shapes.  The device path itself is checked against the oracle
+graph from its second step), a mid-run multi-row round (eager path), the
+tiny and GLM shapes, page-locked buffers (moved by kernels, also unaligned)
+and pageable ones (copies).  The device path itself is checked against the oracle
 in test_gpu_decode.py.
 """
 import numpy as np
@@ -25,8 +26,23 @@ def lib():
     return m
 
 
-@pytest.mark.parametrize("name,layers,steps", [("tiny", 3, 20), ("glm", 2, 12)])
-def test_step_host_equals_device_step(lib, name, layers, steps):
+def _host(a, pinned, offset=0):
+    """A CPU tensor holding a's values: page-locked or pageable, its data
+    starting `offset` elements into a larger buffer (so not 16-byte aligned)."""
+    flat = a.reshape(-1)
+    buf = torch.empty(flat.numel() + offset, dtype=a.dtype)
+    if pinned:
+        buf = buf.pin_memory()
+    t = buf[offset:].view(a.shape)
+    t.copy_(a)
+    return t
+
+
+@pytest.mark.parametrize("name,layers,steps,pinned,offset", [
+    ("tiny", 3, 20, True, 0), ("glm", 2, 12, True, 0),
+    ("tiny", 2, 10, False, 0),     # pageable: the copy path
+    ("tiny", 2, 10, True, 1)])     # page-locked, not 16-byte aligned: the narrow kernel words
+def test_step_host_equals_device_step(lib, name, layers, steps, pinned, offset):
     cfg = workload.CONFIGS[name]
     banks = Banks(cfg, distinct=1)
     E, H = cfg.experts, cfg.hidden
@@ -44,9 +60,9 @@ def test_step_host_equals_device_step(lib, name, layers, steps):
             x_d = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
             out_d = torch.empty((rows, H), dtype=torch.float32, device="cuda")
             dev.step(l, lg_d, x_d, out_d)
-            lg_h = torch.from_numpy(lg).pin_memory()
-            x_h = torch.from_numpy(xb.view(np.int16)).pin_memory().view(torch.bfloat16)
-            out_h = torch.empty((rows, H), dtype=torch.float32).pin_memory()
+            lg_h = _host(torch.from_numpy(lg), pinned, offset)
+            x_h = _host(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16), pinned, offset)
+            out_h = _host(torch.zeros((rows, H), dtype=torch.float32), pinned, offset)
             with torch.cuda.stream(s):
                 host.step_host(l, lg_h, x_h, out_h, s)
             s.synchronize()
