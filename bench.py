@@ -561,6 +561,14 @@ def kernel_table(cfg, res: dict, hbm_peak: float, link_peak: float) -> tuple[dic
                                                 float(t_rt[hm].sum()), link_peak, "host-link", nm),
         "route_remap": {"ms_per_launch": float(t_route.mean())},
     }
+    # the resident passes alone: on steps without a miss nothing shares their SMs
+    if (~hm).any():
+        for n, t_k, per in (("gemv_gateup[resident picks]", t_gu_hit, gu_pick),
+                             ("gemv_down[resident picks]", t_dn_hit, dn_pick)):
+            b = float((n_hit[~hm] * per).sum())
+            a = b / (float(t_k[~hm].sum()) * 1e-3) / 1e9
+            kern[n]["steps_without_miss"] = {"achieved": a, "frac": a / hbm_peak,
+                                             "ms_per_launch": float(t_k[~hm].mean())}
     for n in kern:
         if "resident" in n:
             kern[n]["traffic"] = _traffic(n.split("[")[0], float(n_hit.mean()))
