@@ -21,7 +21,7 @@
 // themselves in on a per-stage mbarrier without waiting; a control warp
 // refills the stage and writes h = silu(gate) * up in fp32.
 //
-// down (resident or missed picks): one CTA per SM serves one pick; each warp
+// down (resident picks): one CTA per SM serves one pick; each warp
 // owns a ring of 2-row stages (TMA bulk copies) and reduces each W2 row with
 // w2_row_warp_g against gscale_j * w_j * h_j held in registers, writing the
 // weighted output y'_j.  At exit a CTA counts its 32-row output blocks; the CTA
@@ -32,10 +32,9 @@
 // the host link.  Its work list (units taken one at a time from a step
 // counter) holds each missed pick's gate/up units, computed on arrival with
 // the functions the resident gate/up uses, then the pick's W2 bytes as copy
-// units; every unit is written through to the pick's victim slot.  Every
-// thread stages 16-byte pieces from host memory with cp.async and an mbarrier
-// counts the threads' completions.  The missed picks' down pass is the down
-// kernel, launched after it.
+// units, each reduced on arrival against the pick's h; every unit is written
+// through to the pick's victim slot.  Every thread stages 16-byte pieces from
+// host memory with cp.async and an mbarrier counts the threads' completions.
 //
 // A pick's computation and reduction order do not depend on the subset, the
 // source or the kernel it runs in, so a cached step and an all-resident step
@@ -476,6 +475,10 @@ gemv_gateup_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   __shared__ const uint8_t* s_s[MOE_MAX_TOPK];
   __shared__ float s_gs[MOE_MAX_TOPK][2];
   const int upp = I / R;  // units per pick
+  // The down pass that follows (programmatic launch) takes an SM only once
+  // this grid's CTAs there have left, and issues its first resident W2
+  // copies while the last gate/up units finish.
+  pdl_launch_dependents();
 
   auto issue = [&](int unit, int stage) {  // control warp, lane 0
     const int jl = unit / upp, rb = unit - jl * upp;
@@ -917,16 +920,17 @@ gemv_down_kernel(const Plan* plan, const float* hbuf, float* ypart, int H, int I
     bulk_g2s(dst + IR * (I / 2), ssrc + (size_t)r0 * (I / 16), IR * (I / 16), &bars[s]);
   };
   const float f = __fmul_rn(plan->gs[j][2], plan->wts[j]);
-  pdl_wait();  // h and the slot bytes may come from the kernel before this one
-  {  // h first: its loads do not queue behind the ring's copy issue
-    for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
-      hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
-  }
+  // The picks this kernel serves are resident (hit picks of a cached step, or
+  // the caller's experts): their slot bytes were in place before the kernel
+  // before this one started, so the first copies go out before the wait.
   if (lane == 0) {
     for (int s = 0; s < NSW; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     for (int s = 0; s < NSW && s < my_items; ++s) issue(s, s);
   }
+  pdl_wait();  // h comes from the kernel before this one
+  for (int e = tid; e < I; e += blockDim.x)  // transposed: lanes read distinct banks
+    hs[(e & 31) * (I / 32) + (e >> 5)] = __fmul_rn(f, __ldcg(hbuf + (size_t)j * I + e));
   __syncthreads();
   // this lane's blocks of the pick's h, kept in registers for the whole kernel
   const int C = I / 32;
@@ -1152,7 +1156,9 @@ cudaError_t launch_gemv_down(cudaStream_t st, const Plan* plan, int H, int I, in
                              const GemvLaunch& how, float* out, uint32_t* ctr) {
   (void)k;
   const DownShape d = down_shape(I, how.stages);
-  if (d.NS < 1 || how.from_host) return cudaErrorInvalidConfiguration;  // slot bytes only
+  // resident slot bytes only: the kernel's first copies precede its wait on
+  // the kernel before it
+  if (d.NS < 1 || how.from_host || how.subset == kPicksMiss) return cudaErrorInvalidConfiguration;
   const int grid = gemv_down_grid(H, num_sms, how);
   const int C = I / 32;  // h blocks per W2 row: in registers up to two per lane
   if (C <= 32)
