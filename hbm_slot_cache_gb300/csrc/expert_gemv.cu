@@ -240,11 +240,6 @@ __device__ __forceinline__ void write_through(const uint8_t* stage, const Segs<N
   }
 }
 
-// Step counters (see kStepCounterWords).
-constexpr int kRtDoneCtr = 0;  // read-through CTAs finished
-constexpr int kWorkCtr = 1;    // read-through units taken
-constexpr int kBlockCtr = 2;   // + b: (pick, row) pairs finished for output block b
-constexpr int kHCtr = 2 + MOE_MAX_DIM / kOutBlockRows;  // + jl: missed pick jl's gate/up units done
 constexpr int kMaxStages = 8;  // gate/up stages at most
 
 // The plan, h and the partial outputs y' are written by a grid that may still
@@ -648,6 +643,7 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   __shared__ int s_hwait;   // the wait for a pick's h ended (1) or gave up (0)
   __shared__ int s_lastb[MOE_MAX_DIM / kOutBlockRows];
   __shared__ int s_nlast;
+  __shared__ int s_u0;
   const int C = H / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int g = tid / C, c = tid - g * C;
@@ -677,6 +673,15 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
       s_pcnt = p.pcnt;
       s_hpick = -1;
     }
+  }
+  // the stages and the CTA's first units, by the second warp while the first
+  // reads the plan (a one-warp CTA: after it)
+  if (tid == (nwarps > 1 ? 32 : 0)) {
+    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], blockDim.x);
+    fence_mbar_init();
+    *S.abort_flag = 0;
+    s_nlast = 0;
+    s_u0 = (int)atomicAdd(&ctr[kWorkCtr], (uint32_t)NS);
   }
   __syncthreads();
   const int pcnt = s_pcnt;
@@ -732,10 +737,7 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
   };
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&S.full[s], blockDim.x);
-    fence_mbar_init();
-    *S.abort_flag = 0;
-    const int u0 = (int)atomicAdd(&ctr[kWorkCtr], (uint32_t)NS);
+    const int u0 = s_u0;
     for (int s = 0; s < kMaxStages; ++s) s_unit[s] = (s < NS && u0 + s < NL) ? u0 + s : -1;
   }
   __syncthreads();
@@ -753,6 +755,7 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
     const int taken = tid == 0 ? (int)atomicAdd(&ctr[kWorkCtr], 1u) : 0;
     if (!mbar_wait_bounded(&S.full[stage], (uint32_t)((i / NS) & 1), flags, wait_ns))
       *S.abort_flag = 1;
+    if (tid == 0) s_nlast = 0;  // every thread read the last count before the previous barrier
     __syncthreads();
     if (*S.abort_flag) {  // flagged; the copies in flight are drained below
       i_abort = i;
@@ -768,13 +771,11 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
       r = unit - jl * upp;
       float a[V];
       gateup_partials<RPT>(st, H, RL, g, c, xh, a);
-      write_through(st, sg, nseg);
       stash_partials<V, WARP_RED>(a, S.red, g, c, C, lane);
     } else {
       const int v = unit - NG;
       jl = v / n2;
       const int r0 = (v - jl * n2) * R2, nr = H - r0 < R2 ? H - r0 : R2;
-      write_through(st, sg, nseg);
       if (s_hpick != jl) {  // uniform: this pick's h into shared memory, once it is complete
         if (tid == 0)
           s_hwait = count_wait_bounded(&ctr[kHCtr + jl], (uint32_t)upp, flags, wait_ns) ? 1 : 0;
@@ -797,16 +798,16 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
                                     lane);
         if (lane == 0) ypart[(size_t)j * H + r0 + rr] = y;
       }
-      __threadfence();
+      if (lane == 0) __threadfence();  // this warp's y' rows before the counts below
       __syncthreads();
-      if (tid == 0) {  // count the rows for their output blocks; combine what completes
-        int nl = 0;
-        for (int b = r0 / kOutBlockRows; b * kOutBlockRows < r0 + nr; ++b) {
+      {  // count the rows for their output blocks, a thread a block; combine what completes
+        const int b = r0 / kOutBlockRows + tid;
+        if (b * kOutBlockRows < r0 + nr) {
           const int lo = b * kOutBlockRows > r0 ? b * kOutBlockRows : r0;
           const int hi = (b + 1) * kOutBlockRows < r0 + nr ? (b + 1) * kOutBlockRows : r0 + nr;
-          if (add_block_rows(ctr, b, (uint32_t)(hi - lo), npicks)) s_lastb[nl++] = b;
+          if (add_block_rows(ctr, b, (uint32_t)(hi - lo), npicks))
+            s_lastb[atomicAdd(&s_nlast, 1)] = b;
         }
-        s_nlast = nl;
       }
       __syncthreads();
       combine_blocks(npicks, ypart, out, H, ctr, s_lastb, s_nlast);
@@ -829,6 +830,10 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
         atomicAdd(&ctr[kHCtr + jl], 1u);
       }
     }
+    // the unit's bytes to its slot, after the signals above so that their
+    // fences do not wait for these stores; nothing reads the slot this step
+    write_through(st, sg, nseg);
+    __syncthreads();  // every thread is done with the stage before its refill
     const int nxt = s_next[i & 1];
     if (nxt >= 0) fill(nxt, stage);
   }
@@ -846,12 +851,6 @@ gemv_readthrough_kernel(const Plan* plan, const uint16_t* __restrict__ x,
           break;
       }
     __syncthreads();
-  }
-  // the last CTA out (no unit is taken after it) resets the launch's counters
-  if (tid == 0 && atomicAdd(&ctr[kRtDoneCtr], 1u) == gridDim.x - 1) {
-    ctr[kWorkCtr] = 0u;
-    for (int q = 0; q < MOE_MAX_TOPK; ++q) ctr[kHCtr + q] = 0u;
-    ctr[kRtDoneCtr] = 0u;
   }
 }
 

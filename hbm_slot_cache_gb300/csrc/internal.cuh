@@ -36,6 +36,8 @@ struct LayerDev {
   moe_step_record_t* trace;  // [trace_cap] or null
   uint32_t* trace_head;      // records written so far
   uint32_t trace_cap;
+  uint32_t* step_ctr = nullptr;  // the handle's one-row step counters: route/remap clears
+                                 // the read-through's (work and h counts) for the step
 };
 
 // The per-step plan written by the remap kernel and read by the copy and
@@ -214,13 +216,20 @@ struct GemvLaunch {
                      // on the previous kernel of their stream (see pdl_wait)
   PickBounds bounds{};
 };
-// Counters of a one-row step (zero between steps; each user resets its own):
-//   [0] read-through CTAs that have finished, [1] read-through units taken,
-//   [2 + b] (pick, row) pairs whose y'_j row of output block b (kOutBlockRows
-//   rows) is written, [2 + H / kOutBlockRows max + jl] gate/up units of missed
-//   pick jl whose h rows are written (read-through).
+// Counters of a one-row step:
+//   [kWorkCtr] read-through units taken,
+//   [kBlockCtr + b] (pick, row) pairs whose y'_j row of output block b
+//   (kOutBlockRows rows) is written: zero between steps, reset by the CTA that
+//   combines the block,
+//   [kHCtr + jl] gate/up units of missed pick jl whose h rows are written
+//   (read-through).
+// The work and h counters are cleared by the step's route/remap (clear_link_ctr),
+// which completes before the read-through starts.
 constexpr int kOutBlockRows = 32;
-constexpr int kStepCounterWords = 2 + MOE_MAX_DIM / kOutBlockRows + MOE_MAX_TOPK;
+constexpr int kWorkCtr = 0;
+constexpr int kBlockCtr = 1;
+constexpr int kHCtr = 1 + MOE_MAX_DIM / kOutBlockRows;
+constexpr int kStepCounterWords = kHCtr + MOE_MAX_TOPK;
 cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t* x, int H, int I,
                                int k, const GemvWorkspace& ws, uint32_t* flags, int num_sms,
                                const GemvLaunch& how);
@@ -229,7 +238,8 @@ cudaError_t launch_gemv_gateup(cudaStream_t st, const Plan* plan, const uint16_t
 // gate/up + SwiGLU computed on its W13 rows on the way in -> ws.hbuf, then
 // its W2 rows reduced on the way in -> ws.ypart, counted for their output
 // blocks (combined into out by whichever launch completes a block).  Takes
-// its work from ctr[1]; its last CTA resets ctr[0..1] and the h counters.
+// its work from ctr[kWorkCtr]; the step's route/remap has cleared that and the h
+// counters.
 cudaError_t launch_gemv_readthrough(cudaStream_t st, const Plan* plan, const uint16_t* x, int H,
                                     int I, int k, const GemvWorkspace& ws, uint32_t* flags,
                                     int num_sms, const GemvLaunch& how, float* out, uint32_t* ctr);
@@ -282,6 +292,16 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 
 // Waits until the grid this one depends on (launch_pdl) has completed and its
 // writes are visible; returns at once for a normal launch.
+// Thread t of a route/remap launch: clears one of the read-through's counters
+// of the step (0 <= t <= MOE_MAX_TOPK; any other t does nothing).
+__device__ __forceinline__ void clear_link_ctr(uint32_t* ctr, int t) {
+  if (!ctr || t < 0 || t > MOE_MAX_TOPK) return;
+  if (t == 0)
+    ctr[kWorkCtr] = 0u;
+  else
+    ctr[kHCtr + t - 1] = 0u;
+}
+
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -244,6 +244,7 @@ LayerDev layer_dev(moe_cache* h, int l) {
   d.trace_cap = (uint32_t)h->opts.trace_capacity;
   d.trace = h->opts.trace_capacity ? h->trace + (size_t)l * h->opts.trace_capacity : nullptr;
   d.trace_head = h->trace_head + l;
+  d.step_ctr = h->gemv.tile_cnt;
   return d;
 }
 

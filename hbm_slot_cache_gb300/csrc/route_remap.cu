@@ -150,6 +150,7 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
 
   // the next kernel of the stream may be scheduled now (it waits for this one)
   asm volatile("griddepcontrol.launch_dependents;");
+  clear_link_ctr(L.step_ctr, tid - (kThreads - 1 - MOE_MAX_TOPK));  // the last 17 threads
 
   // ---- state into shared memory: every global load in flight at once
   constexpr int KPT = (MOE_MAX_EXPERTS + kThreads - 1) / kThreads;
@@ -487,6 +488,7 @@ route_one_kernel(const float* __restrict__ logits, int E, int k, int S, long lon
   asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x;
   const unsigned full = 0xFFFFFFFFu;
+  clear_link_ctr(L.step_ctr, lane - (32 - 1 - MOE_MAX_TOPK));  // lanes 15..31
   uint32_t* const fl = &L.stats->flags;
   if (lane < MOE_MAX_TOPK) {  // in range even where a failed plan check skips a write
     s_ids[lane] = 0;
