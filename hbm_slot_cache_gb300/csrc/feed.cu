@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(kFeedThreads)
 feed_inputs_kernel(const uint4* __restrict__ a_src, uint4* __restrict__ a_dst, long long a_words,
                    const uint4* __restrict__ b_src, uint4* __restrict__ b_dst, long long b_words,
                    uint32_t steps, uint32_t* cursor) {
+  pdl_launch_dependents();  // a step's route/remap, launched programmatically, waits for this grid
   __shared__ uint32_t s_c;
   if (threadIdx.x == 0) s_c = *reinterpret_cast<volatile uint32_t*>(cursor);
   __syncthreads();
@@ -57,6 +58,7 @@ __device__ __forceinline__ bool al16(const void* p) { return ((uintptr_t)p & 15)
 __global__ void __launch_bounds__(kIoThreads)
 host_in_kernel(const float* lg_h, const uint16_t* x_h, float* lg_d, uint16_t* x_d, int nl,
                int nx) {
+  pdl_launch_dependents();  // the step's route/remap waits for this grid
   const int stride = gridDim.x * blockDim.x, i0 = blockIdx.x * blockDim.x + threadIdx.x;
   if (al16(lg_h) && al16(lg_d) && (nl & 3) == 0) {
     for (int i = i0; i < nl / 4; i += stride)

@@ -470,11 +470,14 @@ route_remap_kernel(const float* __restrict__ logits, int rows, int E, int k, int
 }
 
 // One row, one warp: the same decisions as route_remap_kernel's one-row path,
-// without a CTA barrier.  Every global load is issued before any is used; the
-// top-k takes k rounds of a warp max (the rounds of route_row) and reads each
-// selected logit back from its key; hits, misses (ascending id) and victims
-// (k rounds at most of a warp min over the unused slots' (stamp, slot) keys)
-// come from ballots and shuffles; the bookkeeping is spread over lanes.
+// without a CTA barrier.  Launched as a programmatic dependent: its launch
+// overlaps the kernel before it, whose completion it waits for before any
+// access.  Every global load is then issued before any is used; the top-k
+// takes k rounds of a warp max (the rounds of route_row, each a pair of 32-bit
+// warp reductions over the key's high and low words) and reads each selected
+// logit back from its key; hits, misses (ascending id) and victims (k rounds
+// at most of a warp min over the unused slots' (stamp, slot) keys, likewise)
+// come from ballots and warp reductions; the bookkeeping is spread over lanes.
 template <int KPL>  // keys per lane >= ceil(max(E, S) / 32)
 __global__ void __launch_bounds__(32, 1)
 route_one_kernel(const float* __restrict__ logits, int E, int k, int S, long long Bw, long long Bs,
@@ -486,6 +489,9 @@ route_one_kernel(const float* __restrict__ logits, int E, int k, int S, long lon
   __shared__ float s_wts[MOE_MAX_TOPK];
   __shared__ int32_t s_miss_e[MOE_MAX_TOPK], s_victim[MOE_MAX_TOPK];
   asm volatile("griddepcontrol.launch_dependents;");
+  // launched programmatically: nothing is read or written before the kernel
+  // before this one has completed
+  pdl_wait();
   const int lane = threadIdx.x;
   const unsigned full = 0xFFFFFFFFu;
   clear_link_ctr(L.step_ctr, lane - (32 - 1 - MOE_MAX_TOPK));  // lanes 15..31
@@ -538,10 +544,13 @@ route_one_kernel(const float* __restrict__ logits, int E, int k, int S, long lon
   for (int q = 0; q < KPL; ++q) best = umax64(best, key[q]);
   float lsel = 0.f;  // lane j < k: the j-th selected logit
   for (int j = 0; j < k; ++j) {
-    unsigned long long w = best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) w = umax64(w, __shfl_xor_sync(full, w, o));
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
+    // the warp's largest key: the largest high word, then the largest low
+    // word among the keys that carry it (two 32-bit warp reductions)
+    const uint32_t bh = (uint32_t)(best >> 32);
+    const uint32_t mh = __reduce_max_sync(full, bh);
+    const uint32_t ml = __reduce_max_sync(full, bh == mh ? (uint32_t)best : 0u);
+    const unsigned long long w = ((unsigned long long)mh << 32) | ml;
+    const int e = (int)(0xFFFFFFFFu - ml);
     if ((e & 31) == lane) {  // the owning lane drops the winner and rescans
       best = 0ull;
 #pragma unroll
@@ -590,8 +599,11 @@ route_one_kernel(const float* __restrict__ logits, int E, int k, int S, long lon
       const int v = lane + 32 * q;
       if (v < S) m = umin64(m, s_skey[v]);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = umin64(m, __shfl_xor_sync(full, m, o));
+    {  // the warp's smallest key, high word first (two 32-bit warp reductions)
+      const uint32_t mh = __reduce_min_sync(full, (uint32_t)(m >> 32));
+      const uint32_t ml = __reduce_min_sync(full, (uint32_t)(m >> 32) == mh ? (uint32_t)m : ~0u);
+      m = ((unsigned long long)mh << 32) | ml;
+    }
     const int v = (int)(m & 0xFFFFFFFFull);
     if (lane == 0 && plan_ok(m != ~0ull && v < S, fl)) {
       s_victim[r] = v;
@@ -686,8 +698,8 @@ cudaError_t launch_route_remap(cudaStream_t st, const float* logits, int rows, i
   if (rows == 1 && !gp && k <= 32 && S <= E) {  // one row: the one-warp kernel
 #define RO(N)                                                                                   \
     if (kpl <= N) {                                                                            \
-      route_one_kernel<N><<<1, 32, 0, st>>>(logits, E, k, S, Bw, Bs, L, plan);                 \
-      return cudaGetLastError();                                                               \
+      return launch_pdl(route_one_kernel<N>, dim3(1), dim3(32), 0, st, logits, E, k, S, Bw, Bs, \
+                        L, plan);                                                              \
     }
     RO(1) RO(2) RO(4) RO(8) RO(16) RO(32)
 #undef RO
