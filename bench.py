@@ -15,7 +15,8 @@ Our arm: the per-step inputs are resident in HBM; a CUDA graph of a few steps
 is captured once, and its first node (moe_feed_inputs, a device step cursor)
 copies the next step's logits and x into the fixed buffers the step reads, so
 every replay runs on fresh inputs.  The plain graph (programmatic launches on)
-is timed in 5 runs of K steps each; the value is the median run.  Per-kernel
+is timed in runs of K fresh steps each (at least 5, and enough to cover about
+1,500 layer-steps, at most 50); the value is the median run.  Per-kernel
 times come from an event-instrumented graph on further fresh steps after the
 timed runs, and the end-to-end leg (moe_cache_step_host with pinned host
 buffers) runs on steps after those.  N > 1 (torchrun): independent replicas,
