@@ -187,7 +187,7 @@ cudaError_t set_host_out_node(cudaGraphExec_t ex, cudaGraphNode_t node, const fl
 struct GemvWorkspace {
   float* hbuf;        // [MOE_MAX_PICKS][I]
   float* ypart;       // [MOE_MAX_TOPK][H]
-  uint32_t* tile_cnt; // step counters (kStepCounterWords words), zero between steps
+  uint32_t* tile_cnt; // step counters (kStepCounterWords words, laid out below)
   uint32_t* flags;    // error flags word for waits (per layer stats flags)
 };
 // Pick subsets of a one-row step: the picks resident at step start, the
